@@ -1,0 +1,299 @@
+"""Expert computation of the fused MoE forward -- fp64 oracle.
+
+Test infrastructure only.  Sources (page titles and sections):
+
+* "fused_moe.py 分析" §1.1-1.4: y_t = sum_i alpha_{t,i} f_{e_{t,i}}(x_t); routed
+  form C[r, n] = sum_k A[t(r), k] B[e(r), n, k] (B stored [E, N, K]); the
+  router-weight placement equivalence W^T(a z) = a W^T z.
+* same page, "fused_moe_kernel 的核心原理": fp32 accumulation, cast to the
+  compute type; "FP8 W8A8": block-wise C_block ~ dot(qA, qB) * a_scale * b_scale
+  per K block.
+* "Blackwell 上的 DeepGEMM FusedMoE（vLLM）" §1.1 / §2.6: permute -> GEMM1 (bf16
+  mm1_out [M_sum, 2I]) -> SwiGLU + dynamic 1x128 quant -> GEMM2 (bf16 mm2_out)
+  -> ep_gather (fp32 weighted sum in slot order, cast to bf16); padding rows
+  carry zero activation scales; ids < 0 contribute nothing; with
+  apply_router_weight_on_input the reduce uses all-ones weights.
+
+Readings (the pages are silent or disagree):
+* gated activation: z = SiLU(first half) * second half of GEMM1's 2I outputs
+  (SwiGLU; "SiLU-and-mul"), SiLU(g) = g / (1 + exp(-g));
+* intermediate roundings: H1, Z (bf16 mode) and Y2 are rounded to bf16, the
+  final y to bf16; everything else is fp64.  ``exact=True`` skips them;
+* FP8 activation quant per 1x128 group: s = fp32(max(amax, eps) / 448) with
+  eps = fp32(1e-10); UE8M0 option: s rounded up to a power of two; code =
+  e4m3_rne_sat(fp32(v / s)).  Padding rows: codes 0, scale 0;
+* apply_router_weight_on_input (top-k = 1 only): the routed row is
+  bf16(fp32(x_t * w)) before quantisation, and the reduce uses weight 1;
+* MXFP4 weights are dequantised (E2M1 * 2^(e-127)) and multiplied in fp64,
+  which equals the per-32 block-scaled product exactly.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+from . import codecs
+from .routing import align_permute
+
+EPS32 = float(np.float32(1e-10))
+
+
+# ----------------------------------------------------------------- quantisation
+def quant_act_1x128(v, scale_fmt: str = "fp32"):
+    """Dynamic per-(row, 128-column group) FP8 quantisation.
+
+    v: [R, K] fp64 (K % 128 == 0).  Returns (q values [R, K] fp64 on the e4m3
+    grid, s [R, K/128] fp64 holding fp32 (or power-of-two) scales)."""
+    v = np.asarray(v, dtype=np.float64)
+    R, K = v.shape
+    g = v.reshape(R, K // 128, 128)
+    amax = np.abs(g).max(axis=-1) if R else np.zeros((0, K // 128))
+    s = codecs.round_fp32(np.maximum(amax, EPS32) / codecs.E4M3_MAX)
+    if scale_fmt == "ue8m0":
+        s = codecs.ceil_pow2(s)
+    elif scale_fmt != "fp32":
+        raise ValueError(scale_fmt)
+    q = codecs.round_e4m3(codecs.round_fp32(g / s[..., None]))
+    return q.reshape(R, K), s
+
+
+def dequant_weights(w, w_scale, quant: str):
+    """Weights in storage format -> fp64 values [E, N, K].
+
+    bf16: values as given.  fp8: e4m3 codes * fp32 128x128 block scale.
+    mxfp4: E2M1 codes (packed, low nibble even k) * E8M0 scale per 32 along K.
+    """
+    if quant == "bf16":
+        return np.asarray(w, dtype=np.float64)
+    if quant == "fp8":
+        q = codecs.e4m3_decode(w)
+        s = np.asarray(w_scale, dtype=np.float64)
+        s_full = np.repeat(np.repeat(s, 128, axis=1), 128, axis=2)
+        return q * s_full[:, : q.shape[1], : q.shape[2]]
+    if quant == "mxfp4":
+        E, N, Kh = np.asarray(w).shape
+        q = codecs.e2m1_decode(codecs.unpack_fp4(w, 2 * Kh))
+        s = codecs.e8m0_decode(w_scale)
+        return q * np.repeat(s, 32, axis=2)
+    raise ValueError(quant)
+
+
+# ------------------------------------------------------------------ the stages
+def permute_rows(x, route, topk: int, topk_weights=None, scale_fmt=None):
+    """Data half of the permute: x_perm[row] = x[sorted_token_ids[row] // k].
+
+    Padding rows are zero.  With ``topk_weights`` (apply_router_weight_on_input)
+    the row is bf16(fp32(x_t * w_r)).  With ``scale_fmt`` the rows are
+    quantised per 1x128 group; padding rows get code 0 and scale 0.
+    Returns (x_perm [cap, H], scale [cap, H/128] or None)."""
+    x = np.asarray(x, dtype=np.float64)
+    H = x.shape[1]
+    sid = route["sorted_token_ids"]
+    R = route["inv_perm"].size
+    cap = len(sid)
+    live = sid < R
+    xp = np.zeros((cap, H))
+    xp[live] = x[sid[live] // topk]
+    if topk_weights is not None:
+        w = np.asarray(topk_weights, dtype=np.float64).reshape(-1)
+        xp[live] = codecs.round_bf16(codecs.round_fp32(xp[live] * w[sid[live]][:, None]))
+    if scale_fmt is None:
+        return xp, None
+    q, s = quant_act_1x128(xp, scale_fmt)
+    q[~live] = 0.0
+    s[~live] = 0.0
+    return q, s
+
+
+def grouped_gemm(a, a_scale, w, w_scale, route, block_size: int, quant: str):
+    """C[row, n] = sum_k A[row, k] * W[e, n, k] for every padded block with
+    expert e >= 0 below num_tokens_post_padded; other rows are 0.
+
+    bf16: plain fp64 product.  fp8 (block 128x128 weight scales, 1x128
+    activation scales): C = sum_kb sa[row, kb] * sb[e, n/128, kb] *
+    sum_{k in kb} qa * qb.  mxfp4: A = qa * sa (per 128), W dequantised.
+    Returns fp64 [cap, N] (not rounded)."""
+    a = np.asarray(a, dtype=np.float64)
+    cap, K = a.shape
+    block_ids = route["block_expert_ids"]
+    n_blocks = route["num_tokens_post_padded"] // block_size
+    E = np.asarray(w).shape[0]
+    if quant == "fp8":
+        N = np.asarray(w).shape[1]
+    elif quant == "mxfp4":
+        N = np.asarray(w).shape[1]
+    else:
+        N = np.asarray(w).shape[1]
+    out = np.zeros((cap, N))
+    for b in range(n_blocks):
+        e = int(block_ids[b])
+        if e < 0:
+            continue
+        rows = slice(b * block_size, (b + 1) * block_size)
+        if quant == "bf16":
+            out[rows] = a[rows] @ np.asarray(w[e], dtype=np.float64).T
+        elif quant == "fp8":
+            qb = codecs.e4m3_decode(w[e])                  # [N, K]
+            sb = np.asarray(w_scale[e], dtype=np.float64)  # [N/128, K/128]
+            acc = np.zeros((block_size, N))
+            for kb in range(K // 128):
+                ks = slice(kb * 128, (kb + 1) * 128)
+                part = a[rows, ks] @ qb[:, ks].T            # exact: e4m3 products
+                sb_n = np.repeat(sb[:, kb], 128)[:N]
+                acc += a_scale[rows, kb][:, None] * sb_n[None, :] * part
+            out[rows] = acc
+        elif quant == "mxfp4":
+            wd = dequant_weights(np.asarray(w[e])[None], np.asarray(w_scale[e])[None], "mxfp4")[0]
+            ad = a[rows] * np.repeat(a_scale[rows], 128, axis=1)
+            out[rows] = ad @ wd.T
+        else:
+            raise ValueError(quant)
+    return out
+
+
+def silu(g):
+    """SiLU(g) = g * sigmoid(g) = g / (1 + exp(-g))."""
+    g = np.asarray(g, dtype=np.float64)
+    return g / (1.0 + np.exp(-g))
+
+
+def act_mul(h1, I: int, exact: bool = False):
+    """SiLU-and-mul on the 2I outputs of GEMM1: z = SiLU(h[:, :I]) * h[:, I:].
+    Unless ``exact``, h1 is first rounded to bf16 (mm1_out is bf16)."""
+    h1 = np.asarray(h1, dtype=np.float64)
+    if not exact:
+        h1 = codecs.round_bf16(h1)
+    return silu(h1[:, :I]) * h1[:, I:]
+
+
+def unpermute_reduce(y2, inv_perm, topk_weights, apply_router_weight_on_input=False,
+                     exact: bool = False):
+    """y[t] = sum_{i: inv_perm[t,i] >= 0} w'[t,i] * Y2[inv_perm[t,i]], slot order,
+    w' = 1 with apply_router_weight_on_input; cast to bf16 unless ``exact``."""
+    y2 = np.asarray(y2, dtype=np.float64)
+    inv = np.asarray(inv_perm, dtype=np.int64)
+    w = np.asarray(topk_weights, dtype=np.float64)
+    M, k = inv.shape
+    y = np.zeros((M, y2.shape[1]))
+    for i in range(k):
+        ok = inv[:, i] >= 0
+        wi = np.ones(M) if apply_router_weight_on_input else w[:, i]
+        y[ok] += wi[ok, None] * y2[inv[ok, i]]
+    return y if exact else codecs.round_bf16(y)
+
+
+# ------------------------------------------------------------- whole forward
+def _act_scale_fmt(quant: str, act_scale_fmt: str):
+    return None if quant == "bf16" else act_scale_fmt
+
+
+def fused_experts(x, topk_ids, topk_weights, w13, w2, w13_scale=None, w2_scale=None, *,
+                  quant="bf16", act_scale_fmt="fp32", block_size=128,
+                  apply_router_weight_on_input=False, exact=False):
+    """Form 2 (the pages' organisation): routing, permute, grouped GEMM1,
+    SiLU-and-mul (+ quant), grouped GEMM2, weighted unpermute-reduce.
+    Returns a dict with every intermediate and ``y`` [M, H]."""
+    x = np.asarray(x, dtype=np.float64)
+    ids = np.asarray(topk_ids)
+    M, k = ids.shape
+    E = np.asarray(w13).shape[0]
+    I = np.asarray(w2).shape[2] if quant != "mxfp4" else 2 * np.asarray(w2).shape[2]
+    if apply_router_weight_on_input and k != 1:
+        raise ValueError("apply_router_weight_on_input needs top-k = 1")
+    fmt = _act_scale_fmt(quant, act_scale_fmt)
+    route = align_permute(ids, E, block_size)
+    xp, xs = permute_rows(x, route, k,
+                          topk_weights if apply_router_weight_on_input else None, fmt)
+    h1 = grouped_gemm(xp, xs, w13, w13_scale, route, block_size, quant)
+    z = act_mul(h1, I, exact=exact)
+    if fmt is None:
+        zq, zs = (z if exact else codecs.round_bf16(z)), None
+    else:
+        zq, zs = quant_act_1x128(z, fmt)
+        live = route["sorted_token_ids"] < M * k
+        zq[~live] = 0.0
+        zs[~live] = 0.0
+    y2 = grouped_gemm(zq, zs, w2, w2_scale, route, block_size, quant)
+    if not exact:
+        y2 = codecs.round_bf16(y2)
+    y = unpermute_reduce(y2, route["inv_perm"], topk_weights, apply_router_weight_on_input,
+                         exact=exact)
+    return {"route": route, "x_perm": xp, "x_scale": xs, "h1": h1, "z": zq, "z_scale": zs,
+            "y2": y2, "y": y}
+
+
+def fused_experts_per_token(x, topk_ids, topk_weights, w13, w2, w13_scale=None,
+                            w2_scale=None, *, quant="bf16", act_scale_fmt="fp32",
+                            apply_router_weight_on_input=False, exact=False, tokens=None):
+    """Form 1: brute-force loop over tokens and slots, no permutation.
+
+    For each (t, i) with e = id[t, i] >= 0: quantise x_t (quantised modes),
+    h = W13_e x_t, z = SiLU(h_gate) * h_up, o = W2_e z, y_t += w * o.  The
+    same roundings as form 2 are applied item by item.  ``tokens`` restricts
+    the tokens evaluated (outputs of different tokens are independent).
+    Returns y [len(tokens), H]."""
+    x = np.asarray(x, dtype=np.float64)
+    ids = np.asarray(topk_ids, dtype=np.int64)
+    wts = np.asarray(topk_weights, dtype=np.float64)
+    M, k = ids.shape
+    tokens = list(range(M)) if tokens is None else list(tokens)
+    fmt = _act_scale_fmt(quant, act_scale_fmt)
+    w13 = np.asarray(w13)
+    w2 = np.asarray(w2)
+    H = x.shape[1]
+    outs = {}
+    # weights are decoded once per expert; items are still evaluated one by one
+    experts = sorted({int(ids[t, i]) for t in tokens for i in range(k) if ids[t, i] >= 0})
+    for e in experts:
+        W13 = dequant_weights(w13[e][None], None if w13_scale is None else
+                              np.asarray(w13_scale)[e][None], quant)[0]
+        W2 = dequant_weights(w2[e][None], None if w2_scale is None else
+                             np.asarray(w2_scale)[e][None], quant)[0]
+        I = W2.shape[1]
+        for t in tokens:
+            for i in range(k):
+                if ids[t, i] != e:
+                    continue
+                xt = x[t]
+                if apply_router_weight_on_input:
+                    xt = codecs.round_bf16(codecs.round_fp32(xt * wts[t, i]))
+                if fmt is None:
+                    h = W13 @ xt
+                else:
+                    q, s = quant_act_1x128(xt[None], fmt)
+                    if quant == "fp8":
+                        h = _fp8_matvec(q[0], s[0], w13[e], np.asarray(w13_scale)[e])
+                    else:
+                        h = W13 @ (q[0] * np.repeat(s[0], 128))
+                if not exact:
+                    h = codecs.round_bf16(h)
+                z = silu(h[:I]) * h[I:]
+                if fmt is None:
+                    if not exact:
+                        z = codecs.round_bf16(z)
+                    o = W2 @ z
+                else:
+                    q, s = quant_act_1x128(z[None], fmt)
+                    if quant == "fp8":
+                        o = _fp8_matvec(q[0], s[0], w2[e], np.asarray(w2_scale)[e])
+                    else:
+                        o = W2 @ (q[0] * np.repeat(s[0], 128))
+                if not exact:
+                    o = codecs.round_bf16(o)
+                outs[(t, i)] = o
+    y = np.zeros((len(tokens), H))
+    for j, t in enumerate(tokens):
+        for i in range(k):                      # slot order
+            if ids[t, i] < 0:
+                continue
+            wi = 1.0 if apply_router_weight_on_input else wts[t, i]
+            y[j] += wi * outs[(t, i)]
+    return y if exact else codecs.round_bf16(y)
+
+
+def _fp8_matvec(qa, sa, w_codes, w_scale):
+    """h[n] = sum_kb sa[kb] * sb[n/128, kb] * sum_{k in kb} qa[k] * qb[n, k]."""
+    qb = codecs.e4m3_decode(w_codes)             # [N, K]
+    N, K = qb.shape
+    part = np.einsum("nbj,bj->nb", qb.reshape(N, K // 128, 128), qa.reshape(K // 128, 128))
+    sb = np.repeat(np.asarray(w_scale, dtype=np.float64), 128, axis=0)[:N]   # [N, K/128]
+    return (sa[None, :] * sb * part).sum(axis=1)

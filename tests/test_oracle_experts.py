@@ -1,0 +1,249 @@
+"""Pins for oracle/experts.py.
+
+* the permuted form (the pages' five stages) equals a per-token brute-force
+  loop that never permutes;
+* E = 1, k = 1, w = 1 reduces the path to a dense SwiGLU MLP, checked against
+  torch's fp64 matmul and F.silu;
+* the router-weight placement invariant W^T(a z) = a W^T z;
+* the FP8 block formula equals dequantise-then-multiply;
+* activation quantisation checked against torch's float8 cast and the e4m3
+  error bound;
+* planted mistakes (in the oracle, on the CPU) are caught by these pins.
+"""
+import numpy as np
+import pytest
+import torch
+
+from moe_synth import MoEConfig, make_inputs
+from oracle import codecs, experts, routing
+
+
+def _np(t):
+    return None if t is None else (t.float().numpy() if t.dtype in (torch.bfloat16,)
+                                   else t.numpy())
+
+
+def _inputs(cfg):
+    d = make_inputs(cfg)
+    return dict(x=_np(d["x"]), topk_ids=_np(d["topk_ids"]), topk_weights=_np(d["topk_weights"]),
+                w13=_np(d["w13"]), w2=_np(d["w2"]), w13_scale=_np(d["w13_scale"]),
+                w2_scale=_np(d["w2_scale"]))
+
+
+SMALL = {
+    "bf16": MoEConfig("t_bf16", M=16, H=256, I=128, E=8, topk=2, quant="bf16",
+                      routing="softmax", seed=1),
+    "fp8": MoEConfig("t_fp8", M=12, H=256, I=256, E=4, topk=2, quant="fp8",
+                     routing="softmax", seed=11),
+    "fp8_ue8m0": MoEConfig("t_fp8u", M=12, H=256, I=256, E=4, topk=2, quant="fp8",
+                           routing="softmax", seed=12, act_scale_fmt="ue8m0"),
+    "mxfp4": MoEConfig("t_mx", M=10, H=256, I=128, E=4, topk=3, quant="mxfp4",
+                       routing="uniform", seed=13, act_scale_fmt="ue8m0"),
+    "invalid": MoEConfig("t_inv", M=20, H=128, I=128, E=6, topk=3, quant="bf16",
+                         routing="softmax", seed=14, invalid_frac=0.3),
+}
+
+
+def _both_forms(cfg, exact=False, block_size=128):
+    a = _inputs(cfg)
+    kw = dict(quant=cfg.quant, act_scale_fmt=cfg.act_scale_fmt,
+              apply_router_weight_on_input=cfg.apply_router_weight_on_input, exact=exact)
+    f2 = experts.fused_experts(**a, block_size=block_size, **kw)["y"]
+    f1 = experts.fused_experts_per_token(**a, **kw)
+    return f1, f2
+
+
+@pytest.mark.parametrize("name", list(SMALL))
+@pytest.mark.parametrize("exact", [False, True])
+def test_permuted_form_equals_per_token_loop(name, exact):
+    f1, f2 = _both_forms(SMALL[name], exact=exact)
+    assert np.all(np.isfinite(f2))
+    rms = np.sqrt(np.mean(f1 ** 2))
+    np.testing.assert_allclose(f2, f1, rtol=1e-12, atol=1e-12 * rms)
+
+
+def test_block_size_does_not_change_result():
+    cfg = SMALL["bf16"]
+    a = _inputs(cfg)
+    ys = [experts.fused_experts(**a, block_size=A)["y"] for A in (16, 32, 64, 128)]
+    for y in ys[1:]:
+        np.testing.assert_allclose(y, ys[0], rtol=1e-12, atol=0)
+
+
+def test_dense_special_case_is_swiglu_mlp():
+    """E=1, k=1, w=1: y = W2 (silu(Wg x) * (Wu x)) -- a dense SwiGLU MLP."""
+    g = torch.Generator().manual_seed(5)
+    M, H, I = 7, 128, 256
+    x = torch.randn(M, H, generator=g, dtype=torch.float64)
+    w13 = torch.randn(1, 2 * I, H, generator=g, dtype=torch.float64) * 0.05
+    w2 = torch.randn(1, H, I, generator=g, dtype=torch.float64) * 0.05
+    ref = (torch.nn.functional.silu(x @ w13[0, :I].T) * (x @ w13[0, I:].T)) @ w2[0].T
+    out = experts.fused_experts(x.numpy(), np.zeros((M, 1), np.int64), np.ones((M, 1)),
+                                w13.numpy(), w2.numpy(), exact=True)["y"]
+    np.testing.assert_allclose(out, ref.numpy(), rtol=1e-12, atol=1e-14)
+
+
+def test_router_weight_placement_invariant():
+    """Scaling Z rows by w before W2 equals scaling the W2 output (exact mode)."""
+    cfg = SMALL["bf16"]
+    a = _inputs(cfg)
+    E, A, k = a["w13"].shape[0], 128, cfg.topk
+    route = routing.align_permute(a["topk_ids"], E, A)
+    xp, _ = experts.permute_rows(a["x"], route, k)
+    z = experts.act_mul(experts.grouped_gemm(xp, None, a["w13"], None, route, A, "bf16"),
+                        cfg.I, exact=True)
+    R = cfg.M * k
+    sid = route["sorted_token_ids"]
+    w_row = np.where(sid < R, a["topk_weights"].reshape(-1)[np.minimum(sid, R - 1)], 0.0)
+    y_in = experts.unpermute_reduce(
+        experts.grouped_gemm(z * w_row[:, None], None, a["w2"], None, route, A, "bf16"),
+        route["inv_perm"], a["topk_weights"], apply_router_weight_on_input=True, exact=True)
+    y_out = experts.unpermute_reduce(
+        experts.grouped_gemm(z, None, a["w2"], None, route, A, "bf16"),
+        route["inv_perm"], a["topk_weights"], exact=True)
+    np.testing.assert_allclose(y_in, y_out, rtol=1e-12, atol=1e-15)
+
+
+def test_apply_router_weight_on_input_topk1():
+    cfg = SMALL["bf16"].with_(topk=1, apply_router_weight_on_input=True, seed=21)
+    f1, f2 = _both_forms(cfg)
+    np.testing.assert_allclose(f2, f1, rtol=1e-12, atol=0)
+    # for top-1 it matches output weighting up to bf16 rounding of the scaled input
+    a = _inputs(cfg)
+    y_out = experts.fused_experts(**a)["y"]
+    rms = np.sqrt(np.mean(y_out ** 2))
+    assert np.max(np.abs(f2 - y_out)) <= 2e-2 * rms
+    with pytest.raises(ValueError):
+        experts.fused_experts(**_inputs(SMALL["bf16"]), apply_router_weight_on_input=True)
+
+
+def test_fp8_block_formula_equals_dequantised_product():
+    cfg = SMALL["fp8"]
+    a = _inputs(cfg)
+    A = 128
+    route = routing.align_permute(a["topk_ids"], cfg.E, A)
+    xq, xs = experts.permute_rows(a["x"], route, cfg.topk, scale_fmt="fp32")
+    c = experts.grouped_gemm(xq, xs, a["w13"], a["w13_scale"], route, A, "fp8")
+    wd = experts.dequant_weights(a["w13"], a["w13_scale"], "fp8")
+    rows = routing.row_expert_ids(route, A)
+    blocks = route["block_expert_ids"]
+    ref = np.zeros_like(c)
+    for b in range(route["num_tokens_post_padded"] // A):
+        sl = slice(b * A, (b + 1) * A)
+        ref[sl] = (xq[sl] * np.repeat(xs[sl], 128, axis=1)) @ wd[blocks[b]].T
+    np.testing.assert_allclose(c, ref, rtol=1e-12, atol=1e-12)
+    assert np.all(c[rows == -1] == 0)
+
+
+def test_activation_quant_against_torch_cast():
+    rng = np.random.default_rng(3)
+    v = codecs.round_bf16(rng.normal(0, 1, (64, 512)) * rng.uniform(0.01, 100, (64, 1)))
+    q, s = experts.quant_act_1x128(v, "fp32")
+    vt = torch.from_numpy(v.astype(np.float32)).view(64, 4, 128)
+    st = (vt.abs().amax(-1).clamp_min(float(np.float32(1e-10))) / 448.0)
+    qt = (vt / st[..., None]).to(torch.float8_e4m3fn).double().view(64, 512)
+    assert np.array_equal(s, st.double().numpy())
+    assert np.array_equal(q, qt.numpy())
+    # the amax element of each group maps to +-448
+    g = np.abs(q.reshape(64, 4, 128)).max(-1)
+    assert np.all(g == 448.0)
+    # reconstruction within e4m3 half-ulp (2^-4 relative for normal codes)
+    rec = q * np.repeat(s, 128, axis=1)
+    big = np.abs(v) >= 2.0 ** -6 * np.repeat(s, 128, axis=1)
+    assert np.all(np.abs(rec - v)[big] <= 2.0 ** -4 * np.abs(v)[big] * (1 + 1e-6))
+
+
+def test_activation_quant_ue8m0_and_zero_group():
+    rng = np.random.default_rng(4)
+    v = codecs.round_bf16(rng.normal(0, 3, (8, 256)))
+    v[0, :128] = 0.0
+    q32, s32 = experts.quant_act_1x128(v, "fp32")
+    q8, s8 = experts.quant_act_1x128(v, "ue8m0")
+    assert np.all(codecs.ceil_pow2(s8) == s8) and np.all(s8 >= s32) and np.all(s8 < 2 * s32)
+    assert np.all(q8[0, :128] == 0) and s32[0, 0] == codecs.round_fp32(np.float32(1e-10) / 448.0)
+    assert np.all(np.abs(q8) <= 448.0)
+
+
+def test_invalid_ids_contribute_nothing():
+    cfg = SMALL["invalid"]
+    a = _inputs(cfg)
+    assert np.any(a["topk_ids"] < 0)
+    y = experts.fused_experts(**a)["y"]
+    w2 = a["topk_weights"].copy()
+    w2[a["topk_ids"] < 0] = 123.0
+    a2 = dict(a, topk_weights=w2)
+    assert np.array_equal(experts.fused_experts(**a2)["y"], y)
+
+
+def test_empty_batch():
+    cfg = SMALL["bf16"]
+    a = _inputs(cfg)
+    a = dict(a, x=a["x"][:0], topk_ids=a["topk_ids"][:0], topk_weights=a["topk_weights"][:0])
+    assert experts.fused_experts(**a)["y"].shape == (0, cfg.H)
+
+
+def test_silu_against_scipy_and_identity():
+    from scipy.special import expit
+    g = np.linspace(-30, 30, 2001)
+    np.testing.assert_allclose(experts.silu(g), g * expit(g), rtol=1e-14, atol=1e-300)
+    np.testing.assert_allclose(experts.silu(-g), experts.silu(g) - g, rtol=1e-12, atol=1e-12)
+    assert experts.silu(0.0) == 0.0
+
+
+# --------------------------------------------------------------- planted mistakes
+def _catches(monkeypatch, target, replacement):
+    """Plant ``replacement`` for ``target`` in the oracle and report whether a
+    pin now fails."""
+    monkeypatch.setattr(experts, target, replacement)
+    failures = 0
+    for fn in (lambda: test_dense_special_case_is_swiglu_mlp(),
+               lambda: test_permuted_form_equals_per_token_loop("bf16", False),
+               lambda: test_permuted_form_equals_per_token_loop("fp8", False)):
+        try:
+            fn()
+        except AssertionError:
+            failures += 1
+    return failures > 0
+
+
+def test_planted_gate_up_swap_is_caught(monkeypatch):
+    orig = experts.act_mul
+
+    def swapped(h1, I, exact=False):
+        h1 = np.asarray(h1)
+        return orig(np.concatenate([h1[:, I:], h1[:, :I]], axis=1), I, exact)
+    assert _catches(monkeypatch, "act_mul", swapped)
+
+
+def test_planted_token_index_mistake_is_caught(monkeypatch):
+    orig = experts.permute_rows
+
+    def wrong(x, route, topk, topk_weights=None, scale_fmt=None):
+        r2 = dict(route)
+        sid = route["sorted_token_ids"].copy()
+        R = route["inv_perm"].size
+        live = sid < R
+        sid[live] = (sid[live] % topk) * topk + (sid[live] // topk) % topk  # r % k for r // k
+        r2["sorted_token_ids"] = sid
+        return orig(x, r2, topk, topk_weights, scale_fmt)
+    assert _catches(monkeypatch, "permute_rows", wrong)
+
+
+def test_planted_dropped_router_weight_is_caught(monkeypatch):
+    orig = experts.unpermute_reduce
+
+    def dropped(y2, inv_perm, topk_weights, apply_router_weight_on_input=False, exact=False):
+        return orig(y2, inv_perm, topk_weights, True, exact)
+    assert _catches(monkeypatch, "unpermute_reduce", dropped)
+
+
+def test_planted_fp8_scale_mistake_is_caught(monkeypatch):
+    orig = experts.quant_act_1x128
+
+    def wrong(v, scale_fmt="fp32"):
+        q, s = orig(v, scale_fmt)
+        return q, s * 1.5
+    # both forms share the quantiser, so the torch-cast pin is the one that catches it
+    monkeypatch.setattr(experts, "quant_act_1x128", wrong)
+    with pytest.raises(AssertionError):
+        test_activation_quant_against_torch_cast()
