@@ -1,0 +1,357 @@
+"""Benchmark of the fused MoE expert forward on GB300.
+
+Workload: the Mixtral-8x7B-shaped prefill layer (M=4096 tokens, H=4096,
+I=14336, E=8, top-2, bf16; weights N(0, 0.02), router softmax top-2 of N(0,1)
+logits), seeded synthetic inputs resident in HBM.  One step = one pass of the
+whole path over the batch: routing + permute, grouped GEMM1 with the fused
+SiLU-and-mul, grouped GEMM2, weighted unpermute-reduce -- the same launches
+fused_experts makes, issued through the staged C-ABI entry points so CUDA
+events can bracket each stage on the launching stream.  The fused_experts
+call itself is timed as well (fused_call_ms).  The weights (2.82 GB) are far
+larger than L2, so no flush is needed between steps.
+
+Metric: routed tokens/s (M * top-k per second), whole job over all ranks.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+       torchrun ... bench.py --gpus N ...  (replicas: one independent layer per GPU)
+
+--impl reference times the fp64 CPU oracle (oracle/, test infrastructure) on
+the host cores, one token of the same workload per step.
+"""
+from __future__ import annotations
+
+import argparse
+import csv
+import io
+import json
+import os
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "fused-MoE fwd routed tokens/s; % of tensor-core/HBM roofline (1 GB300)"
+UNIT = "routed tokens/s"
+WORKLOAD = "mixtral"
+
+
+def _peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return {"hbm_gbs": p["hbm_gbs"], "bf16_tflops": p["bf16_tflops"],
+                "bf16_tflops_sustained": p["bf16_tflops_sustained"], "source": "measured"}
+    except Exception:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+                "source": "fallback"}
+
+
+def _config_dict(cfg, n):
+    return {"workload": f"{cfg.name}: Mixtral-8x7B-shaped prefill M={cfg.M} H={cfg.H} "
+                        f"I={cfg.I} E={cfg.E} top-{cfg.topk} bf16",
+            "M": cfg.M, "H": cfg.H, "I": cfg.I, "E": cfg.E, "topk": cfg.topk,
+            "block_size": cfg.block_size, "routed_tokens_per_gpu": cfg.R,
+            "l2": "inputs larger than L2 (weights 2.82 GB per GPU), no flush",
+            "parallelism": f"replicas x{n}"}
+
+
+class ClockSampler:
+    """nvidia-smi samples (200 ms) while the timed region runs."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str):
+        self.gpu_id = gpu_id
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", self.gpu_id, f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except Exception:
+                self.proc.kill()
+                self.out = ""
+        return False
+
+    def summary(self, under_load_frac=0.5):
+        if self.proc is None or not getattr(self, "out", ""):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        rows = [r for r in csv.reader(io.StringIO(self.out)) if len(r) >= 9]
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        sm = sorted(float(r[1]) for r in rows)
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[j] for r in rows for j in range(4)
+                          if r[5 + j].strip().lower() == "active"})
+        return {"sm_mhz": sm[len(sm) // 2], "sm_max_mhz": float(rows[0][2]),
+                "samples": len(rows), "power_w_max": max(float(r[3]) for r in rows),
+                "reasons": reasons}
+
+
+def _gpu_id(dev):
+    import torch
+    try:
+        u = str(torch.cuda.get_device_properties(dev).uuid)
+        return u if u.startswith("GPU-") else "GPU-" + u
+    except Exception:
+        return str(dev)
+
+
+def _dist():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+# --------------------------------------------------------------- CPU oracle
+def _oracle_arrays(d):
+    """Host copies of the inputs for the oracle, weights decoded to fp64 once
+    (setup, outside any timed region)."""
+    import numpy as np
+    f = (lambda t: t.float().cpu().numpy() if t.dtype.is_floating_point else t.cpu().numpy())
+    return dict(x=f(d["x"]), topk_ids=f(d["topk_ids"]), topk_weights=f(d["topk_weights"]),
+                w13=f(d["w13"]).astype(np.float64), w2=f(d["w2"]).astype(np.float64))
+
+
+def _time_oracle(arrs, tokens):
+    from oracle import experts
+    t0 = time.perf_counter()
+    experts.fused_experts_per_token(**arrs, tokens=tokens)
+    return time.perf_counter() - t0
+
+
+def _cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count()
+
+
+def run_reference(args):
+    """--impl reference: the fp64 oracle on the host cores, one token of the
+    workload per step (its two routed items through their experts)."""
+    import torch
+    from moe_synth import get_config, make_inputs
+    world, rank, _ = _dist()
+    if rank != 0:
+        return
+    cfg = get_config(WORKLOAD)
+    d = make_inputs(cfg, "cpu")
+    arrs = _oracle_arrays(d)
+    for s in range(args.warmup):
+        _time_oracle(arrs, [s % cfg.M])
+    total = 0.0
+    for s in range(args.steps):
+        total += _time_oracle(arrs, [(args.warmup + s) % cfg.M])
+    routed = args.steps * cfg.topk
+    value = routed / total
+    sample = (f"{args.steps} steps x 1 token ({cfg.topk} routed items) of the {cfg.name} "
+              "workload, per-token fp64 oracle, weights pre-decoded to fp64 outside timing")
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * total / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": _config_dict(cfg, 1),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": _cores(), "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+# ------------------------------------------------------------------ our arm
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    import mixture_experts_ffn_align_gb300 as moe
+    from moe_synth import get_config, make_inputs
+
+    world, rank, local = _dist()
+    if world > 1:
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    moe.lib()
+
+    cfg = get_config(WORKLOAD)
+    if args.tokens:
+        cfg = cfg.with_(M=args.tokens, name=f"{cfg.name}-M{args.tokens}")
+    if rank > 0:
+        cfg = cfg.with_(seed=cfg.seed + 100 * rank)
+    d = make_inputs(cfg, dev)
+    p = moe.Problem.from_config(cfg)
+    b = moe.stage_buffers(p, dev)
+    ws = torch.empty(moe.moe_workspace_bytes(p), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    x, ids, wts, w13, w2 = d["x"], d["topk_ids"], d["topk_weights"], d["w13"], d["w2"]
+
+    def staged(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        moe.moe_align_permute(p, x, ids, None, b["sorted_ids"], b["block_expert_ids"],
+                              b["expert_offsets"], b["num_post_padded"], b["inv_perm"],
+                              b["x_perm"], None, b["align_ws"], stream=stream)
+        if ev is not None:
+            ev[1].record(stream)
+        moe.grouped_gemm_w13(p, b["x_perm"], None, w13, None, b["block_expert_ids"],
+                             b["num_post_padded"], b["z"], None, fuse_act=True, stream=stream)
+        if ev is not None:
+            ev[2].record(stream)
+        moe.grouped_gemm_w2(p, b["z"], None, w2, None, b["block_expert_ids"],
+                            b["num_post_padded"], b["y2"], stream=stream)
+        if ev is not None:
+            ev[3].record(stream)
+        moe.unpermute_reduce(p, b["y2"], b["inv_perm"], wts, b["y"], stream=stream)
+        if ev is not None:
+            ev[4].record(stream)
+
+    launches_per_step = 7   # route hist/scan/scatter, permute, GEMM1+act, GEMM2, reduce
+
+    def barrier():
+        torch.cuda.synchronize(dev)
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+
+    for _ in range(args.warmup):
+        staged()
+    st = moe.moe_sync_status(stream)
+    if st != 0:
+        raise RuntimeError(f"device status {moe.moe_status_string(st)}")
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    barrier()
+    with ClockSampler(_gpu_id(dev)) as clk:
+        start = torch.cuda.Event(enable_timing=True)
+        end = torch.cuda.Event(enable_timing=True)
+        start.record(stream)
+        for s in range(args.steps):
+            staged(evs[s])
+        end.record(stream)
+        barrier()
+    elapsed_ms = start.elapsed_time(end)
+    if moe.moe_sync_status(stream) != 0:
+        raise RuntimeError("device error in the timed region")
+    stage_ms = [sum(e[i].elapsed_time(e[i + 1]) for e in evs) / args.steps for i in range(4)]
+
+    # the fused_experts call itself (same kernels, one entry point)
+    f_steps = max(3, args.steps // 4)
+    for _ in range(3):
+        moe.fused_experts(p, x, w13, None, w2, None, wts, ids, b["y"], ws, stream=stream)
+    barrier()
+    fs, fe = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    fs.record(stream)
+    for _ in range(f_steps):
+        moe.fused_experts(p, x, w13, None, w2, None, wts, ids, b["y"], ws, stream=stream)
+    fe.record(stream)
+    barrier()
+    fused_ms = fs.elapsed_time(fe) / f_steps
+
+    # end to end through the C ABI from pinned host buffers
+    hws = torch.empty(moe.moe_host_workspace_bytes(p), dtype=torch.uint8, device=dev)
+    hx, hid, hw = x.cpu().pin_memory(), ids.cpu().pin_memory(), wts.cpu().pin_memory()
+    hy = torch.empty_like(hx).pin_memory()
+    e_steps = max(3, args.steps // 4)
+    for _ in range(3):
+        moe.fused_experts_from_host(p, hx, hid, hw, hy, w13, None, w2, None, hws, stream=stream)
+    barrier()
+    t0 = time.perf_counter()
+    for _ in range(e_steps):
+        moe.fused_experts_from_host(p, hx, hid, hw, hy, w13, None, w2, None, hws, stream=stream)
+    torch.cuda.synchronize(dev)
+    e2e_s = (time.perf_counter() - t0) / e_steps
+    h2d = hx.numel() * 2 + hid.numel() * 4 + hw.numel() * 4
+    d2h = hy.numel() * 2
+
+    # max over ranks
+    t = torch.tensor([elapsed_ms, e2e_s, fused_ms], dtype=torch.float64, device=dev)
+    if world > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    elapsed_ms, e2e_s, fused_ms = t.tolist()
+    ms = elapsed_ms / args.steps
+    R = cfg.R
+    value = world * R / (ms * 1e-3)
+
+    if rank == 0:
+        peaks = _peaks()
+        gemm1_flops = 2.0 * R * cfg.H * 2 * cfg.I      # padding rows not counted
+        gemm2_flops = 2.0 * R * cfg.I * cfg.H
+        ach = gemm1_flops / (stage_ms[1] * 1e-3) / 1e12
+        peak = peaks["bf16_tflops_sustained"]
+        out = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16", "data": "synthetic (seeded; random-init weights)",
+            "config": _config_dict(cfg, world),
+            "tflops": (gemm1_flops + gemm2_flops) / (ms * 1e-3) / 1e12,
+            "stages_ms": {"align_permute": stage_ms[0], "gemm1_silu_mul": stage_ms[1],
+                          "gemm2": stage_ms[2], "unpermute_reduce": stage_ms[3]},
+            "fused_call_ms": fused_ms,
+            "roofline": {"bound": "tensor", "kernel": "k_ggemm_bf16<fused SiLU-and-mul> (GEMM1)",
+                         "achieved": ach, "peak": peak, "unit": "TFLOP/s",
+                         "frac": ach / peak, "traffic": None,
+                         "peak_source": f"bf16_tflops_sustained ({peaks['source']})",
+                         "algorithmic_per_launch": f"2*R*H*2I = {gemm1_flops:.4e} FLOP"},
+            "gemm2_roofline": {"achieved": gemm2_flops / (stage_ms[2] * 1e-3) / 1e12,
+                               "frac": gemm2_flops / (stage_ms[2] * 1e-3) / 1e12 / peak},
+            "e2e": {"value": world * R / e2e_s, "unit": UNIT, "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h, "ms_per_step": e2e_s * 1e3},
+            "gpu_launches": launches_per_step * args.steps,
+            "clocks": clk.summary(),
+        }
+        if world == 1 and not args.no_cpu_baseline:
+            arrs = _oracle_arrays(d)
+            t2 = _time_oracle(arrs, [0, 1])   # also warms the BLAS threads
+            # about 15 s of CPU work, at least 4 tokens
+            n_tok = int(min(cfg.M - 2, max(4, round(15.0 / max(t2 / 2, 1e-3)))))
+            tokens = list(range(2, 2 + n_tok))
+            secs = _time_oracle(arrs, tokens)
+            out["cpu_baseline"] = {
+                "value": len(tokens) * cfg.topk / secs, "unit": UNIT, "cores": _cores(),
+                "kind": "oracle",
+                "sample": f"{len(tokens)} tokens ({len(tokens) * cfg.topk} routed items) of the "
+                          f"{cfg.name} workload through the per-token fp64 oracle, weights "
+                          f"pre-decoded to fp64 outside timing; {secs:.1f} s"}
+        print(json.dumps(out), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=400)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--tokens", type=int, default=0,
+                    help="override M (smaller cases for profiling captures)")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

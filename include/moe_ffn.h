@@ -1,0 +1,215 @@
+/*
+ * moe_ffn.h -- C ABI of the GB300 (sm_103a) fused MoE expert forward.
+ *
+ * The library computes, for hidden states x[M,H], router outputs
+ * topk_ids[M,k] / topk_weights[M,k] and expert weights w13[E,2I,H] (gate rows
+ * [0,I), up rows [I,2I)) and w2[E,H,I]:
+ *
+ *   y_t = sum_{i: id[t,i] >= 0} w[t,i] * W2_e( SiLU(W1gate_e x_t) * (W1up_e x_t) )
+ *
+ * in the five stages described on the page "Blackwell 上的 DeepGEMM FusedMoE
+ * （vLLM）" (§1.1 six-step table, §2.6) and on the page "fused_moe.py 分析"
+ * (§1.2-1.3, "moe_align_block_size 的作用", "fused_moe_kernel 的核心原理"):
+ *   1. block-aligned routing + permute  (moe_align_permute)
+ *   2. grouped GEMM1 over w13           (grouped_gemm_w13)
+ *   3. SiLU-and-mul (+ dynamic FP8)     (act_mul_quant, or fused into 2)
+ *   4. grouped GEMM2 over w2            (grouped_gemm_w2)
+ *   5. weighted unpermute + reduce      (unpermute_reduce)
+ * and fused_experts runs all five.
+ *
+ * Conventions for every entry point:
+ *  - Pointers named as device pointers must point to device memory of the
+ *    current CUDA device; the caller owns every buffer (inputs, outputs and
+ *    workspaces) and keeps it alive until the work on `stream` completes.
+ *  - All tensors are dense, row-major, with the last dimension contiguous.
+ *    Base addresses must be 16-byte aligned.
+ *  - `stream` is a cudaStream_t (NULL = legacy default stream).  Every call is
+ *    asynchronous on that stream; a call never synchronises the host.
+ *  - Argument errors are detected on the host before any launch and return
+ *    MOE_ERR_INVALID_ARG / MOE_ERR_UNSUPPORTED / MOE_ERR_WORKSPACE_TOO_SMALL
+ *    with nothing enqueued.  Errors found by kernels (an expert id >= E, a
+ *    bounded device wait that ran out) are recorded in a device error word
+ *    and reported by moe_sync_status().
+ *  - M == 0 is valid: nothing is launched and MOE_OK is returned.
+ */
+#ifndef MOE_FFN_H_
+#define MOE_FFN_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = 1,          /* bad shape, null pointer, bad enum */
+  MOE_ERR_UNSUPPORTED = 2,          /* valid problem the kernels do not cover */
+  MOE_ERR_CUDA = 3,                 /* a CUDA runtime call failed */
+  MOE_ERR_DEVICE_TIMEOUT = 4,       /* a bounded device wait ran out */
+  MOE_ERR_WORKSPACE_TOO_SMALL = 5,  /* workspace_bytes below the requirement */
+  MOE_ERR_DEVICE_BAD_INDEX = 6      /* a kernel saw an expert id >= E */
+} moe_status;
+
+/* Weight / activation formats (page "Blackwell 上的 DeepGEMM FusedMoE（vLLM）",
+ * TL;DR table).
+ *  MOE_Q_BF16:          bf16 x, w13, w2; bf16 intermediates.
+ *  MOE_Q_FP8_BLOCK128:  w13/w2 e4m3fn codes (uint8) with fp32 scales per
+ *                       128x128 block, scale arrays [E, ceil(N/128), ceil(K/128)];
+ *                       activations quantised on the fly to e4m3fn per 1x128
+ *                       group (dynamic scale amax/448).
+ *  MOE_Q_MXFP4_W4A8:    w13/w2 E2M1 codes packed two per byte ([E, N, K/2],
+ *                       low nibble = even k) with E8M0 scales per 32 along K
+ *                       ([E, N, K/32] uint8); activations e4m3fn per 1x128.
+ */
+typedef enum { MOE_Q_BF16 = 0, MOE_Q_FP8_BLOCK128 = 1, MOE_Q_MXFP4_W4A8 = 2 } moe_quant;
+
+/* Activation scale format of the quantised modes: fp32 amax/448, or that
+ * value rounded up to a power of two (UE8M0; page "Blackwell 上的 DeepGEMM
+ * FusedMoE（vLLM）", §2.8(f), FLOAT32_CEIL_UE8M0).  Scales are always stored as
+ * fp32 values. */
+typedef enum { MOE_SCALE_FP32 = 0, MOE_SCALE_UE8M0 = 1 } moe_scale_fmt;
+
+/* The problem statement (page 1, "FusedMoEExpertsModular.apply" and
+ * "moe_problem_size": E, M, N = 2I, K = H, topk).  Activation is SiLU-and-mul.
+ *  block_size: padding granularity of each expert's rows (BLOCK_SIZE_M);
+ *              one of 16, 32, 64, 128.  The grouped GEMMs need 128.
+ *  apply_router_weight_on_input: multiply x_t by its router weight before
+ *              GEMM1 and reduce with weight 1 (top-k must be 1).
+ */
+typedef struct {
+  int32_t M, H, I, E, topk, block_size;
+  int32_t quant;          /* moe_quant */
+  int32_t act_scale_fmt;  /* moe_scale_fmt */
+  int32_t apply_router_weight_on_input;
+} moe_problem;
+
+/* Limits checked by every entry point: 0 <= M <= MOE_MAX_TOKENS (the pages'
+ * CHUNK_SIZE, page "fused_moe.py 分析", "分 chunk 执行"), 1 <= topk <= 16,
+ * 1 <= E <= 1024, H and I positive multiples of 128. */
+#define MOE_MAX_TOKENS 16384
+#define MOE_MAX_EXPERTS 1024
+#define MOE_MAX_TOPK 16
+
+/* Rows of the padded (permuted) layout: the worst case over all routings,
+ * round_up(M*k + min(M*k, E)*(block_size-1), block_size) (page "Blackwell 上的
+ * DeepGEMM FusedMoE（vLLM）", §2.6.1, compute_aligned_M_and_alignment).
+ * Returns 0 for an invalid problem. */
+size_t moe_m_sum_bound(const moe_problem* p);
+
+/* Bytes of scratch that moe_align_permute needs in `workspace` (per-segment
+ * expert histograms).  0 for an invalid problem. */
+size_t moe_align_workspace_bytes(const moe_problem* p);
+
+/* Bytes of workspace fused_experts needs (routing scratch, indices and every
+ * intermediate, sized for moe_m_sum_bound rows, with the permuted input and
+ * the GEMM2 output sharing storage as the page's workspace13 does, §2.8(a)).
+ * 0 for an invalid problem. */
+size_t moe_workspace_bytes(const moe_problem* p);
+
+/* Stage 1: block-aligned routing and permute (page "fused_moe.py 分析",
+ * "moe_align_block_size 的作用"; page "Blackwell 上的 DeepGEMM FusedMoE（vLLM）",
+ * §2.6.2 ep_scatter).  Routed item r = t*k + i (token r / k).
+ *  in : topk_ids [M*k] int32 device (-1 = skip the slot; >= E is an error),
+ *       x [M,H] bf16 device, topk_weights [M*k] fp32 device (read only when
+ *       apply_router_weight_on_input, else may be NULL).
+ *  out: sorted_ids [S] int32 (S = moe_m_sum_bound): routed item per padded
+ *         row, ascending r within an expert, padding = M*k;
+ *       block_expert_ids [S/block_size] int32: expert of each block, -1 past
+ *         the used blocks;
+ *       expert_offsets [E+1] int32: first padded row of each expert, [E] = total;
+ *       num_post_padded [1] int32: used rows (a multiple of block_size);
+ *       inv_perm [M*k] int32: padded row of each routed item, -1 for skipped;
+ *       x_perm [S,H]: x[token] per used row, zero rows for padding; bf16 for
+ *         MOE_Q_BF16, e4m3fn codes (uint8) for the quantised modes;
+ *       x_perm_scale [S,H/128] fp32 (quantised modes only, else may be NULL):
+ *         one scale per 1x128 group, 0 for padding rows.
+ *       x and x_perm may both be NULL to run the routing half only.
+ *  workspace: >= moe_align_workspace_bytes(p) bytes of device scratch. */
+moe_status moe_align_permute(const moe_problem* p, const void* x, const int32_t* topk_ids,
+                             const float* topk_weights, int32_t* sorted_ids,
+                             int32_t* block_expert_ids, int32_t* expert_offsets,
+                             int32_t* num_post_padded, int32_t* inv_perm, void* x_perm,
+                             float* x_perm_scale, void* workspace, size_t workspace_bytes,
+                             void* stream);
+
+/* Stage 2: grouped GEMM1, H1[row, n] = sum_k x_perm[row, k] * w13[e, n, k] for
+ * every used block (page "fused_moe.py 分析", §1.3 routed GEMM and
+ * "fused_moe_kernel 的核心原理"; FP8 blocks: "FP8 W8A8").  fp32 accumulation.
+ *  in : x_perm [S,H] (+ x_scale [S,H/128] fp32 for quantised modes),
+ *       w13 [E,2I,H] (+ w13_scale), block_expert_ids, num_post_padded (device).
+ *  out: fuse_act == 0: h1 [S,2I] bf16.
+ *       fuse_act == 1: the SiLU-and-mul result z written directly (MOE_Q_BF16:
+ *       z [S,I] bf16).  Quantised modes currently need fuse_act == 0
+ *       (MOE_ERR_UNSUPPORTED otherwise).
+ *  Rows of blocks past num_post_padded are not written. */
+moe_status grouped_gemm_w13(const moe_problem* p, const void* x_perm, const float* x_scale,
+                            const void* w13, const void* w13_scale,
+                            const int32_t* block_expert_ids, const int32_t* num_post_padded,
+                            void* out, float* out_scale, int fuse_act, void* stream);
+
+/* Stage 3: SiLU-and-mul, z = SiLU(h1[:, :I]) * h1[:, I:], computed in fp32
+ * from the bf16 h1 (page "Blackwell 上的 DeepGEMM FusedMoE（vLLM）", §2.6.4;
+ * page "fused_moe.py 分析", _silu_and_mul_kernel).  MOE_Q_BF16: z [S,I] bf16.
+ * Quantised modes: z [S,I] e4m3fn codes + z_scale [S,I/128] fp32 (dynamic
+ * per 1x128 group).  Only rows below num_post_padded are written. */
+moe_status act_mul_quant(const moe_problem* p, const void* h1, const int32_t* num_post_padded,
+                         void* z, float* z_scale, void* stream);
+
+/* Stage 4: grouped GEMM2, Y2[row, h] = sum_j z[row, j] * w2[e, h, j] (same
+ * passages as stage 2).  out: y2 [S,H] bf16. */
+moe_status grouped_gemm_w2(const moe_problem* p, const void* z, const float* z_scale,
+                           const void* w2, const void* w2_scale,
+                           const int32_t* block_expert_ids, const int32_t* num_post_padded,
+                           void* y2, void* stream);
+
+/* Stage 5: weighted unpermute + top-k reduce (page "Blackwell 上的 DeepGEMM
+ * FusedMoE（vLLM）", §2.6.5 ep_gather): y[t,:] = bf16( sum_{i, inv_perm[t,i] >= 0}
+ * w'[t,i] * y2[inv_perm[t,i], :] ), fp32 accumulation in slot order,
+ * w' = 1 when apply_router_weight_on_input.  y [M,H] bf16. */
+moe_status unpermute_reduce(const moe_problem* p, const void* y2, const int32_t* inv_perm,
+                            const float* topk_weights, void* y, void* stream);
+
+/* All five stages (page 1, FusedMoEKernelModularImpl.apply: prepare ->
+ * experts -> finalize; inplace when y == x, page "fused_moe.py 分析",
+ * "对外入口").  Weights as described for moe_quant; w13_scale/w2_scale NULL
+ * for MOE_Q_BF16.  workspace: >= moe_workspace_bytes(p) device bytes. */
+moe_status fused_experts(const moe_problem* p, const void* x, const void* w13,
+                         const void* w13_scale, const void* w2, const void* w2_scale,
+                         const float* topk_weights, const int32_t* topk_ids, void* y,
+                         void* workspace, size_t workspace_bytes, void* stream);
+
+/* fused_experts fed from host memory: copies x [M,H] bf16, topk_ids and
+ * topk_weights from host (pinned memory gives asynchronous copies) into the
+ * staging part of `workspace`, runs fused_experts, and copies y [M,H] bf16
+ * back to host_y, all on `stream`.  Weights stay device pointers.
+ * workspace: >= moe_host_workspace_bytes(p) device bytes. */
+size_t moe_host_workspace_bytes(const moe_problem* p);
+moe_status fused_experts_from_host(const moe_problem* p, const void* host_x,
+                                   const int32_t* host_topk_ids,
+                                   const float* host_topk_weights, void* host_y,
+                                   const void* w13, const void* w13_scale, const void* w2,
+                                   const void* w2_scale, void* workspace,
+                                   size_t workspace_bytes, void* stream);
+
+/* Synchronises `stream`, reads and clears the device error word, and returns
+ * MOE_OK, MOE_ERR_DEVICE_TIMEOUT, MOE_ERR_DEVICE_BAD_INDEX or MOE_ERR_CUDA. */
+moe_status moe_sync_status(void* stream);
+
+/* Human-readable name of a status code (static storage, never NULL). */
+const char* moe_status_string(moe_status s);
+
+/* Test hook for the device watchdog: with limit_ns > 0, every bounded wait in
+ * the GEMM kernels gives up after limit_ns nanoseconds instead of the default
+ * (2 s); with never_arrive != 0 the GEMM producer skips its first copy, so the
+ * consumer wait runs out.  The kernel then records MOE_ERR_DEVICE_TIMEOUT,
+ * drains what it issued, frees its tensor memory and returns.  Call with
+ * (0, 0) to restore the defaults.  Not thread-safe; affects later launches. */
+void moe_debug_set_watchdog(int64_t limit_ns, int never_arrive);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_FFN_H_ */

@@ -1,0 +1,237 @@
+"""Python binding of the GB300 fused MoE expert forward (libmoe_ffn.so).
+
+Argument marshalling only: every function here has the name of a C entry
+point in ``include/moe_ffn.h``, takes torch tensors (device memory) or None,
+passes their data pointers and the current CUDA stream to the library, and
+raises ``MoEError`` on a non-OK status.  All computation happens in the CUDA
+kernels of the library; there is no fallback.  The library must have been
+built (``__graft_entry__.build()`` or ``python -m
+mixture_experts_ffn_align_gb300._build``); importing a function that needs it
+raises if it is missing.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from dataclasses import dataclass
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libmoe_ffn.so")
+
+QUANT = {"bf16": 0, "fp8": 1, "mxfp4": 2}
+SCALE_FMT = {"fp32": 0, "ue8m0": 1}
+
+STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED", 3: "MOE_ERR_CUDA",
+          4: "MOE_ERR_DEVICE_TIMEOUT", 5: "MOE_ERR_WORKSPACE_TOO_SMALL",
+          6: "MOE_ERR_DEVICE_BAD_INDEX"}
+
+EXPORTS = ["moe_m_sum_bound", "moe_align_workspace_bytes", "moe_workspace_bytes",
+           "moe_host_workspace_bytes", "moe_align_permute", "grouped_gemm_w13", "act_mul_quant",
+           "grouped_gemm_w2", "unpermute_reduce", "fused_experts", "fused_experts_from_host",
+           "moe_sync_status", "moe_status_string", "moe_debug_set_watchdog"]
+
+
+class MoEError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {STATUS.get(status, status)}")
+
+
+class CProblem(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int32) for n in
+                ("M", "H", "I", "E", "topk", "block_size", "quant", "act_scale_fmt",
+                 "apply_router_weight_on_input")]
+
+
+@dataclass(frozen=True)
+class Problem:
+    """Mirror of ``moe_problem``."""
+    M: int
+    H: int
+    I: int
+    E: int
+    topk: int
+    block_size: int = 128
+    quant: str = "bf16"
+    act_scale_fmt: str = "fp32"
+    apply_router_weight_on_input: bool = False
+
+    def c(self) -> CProblem:
+        return CProblem(self.M, self.H, self.I, self.E, self.topk, self.block_size,
+                        QUANT[self.quant], SCALE_FMT[self.act_scale_fmt],
+                        int(self.apply_router_weight_on_input))
+
+    @classmethod
+    def from_config(cls, cfg, **kw):
+        d = dict(M=cfg.M, H=cfg.H, I=cfg.I, E=cfg.E, topk=cfg.topk, block_size=cfg.block_size,
+                 quant=cfg.quant, act_scale_fmt=cfg.act_scale_fmt,
+                 apply_router_weight_on_input=cfg.apply_router_weight_on_input)
+        d.update(kw)
+        return cls(**d)
+
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """Load libmoe_ffn.so (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise ImportError(f"{LIB_PATH} is missing: build it with "
+                              "`python -c 'import __graft_entry__ as g; g.build()'`")
+        L = ctypes.CDLL(LIB_PATH)
+        P = ctypes.POINTER(CProblem)
+        vp, sz, i32 = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int
+        for n in ("moe_m_sum_bound", "moe_align_workspace_bytes", "moe_workspace_bytes",
+                  "moe_host_workspace_bytes"):
+            getattr(L, n).argtypes, getattr(L, n).restype = [P], sz
+        L.moe_align_permute.argtypes = [P] + [vp] * 10 + [vp, sz, vp]
+        L.grouped_gemm_w13.argtypes = [P, vp, vp, vp, vp, vp, vp, vp, vp, i32, vp]
+        L.act_mul_quant.argtypes = [P, vp, vp, vp, vp, vp]
+        L.grouped_gemm_w2.argtypes = [P, vp, vp, vp, vp, vp, vp, vp, vp]
+        L.unpermute_reduce.argtypes = [P, vp, vp, vp, vp, vp]
+        L.fused_experts.argtypes = [P] + [vp] * 9 + [sz, vp]
+        L.fused_experts_from_host.argtypes = [P] + [vp] * 9 + [sz, vp]
+        L.moe_sync_status.argtypes = [vp]
+        L.moe_status_string.argtypes, L.moe_status_string.restype = [i32], ctypes.c_char_p
+        L.moe_debug_set_watchdog.argtypes, L.moe_debug_set_watchdog.restype = \
+            [ctypes.c_int64, i32], None
+        for n in ("moe_align_permute", "grouped_gemm_w13", "act_mul_quant", "grouped_gemm_w2",
+                  "unpermute_reduce", "fused_experts", "fused_experts_from_host",
+                  "moe_sync_status"):
+            getattr(L, n).restype = i32
+        _lib = L
+    return _lib
+
+
+def _p(t):
+    """Data pointer of a tensor (or None -> NULL)."""
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+        return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    return ctypes.c_void_p(stream if isinstance(stream, int) else stream.cuda_stream)
+
+
+def _check(status: int, where: str):
+    if status != 0:
+        raise MoEError(status, where)
+
+
+def _cp(p: Problem):
+    return ctypes.byref(p.c())
+
+
+# ------------------------------------------------------------------ sizes
+def moe_m_sum_bound(p: Problem) -> int:
+    return int(lib().moe_m_sum_bound(_cp(p)))
+
+
+def moe_align_workspace_bytes(p: Problem) -> int:
+    return int(lib().moe_align_workspace_bytes(_cp(p)))
+
+
+def moe_workspace_bytes(p: Problem) -> int:
+    return int(lib().moe_workspace_bytes(_cp(p)))
+
+
+def moe_host_workspace_bytes(p: Problem) -> int:
+    return int(lib().moe_host_workspace_bytes(_cp(p)))
+
+
+# ------------------------------------------------------------------ stages
+def moe_align_permute(p: Problem, x, topk_ids, topk_weights, sorted_ids, block_expert_ids,
+                      expert_offsets, num_post_padded, inv_perm, x_perm, x_perm_scale,
+                      workspace, stream=None):
+    _check(lib().moe_align_permute(
+        _cp(p), _p(x), _p(topk_ids), _p(topk_weights), _p(sorted_ids), _p(block_expert_ids),
+        _p(expert_offsets), _p(num_post_padded), _p(inv_perm), _p(x_perm), _p(x_perm_scale),
+        _p(workspace), workspace.numel() * workspace.element_size(), _stream(stream)),
+        "moe_align_permute")
+
+
+def grouped_gemm_w13(p: Problem, x_perm, x_scale, w13, w13_scale, block_expert_ids,
+                     num_post_padded, out, out_scale=None, fuse_act=False, stream=None):
+    _check(lib().grouped_gemm_w13(
+        _cp(p), _p(x_perm), _p(x_scale), _p(w13), _p(w13_scale), _p(block_expert_ids),
+        _p(num_post_padded), _p(out), _p(out_scale), int(bool(fuse_act)), _stream(stream)),
+        "grouped_gemm_w13")
+
+
+def act_mul_quant(p: Problem, h1, num_post_padded, z, z_scale=None, stream=None):
+    _check(lib().act_mul_quant(_cp(p), _p(h1), _p(num_post_padded), _p(z), _p(z_scale),
+                               _stream(stream)), "act_mul_quant")
+
+
+def grouped_gemm_w2(p: Problem, z, z_scale, w2, w2_scale, block_expert_ids, num_post_padded,
+                    y2, stream=None):
+    _check(lib().grouped_gemm_w2(_cp(p), _p(z), _p(z_scale), _p(w2), _p(w2_scale),
+                                 _p(block_expert_ids), _p(num_post_padded), _p(y2),
+                                 _stream(stream)), "grouped_gemm_w2")
+
+
+def unpermute_reduce(p: Problem, y2, inv_perm, topk_weights, y, stream=None):
+    _check(lib().unpermute_reduce(_cp(p), _p(y2), _p(inv_perm), _p(topk_weights), _p(y),
+                                  _stream(stream)), "unpermute_reduce")
+
+
+def fused_experts(p: Problem, x, w13, w13_scale, w2, w2_scale, topk_weights, topk_ids, y,
+                  workspace, stream=None):
+    _check(lib().fused_experts(
+        _cp(p), _p(x), _p(w13), _p(w13_scale), _p(w2), _p(w2_scale), _p(topk_weights),
+        _p(topk_ids), _p(y), _p(workspace), workspace.numel() * workspace.element_size(),
+        _stream(stream)), "fused_experts")
+
+
+def fused_experts_from_host(p: Problem, host_x, host_topk_ids, host_topk_weights, host_y,
+                            w13, w13_scale, w2, w2_scale, workspace, stream=None):
+    _check(lib().fused_experts_from_host(
+        _cp(p), _p(host_x), _p(host_topk_ids), _p(host_topk_weights), _p(host_y), _p(w13),
+        _p(w13_scale), _p(w2), _p(w2_scale), _p(workspace),
+        workspace.numel() * workspace.element_size(), _stream(stream)),
+        "fused_experts_from_host")
+
+
+def moe_sync_status(stream=None) -> int:
+    return int(lib().moe_sync_status(_stream(stream)))
+
+
+def moe_status_string(status: int) -> str:
+    return lib().moe_status_string(int(status)).decode()
+
+
+def moe_debug_set_watchdog(limit_ns: int, never_arrive: bool = False):
+    lib().moe_debug_set_watchdog(int(limit_ns), int(bool(never_arrive)))
+
+
+# ------------------------------------------------- buffer allocation helper
+def stage_buffers(p: Problem, device="cuda"):
+    """Allocates (torch.empty) the outputs of the staged entry points for
+    problem ``p``, sized by the library's own bound; returns a dict."""
+    import torch
+    cap = moe_m_sum_bound(p)
+    q = p.quant != "bf16"
+    xb = torch.uint8 if q else torch.bfloat16
+    i32 = dict(dtype=torch.int32, device=device)
+    return {
+        "sorted_ids": torch.empty(cap, **i32),
+        "block_expert_ids": torch.empty(cap // p.block_size, **i32),
+        "expert_offsets": torch.empty(p.E + 1, **i32),
+        "num_post_padded": torch.empty(1, **i32),
+        "inv_perm": torch.empty(p.M, p.topk, **i32),
+        "x_perm": torch.empty(cap, p.H, dtype=xb, device=device),
+        "x_perm_scale": torch.empty(cap, p.H // 128, dtype=torch.float32, device=device)
+        if q else None,
+        "h1": torch.empty(cap, 2 * p.I, dtype=torch.bfloat16, device=device),
+        "z": torch.empty(cap, p.I, dtype=xb, device=device),
+        "z_scale": torch.empty(cap, p.I // 128, dtype=torch.float32, device=device)
+        if q else None,
+        "y2": torch.empty(cap, p.H, dtype=torch.bfloat16, device=device),
+        "y": torch.empty(p.M, p.H, dtype=torch.bfloat16, device=device),
+        "align_ws": torch.empty(max(moe_align_workspace_bytes(p), 1), dtype=torch.uint8,
+                                device=device),
+    }

@@ -1,0 +1,360 @@
+// The C ABI (include/moe_ffn.h): argument validation, workspace layout and
+// the stage orchestration of fused_experts.
+//
+// Validation mirrors the checks listed on the page "fused_moe.py 分析",
+// "fused_experts_impl 的执行流程" step 1 (shape agreement, activation fixed to
+// SiLU), the chunk bound CHUNK_SIZE = 16 * 1024 ("分 chunk 执行"), the page
+// "Blackwell 上的 DeepGEMM FusedMoE（vLLM）" §2.6.3 warning that a GEMM block
+// taller than the padding granularity reads another expert's id (so the
+// GEMMs demand block_size == 128 here), and M == 0 returning early (page 1,
+// FusedMoEKernelModularImpl._fused_experts, "M_full == 0").
+#include <cstring>
+#include <mutex>
+
+#include "../../include/moe_ffn.h"
+#include "moe_common.cuh"
+#include "moe_internal.h"
+
+namespace moe {
+
+__device__ int g_dev_error_word = 0;
+
+namespace {
+constexpr int kMaxDevices = 64;
+int g_sms[kMaxDevices];
+int* g_err_ptr[kMaxDevices];
+std::mutex g_dev_mu;
+int64_t g_watchdog_ns = 0;
+int g_never_arrive = 0;
+
+int current_device() {
+  int d = 0;
+  if (cudaGetDevice(&d) != cudaSuccess || d < 0 || d >= kMaxDevices) return 0;
+  return d;
+}
+}  // namespace
+
+int num_sms() {
+  const int d = current_device();
+  if (g_sms[d] == 0) {
+    int n = 0;
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, d);
+    g_sms[d] = n > 0 ? n : 1;
+  }
+  return g_sms[d];
+}
+
+int* dev_error_word() {
+  const int d = current_device();
+  std::lock_guard<std::mutex> lk(g_dev_mu);
+  if (g_err_ptr[d] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_dev_error_word) == cudaSuccess) g_err_ptr[d] = (int*)p;
+  }
+  return g_err_ptr[d];
+}
+
+void watchdog_params(uint64_t* limit_ns, int* never_arrive) {
+  *limit_ns = g_watchdog_ns > 0 ? (uint64_t)g_watchdog_ns : 2000000000ull;
+  *never_arrive = g_never_arrive;
+}
+
+}  // namespace moe
+
+using namespace moe;
+
+namespace {
+
+constexpr size_t kAlign = 256;
+size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
+
+bool valid_problem(const moe_problem* p) {
+  if (p == nullptr) return false;
+  if (p->M < 0 || p->M > MOE_MAX_TOKENS) return false;
+  if (p->H <= 0 || p->H % 128 || p->I <= 0 || p->I % 128) return false;
+  if (p->E < 1 || p->E > MOE_MAX_EXPERTS) return false;
+  if (p->topk < 1 || p->topk > MOE_MAX_TOPK) return false;
+  if (p->block_size != 16 && p->block_size != 32 && p->block_size != 64 &&
+      p->block_size != 128)
+    return false;
+  if (p->quant < MOE_Q_BF16 || p->quant > MOE_Q_MXFP4_W4A8) return false;
+  if (p->act_scale_fmt != MOE_SCALE_FP32 && p->act_scale_fmt != MOE_SCALE_UE8M0) return false;
+  if (p->apply_router_weight_on_input && p->topk != 1) return false;
+  return true;
+}
+
+bool quantised(const moe_problem* p) { return p->quant != MOE_Q_BF16; }
+
+size_t cap_rows(const moe_problem* p) {
+  const size_t R = (size_t)p->M * p->topk;
+  const size_t A = (size_t)p->block_size;
+  const size_t raw = R + std::min(R, (size_t)p->E) * (A - 1);
+  return (raw + A - 1) / A * A;
+}
+
+struct Layout {
+  size_t hist, sorted, blocks, offsets, npp, inv, xperm, xscale, h1, z, zscale, y2, total;
+};
+
+Layout layout(const moe_problem* p) {
+  Layout L{};
+  const size_t cap = cap_rows(p), R = (size_t)p->M * p->topk;
+  const size_t H = p->H, I = p->I;
+  const size_t G = (size_t)route_segments((int)R);
+  const size_t xb = quantised(p) ? 1 : 2;
+  size_t o = 0;
+  auto take = [&](size_t bytes) {
+    const size_t at = o;
+    o = align_up(o + bytes);
+    return at;
+  };
+  L.hist = take(std::max<size_t>(G, 1) * p->E * 4);
+  L.sorted = take(cap * 4);
+  L.blocks = take(cap / p->block_size * 4 + 4);
+  L.offsets = take(((size_t)p->E + 1) * 4);
+  L.npp = take(4);
+  L.inv = take(R * 4);
+  // x_perm is dead once GEMM1 has run, so GEMM2's output reuses its storage
+  L.xperm = take(std::max(cap * H * xb, cap * H * 2));
+  L.y2 = L.xperm;
+  L.xscale = quantised(p) ? take(cap * (H / 128) * 4) : 0;
+  L.h1 = quantised(p) ? take(cap * 2 * I * 2) : 0;
+  L.z = take(cap * I * (quantised(p) ? 1 : 2));
+  L.zscale = quantised(p) ? take(cap * (I / 128) * 4) : 0;
+  L.total = o;
+  return L;
+}
+
+moe_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+// The GEMM tiles are 128 rows high, so the padding granularity must be 128;
+// bf16 GEMM2 tiles are 256 columns wide.  MXFP4 weights have no kernel yet.
+bool gemm_supported(const moe_problem* p) {
+  if (p->block_size != 128) return false;
+  if (p->quant == MOE_Q_BF16) return p->H % 256 == 0;
+  return p->quant == MOE_Q_FP8_BLOCK128;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t moe_m_sum_bound(const moe_problem* p) { return valid_problem(p) ? cap_rows(p) : 0; }
+
+size_t moe_align_workspace_bytes(const moe_problem* p) {
+  if (!valid_problem(p)) return 0;
+  const size_t G = (size_t)route_segments(p->M * p->topk);
+  return align_up(std::max<size_t>(G, 1) * p->E * 4);
+}
+
+size_t moe_workspace_bytes(const moe_problem* p) {
+  return valid_problem(p) ? layout(p).total : 0;
+}
+
+size_t moe_host_workspace_bytes(const moe_problem* p) {
+  if (!valid_problem(p)) return 0;
+  const size_t MH = (size_t)p->M * p->H * 2, Mk = (size_t)p->M * p->topk * 4;
+  return layout(p).total + align_up(MH) + 2 * align_up(Mk) + align_up(MH);
+}
+
+moe_status moe_align_permute(const moe_problem* p, const void* x, const int32_t* topk_ids,
+                             const float* topk_weights, int32_t* sorted_ids,
+                             int32_t* block_expert_ids, int32_t* expert_offsets,
+                             int32_t* num_post_padded, int32_t* inv_perm, void* x_perm,
+                             float* x_perm_scale, void* workspace, size_t workspace_bytes,
+                             void* stream) {
+  if (!valid_problem(p)) return MOE_ERR_INVALID_ARG;
+  if (p->M == 0) return MOE_OK;
+  if (!topk_ids || !sorted_ids || !block_expert_ids || !expert_offsets || !num_post_padded ||
+      !inv_perm || !workspace)
+    return MOE_ERR_INVALID_ARG;
+  if ((x == nullptr) != (x_perm == nullptr)) return MOE_ERR_INVALID_ARG;
+  if (x && quantised(p) && !x_perm_scale) return MOE_ERR_INVALID_ARG;
+  if (x && p->apply_router_weight_on_input && !topk_weights) return MOE_ERR_INVALID_ARG;
+  if (workspace_bytes < moe_align_workspace_bytes(p)) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int R = p->M * p->topk, cap = (int)cap_rows(p);
+  cudaError_t e = launch_route(topk_ids, R, p->E, p->block_size, cap,
+                               static_cast<int32_t*>(workspace), sorted_ids, block_expert_ids,
+                               expert_offsets, num_post_padded, inv_perm, s);
+  if (e != cudaSuccess) return MOE_ERR_CUDA;
+  if (x) {
+    e = launch_permute_rows(x, p->H, p->topk, R, sorted_ids, num_post_padded,
+                            p->apply_router_weight_on_input ? topk_weights : nullptr, x_perm,
+                            quantised(p) ? x_perm_scale : nullptr,
+                            p->act_scale_fmt == MOE_SCALE_UE8M0, cap, s);
+  }
+  return cuda_status(e);
+}
+
+moe_status grouped_gemm_w13(const moe_problem* p, const void* x_perm, const float* x_scale,
+                            const void* w13, const void* w13_scale,
+                            const int32_t* block_expert_ids, const int32_t* num_post_padded,
+                            void* out, float* out_scale, int fuse_act, void* stream) {
+  (void)out_scale;
+  if (!valid_problem(p)) return MOE_ERR_INVALID_ARG;
+  if (p->M == 0) return MOE_OK;
+  if (!x_perm || !w13 || !block_expert_ids || !num_post_padded || !out) return MOE_ERR_INVALID_ARG;
+  if (!gemm_supported(p)) return MOE_ERR_UNSUPPORTED;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int cap = (int)cap_rows(p);
+  if (p->quant == MOE_Q_BF16) {
+    return cuda_status(launch_ggemm_bf16(x_perm, cap, p->H, w13, p->E * 2 * p->I, 2 * p->I,
+                                         2 * p->I, block_expert_ids, num_post_padded, out,
+                                         fuse_act != 0, s));
+  }
+  if (fuse_act) return MOE_ERR_UNSUPPORTED;
+  if (!x_scale || !w13_scale) return MOE_ERR_INVALID_ARG;
+  return cuda_status(launch_ggemm_fp8(x_perm, x_scale, cap, p->H, w13,
+                                      static_cast<const float*>(w13_scale), p->E * 2 * p->I,
+                                      2 * p->I, 2 * p->I, block_expert_ids, num_post_padded, out,
+                                      s));
+}
+
+moe_status act_mul_quant(const moe_problem* p, const void* h1, const int32_t* num_post_padded,
+                         void* z, float* z_scale, void* stream) {
+  if (!valid_problem(p)) return MOE_ERR_INVALID_ARG;
+  if (p->M == 0) return MOE_OK;
+  if (!h1 || !num_post_padded || !z) return MOE_ERR_INVALID_ARG;
+  if (quantised(p) && !z_scale) return MOE_ERR_INVALID_ARG;
+  return cuda_status(launch_act_mul(h1, p->I, num_post_padded, z,
+                                    quantised(p) ? z_scale : nullptr,
+                                    p->act_scale_fmt == MOE_SCALE_UE8M0, (int)cap_rows(p),
+                                    static_cast<cudaStream_t>(stream)));
+}
+
+moe_status grouped_gemm_w2(const moe_problem* p, const void* z, const float* z_scale,
+                           const void* w2, const void* w2_scale,
+                           const int32_t* block_expert_ids, const int32_t* num_post_padded,
+                           void* y2, void* stream) {
+  if (!valid_problem(p)) return MOE_ERR_INVALID_ARG;
+  if (p->M == 0) return MOE_OK;
+  if (!z || !w2 || !block_expert_ids || !num_post_padded || !y2) return MOE_ERR_INVALID_ARG;
+  if (!gemm_supported(p)) return MOE_ERR_UNSUPPORTED;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int cap = (int)cap_rows(p);
+  if (p->quant == MOE_Q_BF16) {
+    return cuda_status(launch_ggemm_bf16(z, cap, p->I, w2, p->E * p->H, p->H, p->H,
+                                         block_expert_ids, num_post_padded, y2, false, s));
+  }
+  if (!z_scale || !w2_scale) return MOE_ERR_INVALID_ARG;
+  return cuda_status(launch_ggemm_fp8(z, z_scale, cap, p->I, w2,
+                                      static_cast<const float*>(w2_scale), p->E * p->H, p->H,
+                                      p->H, block_expert_ids, num_post_padded, y2, s));
+}
+
+moe_status unpermute_reduce(const moe_problem* p, const void* y2, const int32_t* inv_perm,
+                            const float* topk_weights, void* y, void* stream) {
+  if (!valid_problem(p)) return MOE_ERR_INVALID_ARG;
+  if (p->M == 0) return MOE_OK;
+  if (!y2 || !inv_perm || !y) return MOE_ERR_INVALID_ARG;
+  if (!p->apply_router_weight_on_input && !topk_weights) return MOE_ERR_INVALID_ARG;
+  return cuda_status(launch_unpermute_reduce(y2, p->H, p->M, p->topk, inv_perm, topk_weights,
+                                             p->apply_router_weight_on_input != 0, y,
+                                             static_cast<cudaStream_t>(stream)));
+}
+
+moe_status fused_experts(const moe_problem* p, const void* x, const void* w13,
+                         const void* w13_scale, const void* w2, const void* w2_scale,
+                         const float* topk_weights, const int32_t* topk_ids, void* y,
+                         void* workspace, size_t workspace_bytes, void* stream) {
+  if (!valid_problem(p)) return MOE_ERR_INVALID_ARG;
+  if (p->M == 0) return MOE_OK;
+  if (!x || !w13 || !w2 || !topk_ids || !y || !workspace || !topk_weights)
+    return MOE_ERR_INVALID_ARG;
+  if (quantised(p) && (!w13_scale || !w2_scale)) return MOE_ERR_INVALID_ARG;
+  if (!gemm_supported(p)) return MOE_ERR_UNSUPPORTED;
+  const Layout L = layout(p);
+  if (workspace_bytes < L.total) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  auto i32 = [&](size_t off) { return reinterpret_cast<int32_t*>(ws + off); };
+  auto f32 = [&](size_t off) { return reinterpret_cast<float*>(ws + off); };
+  int32_t *sorted = i32(L.sorted), *blocks = i32(L.blocks), *offs = i32(L.offsets),
+          *npp = i32(L.npp), *inv = i32(L.inv);
+  moe_status st = moe_align_permute(p, x, topk_ids, topk_weights, sorted, blocks, offs, npp, inv,
+                                    ws + L.xperm, quantised(p) ? f32(L.xscale) : nullptr,
+                                    ws + L.hist, L.sorted - L.hist, stream);
+  if (st != MOE_OK) return st;
+  if (!quantised(p)) {
+    st = grouped_gemm_w13(p, ws + L.xperm, nullptr, w13, nullptr, blocks, npp, ws + L.z, nullptr,
+                          1, stream);
+    if (st != MOE_OK) return st;
+    st = grouped_gemm_w2(p, ws + L.z, nullptr, w2, nullptr, blocks, npp, ws + L.y2, stream);
+  } else {
+    st = grouped_gemm_w13(p, ws + L.xperm, f32(L.xscale), w13, w13_scale, blocks, npp,
+                          ws + L.h1, nullptr, 0, stream);
+    if (st != MOE_OK) return st;
+    st = act_mul_quant(p, ws + L.h1, npp, ws + L.z, f32(L.zscale), stream);
+    if (st != MOE_OK) return st;
+    st = grouped_gemm_w2(p, ws + L.z, f32(L.zscale), w2, w2_scale, blocks, npp, ws + L.y2,
+                         stream);
+  }
+  if (st != MOE_OK) return st;
+  return unpermute_reduce(p, ws + L.y2, inv, topk_weights, y, stream);
+}
+
+moe_status fused_experts_from_host(const moe_problem* p, const void* host_x,
+                                   const int32_t* host_topk_ids,
+                                   const float* host_topk_weights, void* host_y,
+                                   const void* w13, const void* w13_scale, const void* w2,
+                                   const void* w2_scale, void* workspace,
+                                   size_t workspace_bytes, void* stream) {
+  if (!valid_problem(p)) return MOE_ERR_INVALID_ARG;
+  if (p->M == 0) return MOE_OK;
+  if (!host_x || !host_topk_ids || !host_topk_weights || !host_y || !workspace)
+    return MOE_ERR_INVALID_ARG;
+  if (workspace_bytes < moe_host_workspace_bytes(p)) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  const size_t base = layout(p).total;
+  const size_t MH = (size_t)p->M * p->H * 2, Mk = (size_t)p->M * p->topk * 4;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  void* d_x = ws + base;
+  int32_t* d_ids = reinterpret_cast<int32_t*>(ws + base + align_up(MH));
+  float* d_w = reinterpret_cast<float*>(ws + base + align_up(MH) + align_up(Mk));
+  void* d_y = ws + base + align_up(MH) + 2 * align_up(Mk);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaMemcpyAsync(d_x, host_x, MH, cudaMemcpyHostToDevice, s) != cudaSuccess ||
+      cudaMemcpyAsync(d_ids, host_topk_ids, Mk, cudaMemcpyHostToDevice, s) != cudaSuccess ||
+      cudaMemcpyAsync(d_w, host_topk_weights, Mk, cudaMemcpyHostToDevice, s) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  moe_status st = fused_experts(p, d_x, w13, w13_scale, w2, w2_scale, d_w, d_ids, d_y, workspace,
+                                base, stream);
+  if (st != MOE_OK) return st;
+  return cuda_status(cudaMemcpyAsync(host_y, d_y, MH, cudaMemcpyDeviceToHost, s));
+}
+
+moe_status moe_sync_status(void* stream) {
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  int* err = dev_error_word();
+  if (err == nullptr) return MOE_ERR_CUDA;
+  int v = 0;
+  if (cudaMemcpy(&v, err, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return MOE_ERR_CUDA;
+  if (v != 0) {
+    const int zero = 0;
+    if (cudaMemcpy(err, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess)
+      return MOE_ERR_CUDA;
+  }
+  if (v & kDevErrTimeout) return MOE_ERR_DEVICE_TIMEOUT;
+  if (v & kDevErrBadIndex) return MOE_ERR_DEVICE_BAD_INDEX;
+  return MOE_OK;
+}
+
+const char* moe_status_string(moe_status s) {
+  switch (s) {
+    case MOE_OK: return "MOE_OK";
+    case MOE_ERR_INVALID_ARG: return "MOE_ERR_INVALID_ARG";
+    case MOE_ERR_UNSUPPORTED: return "MOE_ERR_UNSUPPORTED";
+    case MOE_ERR_CUDA: return "MOE_ERR_CUDA";
+    case MOE_ERR_DEVICE_TIMEOUT: return "MOE_ERR_DEVICE_TIMEOUT";
+    case MOE_ERR_WORKSPACE_TOO_SMALL: return "MOE_ERR_WORKSPACE_TOO_SMALL";
+    case MOE_ERR_DEVICE_BAD_INDEX: return "MOE_ERR_DEVICE_BAD_INDEX";
+  }
+  return "MOE_ERR_UNKNOWN";
+}
+
+void moe_debug_set_watchdog(int64_t limit_ns, int never_arrive) {
+  g_watchdog_ns = limit_ns > 0 ? limit_ns : 0;
+  g_never_arrive = never_arrive != 0;
+}
+
+}  // extern "C"

@@ -1,0 +1,301 @@
+// FP8 (e4m3) grouped GEMM with fp32 block scales (stages 2 and 4 of
+// MOE_Q_FP8_BLOCK128).
+//
+// What it computes: page "fused_moe.py 分析", "FP8 W8A8": block-wise scales are
+// read per K block and C_block = dot(qA_block, qB_block) * a_scale * b_scale,
+// accumulated over K blocks; here activation scales are per (row, 128-column
+// group) and weight scales per 128x128 block (page "Blackwell 上的 DeepGEMM
+// FusedMoE（vLLM）", TL;DR: "FP8 block 128x128", dynamic 128 activations):
+//   C[r, n] = sum_kb sa[r, kb] * sb[e, n/128, kb] * sum_{k in kb} qa[r,k] qb[e,n,k].
+//
+// The hardware block-scaled MMA takes power-of-two (UE8M0) scales only, and
+// these scales are arbitrary fp32, so the scales are applied on the CUDA
+// cores ("promotion"):
+//  * warp 0 lane 0: TMA producer, 6-stage ring of (A 128x128, B 128x128) e4m3
+//    tiles -- one stage is exactly one 128-wide K block;
+//  * warp 1 lane 0: four kind::f8f6f4 MMAs (M=128, N=128, K=32) per K block
+//    into one of four 128-column tensor-memory partials, rotating, so the MMA
+//    runs up to four K blocks ahead of the epilogue;
+//  * warps 2-9: each owns 32 rows x 64 columns of the tile, reads the partial
+//    with tcgen05.ld, releases it, and accumulates sa*sb*partial in fp32
+//    registers; at the end of the tile the sum is rounded to bf16 and stored.
+//  * tiles are walked in groups of m-blocks (all column tiles of a group
+//    before the next group) so a group's activations stay in L2 while the
+//    weights stream once.
+//  * every wait is bounded, as in the bf16 kernel.
+#include <mutex>
+
+#include "moe_common.cuh"
+#include "moe_internal.h"
+
+namespace moe {
+
+bool make_tmap_k_sw128(CUtensorMap* map, const void* base, uint64_t rows, uint64_t k_elems,
+                       int elem_bytes, uint32_t box_rows);
+
+namespace {
+
+constexpr int BM = 128, BN = 128, BK = 128, STAGES = 6, NPART = 4;
+constexpr int A_BYTES = BM * BK;
+constexpr int B_BYTES = BN * BK;
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int TMEM_COLS = NPART * BN;
+constexpr int NUM_EPI_WARPS = 8;
+constexpr int NUM_THREADS = 64 + NUM_EPI_WARPS * 32;
+constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + 256;
+
+struct Fp8Args {
+  const int32_t* block_expert_ids;
+  const int32_t* num_post_padded;
+  const float* a_scale;   // [cap, K/128]
+  const float* b_scale;   // [E, N/128, K/128]
+  __nv_bfloat16* out;     // [cap, N]
+  int ldo;                // N
+  int num_kb;             // K / 128
+  int n_tiles;            // N / 128
+  int b_rows_per_expert;  // N
+  int m_blocks_cap;
+  int num_experts;
+  int group_m;            // m-blocks per scheduling group
+  uint64_t limit_ns;
+  int never_arrive;
+  int* err;
+};
+
+__device__ __forceinline__ void tile_coords(int t, int nb_valid, int n_tiles, int group_m,
+                                            int& m_blk, int& n_tile) {
+  const int per_group = group_m * n_tiles;
+  const int g = t / per_group;
+  const int gm = min(group_m, nb_valid - g * group_m);
+  const int local = t - g * per_group;
+  n_tile = local / gm;
+  m_blk = g * group_m + (local - n_tile * gm);
+}
+
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    k_ggemm_fp8(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                const Fp8Args args) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 2 * NPART + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t smem_base = smem_u32(smem);
+  const uint32_t bar_base = smem_u32(bars);
+  auto full_bar = [&](int s) { return bar_base + 8u * s; };
+  auto empty_bar = [&](int s) { return bar_base + 8u * (STAGES + s); };
+  auto pfull_bar = [&](int b) { return bar_base + 8u * (2 * STAGES + b); };
+  auto pempty_bar = [&](int b) { return bar_base + 8u * (2 * STAGES + NPART + b); };
+  const uint32_t drain_bar = bar_base + 8u * (2 * STAGES + 2 * NPART);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(full_bar(s), 1);
+      mbar_init(empty_bar(s), 1);
+    }
+    for (int b = 0; b < NPART; ++b) {
+      mbar_init(pfull_bar(b), 1);
+      mbar_init(pempty_bar(b), NUM_EPI_WARPS);
+    }
+    mbar_init(drain_bar, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+  }
+  if (warp == 1) {
+    __syncwarp();
+    tmem_alloc(smem_u32(tmem_holder), TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_holder;
+
+  const int nb_valid = min(*args.num_post_padded / BM, args.m_blocks_cap);
+  const int total = nb_valid * args.n_tiles;
+  const int group_m = max(1, args.group_m);
+
+  if (warp == 0 && lane == 0) {
+    // ------------------------------------------------------------ producer
+    const uint64_t pol_a = l2_policy_evict_last();
+    const uint64_t pol_b = l2_policy_evict_first();
+    uint32_t stage = 0, phase = 0, issued_mask = 0, issued_parity = 0;
+    bool skip_first = args.never_arrive != 0;
+    for (int t = blockIdx.x; t < total; t += gridDim.x) {
+      int m_blk, n_tile;
+      tile_coords(t, nb_valid, args.n_tiles, group_m, m_blk, n_tile);
+      const int e = args.block_expert_ids[m_blk];
+      if (e < 0 || e >= args.num_experts) continue;
+      const int brow = e * args.b_rows_per_expert + n_tile * BN;
+      bool ok = true;
+      for (int kb = 0; kb < args.num_kb; ++kb) {
+        if (!mbar_wait_bounded(empty_bar(stage), phase ^ 1, abort_flag, args.limit_ns, args.err)) {
+          ok = false;
+          break;
+        }
+        if (skip_first) {
+          skip_first = false;
+        } else {
+          const uint32_t sa = smem_base + stage * STAGE_BYTES;
+          mbar_arrive_expect_tx(full_bar(stage), STAGE_BYTES);
+          tma_load_2d(sa, &tmA, full_bar(stage), kb * BK, m_blk * BM, pol_a);
+          tma_load_2d(sa + A_BYTES, &tmB, full_bar(stage), kb * BK, brow, pol_b);
+          issued_mask |= 1u << stage;
+          issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
+        }
+        if (++stage == STAGES) {
+          stage = 0;
+          phase ^= 1;
+        }
+      }
+      if (!ok) break;
+    }
+    for (int s = 0; s < STAGES; ++s)
+      if (issued_mask & (1u << s))
+        mbar_wait_bounded(full_bar(s), (issued_parity >> s) & 1, nullptr, args.limit_ns, args.err);
+  } else if (warp == 1 && lane == 0) {
+    // ------------------------------------------------------------ MMA issuer
+    constexpr uint32_t idesc = make_idesc(kFmtE4M3, kFmtE4M3, BM, BN);
+    uint32_t stage = 0, phase = 0, pc = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+      int m_blk, n_tile;
+      tile_coords(t, nb_valid, args.n_tiles, group_m, m_blk, n_tile);
+      const int e = args.block_expert_ids[m_blk];
+      if (e < 0 || e >= args.num_experts) continue;
+      for (int kb = 0; kb < args.num_kb; ++kb, ++pc) {
+        const uint32_t buf = pc % NPART, pphase = (pc / NPART) & 1;
+        if (!mbar_wait_bounded(pempty_bar(buf), pphase ^ 1, abort_flag, args.limit_ns, args.err) ||
+            !mbar_wait_bounded(full_bar(stage), phase, abort_flag, args.limit_ns, args.err)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t sa = smem_base + stage * STAGE_BYTES;
+        const uint64_t adesc = sdesc_k_sw128(sa);
+        const uint64_t bdesc = sdesc_k_sw128(sa + A_BYTES);
+        const uint32_t d_tmem = tmem_base + buf * BN;
+#pragma unroll
+        for (int k = 0; k < BK / 32; ++k) umma_f8(d_tmem, adesc + 2 * k, bdesc + 2 * k, idesc, k);
+        tc_commit(empty_bar(stage));
+        tc_commit(pfull_bar(buf));
+        if (++stage == STAGES) {
+          stage = 0;
+          phase ^= 1;
+        }
+      }
+    }
+    tc_commit(drain_bar);
+    mbar_wait_bounded(drain_bar, 0, nullptr, args.limit_ns, args.err);
+  } else if (warp >= 2) {
+    // ------------------------------------------------------------ epilogue
+    const int q = warp & 3;               // TMEM lane quadrant
+    const int half = (warp - 2) >> 2;     // column half of the tile
+    const int row_in_tile = q * 32 + lane;
+    uint32_t pc = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+      int m_blk, n_tile;
+      tile_coords(t, nb_valid, args.n_tiles, group_m, m_blk, n_tile);
+      const int e = args.block_expert_ids[m_blk];
+      if (e < 0 || e >= args.num_experts) continue;
+      const size_t row = (size_t)m_blk * BM + row_in_tile;
+      const float* sa_row = args.a_scale + row * args.num_kb;
+      const float* sb_blk =
+          args.b_scale + ((size_t)e * args.n_tiles + n_tile) * (size_t)args.num_kb;
+      float acc[64];
+#pragma unroll
+      for (int j = 0; j < 64; ++j) acc[j] = 0.0f;
+      for (int kb = 0; kb < args.num_kb; ++kb, ++pc) {
+        const uint32_t buf = pc % NPART, pphase = (pc / NPART) & 1;
+        const float s = __ldg(sa_row + kb) * __ldg(sb_blk + kb);
+        int got = 0;
+        if (lane == 0)
+          got = mbar_wait_bounded(pfull_bar(buf), pphase, abort_flag, args.limit_ns, args.err);
+        got = __shfl_sync(0xffffffffu, got, 0);
+        if (!got) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + buf * BN + half * 64;
+        uint32_t p0[32], p1[32];
+        tmem_ld_32x32b_x32(taddr, p0);
+        tmem_ld_32x32b_x32(taddr + 32, p1);
+        tmem_ld_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(pempty_bar(buf));
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          acc[j] = fmaf(s, __uint_as_float(p0[j]), acc[j]);
+          acc[32 + j] = fmaf(s, __uint_as_float(p1[j]), acc[32 + j]);
+        }
+      }
+      if (!ok) break;
+      uint4* dst = reinterpret_cast<uint4*>(args.out + row * args.ldo + (size_t)n_tile * BN +
+                                            half * 64);
+#pragma unroll
+      for (int v = 0; v < 8; ++v) {
+        uint4 pk;
+        __nv_bfloat16* pb = reinterpret_cast<__nv_bfloat16*>(&pk);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) pb[j] = __float2bfloat16_rn(acc[v * 8 + j]);
+        dst[v] = pk;
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem_base, TMEM_COLS);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_ggemm_fp8(const void* A, const float* a_scale, int cap, int K, const void* B,
+                             const float* b_scale, int b_rows_total, int b_rows_per_expert,
+                             int n_out, const int32_t* block_expert_ids,
+                             const int32_t* num_post_padded, void* out, cudaStream_t stream) {
+  if (cap <= 0) return cudaSuccess;
+  CUtensorMap tmA, tmB;
+  if (!make_tmap_k_sw128(&tmA, A, (uint64_t)cap, (uint64_t)K, 1, 128) ||
+      !make_tmap_k_sw128(&tmB, B, (uint64_t)b_rows_total, (uint64_t)K, 1, 128))
+    return cudaErrorInvalidValue;
+  Fp8Args a;
+  a.block_expert_ids = block_expert_ids;
+  a.num_post_padded = num_post_padded;
+  a.a_scale = a_scale;
+  a.b_scale = b_scale;
+  a.out = static_cast<__nv_bfloat16*>(out);
+  a.ldo = n_out;
+  a.num_kb = K / BK;
+  a.n_tiles = n_out / BN;
+  a.b_rows_per_expert = b_rows_per_expert;
+  a.m_blocks_cap = cap / BM;
+  a.num_experts = b_rows_total / b_rows_per_expert;
+  // keep a group's activations (group_m blocks of 128 x K bytes) near 32 MB
+  a.group_m = (int)std::max<long long>(1, (32ll << 20) / ((long long)BM * K));
+  watchdog_params(&a.limit_ns, &a.never_arrive);
+  a.err = dev_error_word();
+  static bool attr_done = false;
+  if (!attr_done) {
+    cudaFuncSetAttribute(k_ggemm_fp8, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    attr_done = true;
+  }
+  k_ggemm_fp8<<<num_sms(), NUM_THREADS, SMEM_BYTES, stream>>>(tmA, tmB, a);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

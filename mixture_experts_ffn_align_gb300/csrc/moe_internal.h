@@ -1,0 +1,57 @@
+// Host-side launchers shared between the translation units of the library.
+// Every launcher enqueues work on `stream` and returns a cudaError_t from the
+// launch (argument validation happens in capi.cu before these are called).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace moe {
+
+constexpr int kRouteSeg = 512;        // routed items handled by one warp
+constexpr int kRouteWarps = 8;        // warps per routing CTA
+
+inline int route_segments(int R) { return (R + kRouteSeg - 1) / kRouteSeg; }
+
+int num_sms();                                // SMs of the current device
+int* dev_error_word();                        // device address of the error word
+void watchdog_params(uint64_t* limit_ns, int* never_arrive);
+
+// Routing half of moe_align_permute (three launches).
+cudaError_t launch_route(const int32_t* topk_ids, int R, int E, int block_size, int cap,
+                         int32_t* hist, int32_t* sorted_ids, int32_t* block_expert_ids,
+                         int32_t* expert_offsets, int32_t* num_post_padded, int32_t* inv_perm,
+                         cudaStream_t stream);
+
+// Data half: gather x rows into the padded layout (bf16 copy, or fused
+// dynamic 1x128 e4m3 quantisation when x_scale != nullptr).
+cudaError_t launch_permute_rows(const void* x, int H, int topk, int R, const int32_t* sorted_ids,
+                                const int32_t* num_post_padded, const float* row_weights,
+                                void* x_perm, float* x_scale, bool ue8m0, int cap,
+                                cudaStream_t stream);
+
+// SiLU-and-mul over h1 [rows, 2I] bf16 -> z bf16, or e4m3 + scales.
+cudaError_t launch_act_mul(const void* h1, int I, const int32_t* num_post_padded, void* z,
+                           float* z_scale, bool ue8m0, int cap, cudaStream_t stream);
+
+// Weighted top-k gather-reduce into y [M, H] bf16.
+cudaError_t launch_unpermute_reduce(const void* y2, int H, int M, int topk,
+                                    const int32_t* inv_perm, const float* topk_weights,
+                                    bool unit_weights, void* y, cudaStream_t stream);
+
+// bf16 grouped GEMM on tcgen05: out[row, n] = sum_k A[row, k] * B[e*b_rows + n, k].
+//   fuse_act: B tile = 128 gate rows + 128 up rows; writes SiLU(g)*u (bf16).
+cudaError_t launch_ggemm_bf16(const void* A, int cap, int K, const void* B, int b_rows_total,
+                              int b_rows_per_expert, int n_out, const int32_t* block_expert_ids,
+                              const int32_t* num_post_padded, void* out, bool fuse_act,
+                              cudaStream_t stream);
+
+// FP8 (e4m3) grouped GEMM with fp32 1x128 activation scales and 128x128
+// weight block scales: out = sum_kb sa*sb*partial_kb (bf16 output).
+cudaError_t launch_ggemm_fp8(const void* A, const float* a_scale, int cap, int K, const void* B,
+                             const float* b_scale, int b_rows_total, int b_rows_per_expert,
+                             int n_out, const int32_t* block_expert_ids,
+                             const int32_t* num_post_padded, void* out, cudaStream_t stream);
+
+}  // namespace moe

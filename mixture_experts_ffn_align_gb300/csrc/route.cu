@@ -1,0 +1,269 @@
+// Block-aligned routing and permute (stage 1).
+//
+// Page "fused_moe.py 分析", "moe_align_block_size 的作用": routed items
+// (token, slot) are sorted by expert and each expert's count is padded to the
+// block size, giving sorted_token_ids, one expert id per block and
+// num_tokens_post_padded.  Page "Blackwell 上的 DeepGEMM FusedMoE（vLLM）",
+// §2.6.2: per-expert rounded prefix sum (ep_scatter_1), each item's
+// destination row into inv_perm (ep_scatter_2), ids < 0 skipped, padding
+// rows of the activation scale are zero.
+//
+// GB300 design: the pages' scatter claims rows with atomics, which makes the
+// order inside an expert depend on timing.  Here the order is ascending item
+// index, so indices are reproducible bit for bit:
+//   k_route_hist    one warp per 512-item segment: per-segment histogram
+//   k_route_scan    one CTA: per-expert scan over segments + padded prefix
+//                   sum over experts, block ids, padding entries
+//   k_route_scatter one warp per segment: __match_any_sync ranks items of the
+//                   same expert within 32-item chunks; a per-warp running
+//                   count in shared memory carries the rank across chunks.
+// The data gather (k_permute_*) runs per destination row with 16-byte vector
+// loads and stores; the FP8 variant fuses the dynamic 1x128 quantisation.
+#include "moe_common.cuh"
+#include "moe_internal.h"
+
+namespace moe {
+
+__global__ void __launch_bounds__(kRouteWarps * 32)
+    k_route_hist(const int32_t* __restrict__ ids, int R, int E, int G, int32_t* __restrict__ hist,
+                 int* err) {
+  extern __shared__ int32_t sh_hist[];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int g = blockIdx.x * kRouteWarps + warp;
+  int32_t* h = sh_hist + warp * E;
+  for (int e = lane; e < E; e += 32) h[e] = 0;
+  __syncwarp();
+  if (g < G) {
+    const int end = min(R, (g + 1) * kRouteSeg);
+    for (int r = g * kRouteSeg + lane; r < end; r += 32) {
+      const int e = __ldg(ids + r);
+      if (e >= E) {
+        set_dev_error(err, kDevErrBadIndex);
+      } else if (e >= 0) {
+        atomicAdd(h + e, 1);
+      }
+    }
+  }
+  __syncwarp();
+  if (g < G)
+    for (int e = lane; e < E; e += 32) hist[(size_t)g * E + e] = h[e];
+}
+
+// One CTA of 1024 threads; thread e owns expert e (E <= 1024).
+__global__ void __launch_bounds__(1024)
+    k_route_scan(int32_t* __restrict__ hist, int G, int E, int A, int R, int cap,
+                 int32_t* __restrict__ expert_offsets, int32_t* __restrict__ num_post_padded,
+                 int32_t* __restrict__ block_ids, int32_t* __restrict__ sorted_ids) {
+  __shared__ int32_t warp_sums[32];
+  __shared__ int32_t s_total;
+  const int e = threadIdx.x, lane = e & 31, warp = e >> 5;
+  int count = 0;
+  if (e < E) {
+    int g = 0;
+    for (; g + 4 <= G; g += 4) {   // exclusive scan over segments, 4 loads in flight
+      int v0 = hist[(size_t)(g + 0) * E + e], v1 = hist[(size_t)(g + 1) * E + e];
+      int v2 = hist[(size_t)(g + 2) * E + e], v3 = hist[(size_t)(g + 3) * E + e];
+      hist[(size_t)(g + 0) * E + e] = count; count += v0;
+      hist[(size_t)(g + 1) * E + e] = count; count += v1;
+      hist[(size_t)(g + 2) * E + e] = count; count += v2;
+      hist[(size_t)(g + 3) * E + e] = count; count += v3;
+    }
+    for (; g < G; ++g) {
+      int v = hist[(size_t)g * E + e];
+      hist[(size_t)g * E + e] = count;
+      count += v;
+    }
+  }
+  const int padded = (count + A - 1) / A * A;
+  // block-wide exclusive scan of padded counts (expert order)
+  int incl = padded;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    int v = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += v;
+  }
+  if (lane == 31) warp_sums[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    int w = warp_sums[lane];
+    int wi = w;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      int v = __shfl_up_sync(0xffffffffu, wi, o);
+      if (lane >= o) wi += v;
+    }
+    warp_sums[lane] = wi - w;   // exclusive prefix of warp totals
+    if (lane == 31) s_total = wi;
+  }
+  __syncthreads();
+  const int off = incl - padded + warp_sums[warp];
+  const int total = s_total;
+  if (e < E) {
+    expert_offsets[e] = off;
+    for (int g = 0; g < G; ++g) hist[(size_t)g * E + e] += off;
+    for (int b = off / A; b < (off + padded) / A; ++b) block_ids[b] = e;
+    for (int j = off + count; j < off + padded; ++j) sorted_ids[j] = R;
+  }
+  if (e == 0) {
+    expert_offsets[E] = total;
+    num_post_padded[0] = total;
+  }
+  for (int b = total / A + e; b < cap / A; b += blockDim.x) block_ids[b] = -1;
+  for (int j = total + e; j < cap; j += blockDim.x) sorted_ids[j] = R;
+}
+
+__global__ void __launch_bounds__(kRouteWarps * 32)
+    k_route_scatter(const int32_t* __restrict__ ids, int R, int E, int G,
+                    const int32_t* __restrict__ hist, int32_t* __restrict__ sorted_ids,
+                    int32_t* __restrict__ inv_perm) {
+  extern __shared__ int32_t sh_cnt[];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int g = blockIdx.x * kRouteWarps + warp;
+  if (g >= G) return;
+  int32_t* cnt = sh_cnt + warp * E;
+  for (int e = lane; e < E; e += 32) cnt[e] = hist[(size_t)g * E + e];
+  __syncwarp();
+  const unsigned lt_mask = (1u << lane) - 1u;
+  const int end = min(R, (g + 1) * kRouteSeg);
+  for (int base = g * kRouteSeg; base < end; base += 32) {
+    const int r = base + lane;
+    const bool in = r < end;
+    const int e = in ? __ldg(ids + r) : -1;
+    const bool valid = in && e >= 0 && e < E;
+    const unsigned peers = __match_any_sync(0xffffffffu, valid ? e : -1);
+    int pos = -1;
+    if (valid) pos = cnt[e] + __popc(peers & lt_mask);
+    __syncwarp();
+    if (valid) {
+      sorted_ids[pos] = r;
+      if (lane == __ffs(peers) - 1) cnt[e] += __popc(peers);
+    }
+    if (in) inv_perm[r] = pos;
+    __syncwarp();
+  }
+}
+
+cudaError_t launch_route(const int32_t* topk_ids, int R, int E, int block_size, int cap,
+                         int32_t* hist, int32_t* sorted_ids, int32_t* block_expert_ids,
+                         int32_t* expert_offsets, int32_t* num_post_padded, int32_t* inv_perm,
+                         cudaStream_t stream) {
+  const int G = route_segments(R);
+  const int ctas = (G + kRouteWarps - 1) / kRouteWarps;
+  const size_t sh = (size_t)kRouteWarps * E * sizeof(int32_t);
+  if (G > 0) {
+    k_route_hist<<<ctas, kRouteWarps * 32, sh, stream>>>(topk_ids, R, E, G, hist,
+                                                         dev_error_word());
+  }
+  k_route_scan<<<1, 1024, 0, stream>>>(hist, G, E, block_size, R, cap, expert_offsets,
+                                       num_post_padded, block_expert_ids, sorted_ids);
+  if (G > 0) {
+    k_route_scatter<<<ctas, kRouteWarps * 32, sh, stream>>>(topk_ids, R, E, G, hist,
+                                                            sorted_ids, inv_perm);
+  }
+  return cudaGetLastError();
+}
+
+// ------------------------------------------------------------ data permute
+// One CTA (128 threads) per destination row, grid-stride over the used rows.
+__global__ void __launch_bounds__(128)
+    k_permute_bf16(const __nv_bfloat16* __restrict__ x, int H, int topk, int R,
+                   const int32_t* __restrict__ sorted_ids, const int32_t* __restrict__ npp,
+                   const float* __restrict__ row_weights, __nv_bfloat16* __restrict__ xp) {
+  const int rows = *npp;
+  const int nv = H / 8;
+  for (int row = blockIdx.x; row < rows; row += gridDim.x) {
+    const int sid = sorted_ids[row];
+    uint4* dst = reinterpret_cast<uint4*>(xp + (size_t)row * H);
+    if (sid >= R) {
+      for (int v = threadIdx.x; v < nv; v += blockDim.x) dst[v] = make_uint4(0, 0, 0, 0);
+      continue;
+    }
+    const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)(sid / topk) * H);
+    if (row_weights == nullptr) {
+      for (int v = threadIdx.x; v < nv; v += blockDim.x) dst[v] = __ldg(src + v);
+    } else {
+      const float w = row_weights[sid];
+      for (int v = threadIdx.x; v < nv; v += blockDim.x) {
+        uint4 u = __ldg(src + v);
+        __nv_bfloat16* b = reinterpret_cast<__nv_bfloat16*>(&u);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) b[j] = __float2bfloat16_rn(__bfloat162float(b[j]) * w);
+        dst[v] = u;
+      }
+    }
+  }
+}
+
+// FP8 variant: 16 threads per 128-element group, 8 elements per thread.
+__global__ void __launch_bounds__(128)
+    k_permute_fp8(const __nv_bfloat16* __restrict__ x, int H, int topk, int R,
+                  const int32_t* __restrict__ sorted_ids, const int32_t* __restrict__ npp,
+                  const float* __restrict__ row_weights, uint8_t* __restrict__ xq,
+                  float* __restrict__ xs, int ue8m0) {
+  const int rows = *npp;
+  const int nv = H / 8;          // 8-element vectors per row; multiple of 16
+  for (int row = blockIdx.x; row < rows; row += gridDim.x) {
+    const int sid = sorted_ids[row];
+    uint2* dst = reinterpret_cast<uint2*>(xq + (size_t)row * H);
+    float* srow = xs + (size_t)row * (H / 128);
+    if (sid >= R) {
+      for (int v = threadIdx.x; v < nv; v += blockDim.x) {
+        dst[v] = make_uint2(0, 0);
+        if ((v & 15) == 0) srow[v >> 4] = 0.0f;
+      }
+      continue;
+    }
+    const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)(sid / topk) * H);
+    const float w = row_weights ? row_weights[sid] : 1.0f;
+    // every lane takes part in the shuffles; a 16-lane group (one 1x128
+    // quantisation group) is either wholly inside the row or wholly outside
+    for (int base = 0; base < nv; base += blockDim.x) {
+      const int v = base + threadIdx.x;
+      const bool act = v < nv;
+      float f[8];
+      float amax = 0.0f;
+      if (act) {
+        uint4 u = __ldg(src + v);
+        const __nv_bfloat16* b = reinterpret_cast<const __nv_bfloat16*>(&u);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          f[j] = __bfloat162float(b[j]);
+          if (row_weights) f[j] = bf16_round(f[j] * w);
+          amax = fmaxf(amax, fabsf(f[j]));
+        }
+      }
+#pragma unroll
+      for (int o = 8; o >= 1; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+      if (act) {
+        const float s = act_scale(amax, ue8m0 != 0);
+        uint32_t lo = 0, hi = 0;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) lo |= (uint32_t)f32_to_e4m3(__fdiv_rn(f[j], s)) << (8 * j);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) hi |= (uint32_t)f32_to_e4m3(__fdiv_rn(f[4 + j], s)) << (8 * j);
+        dst[v] = make_uint2(lo, hi);
+        if ((v & 15) == 0) srow[v >> 4] = s;
+      }
+    }
+  }
+}
+
+cudaError_t launch_permute_rows(const void* x, int H, int topk, int R, const int32_t* sorted_ids,
+                                const int32_t* num_post_padded, const float* row_weights,
+                                void* x_perm, float* x_scale, bool ue8m0, int cap,
+                                cudaStream_t stream) {
+  if (cap <= 0) return cudaSuccess;
+  const int grid = min(cap, num_sms() * 8);
+  if (x_scale == nullptr) {
+    k_permute_bf16<<<grid, 128, 0, stream>>>(static_cast<const __nv_bfloat16*>(x), H, topk, R,
+                                             sorted_ids, num_post_padded, row_weights,
+                                             static_cast<__nv_bfloat16*>(x_perm));
+  } else {
+    k_permute_fp8<<<grid, 128, 0, stream>>>(static_cast<const __nv_bfloat16*>(x), H, topk, R,
+                                            sorted_ids, num_post_padded, row_weights,
+                                            static_cast<uint8_t*>(x_perm), x_scale, ue8m0);
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -223,14 +223,17 @@ def fused_experts(x, topk_ids, topk_weights, w13, w2, w13_scale=None, w2_scale=N
 
 def fused_experts_per_token(x, topk_ids, topk_weights, w13, w2, w13_scale=None,
                             w2_scale=None, *, quant="bf16", act_scale_fmt="fp32",
-                            apply_router_weight_on_input=False, exact=False, tokens=None):
+                            apply_router_weight_on_input=False, exact=False, tokens=None,
+                            return_items=False):
     """Form 1: brute-force loop over tokens and slots, no permutation.
 
     For each (t, i) with e = id[t, i] >= 0: quantise x_t (quantised modes),
     h = W13_e x_t, z = SiLU(h_gate) * h_up, o = W2_e z, y_t += w * o.  The
     same roundings as form 2 are applied item by item.  ``tokens`` restricts
     the tokens evaluated (outputs of different tokens are independent).
-    Returns y [len(tokens), H]."""
+    Returns y [len(tokens), H]; with ``return_items`` also the per-item W2
+    outputs o [len(tokens), k, H] (zero for skipped slots) and the weights
+    w' [len(tokens), k] they were summed with."""
     x = np.asarray(x, dtype=np.float64)
     ids = np.asarray(topk_ids, dtype=np.int64)
     wts = np.asarray(topk_weights, dtype=np.float64)
@@ -281,13 +284,18 @@ def fused_experts_per_token(x, topk_ids, topk_weights, w13, w2, w13_scale=None,
                     o = codecs.round_bf16(o)
                 outs[(t, i)] = o
     y = np.zeros((len(tokens), H))
+    items = np.zeros((len(tokens), k, H))
+    used_w = np.zeros((len(tokens), k))
     for j, t in enumerate(tokens):
         for i in range(k):                      # slot order
             if ids[t, i] < 0:
                 continue
             wi = 1.0 if apply_router_weight_on_input else wts[t, i]
             y[j] += wi * outs[(t, i)]
-    return y if exact else codecs.round_bf16(y)
+            items[j, i] = outs[(t, i)]
+            used_w[j, i] = wi
+    y = y if exact else codecs.round_bf16(y)
+    return (y, items, used_w) if return_items else y
 
 
 def _fp8_matvec(qa, sa, w_codes, w_scale):

@@ -1,0 +1,100 @@
+"""Host-side checks of the C ABI (no GPU needed): the library loads, exports
+every function declared in include/moe_ffn.h, sizes its buffers by the same
+closed form as the oracle, and rejects bad arguments before any launch."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import mixture_experts_ffn_align_gb300 as moe
+from moe_synth import CONFIGS
+from oracle import routing
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    if not os.path.exists(moe.LIB_PATH):
+        import __graft_entry__
+        __graft_entry__.build()
+
+
+def _declared_functions():
+    text = open(os.path.join(ROOT, "include", "moe_ffn.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^[a-z_ ]+[ *]+(\w+)\s*\(", text, flags=re.M)))
+
+
+def test_exports_every_declared_symbol():
+    names = _declared_functions()
+    assert len(names) >= 14, names
+    L = ctypes.CDLL(moe.LIB_PATH)
+    for n in names:
+        assert hasattr(L, n), n
+    assert set(moe.EXPORTS) == set(names)
+
+
+@pytest.mark.parametrize("name", list(CONFIGS))
+def test_m_sum_bound_matches_oracle(name):
+    c = CONFIGS[name]
+    for A in (16, 32, 64, 128):
+        p = moe.Problem.from_config(c, block_size=A)
+        assert moe.moe_m_sum_bound(p) == routing.m_sum_bound(c.M, c.topk, c.E, A)
+
+
+def test_workspace_sizes_positive_and_monotone():
+    p = moe.Problem.from_config(CONFIGS["mixtral"])
+    ws = moe.moe_workspace_bytes(p)
+    cap = moe.moe_m_sum_bound(p)
+    # at least x_perm (shared with y2) + z, both bf16
+    assert ws >= cap * p.H * 2 + cap * p.I * 2
+    assert moe.moe_host_workspace_bytes(p) > ws
+    assert moe.moe_align_workspace_bytes(p) > 0
+
+
+@pytest.mark.parametrize("bad", [dict(M=-1), dict(M=16385), dict(H=100), dict(I=0), dict(E=0),
+                                 dict(E=1025), dict(topk=0), dict(topk=17), dict(block_size=48),
+                                 dict(quant="bf16", apply_router_weight_on_input=True)])
+def test_invalid_problems_rejected(bad):
+    kw = dict(M=16, H=256, I=128, E=8, topk=2)
+    kw.update(bad)
+    p = moe.Problem(**kw)
+    assert moe.moe_m_sum_bound(p) == 0 and moe.moe_workspace_bytes(p) == 0
+    L = moe.lib()
+    st = L.fused_experts(ctypes.byref(p.c()), *([None] * 9), 0, None)
+    assert st == 1  # MOE_ERR_INVALID_ARG, nothing launched
+
+
+def test_empty_batch_is_a_noop():
+    p = moe.Problem(M=0, H=256, I=128, E=8, topk=2)
+    L = moe.lib()
+    assert L.fused_experts(ctypes.byref(p.c()), *([None] * 9), 0, None) == 0
+    assert L.unpermute_reduce(ctypes.byref(p.c()), None, None, None, None, None) == 0
+
+
+def test_null_pointers_and_small_workspace_rejected():
+    p = moe.Problem(M=16, H=256, I=128, E=8, topk=2)
+    L = moe.lib()
+    dummy = ctypes.c_void_p(16)   # never dereferenced: validation fails first
+    args = [dummy] * 9
+    st = L.fused_experts(ctypes.byref(p.c()), *args, 1, None)
+    assert st == 5  # MOE_ERR_WORKSPACE_TOO_SMALL
+    args[0] = None
+    assert L.fused_experts(ctypes.byref(p.c()), *args, 1 << 40, None) == 1
+
+
+def test_gemm_block_size_must_equal_tile_height():
+    """A GEMM block taller than the padding granularity would read another
+    expert's id (page "Blackwell 上的 DeepGEMM FusedMoE（vLLM）", §2.6.3); the
+    GEMM entry points refuse block_size != 128 before launching."""
+    p = moe.Problem(M=16, H=256, I=128, E=8, topk=2, block_size=64)
+    L = moe.lib()
+    d = ctypes.c_void_p(16)
+    assert L.grouped_gemm_w13(ctypes.byref(p.c()), d, None, d, None, d, d, d, None, 1, None) == 2
+
+
+def test_status_strings():
+    for code, name in moe.STATUS.items():
+        assert moe.moe_status_string(code) == name
