@@ -134,6 +134,38 @@ moe_status moe_align_permute(const moe_problem* p, const void* x, const int32_t*
                              float* x_perm_scale, void* workspace, size_t workspace_bytes,
                              void* stream);
 
+/* Stage 1 without a workspace, for callers that cannot allocate device memory
+ * when they call the library -- for example a serving engine that reserves the
+ * whole device for its own memory pool and does not let plug-ins call
+ * cudaMalloc, or a latency-critical loop that cannot accept cudaMalloc's
+ * implicit device synchronisation.  The paper has no counterpart: this is a
+ * deployment convenience, not a stage of the method.
+ *
+ * Same arguments, outputs and errors as moe_align_permute, minus the
+ * workspace: its scratch (per-segment expert histograms) is a fixed array of
+ * MOE_NOALLOC_SCRATCH_BYTES that the library keeps in each GPU's memory for
+ * the life of the process.  The entry point allocates nothing (no cudaMalloc,
+ * cudaFree or allocating library call).
+ *  - Limit: problems whose moe_align_workspace_bytes(p) exceeds
+ *    MOE_NOALLOC_SCRATCH_BYTES (more than 262144 segment x expert counters,
+ *    e.g. M*k > 131072 with E = 1024) are rejected with
+ *    MOE_ERR_WORKSPACE_TOO_SMALL before anything is enqueued; use
+ *    moe_align_permute with a workspace for those.
+ *  - The first call on a device looks up the array's device address
+ *    (cudaGetSymbolAddress) with that device current; make that first call
+ *    before any stream capture.
+ *  - All calls on a device share the one array and it keeps the last call's
+ *    contents (each call overwrites what it reads, so nothing carries over).
+ *    Calls whose work overlaps on the GPU (different streams without
+ *    ordering between them) race on it: order them on one stream. */
+#define MOE_NOALLOC_SCRATCH_BYTES (1u << 20)
+moe_status moe_align_permute_noalloc(const moe_problem* p, const void* x,
+                                     const int32_t* topk_ids, const float* topk_weights,
+                                     int32_t* sorted_ids, int32_t* block_expert_ids,
+                                     int32_t* expert_offsets, int32_t* num_post_padded,
+                                     int32_t* inv_perm, void* x_perm, float* x_perm_scale,
+                                     void* stream);
+
 /* Stage 2: grouped GEMM1, H1[row, n] = sum_k x_perm[row, k] * w13[e, n, k] for
  * every used block (page "fused_moe.py 分析", §1.3 routed GEMM and
  * "fused_moe_kernel 的核心原理"; FP8 blocks: "FP8 W8A8").  fp32 accumulation.

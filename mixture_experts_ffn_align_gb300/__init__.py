@@ -28,7 +28,10 @@ STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED", 3: "M
 EXPORTS = ["moe_m_sum_bound", "moe_align_workspace_bytes", "moe_workspace_bytes",
            "moe_host_workspace_bytes", "moe_align_permute", "grouped_gemm_w13", "act_mul_quant",
            "grouped_gemm_w2", "unpermute_reduce", "fused_experts", "fused_experts_from_host",
-           "moe_sync_status", "moe_status_string", "moe_debug_set_watchdog"]
+           "moe_sync_status", "moe_status_string", "moe_debug_set_watchdog",
+           "moe_align_permute_noalloc"]
+
+NOALLOC_SCRATCH_BYTES = 1 << 20   # MOE_NOALLOC_SCRATCH_BYTES in include/moe_ffn.h
 
 
 class MoEError(RuntimeError):
@@ -87,6 +90,8 @@ def lib() -> ctypes.CDLL:
                   "moe_host_workspace_bytes"):
             getattr(L, n).argtypes, getattr(L, n).restype = [P], sz
         L.moe_align_permute.argtypes = [P] + [vp] * 10 + [vp, sz, vp]
+        L.moe_align_permute_noalloc.argtypes = [P] + [vp] * 10 + [vp]
+        L.moe_align_permute_noalloc.restype = i32
         L.grouped_gemm_w13.argtypes = [P, vp, vp, vp, vp, vp, vp, vp, vp, i32, vp]
         L.act_mul_quant.argtypes = [P, vp, vp, vp, vp, vp]
         L.grouped_gemm_w2.argtypes = [P, vp, vp, vp, vp, vp, vp, vp, vp]
@@ -152,6 +157,22 @@ def moe_align_permute(p: Problem, x, topk_ids, topk_weights, sorted_ids, block_e
         _p(expert_offsets), _p(num_post_padded), _p(inv_perm), _p(x_perm), _p(x_perm_scale),
         _p(workspace), workspace.numel() * workspace.element_size(), _stream(stream)),
         "moe_align_permute")
+
+
+def moe_align_permute_noalloc(p: Problem, x, topk_ids, topk_weights, sorted_ids,
+                              block_expert_ids, expert_offsets, num_post_padded, inv_perm,
+                              x_perm, x_perm_scale, stream=None):
+    """moe_align_permute without a workspace, for callers that may not
+    allocate device memory at call time (for instance an engine that owns the
+    whole device through its own memory pool).  Its scratch is a fixed
+    MOE_NOALLOC_SCRATCH_BYTES array inside the library, shared by every call on
+    a device; larger problems raise MoEError(MOE_ERR_WORKSPACE_TOO_SMALL).
+    Make the first call on a device before any stream capture, and keep calls
+    ordered on one stream (overlapping calls race on the shared array)."""
+    _check(lib().moe_align_permute_noalloc(
+        _cp(p), _p(x), _p(topk_ids), _p(topk_weights), _p(sorted_ids), _p(block_expert_ids),
+        _p(expert_offsets), _p(num_post_padded), _p(inv_perm), _p(x_perm), _p(x_perm_scale),
+        _stream(stream)), "moe_align_permute_noalloc")
 
 
 def grouped_gemm_w13(p: Problem, x_perm, x_scale, w13, w13_scale, block_expert_ids,
