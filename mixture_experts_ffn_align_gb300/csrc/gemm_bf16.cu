@@ -10,11 +10,12 @@
 // block's expert id; the block height must equal the padding granularity.
 //
 // GB300 design (not the pages' Triton/DeepGEMM kernels):
-//  * persistent CTAs (one per SM), tiles 128 x 256 walked n-strip-major so the
-//    CTAs running together share the same weight strip and all of x_perm
-//    (which stays in the 126 MB L2);
+//  * persistent CTAs (one per SM), tiles 128 x 256 walked expert by expert
+//    (tile_sched.cuh): the CTAs running together share one expert, so each
+//    weight tile is read from HBM once for all of that expert's m-blocks and
+//    the expert's activation blocks stay in L2;
 //  * warp 0 lane 0: TMA producer, 4-stage ring of (A 128x64, B 256x64) bf16
-//    tiles, 128-byte swizzle, weights loaded with an evict-first L2 policy;
+//    tiles, 128-byte swizzle;
 //  * warp 1 lane 0: issues tcgen05.mma (M=128, N=256, K=16) into one of two
 //    256-column fp32 accumulators in tensor memory, tcgen05.commit frees the
 //    smem stage / publishes the accumulator;
@@ -27,6 +28,7 @@
 
 #include "moe_common.cuh"
 #include "moe_internal.h"
+#include "tile_sched.cuh"
 
 namespace moe {
 namespace {
@@ -37,7 +39,8 @@ constexpr int B_BYTES = BN * BK * 2;
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int TMEM_COLS = 2 * BN;
 constexpr int NUM_THREADS = 192;
-constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /*align*/ + 256 /*barriers*/;
+constexpr int SCHED_BYTES = 16 + 4 * kSchedMaxRuns + 4 * kSchedMaxBlocks;
+constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /*align*/ + 256 /*barriers*/ + SCHED_BYTES;
 
 struct GemmArgs {
   const int32_t* block_expert_ids;
@@ -52,6 +55,7 @@ struct GemmArgs {
   int out_cols_per_tile;  // output columns per tile (256, or 128 when fused)
   int m_blocks_cap;       // blocks the A / output buffers hold
   int num_experts;
+  int group_max;          // m-blocks per scheduling group (L2 budget)
   uint64_t limit_ns;
   int never_arrive;
   int* err;
@@ -68,6 +72,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   // bars[0..S) full, [S..2S) empty, 2S..2S+1 tmem_full, 2S+2..2S+3 tmem_empty, 2S+4 drain
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 5);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+  int* s_nruns = reinterpret_cast<int*>(smem + STAGES * STAGE_BYTES + 256);
+  int* s_runs = s_nruns + 4;
+  int* s_ids = s_runs + kSchedMaxRuns;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t smem_base = smem_u32(smem);
@@ -106,19 +113,26 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   const uint32_t tmem_base = *tmem_holder;
 
   // never walk past the buffers, whatever the routing wrote
-  const int nb_valid = min(*args.num_post_padded / BM, args.m_blocks_cap);
+  const int nb_valid =
+      min(min(*args.num_post_padded / BM, args.m_blocks_cap), kSchedMaxBlocks);
   const int total = nb_valid * args.n_tiles;
+  TileSched sched;
+  sched.nruns = sched_build(args.block_expert_ids, nb_valid, s_ids, s_runs, s_nruns);
+  sched.runs = s_runs;
+  sched.n_tiles = args.n_tiles;
+  sched.group_max = args.group_max;
 
   if (warp == 0 && lane == 0) {
     // ------------------------------------------------------------ producer
-    const uint64_t pol_a = l2_policy_evict_last();
-    const uint64_t pol_b = l2_policy_evict_first();
+    const uint64_t pol_a = l2_policy(MOE_GEMM_L2_A);
+    const uint64_t pol_b = l2_policy(MOE_GEMM_L2_B);
     uint32_t stage = 0, phase = 0;
     uint32_t issued_mask = 0, issued_parity = 0;
     bool skip_first = args.never_arrive != 0;
     for (int t = blockIdx.x; t < total; t += gridDim.x) {
-      const int n_tile = t / nb_valid, m_blk = t - n_tile * nb_valid;
-      const int e = args.block_expert_ids[m_blk];
+      int m_blk, n_tile;
+      sched_tile(sched, t, m_blk, n_tile);
+      const int e = s_ids[m_blk];
       if (e < 0 || e >= args.num_experts) continue;
       const int brow = e * args.b_rows_per_expert + n_tile * args.n_tile_rows;
       bool ok = true;
@@ -157,9 +171,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     uint32_t stage = 0, phase = 0;
     int local = 0;
     for (int t = blockIdx.x; t < total; t += gridDim.x) {
-      const int n_tile = t / nb_valid, m_blk = t - n_tile * nb_valid;
-      (void)n_tile;
-      const int e = args.block_expert_ids[m_blk];
+      int m_blk, n_tile;
+      sched_tile(sched, t, m_blk, n_tile);
+      const int e = s_ids[m_blk];
       if (e < 0 || e >= args.num_experts) continue;
       const int acc = local & 1;
       const uint32_t acc_phase = (local >> 1) & 1;
@@ -201,8 +215,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const int row_in_tile = q * 32 + lane;
     int local = 0;
     for (int t = blockIdx.x; t < total; t += gridDim.x) {
-      const int n_tile = t / nb_valid, m_blk = t - n_tile * nb_valid;
-      const int e = args.block_expert_ids[m_blk];
+      int m_blk, n_tile;
+      sched_tile(sched, t, m_blk, n_tile);
+      const int e = s_ids[m_blk];
       if (e < 0 || e >= args.num_experts) continue;
       const int acc = local & 1;
       const uint32_t acc_phase = (local >> 1) & 1;
@@ -321,6 +336,7 @@ cudaError_t launch_ggemm_bf16(const void* A, int cap, int K, const void* B, int 
   a.b_rows_per_expert = b_rows_per_expert;
   a.m_blocks_cap = cap / BM;
   a.num_experts = b_rows_total / b_rows_per_expert;
+  a.group_max = sched_group_max(K, 2);
   if (fuse_act) {
     const int I = b_rows_per_expert / 2;
     a.ldo = I;

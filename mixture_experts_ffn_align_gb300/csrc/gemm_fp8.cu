@@ -19,14 +19,15 @@
 //  * warps 2-9: each owns 32 rows x 64 columns of the tile, reads the partial
 //    with tcgen05.ld, releases it, and accumulates sa*sb*partial in fp32
 //    registers; at the end of the tile the sum is rounded to bf16 and stored.
-//  * tiles are walked in groups of m-blocks (all column tiles of a group
-//    before the next group) so a group's activations stay in L2 while the
-//    weights stream once.
+//  * tiles are walked expert by expert (tile_sched.cuh), so each weight tile
+//    is fetched once for all of the expert's m-blocks and the expert's
+//    activations stay in L2.
 //  * every wait is bounded, as in the bf16 kernel.
 #include <mutex>
 
 #include "moe_common.cuh"
 #include "moe_internal.h"
+#include "tile_sched.cuh"
 
 namespace moe {
 
@@ -42,7 +43,8 @@ constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int TMEM_COLS = NPART * BN;
 constexpr int NUM_EPI_WARPS = 8;
 constexpr int NUM_THREADS = 64 + NUM_EPI_WARPS * 32;
-constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + 256;
+constexpr int SCHED_BYTES = 16 + 4 * kSchedMaxRuns + 4 * kSchedMaxBlocks;
+constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + 256 + SCHED_BYTES;
 
 struct Fp8Args {
   const int32_t* block_expert_ids;
@@ -56,21 +58,11 @@ struct Fp8Args {
   int b_rows_per_expert;  // N
   int m_blocks_cap;
   int num_experts;
-  int group_m;            // m-blocks per scheduling group
+  int group_max;          // m-blocks per scheduling group (L2 budget)
   uint64_t limit_ns;
   int never_arrive;
   int* err;
 };
-
-__device__ __forceinline__ void tile_coords(int t, int nb_valid, int n_tiles, int group_m,
-                                            int& m_blk, int& n_tile) {
-  const int per_group = group_m * n_tiles;
-  const int g = t / per_group;
-  const int gm = min(group_m, nb_valid - g * group_m);
-  const int local = t - g * per_group;
-  n_tile = local / gm;
-  m_blk = g * group_m + (local - n_tile * gm);
-}
 
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     k_ggemm_fp8(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
@@ -81,6 +73,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 2 * NPART + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+  int* s_nruns = reinterpret_cast<int*>(smem + STAGES * STAGE_BYTES + 256);
+  int* s_runs = s_nruns + 4;
+  int* s_ids = s_runs + kSchedMaxRuns;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t smem_base = smem_u32(smem);
@@ -118,20 +113,25 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   tc_fence_after();
   const uint32_t tmem_base = *tmem_holder;
 
-  const int nb_valid = min(*args.num_post_padded / BM, args.m_blocks_cap);
+  const int nb_valid =
+      min(min(*args.num_post_padded / BM, args.m_blocks_cap), kSchedMaxBlocks);
   const int total = nb_valid * args.n_tiles;
-  const int group_m = max(1, args.group_m);
+  TileSched sched;
+  sched.nruns = sched_build(args.block_expert_ids, nb_valid, s_ids, s_runs, s_nruns);
+  sched.runs = s_runs;
+  sched.n_tiles = args.n_tiles;
+  sched.group_max = args.group_max;
 
   if (warp == 0 && lane == 0) {
     // ------------------------------------------------------------ producer
-    const uint64_t pol_a = l2_policy_evict_last();
-    const uint64_t pol_b = l2_policy_evict_first();
+    const uint64_t pol_a = l2_policy(MOE_GEMM_L2_A);
+    const uint64_t pol_b = l2_policy(MOE_GEMM_L2_B);
     uint32_t stage = 0, phase = 0, issued_mask = 0, issued_parity = 0;
     bool skip_first = args.never_arrive != 0;
     for (int t = blockIdx.x; t < total; t += gridDim.x) {
       int m_blk, n_tile;
-      tile_coords(t, nb_valid, args.n_tiles, group_m, m_blk, n_tile);
-      const int e = args.block_expert_ids[m_blk];
+      sched_tile(sched, t, m_blk, n_tile);
+      const int e = s_ids[m_blk];
       if (e < 0 || e >= args.num_experts) continue;
       const int brow = e * args.b_rows_per_expert + n_tile * BN;
       bool ok = true;
@@ -167,8 +167,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     bool ok = true;
     for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
       int m_blk, n_tile;
-      tile_coords(t, nb_valid, args.n_tiles, group_m, m_blk, n_tile);
-      const int e = args.block_expert_ids[m_blk];
+      sched_tile(sched, t, m_blk, n_tile);
+      const int e = s_ids[m_blk];
       if (e < 0 || e >= args.num_experts) continue;
       for (int kb = 0; kb < args.num_kb; ++kb, ++pc) {
         const uint32_t buf = pc % NPART, pphase = (pc / NPART) & 1;
@@ -203,8 +203,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     bool ok = true;
     for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
       int m_blk, n_tile;
-      tile_coords(t, nb_valid, args.n_tiles, group_m, m_blk, n_tile);
-      const int e = args.block_expert_ids[m_blk];
+      sched_tile(sched, t, m_blk, n_tile);
+      const int e = s_ids[m_blk];
       if (e < 0 || e >= args.num_experts) continue;
       const size_t row = (size_t)m_blk * BM + row_in_tile;
       const float* sa_row = args.a_scale + row * args.num_kb;
@@ -285,8 +285,7 @@ cudaError_t launch_ggemm_fp8(const void* A, const float* a_scale, int cap, int K
   a.b_rows_per_expert = b_rows_per_expert;
   a.m_blocks_cap = cap / BM;
   a.num_experts = b_rows_total / b_rows_per_expert;
-  // keep a group's activations (group_m blocks of 128 x K bytes) near 32 MB
-  a.group_m = (int)std::max<long long>(1, (32ll << 20) / ((long long)BM * K));
+  a.group_max = sched_group_max(K, 1);
   watchdog_params(&a.limit_ns, &a.never_arrive);
   a.err = dev_error_word();
   static bool attr_done = false;

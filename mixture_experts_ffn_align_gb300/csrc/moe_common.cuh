@@ -98,6 +98,11 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
       : "memory");
 }
 
+__device__ __forceinline__ uint64_t l2_policy_evict_normal() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
 __device__ __forceinline__ uint64_t l2_policy_evict_first() {
   uint64_t p;
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
@@ -108,6 +113,22 @@ __device__ __forceinline__ uint64_t l2_policy_evict_last() {
   asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
   return p;
 }
+
+// 0: evict_normal, 1: evict_last, 2: evict_first.
+__device__ __forceinline__ uint64_t l2_policy(int mode) {
+  return mode == 1 ? l2_policy_evict_last() : (mode == 2 ? l2_policy_evict_first()
+                                                         : l2_policy_evict_normal());
+}
+// L2 hints of the GEMM operand loads: activations (A) and weights (B).  A
+// block is re-read for every n-tile of its expert, a weight tile only by the
+// expert's m-blocks running at the same time; evict_last on A and no hint on
+// B measured best on the Mixtral-shaped and DeepSeek-class layers.
+#ifndef MOE_GEMM_L2_A
+#define MOE_GEMM_L2_A 1
+#endif
+#ifndef MOE_GEMM_L2_B
+#define MOE_GEMM_L2_B 0
+#endif
 
 // ---------------------------------------------------------------- tcgen05
 __device__ __forceinline__ void tmem_alloc(uint32_t holder_smem, uint32_t ncols) {
