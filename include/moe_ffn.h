@@ -232,6 +232,11 @@ moe_status moe_sync_status(void* stream);
 /* Human-readable name of a status code (static storage, never NULL). */
 const char* moe_status_string(moe_status s);
 
+/* Name and description of the CUDA error behind the calling thread's most
+ * recent MOE_ERR_CUDA from a launch ("" if none yet).  Thread-local storage,
+ * valid until the thread's next failing call. */
+const char* moe_last_error_string(void);
+
 /* Test hook for the device watchdog: with limit_ns > 0, every bounded wait in
  * the GEMM kernels gives up after limit_ns nanoseconds instead of the default
  * (2 s); with never_arrive != 0 the GEMM producer skips its first copy, so the

@@ -29,15 +29,15 @@ EXPORTS = ["moe_m_sum_bound", "moe_align_workspace_bytes", "moe_workspace_bytes"
            "moe_host_workspace_bytes", "moe_align_permute", "grouped_gemm_w13", "act_mul_quant",
            "grouped_gemm_w2", "unpermute_reduce", "fused_experts", "fused_experts_from_host",
            "moe_sync_status", "moe_status_string", "moe_debug_set_watchdog",
-           "moe_align_permute_noalloc"]
+           "moe_align_permute_noalloc", "moe_last_error_string"]
 
 NOALLOC_SCRATCH_BYTES = 1 << 20   # MOE_NOALLOC_SCRATCH_BYTES in include/moe_ffn.h
 
 
 class MoEError(RuntimeError):
-    def __init__(self, status: int, where: str):
+    def __init__(self, status: int, where: str, detail: str = ""):
         self.status = status
-        super().__init__(f"{where}: {STATUS.get(status, status)}")
+        super().__init__(f"{where}: {STATUS.get(status, status)}" + (f" ({detail})" if detail else ""))
 
 
 class CProblem(ctypes.Structure):
@@ -100,6 +100,7 @@ def lib() -> ctypes.CDLL:
         L.fused_experts_from_host.argtypes = [P] + [vp] * 9 + [sz, vp]
         L.moe_sync_status.argtypes = [vp]
         L.moe_status_string.argtypes, L.moe_status_string.restype = [i32], ctypes.c_char_p
+        L.moe_last_error_string.argtypes, L.moe_last_error_string.restype = [], ctypes.c_char_p
         L.moe_debug_set_watchdog.argtypes, L.moe_debug_set_watchdog.restype = \
             [ctypes.c_int64, i32], None
         for n in ("moe_align_permute", "grouped_gemm_w13", "act_mul_quant", "grouped_gemm_w2",
@@ -124,7 +125,8 @@ def _stream(stream):
 
 def _check(status: int, where: str):
     if status != 0:
-        raise MoEError(status, where)
+        detail = moe_last_error_string() if status == 3 else ""
+        raise MoEError(status, where, detail)
 
 
 def _cp(p: Problem):
@@ -223,6 +225,10 @@ def moe_sync_status(stream=None) -> int:
 
 def moe_status_string(status: int) -> str:
     return lib().moe_status_string(int(status)).decode()
+
+
+def moe_last_error_string() -> str:
+    return lib().moe_last_error_string().decode()
 
 
 def moe_debug_set_watchdog(limit_ns: int, never_arrive: bool = False):

@@ -8,6 +8,7 @@
 // taller than the padding granularity reads another expert's id (so the
 // GEMMs demand block_size == 128 here), and M == 0 returning early (page 1,
 // FusedMoEKernelModularImpl._fused_experts, "M_full == 0").
+#include <cstdio>
 #include <cstring>
 #include <mutex>
 
@@ -125,7 +126,15 @@ Layout layout(const moe_problem* p) {
   return L;
 }
 
-moe_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+thread_local char g_last_error[256] = "";
+
+// Records the CUDA error of a failed call for moe_last_error_string.
+moe_status cuda_status(cudaError_t e) {
+  if (e == cudaSuccess) return MOE_OK;
+  snprintf(g_last_error, sizeof(g_last_error), "%s: %s", cudaGetErrorName(e),
+           cudaGetErrorString(e));
+  return MOE_ERR_CUDA;
+}
 
 // The GEMM tiles are 128 rows high, so the padding granularity must be 128;
 // bf16 GEMM2 tiles are 256 columns wide.  MXFP4 weights have no kernel yet.
@@ -177,7 +186,7 @@ moe_status moe_align_permute(const moe_problem* p, const void* x, const int32_t*
   cudaError_t e = launch_route(topk_ids, R, p->E, p->block_size, cap,
                                static_cast<int32_t*>(workspace), sorted_ids, block_expert_ids,
                                expert_offsets, num_post_padded, inv_perm, s);
-  if (e != cudaSuccess) return MOE_ERR_CUDA;
+  if (e != cudaSuccess) return cuda_status(e);
   if (x) {
     e = launch_permute_rows(x, p->H, p->topk, R, sorted_ids, num_post_padded,
                             p->apply_router_weight_on_input ? topk_weights : nullptr, x_perm,
@@ -338,6 +347,8 @@ moe_status moe_sync_status(void* stream) {
   if (v & kDevErrBadIndex) return MOE_ERR_DEVICE_BAD_INDEX;
   return MOE_OK;
 }
+
+const char* moe_last_error_string(void) { return g_last_error; }
 
 const char* moe_status_string(moe_status s) {
   switch (s) {

@@ -11,14 +11,18 @@
 // The hardware block-scaled MMA takes power-of-two (UE8M0) scales only, and
 // these scales are arbitrary fp32, so the scales are applied on the CUDA
 // cores ("promotion"):
-//  * warp 0 lane 0: TMA producer, 6-stage ring of (A 128x128, B 128x128) e4m3
+//  * warp 0 lane 0: TMA producer, 4-stage ring of (A 128x128, B 256x128) e4m3
 //    tiles -- one stage is exactly one 128-wide K block;
-//  * warp 1 lane 0: four kind::f8f6f4 MMAs (M=128, N=128, K=32) per K block
-//    into one of four 128-column tensor-memory partials, rotating, so the MMA
-//    runs up to four K blocks ahead of the epilogue;
-//  * warps 2-9: each owns 32 rows x 64 columns of the tile, reads the partial
-//    with tcgen05.ld, releases it, and accumulates sa*sb*partial in fp32
-//    registers; at the end of the tile the sum is rounded to bf16 and stored.
+//  * warp 1 lane 0: four kind::f8f6f4 MMAs (M=128, N=256, K=32) per K block
+//    into one of two 256-column tensor-memory partials, alternating.  (128x128
+//    MMAs ran at about half the tensor rate on GB300; N=256 keeps the pipe fed.)
+//  * warps 2-9: warp w owns TMEM lane quadrant w%4 (32 rows) and one
+//    128-column half of the tile -- exactly one 128x128 weight-scale block, so
+//    one scale product sa[row,kb]*sb[kb] per thread and K block; it reads the
+//    partial with tcgen05.ld, releases it, and accumulates in fp32 registers;
+//    at the end of the tile the sum is rounded to bf16 and stored.
+//  * a last column tile narrower than 256 (N % 256 == 128) computes its upper
+//    half on whatever the weight box held and never stores it.
 //  * tiles are walked expert by expert (tile_sched.cuh), so each weight tile
 //    is fetched once for all of the expert's m-blocks and the expert's
 //    activations stay in L2.
@@ -36,7 +40,7 @@ bool make_tmap_k_sw128(CUtensorMap* map, const void* base, uint64_t rows, uint64
 
 namespace {
 
-constexpr int BM = 128, BN = 128, BK = 128, STAGES = 6, NPART = 4;
+constexpr int BM = 128, BN = 256, BK = 128, STAGES = 4, NPART = 2;
 constexpr int A_BYTES = BM * BK;
 constexpr int B_BYTES = BN * BK;
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
@@ -54,7 +58,8 @@ struct Fp8Args {
   __nv_bfloat16* out;     // [cap, N]
   int ldo;                // N
   int num_kb;             // K / 128
-  int n_tiles;            // N / 128
+  int n_tiles;            // ceil(N / 256)
+  int n_blocks;           // N / 128 (weight-scale blocks per expert)
   int b_rows_per_expert;  // N
   int m_blocks_cap;
   int num_experts;
@@ -64,6 +69,8 @@ struct Fp8Args {
   int* err;
 };
 
+// 10 warps put 3 warps on two of the SM's four register-file partitions
+// (16384 registers each), so a thread may hold at most 168 registers.
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     k_ggemm_fp8(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const Fp8Args args) {
@@ -147,6 +154,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           mbar_arrive_expect_tx(full_bar(stage), STAGE_BYTES);
           tma_load_2d(sa, &tmA, full_bar(stage), kb * BK, m_blk * BM, pol_a);
           tma_load_2d(sa + A_BYTES, &tmB, full_bar(stage), kb * BK, brow, pol_b);
+          tma_load_2d(sa + A_BYTES + 128 * BK, &tmB, full_bar(stage), kb * BK, brow + 128, pol_b);
           issued_mask |= 1u << stage;
           issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
         }
@@ -197,7 +205,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   } else if (warp >= 2) {
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;               // TMEM lane quadrant
-    const int half = (warp - 2) >> 2;     // column half of the tile
+    const int half = (warp - 2) >> 2;     // 128-column half of the tile
     const int row_in_tile = q * 32 + lane;
     uint32_t pc = 0;
     bool ok = true;
@@ -206,49 +214,70 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       sched_tile(sched, t, m_blk, n_tile);
       const int e = s_ids[m_blk];
       if (e < 0 || e >= args.num_experts) continue;
+      const int nblk = 2 * n_tile + half;            // weight-scale block of this warp
+      const bool active = nblk < args.n_blocks;      // false: past N on a ragged last tile
       const size_t row = (size_t)m_blk * BM + row_in_tile;
       const float* sa_row = args.a_scale + row * args.num_kb;
       const float* sb_blk =
-          args.b_scale + ((size_t)e * args.n_tiles + n_tile) * (size_t)args.num_kb;
-      float acc[64];
+          args.b_scale + ((size_t)e * args.n_blocks + (active ? nblk : 0)) * (size_t)args.num_kb;
+      float acc[128];
 #pragma unroll
-      for (int j = 0; j < 64; ++j) acc[j] = 0.0f;
-      for (int kb = 0; kb < args.num_kb; ++kb, ++pc) {
-        const uint32_t buf = pc % NPART, pphase = (pc / NPART) & 1;
-        const float s = __ldg(sa_row + kb) * __ldg(sb_blk + kb);
-        int got = 0;
-        if (lane == 0)
-          got = mbar_wait_bounded(pfull_bar(buf), pphase, abort_flag, args.limit_ns, args.err);
-        got = __shfl_sync(0xffffffffu, got, 0);
-        if (!got) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + buf * BN + half * 64;
-        uint32_t p0[32], p1[32];
-        tmem_ld_32x32b_x32(taddr, p0);
-        tmem_ld_32x32b_x32(taddr + 32, p1);
-        tmem_ld_wait();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(pempty_bar(buf));
+      for (int j = 0; j < 128; ++j) acc[j] = 0.0f;
+      constexpr int SCALE_AHEAD = 4;
+      float ra[SCALE_AHEAD], rb[SCALE_AHEAD];
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          acc[j] = fmaf(s, __uint_as_float(p0[j]), acc[j]);
-          acc[32 + j] = fmaf(s, __uint_as_float(p1[j]), acc[32 + j]);
+      for (int j = 0; j < SCALE_AHEAD; ++j) {
+        ra[j] = j < args.num_kb ? __ldg(sa_row + j) : 0.0f;
+        rb[j] = j < args.num_kb ? __ldg(sb_blk + j) : 0.0f;
+      }
+      for (int kb0 = 0; kb0 < args.num_kb && ok; kb0 += SCALE_AHEAD) {
+#pragma unroll
+        for (int j = 0; j < SCALE_AHEAD; ++j) {
+          const int kb = kb0 + j;
+          if (kb >= args.num_kb) break;
+          const float s = ra[j] * rb[j];
+          if (kb + SCALE_AHEAD < args.num_kb) {
+            ra[j] = __ldg(sa_row + kb + SCALE_AHEAD);
+            rb[j] = __ldg(sb_blk + kb + SCALE_AHEAD);
+          }
+          const uint32_t buf = pc % NPART, pphase = (pc / NPART) & 1;
+          int got = 0;
+          if (lane == 0)
+            got = mbar_wait_bounded(pfull_bar(buf), pphase, abort_flag, args.limit_ns, args.err);
+          got = __shfl_sync(0xffffffffu, got, 0);
+          if (!got) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + buf * BN + half * 128;
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            uint32_t p[16];
+            tmem_ld_32x32b_x16(taddr + c * 16, p);
+            tmem_ld_wait();
+            if (c == 7) {     // every read of this buffer by this warp is done
+              tc_fence_before();
+              __syncwarp();
+              if (lane == 0) mbar_arrive(pempty_bar(buf));
+            }
+#pragma unroll
+            for (int i = 0; i < 16; ++i) acc[c * 16 + i] = fmaf(s, __uint_as_float(p[i]), acc[c * 16 + i]);
+          }
+          ++pc;
         }
       }
       if (!ok) break;
-      uint4* dst = reinterpret_cast<uint4*>(args.out + row * args.ldo + (size_t)n_tile * BN +
-                                            half * 64);
+      if (active) {
+        uint4* dst = reinterpret_cast<uint4*>(args.out + row * args.ldo + (size_t)nblk * 128);
 #pragma unroll
-      for (int v = 0; v < 8; ++v) {
-        uint4 pk;
-        __nv_bfloat16* pb = reinterpret_cast<__nv_bfloat16*>(&pk);
+        for (int v = 0; v < 16; ++v) {
+          uint4 pk;
+          __nv_bfloat16* pb = reinterpret_cast<__nv_bfloat16*>(&pk);
 #pragma unroll
-        for (int j = 0; j < 8; ++j) pb[j] = __float2bfloat16_rn(acc[v * 8 + j]);
-        dst[v] = pk;
+          for (int j = 0; j < 8; ++j) pb[j] = __float2bfloat16_rn(acc[v * 8 + j]);
+          dst[v] = pk;
+        }
       }
     }
   }
@@ -281,7 +310,8 @@ cudaError_t launch_ggemm_fp8(const void* A, const float* a_scale, int cap, int K
   a.out = static_cast<__nv_bfloat16*>(out);
   a.ldo = n_out;
   a.num_kb = K / BK;
-  a.n_tiles = n_out / BN;
+  a.n_blocks = n_out / 128;
+  a.n_tiles = (n_out + BN - 1) / BN;
   a.b_rows_per_expert = b_rows_per_expert;
   a.m_blocks_cap = cap / BM;
   a.num_experts = b_rows_total / b_rows_per_expert;
