@@ -137,10 +137,12 @@ moe_status cuda_status(cudaError_t e) {
 }
 
 // The GEMM tiles are 128 rows high, so the padding granularity must be 128;
-// bf16 GEMM2 tiles are 256 columns wide.  MXFP4 weights have no kernel yet.
+// bf16 GEMM2 tiles are 256 columns wide.  The MXFP4 kernel applies scales in
+// the tensor core, which takes powers of two only: activations need UE8M0.
 bool gemm_supported(const moe_problem* p) {
   if (p->block_size != 128) return false;
   if (p->quant == MOE_Q_BF16) return p->H % 256 == 0;
+  if (p->quant == MOE_Q_MXFP4_W4A8) return p->act_scale_fmt == MOE_SCALE_UE8M0;
   return p->quant == MOE_Q_FP8_BLOCK128;
 }
 
@@ -214,6 +216,11 @@ moe_status grouped_gemm_w13(const moe_problem* p, const void* x_perm, const floa
   }
   if (fuse_act) return MOE_ERR_UNSUPPORTED;
   if (!x_scale || !w13_scale) return MOE_ERR_INVALID_ARG;
+  if (p->quant == MOE_Q_MXFP4_W4A8)
+    return cuda_status(launch_ggemm_mxfp4(x_perm, x_scale, cap, p->H, w13,
+                                          static_cast<const uint8_t*>(w13_scale),
+                                          p->E * 2 * p->I, 2 * p->I, 2 * p->I, block_expert_ids,
+                                          num_post_padded, out, s));
   return cuda_status(launch_ggemm_fp8(x_perm, x_scale, cap, p->H, w13,
                                       static_cast<const float*>(w13_scale), p->E * 2 * p->I,
                                       2 * p->I, 2 * p->I, block_expert_ids, num_post_padded, out,
@@ -247,6 +254,10 @@ moe_status grouped_gemm_w2(const moe_problem* p, const void* z, const float* z_s
                                          block_expert_ids, num_post_padded, y2, false, s));
   }
   if (!z_scale || !w2_scale) return MOE_ERR_INVALID_ARG;
+  if (p->quant == MOE_Q_MXFP4_W4A8)
+    return cuda_status(launch_ggemm_mxfp4(z, z_scale, cap, p->I, w2,
+                                          static_cast<const uint8_t*>(w2_scale), p->E * p->H,
+                                          p->H, p->H, block_expert_ids, num_post_padded, y2, s));
   return cuda_status(launch_ggemm_fp8(z, z_scale, cap, p->I, w2,
                                       static_cast<const float*>(w2_scale), p->E * p->H, p->H,
                                       p->H, block_expert_ids, num_post_padded, y2, s));

@@ -319,6 +319,24 @@ bool make_tmap_k_sw128(CUtensorMap* map, const void* base, uint64_t rows, uint64
   return r == CUDA_SUCCESS;
 }
 
+// 2-D K-major tensor map over packed E2M1 values ([rows, k_elems / 2] bytes,
+// low nibble first) that lands each 16 values as 8 bytes followed by an
+// 8-byte gap, so a 128-value K row fills one 128-byte swizzled smem row --
+// the layout the 8-bit-container f8f6f4 MMAs read for 4-bit operands.
+bool make_tmap_fp4_k_sw128(CUtensorMap* map, const void* base, uint64_t rows, uint64_t k_elems,
+                           uint32_t box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (fn == nullptr) return false;
+  const cuuint64_t dims[2] = {k_elems, rows};
+  const cuuint64_t strides[1] = {k_elems / 2};
+  const cuuint32_t box[2] = {128, box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, 2, const_cast<void*>(base), dims,
+                  strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 cudaError_t launch_ggemm_bf16(const void* A, int cap, int K, const void* B, int b_rows_total,
                               int b_rows_per_expert, int n_out, const int32_t* block_expert_ids,
                               const int32_t* num_post_padded, void* out, bool fuse_act,

@@ -1,0 +1,375 @@
+// MXFP4 x FP8 (W4A8) grouped GEMM (stages 2 and 4 of MOE_Q_MXFP4_W4A8).
+//
+// What it computes: page "Blackwell 上的 DeepGEMM FusedMoE（vLLM）", TL;DR table,
+// W4A8 MXFP4 row: weights E2M1 with one E8M0 scale per 32 along K, activations
+// e4m3 with dynamic 128-element scales (here rounded up to powers of two,
+// UE8M0, so that the tensor core can apply them); §2.8(d): weights stay packed
+// two per byte.  For every used 128-row block with expert e:
+//   C[r, n] = sum_k (qa[r,k] * sa[r, k/128]) * (e2m1(qb[e,n,k]) * 2^(sb[e,n,k/32]-127)).
+// All scales are powers of two, so the block-scaled MMA
+// (tcgen05.mma kind::mxf8f6f4.block_scale.scale_vec::1X) applies them in
+// hardware and accumulates the whole K range in one fp32 TMEM accumulator.
+//
+//  * warp 0 lane 0: TMA producer, 6-stage ring; per 128-wide K block an e4m3
+//    A tile (128 x 128 B) and an E2M1 B tile loaded with the padded 4-bit TMA
+//    type (each 16 values -> 8 bytes + 8-byte gap), 128-byte swizzle;
+//  * warps 2-5: scale writers -- per K block, the A scale operand (each row's
+//    UE8M0 exponent in all 4 bytes: one scale covers 128 = 4 x 32) and the B
+//    scale operand (the 4 E8M0 bytes of each column's 4 K chunks), written
+//    into tensor memory with tcgen05.st; byte j is picked by the scale-ID
+//    fields of MMA j;
+//  * warp 1 lane 0: four MMAs (M=128, N=128, K=32) per K block into one of two
+//    128-column accumulators; tcgen05.commit frees the stage and its scales;
+//  * warps 6-9: epilogue, tcgen05.ld -> bf16 -> global.
+//  * tiles walked expert by expert (tile_sched.cuh); every wait is bounded.
+#include <mutex>
+
+#include "moe_common.cuh"
+#include "moe_internal.h"
+#include "tile_sched.cuh"
+
+namespace moe {
+
+bool make_tmap_k_sw128(CUtensorMap* map, const void* base, uint64_t rows, uint64_t k_elems,
+                       int elem_bytes, uint32_t box_rows);
+bool make_tmap_fp4_k_sw128(CUtensorMap* map, const void* base, uint64_t rows, uint64_t k_elems,
+                           uint32_t box_rows);
+
+namespace {
+
+constexpr int BM = 128, BN = 128, BK = 128, STAGES = 6;
+constexpr int A_BYTES = BM * BK;          // e4m3
+constexpr int B_BYTES = BN * BK;          // 4-bit values padded to one byte each in smem
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int ACC_COLS = 2 * BN;          // two accumulators
+// Scale operands: 128 rows (or columns) of one 32-bit word (4 E8M0 bytes, one
+// per 32-wide K chunk) laid out as 32 lanes x 4 columns -- row r at lane
+// r % 32, column r / 32 -- and repeated in each 32-lane quadrant.  Each operand
+// gets its own 16-column-aligned slot: stage s, A at SF_COL0 + 32 s, B at +16.
+constexpr int SF_COL0 = ACC_COLS;
+constexpr int SF_SLOT = 16;
+constexpr int TMEM_COLS = 512;
+constexpr int NUM_THREADS = 320;
+constexpr int SCHED_BYTES = 16 + 4 * kSchedMaxRuns + 4 * kSchedMaxBlocks;
+constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + 256 + SCHED_BYTES;
+static_assert(SF_COL0 + SF_SLOT * (2 * STAGES - 1) + 4 <= TMEM_COLS, "tensor memory budget");
+
+struct Mx4Args {
+  const int32_t* block_expert_ids;
+  const int32_t* num_post_padded;
+  const float* a_scale;     // [cap, K/128] fp32 powers of two
+  const uint8_t* b_scale;   // [E, N, K/32] E8M0
+  __nv_bfloat16* out;       // [cap, N]
+  int ldo;                  // N
+  int num_kb;               // K / 128
+  int n_tiles;              // N / 128
+  int b_rows_per_expert;    // N
+  int m_blocks_cap;
+  int num_experts;
+  int group_max;
+  uint64_t limit_ns;
+  int never_arrive;
+  int* err;
+};
+
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    k_ggemm_mxfp4(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                  const Mx4Args args) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
+  // full[S], sfull[S], empty[S], tfull[2], tempty[2], drain
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 3 * STAGES + 5);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+  int* s_nruns = reinterpret_cast<int*>(smem + STAGES * STAGE_BYTES + 256);
+  int* s_runs = s_nruns + 4;
+  int* s_ids = s_runs + kSchedMaxRuns;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t smem_base = smem_u32(smem);
+  const uint32_t bar_base = smem_u32(bars);
+  auto full_bar = [&](int s) { return bar_base + 8u * s; };
+  auto sfull_bar = [&](int s) { return bar_base + 8u * (STAGES + s); };
+  auto empty_bar = [&](int s) { return bar_base + 8u * (2 * STAGES + s); };
+  auto tfull_bar = [&](int a) { return bar_base + 8u * (3 * STAGES + a); };
+  auto tempty_bar = [&](int a) { return bar_base + 8u * (3 * STAGES + 2 + a); };
+  const uint32_t drain_bar = bar_base + 8u * (3 * STAGES + 4);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(full_bar(s), 1);
+      mbar_init(sfull_bar(s), 4);
+      mbar_init(empty_bar(s), 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(tfull_bar(a), 1);
+      mbar_init(tempty_bar(a), 4);
+    }
+    mbar_init(drain_bar, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+  }
+  if (warp == 1) {
+    __syncwarp();
+    tmem_alloc(smem_u32(tmem_holder), TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_holder;
+
+  const int nb_valid =
+      min(min(*args.num_post_padded / BM, args.m_blocks_cap), kSchedMaxBlocks);
+  const int total = nb_valid * args.n_tiles;
+  TileSched sched;
+  sched.nruns = sched_build(args.block_expert_ids, nb_valid, s_ids, s_runs, s_nruns);
+  sched.runs = s_runs;
+  sched.n_tiles = args.n_tiles;
+  sched.group_max = args.group_max;
+
+  if (warp == 0 && lane == 0) {
+    // ------------------------------------------------------------ producer
+    const uint64_t pol_a = l2_policy(MOE_GEMM_L2_A);
+    const uint64_t pol_b = l2_policy(MOE_GEMM_L2_B);
+    uint32_t stage = 0, phase = 0, issued_mask = 0, issued_parity = 0;
+    bool skip_first = args.never_arrive != 0;
+    for (int t = blockIdx.x; t < total; t += gridDim.x) {
+      int m_blk, n_tile;
+      sched_tile(sched, t, m_blk, n_tile);
+      const int e = s_ids[m_blk];
+      if (e < 0 || e >= args.num_experts) continue;
+      const int brow = e * args.b_rows_per_expert + n_tile * BN;
+      bool ok = true;
+      for (int kb = 0; kb < args.num_kb; ++kb) {
+        if (!mbar_wait_bounded(empty_bar(stage), phase ^ 1, abort_flag, args.limit_ns, args.err)) {
+          ok = false;
+          break;
+        }
+        if (skip_first) {
+          skip_first = false;
+        } else {
+          const uint32_t sa = smem_base + stage * STAGE_BYTES;
+          // the padded 4-bit tile occupies B_BYTES of shared memory but the
+          // copy counts the packed bytes it reads (B_BYTES / 2); expecting the
+          // padded size left the stage incomplete until the watchdog fired
+          mbar_arrive_expect_tx(full_bar(stage), A_BYTES + B_BYTES / 2);
+          tma_load_2d(sa, &tmA, full_bar(stage), kb * BK, m_blk * BM, pol_a);
+          tma_load_2d(sa + A_BYTES, &tmB, full_bar(stage), kb * BK, brow, pol_b);
+          issued_mask |= 1u << stage;
+          issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
+        }
+        if (++stage == STAGES) {
+          stage = 0;
+          phase ^= 1;
+        }
+      }
+      if (!ok) break;
+    }
+    for (int s = 0; s < STAGES; ++s)
+      if (issued_mask & (1u << s))
+        mbar_wait_bounded(full_bar(s), (issued_parity >> s) & 1, nullptr, args.limit_ns, args.err);
+  } else if (warp >= 2 && warp < 6) {
+    // ------------------------------------------------------------ scale writers
+    const int q = warp & 3;
+    const uint32_t lane_base = tmem_base + ((uint32_t)(q * 32) << 16);
+    const int kq = args.num_kb * 4;            // E8M0 bytes per weight row
+    uint32_t stage = 0, phase = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+      int m_blk, n_tile;
+      sched_tile(sched, t, m_blk, n_tile);
+      const int e = s_ids[m_blk];
+      if (e < 0 || e >= args.num_experts) continue;
+      // this lane writes rows (A) / columns (B) lane + 32 c, c = 0..3
+      const float* sa_row[4];
+      const uint32_t* sb_row[4];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const int i = lane + 32 * c;
+        sa_row[c] = args.a_scale + ((size_t)m_blk * BM + i) * args.num_kb;
+        sb_row[c] = reinterpret_cast<const uint32_t*>(
+            args.b_scale + ((size_t)e * args.b_rows_per_expert + (size_t)n_tile * BN + i) * kq);
+      }
+      float a_next[4];
+      uint32_t b_next[4];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        a_next[c] = __ldg(sa_row[c]);
+        b_next[c] = __ldg(sb_row[c]);
+      }
+      for (int kb = 0; kb < args.num_kb; ++kb) {
+        uint32_t aw[4], bw[4];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          // a power-of-two fp32 scale 2^(x-127) has biased exponent x = its E8M0 code
+          aw[c] = ((__float_as_uint(a_next[c]) >> 23) & 0xFFu) * 0x01010101u;
+          bw[c] = b_next[c];
+        }
+        if (kb + 1 < args.num_kb) {
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            a_next[c] = __ldg(sa_row[c] + kb + 1);
+            b_next[c] = __ldg(sb_row[c] + kb + 1);
+          }
+        }
+        int got = 1;
+        if (lane == 0)
+          got = mbar_wait_bounded(empty_bar(stage), phase ^ 1, abort_flag, args.limit_ns, args.err);
+        got = __shfl_sync(0xffffffffu, got, 0);
+        if (!got) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t slot = SF_COL0 + SF_SLOT * 2 * stage;
+        tmem_st_32x32b_x4(lane_base + slot, aw[0], aw[1], aw[2], aw[3]);
+        tmem_st_32x32b_x4(lane_base + slot + SF_SLOT, bw[0], bw[1], bw[2], bw[3]);
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(sfull_bar(stage));
+        if (++stage == STAGES) {
+          stage = 0;
+          phase ^= 1;
+        }
+      }
+    }
+  } else if (warp == 1 && lane == 0) {
+    // ------------------------------------------------------------ MMA issuer
+    uint32_t stage = 0, phase = 0;
+    int local = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+      int m_blk, n_tile;
+      sched_tile(sched, t, m_blk, n_tile);
+      const int e = s_ids[m_blk];
+      if (e < 0 || e >= args.num_experts) continue;
+      const int acc = local & 1;
+      const uint32_t acc_phase = (local >> 1) & 1;
+      if (!mbar_wait_bounded(tempty_bar(acc), acc_phase ^ 1, abort_flag, args.limit_ns, args.err))
+        break;
+      tc_fence_after();
+      const uint32_t d_tmem = tmem_base + acc * BN;
+      for (int kb = 0; kb < args.num_kb; ++kb) {
+        if (!mbar_wait_bounded(full_bar(stage), phase, abort_flag, args.limit_ns, args.err) ||
+            !mbar_wait_bounded(sfull_bar(stage), phase, abort_flag, args.limit_ns, args.err)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t sa = smem_base + stage * STAGE_BYTES;
+        const uint64_t adesc = sdesc_k_sw128(sa);
+        const uint64_t bdesc = sdesc_k_sw128(sa + A_BYTES);
+        const uint32_t sfa = tmem_base + SF_COL0 + SF_SLOT * 2 * stage;
+#pragma unroll
+        for (int j = 0; j < BK / 32; ++j) {
+          umma_mxf8f6f4(d_tmem, adesc + 2 * j, bdesc + 2 * j,
+                        make_idesc_block_scaled(kFmtE4M3, kFmtE2M1, BM, BN, j), sfa, sfa + SF_SLOT,
+                        (kb | j) != 0);
+        }
+        tc_commit(empty_bar(stage));
+        if (++stage == STAGES) {
+          stage = 0;
+          phase ^= 1;
+        }
+      }
+      if (!ok) break;
+      tc_commit(tfull_bar(acc));
+      ++local;
+    }
+    tc_commit(drain_bar);
+    mbar_wait_bounded(drain_bar, 0, nullptr, args.limit_ns, args.err);
+  } else if (warp >= 6) {
+    // ------------------------------------------------------------ epilogue
+    const int q = warp & 3;
+    const int row_in_tile = q * 32 + lane;
+    int local = 0;
+    for (int t = blockIdx.x; t < total; t += gridDim.x) {
+      int m_blk, n_tile;
+      sched_tile(sched, t, m_blk, n_tile);
+      const int e = s_ids[m_blk];
+      if (e < 0 || e >= args.num_experts) continue;
+      const int acc = local & 1;
+      const uint32_t acc_phase = (local >> 1) & 1;
+      int ok = 0;
+      if (lane == 0)
+        ok = mbar_wait_bounded(tfull_bar(acc), acc_phase, abort_flag, args.limit_ns, args.err);
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) break;
+      tc_fence_after();
+      const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + acc * BN;
+      const size_t row = (size_t)m_blk * BM + row_in_tile;
+      __nv_bfloat16* out_row = args.out + row * args.ldo + (size_t)n_tile * BN;
+#pragma unroll 1
+      for (int c = 0; c < BN / 32; ++c) {
+        uint32_t r[32];
+        tmem_ld_32x32b_x32(taddr + c * 32, r);
+        tmem_ld_wait();
+        uint4 pk[4];
+        __nv_bfloat16* pb = reinterpret_cast<__nv_bfloat16*>(pk);
+#pragma unroll
+        for (int j = 0; j < 32; ++j) pb[j] = __float2bfloat16_rn(__uint_as_float(r[j]));
+        uint4* dst = reinterpret_cast<uint4*>(out_row + c * 32);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) dst[j] = pk[j];
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(tempty_bar(acc));
+      ++local;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem_base, TMEM_COLS);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_ggemm_mxfp4(const void* A, const float* a_scale, int cap, int K, const void* B,
+                               const uint8_t* b_scale, int b_rows_total, int b_rows_per_expert,
+                               int n_out, const int32_t* block_expert_ids,
+                               const int32_t* num_post_padded, void* out, cudaStream_t stream) {
+  if (cap <= 0) return cudaSuccess;
+  if ((reinterpret_cast<uintptr_t>(B) & 31u) != 0 || (reinterpret_cast<uintptr_t>(b_scale) & 3u))
+    return cudaErrorInvalidValue;
+  CUtensorMap tmA, tmB;
+  if (!make_tmap_k_sw128(&tmA, A, (uint64_t)cap, (uint64_t)K, 1, 128) ||
+      !make_tmap_fp4_k_sw128(&tmB, B, (uint64_t)b_rows_total, (uint64_t)K, 128))
+    return cudaErrorInvalidValue;
+  Mx4Args a;
+  a.block_expert_ids = block_expert_ids;
+  a.num_post_padded = num_post_padded;
+  a.a_scale = a_scale;
+  a.b_scale = b_scale;
+  a.out = static_cast<__nv_bfloat16*>(out);
+  a.ldo = n_out;
+  a.num_kb = K / BK;
+  a.n_tiles = n_out / BN;
+  a.b_rows_per_expert = b_rows_per_expert;
+  a.m_blocks_cap = cap / BM;
+  a.num_experts = b_rows_total / b_rows_per_expert;
+  a.group_max = sched_group_max(K, 1);
+  watchdog_params(&a.limit_ns, &a.never_arrive);
+  a.err = dev_error_word();
+  static bool attr_done = false;
+  if (!attr_done) {
+    cudaFuncSetAttribute(k_ggemm_mxfp4, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    attr_done = true;
+  }
+  k_ggemm_mxfp4<<<num_sms(), NUM_THREADS, SMEM_BYTES, stream>>>(tmA, tmB, a);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -180,6 +180,41 @@ __device__ __forceinline__ void umma_f8(uint32_t d_tmem, uint64_t a_desc, uint64
       : "memory");
 }
 
+// Block-scaled MMA (kind::mxf8f6f4, one E8M0 scale per 32 elements along K
+// for each row of A and each column of B, read from tensor memory).
+__device__ __forceinline__ void umma_mxf8f6f4(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                              uint32_t idesc, uint32_t sfa_tmem,
+                                              uint32_t sfb_tmem, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X "
+      "[%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+      : "memory");
+}
+
+// Instruction descriptor of kind::mxf8f6f4 with block scales, both operands
+// K-major: bits 4-5 B scale-factor byte, 7-9 A format, 10-12 B format, 17-22
+// N >> 3, 23 scale format (1 = E8M0), 24-28 M >> 4, 29-30 A scale-factor byte.
+__host__ __device__ constexpr uint32_t make_idesc_block_scaled(uint32_t a_fmt, uint32_t b_fmt,
+                                                                int M, int N, uint32_t sf_id) {
+  return (sf_id << 4) | (a_fmt << 7) | (b_fmt << 10) | ((uint32_t)(N >> 3) << 17) | (1u << 23) |
+         ((uint32_t)(M >> 4) << 24) | (sf_id << 29);
+}
+constexpr uint32_t kFmtE2M1 = 5;  // kind::mxf8f6f4 operand format code for e2m1
+
+// Write four consecutive 32-bit columns of this warp's 32 TMEM lanes.
+__device__ __forceinline__ void tmem_st_32x32b_x4(uint32_t taddr, uint32_t a, uint32_t b,
+                                                  uint32_t c, uint32_t d) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1, %2, %3, %4};" ::"r"(taddr),
+               "r"(a), "r"(b), "r"(c), "r"(d)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_st_wait() {
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
 // Instruction descriptor (kind::f16 / kind::f8f6f4, dense, both operands
 // K-major, fp32 accumulator): bits 4-5 D format (1 = f32), 7-9 A format,
 // 10-12 B format, 17-22 N >> 3, 24-28 M >> 4.

@@ -54,4 +54,11 @@ cudaError_t launch_ggemm_fp8(const void* A, const float* a_scale, int cap, int K
                              int n_out, const int32_t* block_expert_ids,
                              const int32_t* num_post_padded, void* out, cudaStream_t stream);
 
+// MXFP4 (E2M1 + E8M0 per 32) weights x e4m3 activations with power-of-two
+// 1x128 scales, block-scaled tensor-core MMA (bf16 output).
+cudaError_t launch_ggemm_mxfp4(const void* A, const float* a_scale, int cap, int K, const void* B,
+                               const uint8_t* b_scale, int b_rows_total, int b_rows_per_expert,
+                               int n_out, const int32_t* block_expert_ids,
+                               const int32_t* num_post_padded, void* out, cudaStream_t stream);
+
 }  // namespace moe
