@@ -10,17 +10,27 @@
 // (tcgen05.mma kind::mxf8f6f4.block_scale.scale_vec::1X) applies them in
 // hardware and accumulates the whole K range in one fp32 TMEM accumulator.
 //
-//  * warp 0 lane 0: TMA producer, 6-stage ring; per 128-wide K block an e4m3
-//    A tile (128 x 128 B) and an E2M1 B tile loaded with the padded 4-bit TMA
-//    type (each 16 values -> 8 bytes + 8-byte gap), 128-byte swizzle;
+//  * warp 0 lane 0: TMA producer, 4-stage ring; per 128-wide K block an e4m3
+//    A tile (128 x 128 B) and an E2M1 B tile of 256 rows loaded with the
+//    padded 4-bit TMA type (each 16 values -> 8 bytes + 8-byte gap, so a row
+//    of 128 values fills one 128-byte swizzled smem row; the copy counts the
+//    packed bytes toward the barrier), 128-byte swizzle;
 //  * warps 2-5: scale writers -- per K block, the A scale operand (each row's
 //    UE8M0 exponent in all 4 bytes: one scale covers 128 = 4 x 32) and the B
 //    scale operand (the 4 E8M0 bytes of each column's 4 K chunks), written
 //    into tensor memory with tcgen05.st; byte j is picked by the scale-ID
-//    fields of MMA j;
-//  * warp 1 lane 0: four MMAs (M=128, N=128, K=32) per K block into one of two
-//    128-column accumulators; tcgen05.commit frees the stage and its scales;
-//  * warps 6-9: epilogue, tcgen05.ld -> bf16 -> global.
+//    fields of MMA j.  An operand of R rows (columns) is laid out as 32 lanes x
+//    R/32 columns -- row r at lane r % 32, column r / 32 -- repeated in every
+//    32-lane quadrant, each operand in its own 16-column-aligned slot (an
+//    odd-column scale address raised a misaligned-address fault);
+//  * warp 1 lane 0: four MMAs (M=128, N=256, K=32) per K block into the
+//    256-column accumulator (N=128 MMAs run at about half the tensor rate);
+//    tcgen05.commit frees the stage and its scales;
+//  * warps 6-9: epilogue, tcgen05.ld -> bf16 -> global.  Tensor memory holds
+//    one 256-column accumulator plus the scale slots, so the next tile's MMAs
+//    wait for the epilogue (about a microsecond against ~15 of MMA per tile).
+//  * a last column tile narrower than 256 (N % 256 == 128) is computed on
+//    whatever the weight box held above N and its upper half is not stored.
 //  * tiles walked expert by expert (tile_sched.cuh); every wait is bounded.
 #include <mutex>
 
@@ -37,22 +47,18 @@ bool make_tmap_fp4_k_sw128(CUtensorMap* map, const void* base, uint64_t rows, ui
 
 namespace {
 
-constexpr int BM = 128, BN = 128, BK = 128, STAGES = 6;
+constexpr int BM = 128, BN = 256, BK = 128, STAGES = 4;
 constexpr int A_BYTES = BM * BK;          // e4m3
 constexpr int B_BYTES = BN * BK;          // 4-bit values padded to one byte each in smem
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-constexpr int ACC_COLS = 2 * BN;          // two accumulators
-// Scale operands: 128 rows (or columns) of one 32-bit word (4 E8M0 bytes, one
-// per 32-wide K chunk) laid out as 32 lanes x 4 columns -- row r at lane
-// r % 32, column r / 32 -- and repeated in each 32-lane quadrant.  Each operand
-// gets its own 16-column-aligned slot: stage s, A at SF_COL0 + 32 s, B at +16.
-constexpr int SF_COL0 = ACC_COLS;
-constexpr int SF_SLOT = 16;
+constexpr int TX_BYTES = A_BYTES + B_BYTES / 2;   // bytes the copies of one stage count
+constexpr int SF_COL0 = BN;               // scale slots after the accumulator
+constexpr int SF_SLOT = 16;               // stage s: A at SF_COL0 + 32 s, B at + 16
 constexpr int TMEM_COLS = 512;
 constexpr int NUM_THREADS = 320;
 constexpr int SCHED_BYTES = 16 + 4 * kSchedMaxRuns + 4 * kSchedMaxBlocks;
 constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + 256 + SCHED_BYTES;
-static_assert(SF_COL0 + SF_SLOT * (2 * STAGES - 1) + 4 <= TMEM_COLS, "tensor memory budget");
+static_assert(SF_COL0 + SF_SLOT * (2 * STAGES - 1) + BN / 32 <= TMEM_COLS, "tensor memory");
 
 struct Mx4Args {
   const int32_t* block_expert_ids;
@@ -62,7 +68,7 @@ struct Mx4Args {
   __nv_bfloat16* out;       // [cap, N]
   int ldo;                  // N
   int num_kb;               // K / 128
-  int n_tiles;              // N / 128
+  int n_tiles;              // ceil(N / 256)
   int b_rows_per_expert;    // N
   int m_blocks_cap;
   int num_experts;
@@ -79,8 +85,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
-  // full[S], sfull[S], empty[S], tfull[2], tempty[2], drain
-  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 3 * STAGES + 5);
+  // full[S], sfull[S], empty[S], tfull, tempty, drain
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 3 * STAGES + 3);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
   int* s_nruns = reinterpret_cast<int*>(smem + STAGES * STAGE_BYTES + 256);
   int* s_runs = s_nruns + 4;
@@ -92,9 +98,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   auto full_bar = [&](int s) { return bar_base + 8u * s; };
   auto sfull_bar = [&](int s) { return bar_base + 8u * (STAGES + s); };
   auto empty_bar = [&](int s) { return bar_base + 8u * (2 * STAGES + s); };
-  auto tfull_bar = [&](int a) { return bar_base + 8u * (3 * STAGES + a); };
-  auto tempty_bar = [&](int a) { return bar_base + 8u * (3 * STAGES + 2 + a); };
-  const uint32_t drain_bar = bar_base + 8u * (3 * STAGES + 4);
+  const uint32_t tfull_bar = bar_base + 8u * (3 * STAGES);
+  const uint32_t tempty_bar = bar_base + 8u * (3 * STAGES + 1);
+  const uint32_t drain_bar = bar_base + 8u * (3 * STAGES + 2);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -102,10 +108,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       mbar_init(sfull_bar(s), 4);
       mbar_init(empty_bar(s), 1);
     }
-    for (int a = 0; a < 2; ++a) {
-      mbar_init(tfull_bar(a), 1);
-      mbar_init(tempty_bar(a), 4);
-    }
+    mbar_init(tfull_bar, 1);
+    mbar_init(tempty_bar, 4);
     mbar_init(drain_bar, 1);
     *abort_flag = 0;
     fence_barrier_init();
@@ -132,6 +136,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   sched.runs = s_runs;
   sched.n_tiles = args.n_tiles;
   sched.group_max = args.group_max;
+  const int N = args.b_rows_per_expert;
 
   if (warp == 0 && lane == 0) {
     // ------------------------------------------------------------ producer
@@ -144,7 +149,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       sched_tile(sched, t, m_blk, n_tile);
       const int e = s_ids[m_blk];
       if (e < 0 || e >= args.num_experts) continue;
-      const int brow = e * args.b_rows_per_expert + n_tile * BN;
+      const int brow = e * N + n_tile * BN;
       bool ok = true;
       for (int kb = 0; kb < args.num_kb; ++kb) {
         if (!mbar_wait_bounded(empty_bar(stage), phase ^ 1, abort_flag, args.limit_ns, args.err)) {
@@ -155,12 +160,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           skip_first = false;
         } else {
           const uint32_t sa = smem_base + stage * STAGE_BYTES;
-          // the padded 4-bit tile occupies B_BYTES of shared memory but the
-          // copy counts the packed bytes it reads (B_BYTES / 2); expecting the
-          // padded size left the stage incomplete until the watchdog fired
-          mbar_arrive_expect_tx(full_bar(stage), A_BYTES + B_BYTES / 2);
+          mbar_arrive_expect_tx(full_bar(stage), TX_BYTES);
           tma_load_2d(sa, &tmA, full_bar(stage), kb * BK, m_blk * BM, pol_a);
           tma_load_2d(sa + A_BYTES, &tmB, full_bar(stage), kb * BK, brow, pol_b);
+          tma_load_2d(sa + A_BYTES + B_BYTES / 2, &tmB, full_bar(stage), kb * BK, brow + 128,
+                      pol_b);
           issued_mask |= 1u << stage;
           issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
         }
@@ -179,6 +183,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const int q = warp & 3;
     const uint32_t lane_base = tmem_base + ((uint32_t)(q * 32) << 16);
     const int kq = args.num_kb * 4;            // E8M0 bytes per weight row
+    const bool vec = (args.num_kb & 3) == 0;   // rows 16-byte aligned: vector loads
     uint32_t stage = 0, phase = 0;
     bool ok = true;
     for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
@@ -186,58 +191,87 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       sched_tile(sched, t, m_blk, n_tile);
       const int e = s_ids[m_blk];
       if (e < 0 || e >= args.num_experts) continue;
-      // this lane writes rows (A) / columns (B) lane + 32 c, c = 0..3
-      const float* sa_row[4];
-      const uint32_t* sb_row[4];
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        const int i = lane + 32 * c;
-        sa_row[c] = args.a_scale + ((size_t)m_blk * BM + i) * args.num_kb;
-        sb_row[c] = reinterpret_cast<const uint32_t*>(
-            args.b_scale + ((size_t)e * args.b_rows_per_expert + (size_t)n_tile * BN + i) * kq);
-      }
-      float a_next[4];
-      uint32_t b_next[4];
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        a_next[c] = __ldg(sa_row[c]);
-        b_next[c] = __ldg(sb_row[c]);
-      }
-      for (int kb = 0; kb < args.num_kb; ++kb) {
-        uint32_t aw[4], bw[4];
+      // this lane writes rows lane + 32 c of A (c < 4) and columns lane + 32 c
+      // of B (c < 8); B columns past N (ragged last tile) read nothing
+      const float* sa_base = args.a_scale + ((size_t)m_blk * BM + lane) * args.num_kb;
+      const size_t sa_step = (size_t)32 * args.num_kb;             // floats per 32 rows
+      const uint8_t* sb_base = args.b_scale + ((size_t)e * N + (size_t)n_tile * BN + lane) * kq;
+      const size_t sb_step = (size_t)32 * kq;                      // bytes per 32 rows
+      const int n_valid = N - n_tile * BN - lane;                  // B column c valid if 32c < this
+      // scales of 4 K blocks per load, one group of 4 in flight ahead
+      auto load_group = [&](int g, float4 (&A)[4], uint4 (&B)[8]) {
+        const int n = args.num_kb - g;
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
-          // a power-of-two fp32 scale 2^(x-127) has biased exponent x = its E8M0 code
-          aw[c] = ((__float_as_uint(a_next[c]) >> 23) & 0xFFu) * 0x01010101u;
-          bw[c] = b_next[c];
-        }
-        if (kb + 1 < args.num_kb) {
-#pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            a_next[c] = __ldg(sa_row[c] + kb + 1);
-            b_next[c] = __ldg(sb_row[c] + kb + 1);
+          const float* pa = sa_base + c * sa_step + g;
+          if (vec) {
+            A[c] = __ldg(reinterpret_cast<const float4*>(pa));
+          } else {
+            A[c] = make_float4(__ldg(pa), n > 1 ? __ldg(pa + 1) : 1.0f,
+                               n > 2 ? __ldg(pa + 2) : 1.0f, n > 3 ? __ldg(pa + 3) : 1.0f);
           }
         }
-        int got = 1;
-        if (lane == 0)
-          got = mbar_wait_bounded(empty_bar(stage), phase ^ 1, abort_flag, args.limit_ns, args.err);
-        got = __shfl_sync(0xffffffffu, got, 0);
-        if (!got) {
-          ok = false;
-          break;
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          const uint32_t* pb = reinterpret_cast<const uint32_t*>(sb_base + c * sb_step) + g;
+          if (32 * c >= n_valid) {
+            B[c] = make_uint4(0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu);
+          } else if (vec) {
+            B[c] = __ldg(reinterpret_cast<const uint4*>(pb));
+          } else {
+            B[c] = make_uint4(__ldg(pb), n > 1 ? __ldg(pb + 1) : 0u, n > 2 ? __ldg(pb + 2) : 0u,
+                              n > 3 ? __ldg(pb + 3) : 0u);
+          }
         }
-        tc_fence_after();
-        const uint32_t slot = SF_COL0 + SF_SLOT * 2 * stage;
-        tmem_st_32x32b_x4(lane_base + slot, aw[0], aw[1], aw[2], aw[3]);
-        tmem_st_32x32b_x4(lane_base + slot + SF_SLOT, bw[0], bw[1], bw[2], bw[3]);
-        tmem_st_wait();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(sfull_bar(stage));
-        if (++stage == STAGES) {
-          stage = 0;
-          phase ^= 1;
+      };
+      float4 a_cur[4], a_nxt[4];
+      uint4 b_cur[8], b_nxt[8];
+      load_group(0, a_cur, b_cur);
+      if (args.num_kb > 4) load_group(4, a_nxt, b_nxt);
+      for (int kb0 = 0; kb0 < args.num_kb && ok; kb0 += 4) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int kb = kb0 + j;
+          if (kb >= args.num_kb) break;
+          uint32_t aw[4], bw[8];
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            const float av = j == 0 ? a_cur[c].x : j == 1 ? a_cur[c].y : j == 2 ? a_cur[c].z
+                                                                                : a_cur[c].w;
+            // a power-of-two fp32 scale 2^(x-127) has biased exponent x = its E8M0 code
+            aw[c] = ((__float_as_uint(av) >> 23) & 0xFFu) * 0x01010101u;
+          }
+#pragma unroll
+          for (int c = 0; c < 8; ++c)
+            bw[c] = j == 0 ? b_cur[c].x : j == 1 ? b_cur[c].y : j == 2 ? b_cur[c].z : b_cur[c].w;
+          int got = 1;
+          if (lane == 0)
+            got = mbar_wait_bounded(empty_bar(stage), phase ^ 1, abort_flag, args.limit_ns,
+                                    args.err);
+          got = __shfl_sync(0xffffffffu, got, 0);
+          if (!got) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t slot = SF_COL0 + SF_SLOT * 2 * stage;
+          tmem_st_32x32b_x4(lane_base + slot, aw[0], aw[1], aw[2], aw[3]);
+          tmem_st_32x32b_x4(lane_base + slot + SF_SLOT, bw[0], bw[1], bw[2], bw[3]);
+          tmem_st_32x32b_x4(lane_base + slot + SF_SLOT + 4, bw[4], bw[5], bw[6], bw[7]);
+          tmem_st_wait();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(sfull_bar(stage));
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1;
+          }
         }
+#pragma unroll
+        for (int c = 0; c < 4; ++c) a_cur[c] = a_nxt[c];
+#pragma unroll
+        for (int c = 0; c < 8; ++c) b_cur[c] = b_nxt[c];
+        if (kb0 + 8 < args.num_kb) load_group(kb0 + 8, a_nxt, b_nxt);
       }
     }
   } else if (warp == 1 && lane == 0) {
@@ -250,12 +284,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       sched_tile(sched, t, m_blk, n_tile);
       const int e = s_ids[m_blk];
       if (e < 0 || e >= args.num_experts) continue;
-      const int acc = local & 1;
-      const uint32_t acc_phase = (local >> 1) & 1;
-      if (!mbar_wait_bounded(tempty_bar(acc), acc_phase ^ 1, abort_flag, args.limit_ns, args.err))
+      if (!mbar_wait_bounded(tempty_bar, (local & 1) ^ 1, abort_flag, args.limit_ns, args.err))
         break;
       tc_fence_after();
-      const uint32_t d_tmem = tmem_base + acc * BN;
       for (int kb = 0; kb < args.num_kb; ++kb) {
         if (!mbar_wait_bounded(full_bar(stage), phase, abort_flag, args.limit_ns, args.err) ||
             !mbar_wait_bounded(sfull_bar(stage), phase, abort_flag, args.limit_ns, args.err)) {
@@ -269,9 +300,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const uint32_t sfa = tmem_base + SF_COL0 + SF_SLOT * 2 * stage;
 #pragma unroll
         for (int j = 0; j < BK / 32; ++j) {
-          umma_mxf8f6f4(d_tmem, adesc + 2 * j, bdesc + 2 * j,
-                        make_idesc_block_scaled(kFmtE4M3, kFmtE2M1, BM, BN, j), sfa, sfa + SF_SLOT,
-                        (kb | j) != 0);
+          umma_mxf8f6f4(tmem_base, adesc + 2 * j, bdesc + 2 * j,
+                        make_idesc_block_scaled(kFmtE4M3, kFmtE2M1, BM, BN, j), sfa,
+                        sfa + SF_SLOT, (kb | j) != 0);
         }
         tc_commit(empty_bar(stage));
         if (++stage == STAGES) {
@@ -280,7 +311,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
       }
       if (!ok) break;
-      tc_commit(tfull_bar(acc));
+      tc_commit(tfull_bar);
       ++local;
     }
     tc_commit(drain_bar);
@@ -295,22 +326,22 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       sched_tile(sched, t, m_blk, n_tile);
       const int e = s_ids[m_blk];
       if (e < 0 || e >= args.num_experts) continue;
-      const int acc = local & 1;
-      const uint32_t acc_phase = (local >> 1) & 1;
       int ok = 0;
       if (lane == 0)
-        ok = mbar_wait_bounded(tfull_bar(acc), acc_phase, abort_flag, args.limit_ns, args.err);
+        ok = mbar_wait_bounded(tfull_bar, local & 1, abort_flag, args.limit_ns, args.err);
       ok = __shfl_sync(0xffffffffu, ok, 0);
       if (!ok) break;
       tc_fence_after();
-      const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + acc * BN;
+      const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16);
       const size_t row = (size_t)m_blk * BM + row_in_tile;
       __nv_bfloat16* out_row = args.out + row * args.ldo + (size_t)n_tile * BN;
+      const int ncols = min(BN, N - n_tile * BN);    // 256, or 128 on a ragged last tile
 #pragma unroll 1
       for (int c = 0; c < BN / 32; ++c) {
         uint32_t r[32];
         tmem_ld_32x32b_x32(taddr + c * 32, r);
         tmem_ld_wait();
+        if (c * 32 >= ncols) continue;
         uint4 pk[4];
         __nv_bfloat16* pb = reinterpret_cast<__nv_bfloat16*>(pk);
 #pragma unroll
@@ -321,7 +352,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(tempty_bar(acc));
+      if (lane == 0) mbar_arrive(tempty_bar);
       ++local;
     }
   }
@@ -356,7 +387,7 @@ cudaError_t launch_ggemm_mxfp4(const void* A, const float* a_scale, int cap, int
   a.out = static_cast<__nv_bfloat16*>(out);
   a.ldo = n_out;
   a.num_kb = K / BK;
-  a.n_tiles = n_out / BN;
+  a.n_tiles = (n_out + BN - 1) / BN;
   a.b_rows_per_expert = b_rows_per_expert;
   a.m_blocks_cap = cap / BM;
   a.num_experts = b_rows_total / b_rows_per_expert;
