@@ -9,73 +9,115 @@
 // skipped) -- the same result as weighting then moe_sum on page 1 (§4,
 // TopKWeightAndReduceContiguous).
 //
-// Both are HBM-bound elementwise/gather kernels: 16-byte vector loads and
-// stores, one CTA per row (token), grid-stride over rows, no shared memory.
+// Both are HBM-bound: one warp per row (token), grid-stride, 16-byte vector
+// loads issued in batches ahead of the arithmetic so each warp keeps several
+// KB in flight; the reduce issues all k gathers of a vector pair before it
+// accumulates.
 #include "moe_common.cuh"
 #include "moe_internal.h"
 
 namespace moe {
 
+constexpr int ACT_U = 4;             // 16-byte vectors of g (and of u) per lane in flight
+constexpr int ACT_THREADS = 256;
+
+// SiLU(g) with the fast exponential; z tolerates its few-ulp error.
+__device__ __forceinline__ float silu_fast(float g) { return __fdividef(g, 1.0f + __expf(-g)); }
+
 // z[row, :] = bf16(SiLU(bf16 g) * bf16 u) for rows below num_post_padded.
-__global__ void __launch_bounds__(128)
+__global__ void __launch_bounds__(ACT_THREADS)
     k_act_mul_bf16(const __nv_bfloat16* __restrict__ h1, int I, const int32_t* __restrict__ npp,
                    __nv_bfloat16* __restrict__ z) {
+  const int lane = threadIdx.x & 31;
+  const int wpc = blockDim.x >> 5;
   const int rows = *npp;
   const int nv = I / 8;
-  for (int row = blockIdx.x; row < rows; row += gridDim.x) {
+  for (int row = blockIdx.x * wpc + (threadIdx.x >> 5); row < rows; row += gridDim.x * wpc) {
     const uint4* g4 = reinterpret_cast<const uint4*>(h1 + (size_t)row * 2 * I);
     const uint4* u4 = reinterpret_cast<const uint4*>(h1 + (size_t)row * 2 * I + I);
     uint4* z4 = reinterpret_cast<uint4*>(z + (size_t)row * I);
-    for (int v = threadIdx.x; v < nv; v += blockDim.x) {
-      uint4 gv = __ldg(g4 + v), uv = __ldg(u4 + v), out;
-      const __nv_bfloat16* gb = reinterpret_cast<const __nv_bfloat16*>(&gv);
-      const __nv_bfloat16* ub = reinterpret_cast<const __nv_bfloat16*>(&uv);
-      __nv_bfloat16* ob = reinterpret_cast<__nv_bfloat16*>(&out);
+    for (int base = 0; base < nv; base += 32 * ACT_U) {
+      uint4 gv[ACT_U], uv[ACT_U];
 #pragma unroll
-      for (int j = 0; j < 8; ++j)
-        ob[j] = __float2bfloat16_rn(silu_f32(__bfloat162float(gb[j])) * __bfloat162float(ub[j]));
-      z4[v] = out;
+      for (int k = 0; k < ACT_U; ++k) {
+        const int v = base + 32 * k + lane;
+        if (v < nv) {
+          gv[k] = __ldg(g4 + v);
+          uv[k] = __ldg(u4 + v);
+        }
+      }
+#pragma unroll
+      for (int k = 0; k < ACT_U; ++k) {
+        const int v = base + 32 * k + lane;
+        if (v >= nv) continue;
+        const __nv_bfloat16* gb = reinterpret_cast<const __nv_bfloat16*>(&gv[k]);
+        const __nv_bfloat16* ub = reinterpret_cast<const __nv_bfloat16*>(&uv[k]);
+        uint4 out;
+        __nv_bfloat16* ob = reinterpret_cast<__nv_bfloat16*>(&out);
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+          ob[j] = __float2bfloat16_rn(silu_fast(__bfloat162float(gb[j])) * __bfloat162float(ub[j]));
+        z4[v] = out;
+      }
     }
   }
 }
 
-// Quantised variant: z in fp32, then per 1x128 group amax -> scale -> e4m3.
-__global__ void __launch_bounds__(128)
+// Quantised variant: z in fp32, then per 1x128 group (one half-warp) amax ->
+// scale -> e4m3 with one reciprocal per group.
+__global__ void __launch_bounds__(ACT_THREADS)
     k_act_mul_fp8(const __nv_bfloat16* __restrict__ h1, int I, const int32_t* __restrict__ npp,
                   uint8_t* __restrict__ zq, float* __restrict__ zs, int ue8m0) {
+  const int lane = threadIdx.x & 31;
+  const int wpc = blockDim.x >> 5;
   const int rows = *npp;
-  const int nv = I / 8;   // multiple of 16: a 16-lane group is one 1x128 group
-  for (int row = blockIdx.x; row < rows; row += gridDim.x) {
+  const int nv = I / 8;   // multiple of 16: a half-warp is one 1x128 group
+  for (int row = blockIdx.x * wpc + (threadIdx.x >> 5); row < rows; row += gridDim.x * wpc) {
     const uint4* g4 = reinterpret_cast<const uint4*>(h1 + (size_t)row * 2 * I);
     const uint4* u4 = reinterpret_cast<const uint4*>(h1 + (size_t)row * 2 * I + I);
     uint2* q2 = reinterpret_cast<uint2*>(zq + (size_t)row * I);
     float* srow = zs + (size_t)row * (I / 128);
-    for (int base = 0; base < nv; base += blockDim.x) {
-      const int v = base + threadIdx.x;
-      const bool act = v < nv;
-      float f[8];
-      float amax = 0.0f;
-      if (act) {
-        uint4 gv = __ldg(g4 + v), uv = __ldg(u4 + v);
-        const __nv_bfloat16* gb = reinterpret_cast<const __nv_bfloat16*>(&gv);
-        const __nv_bfloat16* ub = reinterpret_cast<const __nv_bfloat16*>(&uv);
+    for (int base = 0; base < nv; base += 32 * ACT_U) {
+      uint4 gv[ACT_U], uv[ACT_U];
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          f[j] = silu_f32(__bfloat162float(gb[j])) * __bfloat162float(ub[j]);
-          amax = fmaxf(amax, fabsf(f[j]));
+      for (int k = 0; k < ACT_U; ++k) {
+        const int v = base + 32 * k + lane;
+        if (v < nv) {
+          gv[k] = __ldg(g4 + v);
+          uv[k] = __ldg(u4 + v);
         }
       }
 #pragma unroll
-      for (int o = 8; o >= 1; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-      if (act) {
-        const float s = act_scale(amax, ue8m0 != 0);
-        uint32_t lo = 0, hi = 0;
+      for (int k = 0; k < ACT_U; ++k) {
+        const int v = base + 32 * k + lane;
+        const bool act = v < nv;
+        float f[8];
+        float amax = 0.0f;
+        if (act) {
+          const __nv_bfloat16* gb = reinterpret_cast<const __nv_bfloat16*>(&gv[k]);
+          const __nv_bfloat16* ub = reinterpret_cast<const __nv_bfloat16*>(&uv[k]);
 #pragma unroll
-        for (int j = 0; j < 4; ++j) lo |= (uint32_t)f32_to_e4m3(__fdiv_rn(f[j], s)) << (8 * j);
+          for (int j = 0; j < 8; ++j) {
+            f[j] = silu_fast(__bfloat162float(gb[j])) * __bfloat162float(ub[j]);
+            amax = fmaxf(amax, fabsf(f[j]));
+          }
+        }
 #pragma unroll
-        for (int j = 0; j < 4; ++j) hi |= (uint32_t)f32_to_e4m3(__fdiv_rn(f[4 + j], s)) << (8 * j);
-        q2[v] = make_uint2(lo, hi);
-        if ((v & 15) == 0) srow[v >> 4] = s;
+        for (int o = 8; o >= 1; o >>= 1)
+          amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+        if (act) {
+          const float s = act_scale(amax, ue8m0 != 0);
+          const float r = __frcp_rn(s);
+          uint32_t lo = 0, hi = 0;
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            lo |= (uint32_t)f32_to_e4m3(div_rn_shared(f[j], s, r)) << (8 * j);
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            hi |= (uint32_t)f32_to_e4m3(div_rn_shared(f[4 + j], s, r)) << (8 * j);
+          q2[v] = make_uint2(lo, hi);
+          if ((v & 15) == 0) srow[v >> 4] = s;
+        }
       }
     }
   }
@@ -84,43 +126,102 @@ __global__ void __launch_bounds__(128)
 cudaError_t launch_act_mul(const void* h1, int I, const int32_t* num_post_padded, void* z,
                            float* z_scale, bool ue8m0, int cap, cudaStream_t stream) {
   if (cap <= 0) return cudaSuccess;
-  const int grid = min(cap, num_sms() * 8);
+  const int wpc = ACT_THREADS / 32;
+  const int grid = min((cap + wpc - 1) / wpc, num_sms() * 8);
   if (z_scale == nullptr) {
-    k_act_mul_bf16<<<grid, 128, 0, stream>>>(static_cast<const __nv_bfloat16*>(h1), I,
-                                             num_post_padded, static_cast<__nv_bfloat16*>(z));
+    k_act_mul_bf16<<<grid, ACT_THREADS, 0, stream>>>(static_cast<const __nv_bfloat16*>(h1), I,
+                                                     num_post_padded,
+                                                     static_cast<__nv_bfloat16*>(z));
   } else {
-    k_act_mul_fp8<<<grid, 128, 0, stream>>>(static_cast<const __nv_bfloat16*>(h1), I,
-                                            num_post_padded, static_cast<uint8_t*>(z), z_scale,
-                                            ue8m0);
+    k_act_mul_fp8<<<grid, ACT_THREADS, 0, stream>>>(static_cast<const __nv_bfloat16*>(h1), I,
+                                                    num_post_padded, static_cast<uint8_t*>(z),
+                                                    z_scale, ue8m0);
   }
   return cudaGetLastError();
 }
 
 // y[t, :] = bf16( sum_i w[t,i] * y2[inv_perm[t,i], :] ), fp32, slot order.
-__global__ void __launch_bounds__(128)
+// One warp per token; its k row indices and weights are held by lanes 0..k-1
+// and broadcast by shuffles.  Per lane, two vectors x k gathers are issued
+// before any accumulation (KMAX slots unrolled, the rest in a loop).
+constexpr int REDUCE_THREADS = 256;
+
+template <int KMAX>
+__global__ void __launch_bounds__(REDUCE_THREADS)
     k_unpermute_reduce(const __nv_bfloat16* __restrict__ y2, int H, int M, int topk,
                        const int32_t* __restrict__ inv_perm, const float* __restrict__ w,
                        int unit_weights, __nv_bfloat16* __restrict__ y) {
+  const int lane = threadIdx.x & 31;
+  const int wpc = blockDim.x >> 5;
   const int nv = H / 8;
-  for (int t = blockIdx.x; t < M; t += gridDim.x) {
-    for (int v = threadIdx.x; v < nv; v += blockDim.x) {
-      float acc[8];
+  for (int t = blockIdx.x * wpc + (threadIdx.x >> 5); t < M; t += gridDim.x * wpc) {
+    int my_p = -1;
+    float my_w = 0.0f;
+    if (lane < topk) {
+      my_p = __ldg(inv_perm + (size_t)t * topk + lane);
+      my_w = unit_weights ? 1.0f : __ldg(w + (size_t)t * topk + lane);
+    }
+    int p[KMAX];
+    float wi[KMAX];
 #pragma unroll
-      for (int j = 0; j < 8; ++j) acc[j] = 0.0f;
-      for (int i = 0; i < topk; ++i) {
-        const int p = __ldg(inv_perm + (size_t)t * topk + i);
-        if (p < 0) continue;
-        const float wi = unit_weights ? 1.0f : __ldg(w + (size_t)t * topk + i);
-        uint4 u = __ldg(reinterpret_cast<const uint4*>(y2 + (size_t)p * H) + v);
-        const __nv_bfloat16* b = reinterpret_cast<const __nv_bfloat16*>(&u);
+    for (int i = 0; i < KMAX; ++i) {
+      p[i] = __shfl_sync(0xffffffffu, my_p, i);
+      wi[i] = __shfl_sync(0xffffffffu, my_w, i);
+    }
+    uint4* yt = reinterpret_cast<uint4*>(y + (size_t)t * H);
+    for (int v0 = lane; v0 < nv; v0 += 64) {
+      const int v1 = v0 + 32;
+      const bool has1 = v1 < nv;
+      uint4 a[KMAX], b[KMAX];
 #pragma unroll
-        for (int j = 0; j < 8; ++j) acc[j] = fmaf(wi, __bfloat162float(b[j]), acc[j]);
+      for (int i = 0; i < KMAX; ++i) {
+        if (i < topk && p[i] >= 0) {
+          const uint4* row = reinterpret_cast<const uint4*>(y2 + (size_t)p[i] * H);
+          a[i] = __ldg(row + v0);
+          if (has1) b[i] = __ldg(row + v1);
+        }
       }
-      uint4 out;
-      __nv_bfloat16* ob = reinterpret_cast<__nv_bfloat16*>(&out);
+      float acc0[8], acc1[8];
 #pragma unroll
-      for (int j = 0; j < 8; ++j) ob[j] = __float2bfloat16_rn(acc[j]);
-      reinterpret_cast<uint4*>(y + (size_t)t * H)[v] = out;
+      for (int j = 0; j < 8; ++j) acc0[j] = acc1[j] = 0.0f;
+#pragma unroll
+      for (int i = 0; i < KMAX; ++i) {
+        if (i < topk && p[i] >= 0) {
+          const __nv_bfloat16* ab = reinterpret_cast<const __nv_bfloat16*>(&a[i]);
+          const __nv_bfloat16* bb = reinterpret_cast<const __nv_bfloat16*>(&b[i]);
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            acc0[j] = fmaf(wi[i], __bfloat162float(ab[j]), acc0[j]);
+            if (has1) acc1[j] = fmaf(wi[i], __bfloat162float(bb[j]), acc1[j]);
+          }
+        }
+      }
+      // slots beyond KMAX (top-k up to 16): one at a time, same slot order;
+      // lanes may have left the vector loop, so no shuffles here
+      for (int i = KMAX; i < topk; ++i) {
+        const int pi = __ldg(inv_perm + (size_t)t * topk + i);
+        const float wv = unit_weights ? 1.0f : __ldg(w + (size_t)t * topk + i);
+        if (pi < 0) continue;
+        const uint4* row = reinterpret_cast<const uint4*>(y2 + (size_t)pi * H);
+        uint4 ua = __ldg(row + v0), ub = has1 ? __ldg(row + v1) : make_uint4(0, 0, 0, 0);
+        const __nv_bfloat16* ab = reinterpret_cast<const __nv_bfloat16*>(&ua);
+        const __nv_bfloat16* bb = reinterpret_cast<const __nv_bfloat16*>(&ub);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          acc0[j] = fmaf(wv, __bfloat162float(ab[j]), acc0[j]);
+          acc1[j] = fmaf(wv, __bfloat162float(bb[j]), acc1[j]);
+        }
+      }
+      uint4 o0, o1;
+      __nv_bfloat16* ob0 = reinterpret_cast<__nv_bfloat16*>(&o0);
+      __nv_bfloat16* ob1 = reinterpret_cast<__nv_bfloat16*>(&o1);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        ob0[j] = __float2bfloat16_rn(acc0[j]);
+        ob1[j] = __float2bfloat16_rn(acc1[j]);
+      }
+      yt[v0] = o0;
+      if (has1) yt[v1] = o1;
     }
   }
 }
@@ -129,10 +230,20 @@ cudaError_t launch_unpermute_reduce(const void* y2, int H, int M, int topk,
                                     const int32_t* inv_perm, const float* topk_weights,
                                     bool unit_weights, void* y, cudaStream_t stream) {
   if (M <= 0) return cudaSuccess;
-  const int grid = min(M, num_sms() * 8);
-  k_unpermute_reduce<<<grid, 128, 0, stream>>>(static_cast<const __nv_bfloat16*>(y2), H, M, topk,
-                                               inv_perm, topk_weights, unit_weights ? 1 : 0,
-                                               static_cast<__nv_bfloat16*>(y));
+  const int wpc = REDUCE_THREADS / 32;
+  const int grid = min((M + wpc - 1) / wpc, num_sms() * 8);
+  const auto* yy = static_cast<const __nv_bfloat16*>(y2);
+  auto* out = static_cast<__nv_bfloat16*>(y);
+  const int uw = unit_weights ? 1 : 0;
+  if (topk <= 2)
+    k_unpermute_reduce<2><<<grid, REDUCE_THREADS, 0, stream>>>(yy, H, M, topk, inv_perm,
+                                                               topk_weights, uw, out);
+  else if (topk <= 4)
+    k_unpermute_reduce<4><<<grid, REDUCE_THREADS, 0, stream>>>(yy, H, M, topk, inv_perm,
+                                                               topk_weights, uw, out);
+  else
+    k_unpermute_reduce<8><<<grid, REDUCE_THREADS, 0, stream>>>(yy, H, M, topk, inv_perm,
+                                                               topk_weights, uw, out);
   return cudaGetLastError();
 }
 

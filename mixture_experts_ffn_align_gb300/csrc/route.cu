@@ -17,8 +17,9 @@
 //   k_route_scatter one warp per segment: __match_any_sync ranks items of the
 //                   same expert within 32-item chunks; a per-warp running
 //                   count in shared memory carries the rank across chunks.
-// The data gather (k_permute_*) runs per destination row with 16-byte vector
-// loads and stores; the FP8 variant fuses the dynamic 1x128 quantisation.
+// The data gather (k_permute_*) runs one warp per destination row with
+// 16-byte vector loads batched ahead of the stores; the FP8 variant fuses the
+// dynamic 1x128 quantisation.
 #include "moe_common.cuh"
 #include "moe_internal.h"
 
@@ -164,50 +165,69 @@ cudaError_t launch_route(const int32_t* topk_ids, int R, int E, int block_size, 
 }
 
 // ------------------------------------------------------------ data permute
-// One CTA (128 threads) per destination row, grid-stride over the used rows.
-__global__ void __launch_bounds__(128)
+// One warp per destination row (grid-stride over the used rows); each lane
+// issues PERMUTE_U 16-byte loads before it stores any, so a warp keeps
+// PERMUTE_U * 512 B of the row in flight.
+constexpr int PERMUTE_U = 8;
+constexpr int PERMUTE_THREADS = 256;
+
+__global__ void __launch_bounds__(PERMUTE_THREADS)
     k_permute_bf16(const __nv_bfloat16* __restrict__ x, int H, int topk, int R,
                    const int32_t* __restrict__ sorted_ids, const int32_t* __restrict__ npp,
                    const float* __restrict__ row_weights, __nv_bfloat16* __restrict__ xp) {
+  const int lane = threadIdx.x & 31;
+  const int wpc = blockDim.x >> 5;
   const int rows = *npp;
   const int nv = H / 8;
-  for (int row = blockIdx.x; row < rows; row += gridDim.x) {
+  for (int row = blockIdx.x * wpc + (threadIdx.x >> 5); row < rows; row += gridDim.x * wpc) {
     const int sid = sorted_ids[row];
     uint4* dst = reinterpret_cast<uint4*>(xp + (size_t)row * H);
     if (sid >= R) {
-      for (int v = threadIdx.x; v < nv; v += blockDim.x) dst[v] = make_uint4(0, 0, 0, 0);
+      for (int v = lane; v < nv; v += 32) dst[v] = make_uint4(0, 0, 0, 0);
       continue;
     }
     const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)(sid / topk) * H);
-    if (row_weights == nullptr) {
-      for (int v = threadIdx.x; v < nv; v += blockDim.x) dst[v] = __ldg(src + v);
-    } else {
-      const float w = row_weights[sid];
-      for (int v = threadIdx.x; v < nv; v += blockDim.x) {
-        uint4 u = __ldg(src + v);
-        __nv_bfloat16* b = reinterpret_cast<__nv_bfloat16*>(&u);
+    const float w = row_weights ? row_weights[sid] : 1.0f;
+    for (int base = 0; base < nv; base += 32 * PERMUTE_U) {
+      uint4 buf[PERMUTE_U];
 #pragma unroll
-        for (int j = 0; j < 8; ++j) b[j] = __float2bfloat16_rn(__bfloat162float(b[j]) * w);
-        dst[v] = u;
+      for (int u = 0; u < PERMUTE_U; ++u) {
+        const int v = base + 32 * u + lane;
+        if (v < nv) buf[u] = __ldg(src + v);
+      }
+#pragma unroll
+      for (int u = 0; u < PERMUTE_U; ++u) {
+        const int v = base + 32 * u + lane;
+        if (v >= nv) continue;
+        if (row_weights) {
+          __nv_bfloat16* b = reinterpret_cast<__nv_bfloat16*>(&buf[u]);
+#pragma unroll
+          for (int j = 0; j < 8; ++j) b[j] = __float2bfloat16_rn(__bfloat162float(b[j]) * w);
+        }
+        dst[v] = buf[u];
       }
     }
   }
 }
 
-// FP8 variant: 16 threads per 128-element group, 8 elements per thread.
-__global__ void __launch_bounds__(128)
+// FP8 variant: each half-warp (16 lanes x 8 values) is one 1x128 group; the
+// lanes of a group share one scale, so the quotient uses one reciprocal and
+// a correction step instead of a division per value.
+__global__ void __launch_bounds__(PERMUTE_THREADS)
     k_permute_fp8(const __nv_bfloat16* __restrict__ x, int H, int topk, int R,
                   const int32_t* __restrict__ sorted_ids, const int32_t* __restrict__ npp,
                   const float* __restrict__ row_weights, uint8_t* __restrict__ xq,
                   float* __restrict__ xs, int ue8m0) {
+  const int lane = threadIdx.x & 31;
+  const int wpc = blockDim.x >> 5;
   const int rows = *npp;
-  const int nv = H / 8;          // 8-element vectors per row; multiple of 16
-  for (int row = blockIdx.x; row < rows; row += gridDim.x) {
+  const int nv = H / 8;          // 8-element vectors per row; a multiple of 16
+  for (int row = blockIdx.x * wpc + (threadIdx.x >> 5); row < rows; row += gridDim.x * wpc) {
     const int sid = sorted_ids[row];
     uint2* dst = reinterpret_cast<uint2*>(xq + (size_t)row * H);
     float* srow = xs + (size_t)row * (H / 128);
     if (sid >= R) {
-      for (int v = threadIdx.x; v < nv; v += blockDim.x) {
+      for (int v = lane; v < nv; v += 32) {
         dst[v] = make_uint2(0, 0);
         if ((v & 15) == 0) srow[v >> 4] = 0.0f;
       }
@@ -215,34 +235,46 @@ __global__ void __launch_bounds__(128)
     }
     const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)(sid / topk) * H);
     const float w = row_weights ? row_weights[sid] : 1.0f;
-    // every lane takes part in the shuffles; a 16-lane group (one 1x128
-    // quantisation group) is either wholly inside the row or wholly outside
-    for (int base = 0; base < nv; base += blockDim.x) {
-      const int v = base + threadIdx.x;
-      const bool act = v < nv;
-      float f[8];
-      float amax = 0.0f;
-      if (act) {
-        uint4 u = __ldg(src + v);
-        const __nv_bfloat16* b = reinterpret_cast<const __nv_bfloat16*>(&u);
+    for (int base = 0; base < nv; base += 32 * PERMUTE_U) {
+      uint4 buf[PERMUTE_U];
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          f[j] = __bfloat162float(b[j]);
-          if (row_weights) f[j] = bf16_round(f[j] * w);
-          amax = fmaxf(amax, fabsf(f[j]));
-        }
+      for (int u = 0; u < PERMUTE_U; ++u) {
+        const int v = base + 32 * u + lane;
+        if (v < nv) buf[u] = __ldg(src + v);
       }
 #pragma unroll
-      for (int o = 8; o >= 1; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-      if (act) {
-        const float s = act_scale(amax, ue8m0 != 0);
-        uint32_t lo = 0, hi = 0;
+      for (int u = 0; u < PERMUTE_U; ++u) {
+        const int v = base + 32 * u + lane;
+        // a half-warp is wholly inside or outside the row (nv % 16 == 0), but
+        // every lane takes part in the shuffles
+        const bool act = v < nv;
+        float f[8];
+        float amax = 0.0f;
+        if (act) {
+          const __nv_bfloat16* b = reinterpret_cast<const __nv_bfloat16*>(&buf[u]);
 #pragma unroll
-        for (int j = 0; j < 4; ++j) lo |= (uint32_t)f32_to_e4m3(__fdiv_rn(f[j], s)) << (8 * j);
+          for (int j = 0; j < 8; ++j) {
+            f[j] = __bfloat162float(b[j]);
+            if (row_weights) f[j] = bf16_round(f[j] * w);
+            amax = fmaxf(amax, fabsf(f[j]));
+          }
+        }
 #pragma unroll
-        for (int j = 0; j < 4; ++j) hi |= (uint32_t)f32_to_e4m3(__fdiv_rn(f[4 + j], s)) << (8 * j);
-        dst[v] = make_uint2(lo, hi);
-        if ((v & 15) == 0) srow[v >> 4] = s;
+        for (int o = 8; o >= 1; o >>= 1)
+          amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+        if (act) {
+          const float s = act_scale(amax, ue8m0 != 0);
+          const float r = __frcp_rn(s);
+          uint32_t lo = 0, hi = 0;
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            lo |= (uint32_t)f32_to_e4m3(div_rn_shared(f[j], s, r)) << (8 * j);
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            hi |= (uint32_t)f32_to_e4m3(div_rn_shared(f[4 + j], s, r)) << (8 * j);
+          dst[v] = make_uint2(lo, hi);
+          if ((v & 15) == 0) srow[v >> 4] = s;
+        }
       }
     }
   }
@@ -253,15 +285,16 @@ cudaError_t launch_permute_rows(const void* x, int H, int topk, int R, const int
                                 void* x_perm, float* x_scale, bool ue8m0, int cap,
                                 cudaStream_t stream) {
   if (cap <= 0) return cudaSuccess;
-  const int grid = min(cap, num_sms() * 8);
+  const int wpc = PERMUTE_THREADS / 32;
+  const int grid = min((cap + wpc - 1) / wpc, num_sms() * 8);
   if (x_scale == nullptr) {
-    k_permute_bf16<<<grid, 128, 0, stream>>>(static_cast<const __nv_bfloat16*>(x), H, topk, R,
-                                             sorted_ids, num_post_padded, row_weights,
-                                             static_cast<__nv_bfloat16*>(x_perm));
+    k_permute_bf16<<<grid, PERMUTE_THREADS, 0, stream>>>(
+        static_cast<const __nv_bfloat16*>(x), H, topk, R, sorted_ids, num_post_padded,
+        row_weights, static_cast<__nv_bfloat16*>(x_perm));
   } else {
-    k_permute_fp8<<<grid, 128, 0, stream>>>(static_cast<const __nv_bfloat16*>(x), H, topk, R,
-                                            sorted_ids, num_post_padded, row_weights,
-                                            static_cast<uint8_t*>(x_perm), x_scale, ue8m0);
+    k_permute_fp8<<<grid, PERMUTE_THREADS, 0, stream>>>(
+        static_cast<const __nv_bfloat16*>(x), H, topk, R, sorted_ids, num_post_padded,
+        row_weights, static_cast<uint8_t*>(x_perm), x_scale, ue8m0);
   }
   return cudaGetLastError();
 }
