@@ -16,11 +16,14 @@
 //  * warp 1 lane 0: four kind::f8f6f4 MMAs (M=128, N=256, K=32) per K block
 //    into one of two 256-column tensor-memory partials, alternating.  (128x128
 //    MMAs ran at about half the tensor rate on GB300; N=256 keeps the pipe fed.)
-//  * warps 2-9: warp w owns TMEM lane quadrant w%4 (32 rows) and one
-//    128-column half of the tile -- exactly one 128x128 weight-scale block, so
-//    one scale product sa[row,kb]*sb[kb] per thread and K block; it reads the
-//    partial with tcgen05.ld, releases it, and accumulates in fp32 registers;
-//    at the end of the tile the sum is rounded to bf16 and stored.
+//  * warps 4-11 (warpgroups 1 and 2): warp w owns TMEM lane quadrant w%4 (32
+//    rows) and one 128-column half of the tile -- exactly one 128x128
+//    weight-scale block, so one scale product sa[row,kb]*sb[kb] per thread
+//    and K block; it reads the partial with tcgen05.ld (four 16-column loads
+//    per wait), releases it, and accumulates in fp32 registers; at the end of
+//    the tile the sum is rounded to bf16 and stored.  The 128 accumulators a
+//    thread holds need the register split below (setmaxnreg): warpgroup 0
+//    (producer, MMA issuer, two idle warps) gives registers up.
 //  * a last column tile narrower than 256 (N % 256 == 128) computes its upper
 //    half on whatever the weight box held and never stores it.
 //  * tiles are walked expert by expert (tile_sched.cuh), so each weight tile
@@ -46,7 +49,16 @@ constexpr int B_BYTES = BN * BK;
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int TMEM_COLS = NPART * BN;
 constexpr int NUM_EPI_WARPS = 8;
-constexpr int NUM_THREADS = 64 + NUM_EPI_WARPS * 32;
+constexpr int EPI_WARP0 = 4;                      // epilogue = warpgroups 1 and 2
+constexpr int NUM_THREADS = (EPI_WARP0 + NUM_EPI_WARPS) * 32;
+// Register split (setmaxnreg): launched at LAUNCH_REGS a thread (3 warps on
+// each register-file partition -> at most 168); warpgroup 0 (producer, MMA
+// issuer, two idle warps) drops to CTRL_REGS, the epilogue warpgroups rise to
+// EPI_REGS.  The increases can only be met if the sum fits the launch pool.
+constexpr int LAUNCH_REGS = 168, CTRL_REGS = 56, EPI_REGS = 216;
+static_assert(128 * CTRL_REGS + 256 * EPI_REGS <= NUM_THREADS * LAUNCH_REGS,
+              "register split exceeds the launch allocation");
+static_assert(32 * (CTRL_REGS + 2 * EPI_REGS) <= 16384, "register-file partition");
 constexpr int SCHED_BYTES = 16 + 4 * kSchedMaxRuns + 4 * kSchedMaxBlocks;
 constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + 256 + SCHED_BYTES;
 
@@ -69,8 +81,6 @@ struct Fp8Args {
   int* err;
 };
 
-// 10 warps put 3 warps on two of the SM's four register-file partitions
-// (16384 registers each), so a thread may hold at most 168 registers.
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     k_ggemm_fp8(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const Fp8Args args) {
@@ -129,7 +139,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   sched.n_tiles = args.n_tiles;
   sched.group_max = args.group_max;
 
-  if (warp == 0 && lane == 0) {
+  if (warp < EPI_WARP0) {
+   setmaxnreg_dec<CTRL_REGS>();     // all of warpgroup 0, before its role split
+   if (warp == 0 && lane == 0) {
     // ------------------------------------------------------------ producer
     const uint64_t pol_a = l2_policy(MOE_GEMM_L2_A);
     const uint64_t pol_b = l2_policy(MOE_GEMM_L2_B);
@@ -202,10 +214,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
     tc_commit(drain_bar);
     mbar_wait_bounded(drain_bar, 0, nullptr, args.limit_ns, args.err);
-  } else if (warp >= 2) {
+   }
+  } else {
+    setmaxnreg_inc<EPI_REGS>();      // all of warpgroups 1 and 2
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;               // TMEM lane quadrant
-    const int half = (warp - 2) >> 2;     // 128-column half of the tile
+    const int half = (warp - EPI_WARP0) >> 2;   // 128-column half of the tile
     const int row_in_tile = q * 32 + lane;
     uint32_t pc = 0;
     bool ok = true;
@@ -252,17 +266,25 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           tc_fence_after();
           const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + buf * BN + half * 128;
 #pragma unroll
-          for (int c = 0; c < 8; ++c) {
-            uint32_t p[16];
-            tmem_ld_32x32b_x16(taddr + c * 16, p);
+          for (int c = 0; c < 2; ++c) {     // two rounds of four 16-column loads
+            uint32_t p0[16], p1[16], p2[16], p3[16];
+            tmem_ld_32x32b_x16(taddr + c * 64, p0);
+            tmem_ld_32x32b_x16(taddr + c * 64 + 16, p1);
+            tmem_ld_32x32b_x16(taddr + c * 64 + 32, p2);
+            tmem_ld_32x32b_x16(taddr + c * 64 + 48, p3);
             tmem_ld_wait();
-            if (c == 7) {     // every read of this buffer by this warp is done
+            if (c == 1) {     // every read of this buffer by this warp is done
               tc_fence_before();
               __syncwarp();
               if (lane == 0) mbar_arrive(pempty_bar(buf));
             }
 #pragma unroll
-            for (int i = 0; i < 16; ++i) acc[c * 16 + i] = fmaf(s, __uint_as_float(p[i]), acc[c * 16 + i]);
+            for (int i = 0; i < 16; ++i) {
+              acc[c * 64 + i] = fmaf(s, __uint_as_float(p0[i]), acc[c * 64 + i]);
+              acc[c * 64 + 16 + i] = fmaf(s, __uint_as_float(p1[i]), acc[c * 64 + 16 + i]);
+              acc[c * 64 + 32 + i] = fmaf(s, __uint_as_float(p2[i]), acc[c * 64 + 32 + i]);
+              acc[c * 64 + 48 + i] = fmaf(s, __uint_as_float(p3[i]), acc[c * 64 + 48 + i]);
+            }
           }
           ++pc;
         }
@@ -319,10 +341,15 @@ cudaError_t launch_ggemm_fp8(const void* A, const float* a_scale, int cap, int K
   watchdog_params(&a.limit_ns, &a.never_arrive);
   a.err = dev_error_word();
   static bool attr_done = false;
+  static bool regs_ok = false;
   if (!attr_done) {
     cudaFuncSetAttribute(k_ggemm_fp8, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    // the register split above is only safe at exactly LAUNCH_REGS a thread
+    cudaFuncAttributes fa;
+    regs_ok = cudaFuncGetAttributes(&fa, k_ggemm_fp8) == cudaSuccess && fa.numRegs == LAUNCH_REGS;
     attr_done = true;
   }
+  if (!regs_ok) return cudaErrorInvalidConfiguration;
   k_ggemm_fp8<<<num_sms(), NUM_THREADS, SMEM_BYTES, stream>>>(tmA, tmB, a);
   return cudaGetLastError();
 }
