@@ -128,6 +128,17 @@ def _gpu_id(dev):
         return str(dev)
 
 
+def max_over_ranks(values, world, device="cpu"):
+    """Element-wise maximum of a list of floats over all ranks (the job's
+    time is its slowest rank's); a no-op for one rank."""
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor(values, dtype=torch.float64, device=device)
+    if world > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.tolist()
+
+
 def _dist():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -356,10 +367,7 @@ def run_ours(args):
         raise RuntimeError("device error in the e2e region")
 
     # max over ranks
-    t = torch.tensor([elapsed_ms, e2e_s, fused_ms], dtype=torch.float64, device=dev)
-    if world > 1:
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    elapsed_ms, e2e_s, fused_ms = t.tolist()
+    elapsed_ms, e2e_s, fused_ms = max_over_ranks([elapsed_ms, e2e_s, fused_ms], world, dev)
     ms = elapsed_ms / args.steps
     R = cfg.R
     value = world * R / (ms * 1e-3)
