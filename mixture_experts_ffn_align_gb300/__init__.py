@@ -29,6 +29,7 @@ EXPORTS = ["moe_m_sum_bound", "moe_align_workspace_bytes", "moe_workspace_bytes"
            "moe_host_workspace_bytes", "moe_align_permute", "grouped_gemm_w13", "act_mul_quant",
            "grouped_gemm_w2", "unpermute_reduce", "fused_experts", "fused_experts_from_host",
            "moe_sync_status", "moe_status_string", "moe_debug_set_watchdog",
+           "moe_debug_set_bf16_gemm_form",
            "moe_align_permute_noalloc", "moe_last_error_string"]
 
 NOALLOC_SCRATCH_BYTES = 1 << 20   # MOE_NOALLOC_SCRATCH_BYTES in include/moe_ffn.h
@@ -103,6 +104,8 @@ def lib() -> ctypes.CDLL:
         L.moe_last_error_string.argtypes, L.moe_last_error_string.restype = [], ctypes.c_char_p
         L.moe_debug_set_watchdog.argtypes, L.moe_debug_set_watchdog.restype = \
             [ctypes.c_int64, i32], None
+        L.moe_debug_set_bf16_gemm_form.argtypes, L.moe_debug_set_bf16_gemm_form.restype = \
+            [i32], None
         for n in ("moe_align_permute", "grouped_gemm_w13", "act_mul_quant", "grouped_gemm_w2",
                   "unpermute_reduce", "fused_experts", "fused_experts_from_host",
                   "moe_sync_status"):
@@ -233,6 +236,15 @@ def moe_last_error_string() -> str:
 
 def moe_debug_set_watchdog(limit_ns: int, never_arrive: bool = False):
     lib().moe_debug_set_watchdog(int(limit_ns), int(bool(never_arrive)))
+
+
+BF16_GEMM_FORMS = {"auto": 0, "single": 1, "pairs": 2}
+
+
+def moe_debug_set_bf16_gemm_form(form: str = "auto"):
+    """Force the single-SM or the SM-pair bf16 GEMM (tests), or restore the
+    size-based choice."""
+    lib().moe_debug_set_bf16_gemm_form(BF16_GEMM_FORMS[form])
 
 
 # ------------------------------------------------- buffer allocation helper

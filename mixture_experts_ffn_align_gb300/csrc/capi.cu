@@ -27,6 +27,7 @@ int* g_err_ptr[kMaxDevices];
 std::mutex g_dev_mu;
 int64_t g_watchdog_ns = 0;
 int g_never_arrive = 0;
+int g_bf16_form = 0;   // 0: by size, 1: single SM, 2: SM pairs
 
 int current_device() {
   int d = 0;
@@ -198,6 +199,27 @@ moe_status moe_align_permute(const moe_problem* p, const void* x, const int32_t*
   return cuda_status(e);
 }
 
+}  // extern "C"
+
+namespace {
+// bf16 grouped GEMM form.  SM-pair tiles halve the weight bytes each SM
+// stages per MMA, which pays once the experts average two or more 128-row
+// blocks; below that most pairs would carry a lone block whose second half
+// repeats the first.
+cudaError_t launch_bf16_gemm(const moe_problem* p, const void* A, int cap, int K, const void* B,
+                             int b_rows_total, int b_rows_per_expert, int n_out,
+                             const int32_t* block_expert_ids, const int32_t* num_post_padded,
+                             void* out, bool fuse_act, cudaStream_t s) {
+  const bool pairs = g_bf16_form == 2 ||
+                     (g_bf16_form == 0 && (int64_t)p->M * p->topk >= 2LL * 128 * p->E);
+  return (pairs ? launch_ggemm_bf16_2sm : launch_ggemm_bf16)(
+      A, cap, K, B, b_rows_total, b_rows_per_expert, n_out, block_expert_ids, num_post_padded,
+      out, fuse_act, s);
+}
+}  // namespace
+
+extern "C" {
+
 moe_status grouped_gemm_w13(const moe_problem* p, const void* x_perm, const float* x_scale,
                             const void* w13, const void* w13_scale,
                             const int32_t* block_expert_ids, const int32_t* num_post_padded,
@@ -210,7 +232,7 @@ moe_status grouped_gemm_w13(const moe_problem* p, const void* x_perm, const floa
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const int cap = (int)cap_rows(p);
   if (p->quant == MOE_Q_BF16) {
-    return cuda_status(launch_ggemm_bf16(x_perm, cap, p->H, w13, p->E * 2 * p->I, 2 * p->I,
+    return cuda_status(launch_bf16_gemm(p, x_perm, cap, p->H, w13, p->E * 2 * p->I, 2 * p->I,
                                          2 * p->I, block_expert_ids, num_post_padded, out,
                                          fuse_act != 0, s));
   }
@@ -250,7 +272,7 @@ moe_status grouped_gemm_w2(const moe_problem* p, const void* z, const float* z_s
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const int cap = (int)cap_rows(p);
   if (p->quant == MOE_Q_BF16) {
-    return cuda_status(launch_ggemm_bf16(z, cap, p->I, w2, p->E * p->H, p->H, p->H,
+    return cuda_status(launch_bf16_gemm(p, z, cap, p->I, w2, p->E * p->H, p->H, p->H,
                                          block_expert_ids, num_post_padded, y2, false, s));
   }
   if (!z_scale || !w2_scale) return MOE_ERR_INVALID_ARG;
@@ -378,5 +400,7 @@ void moe_debug_set_watchdog(int64_t limit_ns, int never_arrive) {
   g_watchdog_ns = limit_ns > 0 ? limit_ns : 0;
   g_never_arrive = never_arrive != 0;
 }
+
+void moe_debug_set_bf16_gemm_form(int mode) { g_bf16_form = (mode == 1 || mode == 2) ? mode : 0; }
 
 }  // extern "C"

@@ -46,6 +46,12 @@ cudaError_t launch_ggemm_bf16(const void* A, int cap, int K, const void* B, int 
                               int b_rows_per_expert, int n_out, const int32_t* block_expert_ids,
                               const int32_t* num_post_padded, void* out, bool fuse_act,
                               cudaStream_t stream);
+// The same GEMM issued on SM pairs (cta_group::2, 256 x 256 tiles).
+cudaError_t launch_ggemm_bf16_2sm(const void* A, int cap, int K, const void* B,
+                                  int b_rows_total, int b_rows_per_expert, int n_out,
+                                  const int32_t* block_expert_ids,
+                                  const int32_t* num_post_padded, void* out, bool fuse_act,
+                                  cudaStream_t stream);
 
 // FP8 (e4m3) grouped GEMM with fp32 1x128 activation scales and 128x128
 // weight block scales: out = sum_kb sa*sb*partial_kb (bf16 output).

@@ -14,6 +14,7 @@ systematic mistake would break.  Indices and copies are compared bit for bit.
 """
 from __future__ import annotations
 
+import contextlib
 import numpy as np
 import torch
 
@@ -85,3 +86,15 @@ def oracle_inputs(d):
     return dict(x=np32(d["x"]), topk_ids=np32(d["topk_ids"]), topk_weights=np32(d["topk_weights"]),
                 w13=np32(d["w13"]), w2=np32(d["w2"]), w13_scale=np32(d.get("w13_scale")),
                 w2_scale=np32(d.get("w2_scale")))
+
+
+@contextlib.contextmanager
+def bf16_gemm_form(form):
+    """Run the block with the bf16 GEMMs forced to one form ("single": 128 x 256
+    tiles on one SM, "pairs": 256 x 256 tiles on SM pairs, "auto": by size)."""
+    import mixture_experts_ffn_align_gb300 as moe
+    moe.moe_debug_set_bf16_gemm_form(form)
+    try:
+        yield
+    finally:
+        moe.moe_debug_set_bf16_gemm_form("auto")

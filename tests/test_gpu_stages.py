@@ -10,8 +10,8 @@ import torch
 import mixture_experts_ffn_align_gb300 as moe
 from oracle import codecs, experts, routing
 
-from .gpu_util import (BF16_TOL, QUANT_TOL, act_allowance, check_close, flip_allowance,
-                       np32)
+from .gpu_util import (BF16_TOL, QUANT_TOL, act_allowance, bf16_gemm_form, check_close,
+                       flip_allowance, np32)
 
 pytestmark = pytest.mark.gpu
 
@@ -61,9 +61,11 @@ def _staged(d, H, I, fuse):
 
 @pytest.mark.parametrize("counts,H,I", RAGGED)
 @pytest.mark.parametrize("fuse", [False, True])
-def test_stages_bf16_ragged(counts, H, I, fuse):
+@pytest.mark.parametrize("form", ["single", "pairs"])
+def test_stages_bf16_ragged(counts, H, I, fuse, form):
     d = _ragged_problem(counts, H, I)
-    p, b = _staged(d, H, I, fuse)
+    with bf16_gemm_form(form):
+        p, b = _staged(d, H, I, fuse)
     ids = d["ids"].numpy()
     route = routing.align_permute(ids, d["E"], 128)
     n = route["num_tokens_post_padded"]

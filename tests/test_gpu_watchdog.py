@@ -15,7 +15,8 @@ import mixture_experts_ffn_align_gb300 as moe
 from moe_synth import MoEConfig, make_inputs
 from oracle import experts
 
-from .gpu_util import BF16_TOL, QUANT_TOL, check_close, flip_allowance, np32, oracle_inputs
+from .gpu_util import (BF16_TOL, QUANT_TOL, bf16_gemm_form, check_close, flip_allowance, np32,
+                       oracle_inputs)
 
 pytestmark = pytest.mark.gpu
 
@@ -36,8 +37,13 @@ def _fused(cfg, d):
     return y
 
 
-@pytest.mark.parametrize("name", list(CASES))
-def test_wait_that_runs_out_reports_timeout_and_context_survives(name):
+@pytest.mark.parametrize("name,form", [("bf16", "single"), ("bf16", "pairs"), ("fp8", "auto")])
+def test_wait_that_runs_out_reports_timeout_and_context_survives(name, form):
+    with bf16_gemm_form(form):
+        _timeout_then_recover(name)
+
+
+def _timeout_then_recover(name):
     cfg = CASES[name]
     d = make_inputs(cfg, "cuda")
     assert moe.moe_sync_status() == 0
