@@ -173,12 +173,26 @@ def _time_oracle(arrs, tokens, cfg):
 
 _KERNEL_SOURCES = {
     "bf16": ["gemm_bf16.cu", "moe_common.cuh", "tile_sched.cuh"],
+    "bf16_2sm": ["gemm_bf16_2sm.cu", "moe_common.cuh", "tile_sched.cuh"],
     "fp8": ["gemm_fp8.cu", "moe_common.cuh", "tile_sched.cuh"],
+    "mxfp4": ["gemm_mxfp4.cu", "moe_common.cuh", "tile_sched.cuh"],
 }
 
 
+def gemm1_kernel(cfg):
+    """(source key, kernel label) of the GEMM1 launch the library picks for cfg:
+    the bf16 GEMMs run on SM pairs once the experts average two 128-row blocks."""
+    if cfg.quant == "fp8":
+        return "fp8", "k_ggemm_fp8 (GEMM1)"
+    if cfg.quant == "mxfp4":
+        return "mxfp4", "k_ggemm_mxfp4 (GEMM1)"
+    if cfg.M * cfg.topk >= 2 * 128 * cfg.E:
+        return "bf16_2sm", "k_ggemm_bf16_2sm<fused SiLU-and-mul> (GEMM1, SM pairs)"
+    return "bf16", "k_ggemm_bf16<fused SiLU-and-mul> (GEMM1)"
+
+
 def kernel_source_sha(kind):
-    """sha256 over the sources of the GEMM kernel `kind` (bf16 | fp8)."""
+    """sha256 over the sources of the GEMM kernel `kind` (a key of _KERNEL_SOURCES)."""
     import hashlib
     h = hashlib.sha256()
     for f in _KERNEL_SOURCES[kind]:
@@ -187,7 +201,7 @@ def kernel_source_sha(kind):
     return h.hexdigest()
 
 
-def _traffic(cfg, quantised):
+def _traffic(cfg):
     """DRAM bytes (read + write) per GEMM1 launch from the committed ncu record
     in profiles/gemm1_dram_traffic.json, if it was taken on this workload with
     the current kernel sources; else None."""
@@ -196,7 +210,7 @@ def _traffic(cfg, quantised):
             recs = json.load(f)
     except Exception:
         return None
-    kind = "fp8" if quantised else "bf16"
+    kind = gemm1_kernel(cfg)[0]
     for r in recs:
         if (r.get("kernel") == kind and r.get("workload") == cfg.name
                 and r.get("source_sha") == kernel_source_sha(kind)):
@@ -396,10 +410,9 @@ def run_ours(args):
             "tflops": (gemm1_flops + gemm2_flops) / (ms * 1e-3) / 1e12,
             "stages_ms": stage_ms,
             "fused_call_ms": fused_ms,
-            "roofline": {"bound": "tensor", "kernel": ("k_ggemm_fp8 (GEMM1)" if q else
-                                                       "k_ggemm_bf16<fused SiLU-and-mul> (GEMM1)"),
+            "roofline": {"bound": "tensor", "kernel": gemm1_kernel(cfg)[1],
                          "achieved": ach, "peak": peak, "unit": "TFLOP/s",
-                         "frac": ach / peak, "traffic": _traffic(cfg, q),
+                         "frac": ach / peak, "traffic": _traffic(cfg),
                          "peak_source": (f"bf16_tflops_sustained x {ratio:g} ({peaks['source']})"),
                          "algorithmic_per_launch": f"2*R*H*2I = {gemm1_flops:.4e} FLOP",
                          "weight_hbm_frac": w13_bytes / (stage_ms[g1] * 1e-3) / 1e9 /
