@@ -21,9 +21,6 @@ namespace moe {
 constexpr int ACT_U = 4;             // 16-byte vectors of g (and of u) per lane in flight
 constexpr int ACT_THREADS = 256;
 
-// SiLU(g) with the fast exponential; z tolerates its few-ulp error.
-__device__ __forceinline__ float silu_fast(float g) { return __fdividef(g, 1.0f + __expf(-g)); }
-
 // z[row, :] = bf16(SiLU(bf16 g) * bf16 u) for rows below num_post_padded.
 __global__ void __launch_bounds__(ACT_THREADS)
     k_act_mul_bf16(const __nv_bfloat16* __restrict__ h1, int I, const int32_t* __restrict__ npp,

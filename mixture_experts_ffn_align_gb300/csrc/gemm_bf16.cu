@@ -242,7 +242,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           for (int j = 0; j < 32; ++j) {
             const float gv = bf16_round(__uint_as_float(g[j]));
             const float uv = bf16_round(__uint_as_float(u[j]));
-            pb[j] = __float2bfloat16_rn(silu_f32(gv) * uv);
+            pb[j] = __float2bfloat16_rn(silu_fast(gv) * uv);
           }
           uint4* dst = reinterpret_cast<uint4*>(out_row + c * 32);
 #pragma unroll

@@ -202,13 +202,25 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const uint64_t pol_b = l2_policy(MOE_GEMM_L2_B);
     uint32_t stage = 0, phase = 0, issued_mask = 0, issued_parity = 0;
     bool skip_first = leader && args.never_arrive != 0;
-    int next = leader ? atomicAdd(args.tile_ctr, 1) : 0;
+    // The leader publishes tile j + 1 as it starts issuing tile j, so the
+    // peer has its next index before it reaches the tile boundary; the
+    // counter read for tile j + 2 is in flight meanwhile.
+    int t_lead = -1, pending = 0;
+    bool ring_ok = true;
+    if (leader) {
+      const int f = atomicAdd(args.tile_ctr, 1);
+      t_lead = f < total ? f : -1;
+      ring_ok = ring_put(0, t_lead);
+      if (t_lead >= 0) pending = atomicAdd(args.tile_ctr, 1);
+    }
     for (int j = 0;; ++j) {
       int t;
       if (leader) {
-        t = next < total ? next : -1;
-        if (!ring_put(j, t) || t < 0) break;
-        next = atomicAdd(args.tile_ctr, 1);   // in flight while this tile is issued
+        t = t_lead;
+        if (!ring_ok || t < 0) break;
+        t_lead = pending < total ? pending : -1;
+        ring_ok = ring_put(j + 1, t_lead);
+        if (t_lead >= 0) pending = atomicAdd(args.tile_ctr, 1);
       } else {
         t = ring_take(j);
         if (t < 0) break;
@@ -339,7 +351,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           for (int j = 0; j < 32; ++j) {
             const float gv = bf16_round(__uint_as_float(g[j]));
             const float uv = bf16_round(__uint_as_float(u[j]));
-            pb[j] = __float2bfloat16_rn(silu_f32(gv) * uv);
+            pb[j] = __float2bfloat16_rn(silu_fast(gv) * uv);
           }
           uint4* dst = reinterpret_cast<uint4*>(out_row + c * 32);
 #pragma unroll
