@@ -15,20 +15,32 @@
 //    padded 4-bit TMA type (each 16 values -> 8 bytes + 8-byte gap, so a row
 //    of 128 values fills one 128-byte swizzled smem row; the copy counts the
 //    packed bytes toward the barrier), 128-byte swizzle;
-//  * warps 2-5: scale writers -- per K block, the A scale operand (each row's
-//    UE8M0 exponent in all 4 bytes: one scale covers 128 = 4 x 32) and the B
-//    scale operand (the 4 E8M0 bytes of each column's 4 K chunks), written
-//    into tensor memory with tcgen05.st; byte j is picked by the scale-ID
-//    fields of MMA j.  An operand of R rows (columns) is laid out as 32 lanes x
-//    R/32 columns -- row r at lane r % 32, column r / 32 -- repeated in every
-//    32-lane quadrant, each operand in its own 16-column-aligned slot (an
-//    odd-column scale address raised a misaligned-address fault);
-//  * warp 1 lane 0: four MMAs (M=128, N=256, K=32) per K block into the
-//    256-column accumulator (N=128 MMAs run at about half the tensor rate);
-//    tcgen05.commit frees the stage and its scales;
-//  * warps 6-9: epilogue, tcgen05.ld -> bf16 -> global.  Tensor memory holds
-//    one 256-column accumulator plus the scale slots, so the next tile's MMAs
-//    wait for the epilogue (about a microsecond against ~15 of MMA per tile).
+//  * warp 2: scale writer.  Per K block it builds the two scale operands in
+//    a shared-memory ring of SSLOTS slots: the A operand (each row's UE8M0
+//    exponent in all 4 bytes: one scale covers 128 = 4 x 32) and the B
+//    operand (the 4 E8M0 bytes of each column's 4 K chunks), each 128-row
+//    group as 32 rows of 16 bytes -- row r at byte 16 (r % 32) + 4 (r / 32),
+//    byte j of the word for K chunk j, which is the tensor-memory layout the
+//    block-scaled MMA reads (32 lanes x 4 columns, row r at lane r % 32,
+//    column r / 32, repeated in every lane quadrant; byte j picked by the
+//    scale-ID field of MMA j).  Scales are loaded 16 bytes (4 K blocks) at a
+//    time, one group ahead.  (4-byte cp.async copies straight into the
+//    packed places were slower: four times the L1 wavefronts.)
+//  * warp 1 lane 0: copies the K block's scale operands into tensor memory
+//    with tcgen05.cp (32x128b, repeated to the four lane quadrants), then
+//    issues four MMAs (M=128, N=256, K=32) into the 256-column accumulator
+//    (N=128 MMAs run at about half the tensor rate); copy and MMAs run in
+//    issue order in the tensor pipe, so no thread waits between them, and
+//    tcgen05.commit frees the stage and the scale slot.  (Writing the scales
+//    into tensor memory with tcgen05.st from four warps cost 0.34 of 1.13 ms
+//    on the DeepSeek-shaped GEMM1.)  Each smem stage has its own tensor-memory
+//    scale slot (16-column aligned: an odd-column scale address raised a
+//    misaligned-address fault), rewritten only after the stage's producer
+//    wait has seen that slot's MMAs complete;
+//  * warps 4-11: epilogue, two warps per TMEM lane quadrant, 128 columns
+//    each: tcgen05.ld -> bf16 -> global.  Tensor memory holds one 256-column
+//    accumulator plus the scale slots, so the next tile's MMAs wait for the
+//    epilogue; eight warps halve that wait.
 //  * a last column tile narrower than 256 (N % 256 == 128) is computed on
 //    whatever the weight box held above N and its upper half is not stored.
 //  * tiles walked expert by expert (tile_sched.cuh); every wait is bounded.
@@ -47,18 +59,22 @@ bool make_tmap_fp4_k_sw128(CUtensorMap* map, const void* base, uint64_t rows, ui
 
 namespace {
 
-constexpr int BM = 128, BN = 256, BK = 128, STAGES = 4;
+constexpr int BM = 128, BN = 256, BK = 128, STAGES = 4, SSLOTS = 8;
 constexpr int A_BYTES = BM * BK;          // e4m3
 constexpr int B_BYTES = BN * BK;          // 4-bit values padded to one byte each in smem
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int TX_BYTES = A_BYTES + B_BYTES / 2;   // bytes the copies of one stage count
-constexpr int SF_COL0 = BN;               // scale slots after the accumulator
+constexpr int SF_A_BYTES = 512;           // 128 rows x 4 K chunks
+constexpr int SF_BYTES = SF_A_BYTES + 2 * 512;    // + 256 columns x 4 K chunks
+constexpr int SF_COL0 = BN;               // tensor-memory scale slots after the accumulator
 constexpr int SF_SLOT = 16;               // stage s: A at SF_COL0 + 32 s, B at + 16
 constexpr int TMEM_COLS = 512;
-constexpr int NUM_THREADS = 320;
+constexpr int NUM_EPI_WARPS = 8, EPI_WARP0 = 4;
+constexpr int NUM_THREADS = (EPI_WARP0 + NUM_EPI_WARPS) * 32;
 constexpr int SCHED_BYTES = 16 + 4 * kSchedMaxRuns + 4 * kSchedMaxBlocks;
-constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + 256 + SCHED_BYTES;
+constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + SSLOTS * SF_BYTES + 1024 + 256 + SCHED_BYTES;
 static_assert(SF_COL0 + SF_SLOT * (2 * STAGES - 1) + BN / 32 <= TMEM_COLS, "tensor memory");
+static_assert(SMEM_BYTES <= 232448, "shared memory");
 
 struct Mx4Args {
   const int32_t* block_expert_ids;
@@ -84,32 +100,38 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
-  // full[S], sfull[S], empty[S], tfull, tempty, drain
-  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 3 * STAGES + 3);
+  uint8_t* sf_ring = smem + STAGES * STAGE_BYTES;    // SSLOTS x SF_BYTES, 16-byte aligned
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sf_ring + SSLOTS * SF_BYTES);
+  // full[S], empty[S], sfull[SS], sempty[SS], tfull, tempty, drain
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 2 * SSLOTS + 3);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
-  int* s_nruns = reinterpret_cast<int*>(smem + STAGES * STAGE_BYTES + 256);
+  int* s_nruns = reinterpret_cast<int*>(sf_ring + SSLOTS * SF_BYTES + 256);
   int* s_runs = s_nruns + 4;
   int* s_ids = s_runs + kSchedMaxRuns;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t smem_base = smem_u32(smem);
   const uint32_t bar_base = smem_u32(bars);
+  const uint32_t sf_base = smem_u32(sf_ring);
   auto full_bar = [&](int s) { return bar_base + 8u * s; };
-  auto sfull_bar = [&](int s) { return bar_base + 8u * (STAGES + s); };
-  auto empty_bar = [&](int s) { return bar_base + 8u * (2 * STAGES + s); };
-  const uint32_t tfull_bar = bar_base + 8u * (3 * STAGES);
-  const uint32_t tempty_bar = bar_base + 8u * (3 * STAGES + 1);
-  const uint32_t drain_bar = bar_base + 8u * (3 * STAGES + 2);
+  auto empty_bar = [&](int s) { return bar_base + 8u * (STAGES + s); };
+  auto sfull_bar = [&](int s) { return bar_base + 8u * (2 * STAGES + s); };
+  auto sempty_bar = [&](int s) { return bar_base + 8u * (2 * STAGES + SSLOTS + s); };
+  const uint32_t tfull_bar = bar_base + 8u * (2 * STAGES + 2 * SSLOTS);
+  const uint32_t tempty_bar = bar_base + 8u * (2 * STAGES + 2 * SSLOTS + 1);
+  const uint32_t drain_bar = bar_base + 8u * (2 * STAGES + 2 * SSLOTS + 2);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(full_bar(s), 1);
-      mbar_init(sfull_bar(s), 4);
       mbar_init(empty_bar(s), 1);
     }
+    for (int s = 0; s < SSLOTS; ++s) {
+      mbar_init(sfull_bar(s), 1);
+      mbar_init(sempty_bar(s), 1);
+    }
     mbar_init(tfull_bar, 1);
-    mbar_init(tempty_bar, 4);
+    mbar_init(tempty_bar, NUM_EPI_WARPS);
     mbar_init(drain_bar, 1);
     *abort_flag = 0;
     fence_barrier_init();
@@ -178,26 +200,24 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     for (int s = 0; s < STAGES; ++s)
       if (issued_mask & (1u << s))
         mbar_wait_bounded(full_bar(s), (issued_parity >> s) & 1, nullptr, args.limit_ns, args.err);
-  } else if (warp >= 2 && warp < 6) {
-    // ------------------------------------------------------------ scale writers
-    const int q = warp & 3;
-    const uint32_t lane_base = tmem_base + ((uint32_t)(q * 32) << 16);
+  } else if (warp == 2) {
+    // ------------------------------------------------------------ scale writer
     const int kq = args.num_kb * 4;            // E8M0 bytes per weight row
     const bool vec = (args.num_kb & 3) == 0;   // rows 16-byte aligned: vector loads
-    uint32_t stage = 0, phase = 0;
+    uint32_t sslot = 0, sphase = 0;
     bool ok = true;
     for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
       int m_blk, n_tile;
       sched_tile(sched, t, m_blk, n_tile);
       const int e = s_ids[m_blk];
       if (e < 0 || e >= args.num_experts) continue;
-      // this lane writes rows lane + 32 c of A (c < 4) and columns lane + 32 c
-      // of B (c < 8); B columns past N (ragged last tile) read nothing
+      // lane l builds rows l + 32 c of A (c < 4) and of B (c < 8); B rows
+      // past N (ragged last tile) read nothing
       const float* sa_base = args.a_scale + ((size_t)m_blk * BM + lane) * args.num_kb;
       const size_t sa_step = (size_t)32 * args.num_kb;             // floats per 32 rows
       const uint8_t* sb_base = args.b_scale + ((size_t)e * N + (size_t)n_tile * BN + lane) * kq;
       const size_t sb_step = (size_t)32 * kq;                      // bytes per 32 rows
-      const int n_valid = N - n_tile * BN - lane;                  // B column c valid if 32c < this
+      const int n_valid = N - n_tile * BN - lane;                  // B row c valid if 32c < this
       // scales of 4 K blocks per load, one group of 4 in flight ahead
       auto load_group = [&](int g, float4 (&A)[4], uint4 (&B)[8]) {
         const int n = args.num_kb - g;
@@ -246,25 +266,24 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             bw[c] = j == 0 ? b_cur[c].x : j == 1 ? b_cur[c].y : j == 2 ? b_cur[c].z : b_cur[c].w;
           int got = 1;
           if (lane == 0)
-            got = mbar_wait_bounded(empty_bar(stage), phase ^ 1, abort_flag, args.limit_ns,
+            got = mbar_wait_bounded(sempty_bar(sslot), sphase ^ 1, abort_flag, args.limit_ns,
                                     args.err);
           got = __shfl_sync(0xffffffffu, got, 0);
           if (!got) {
             ok = false;
             break;
           }
-          tc_fence_after();
-          const uint32_t slot = SF_COL0 + SF_SLOT * 2 * stage;
-          tmem_st_32x32b_x4(lane_base + slot, aw[0], aw[1], aw[2], aw[3]);
-          tmem_st_32x32b_x4(lane_base + slot + SF_SLOT, bw[0], bw[1], bw[2], bw[3]);
-          tmem_st_32x32b_x4(lane_base + slot + SF_SLOT + 4, bw[4], bw[5], bw[6], bw[7]);
-          tmem_st_wait();
-          tc_fence_before();
+          // lane l: 16 bytes at row l of the A block and of both B blocks
+          uint4* dst = reinterpret_cast<uint4*>(sf_ring + sslot * SF_BYTES) + lane;
+          dst[0] = make_uint4(aw[0], aw[1], aw[2], aw[3]);
+          dst[32] = make_uint4(bw[0], bw[1], bw[2], bw[3]);
+          dst[64] = make_uint4(bw[4], bw[5], bw[6], bw[7]);
+          fence_proxy_async_smem();
           __syncwarp();
-          if (lane == 0) mbar_arrive(sfull_bar(stage));
-          if (++stage == STAGES) {
-            stage = 0;
-            phase ^= 1;
+          if (lane == 0) mbar_arrive(sfull_bar(sslot));
+          if (++sslot == SSLOTS) {
+            sslot = 0;
+            sphase ^= 1;
           }
         }
 #pragma unroll
@@ -276,7 +295,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
   } else if (warp == 1 && lane == 0) {
     // ------------------------------------------------------------ MMA issuer
-    uint32_t stage = 0, phase = 0;
+    uint32_t stage = 0, phase = 0, sslot = 0, sphase = 0;
     int local = 0;
     bool ok = true;
     for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
@@ -289,7 +308,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       tc_fence_after();
       for (int kb = 0; kb < args.num_kb; ++kb) {
         if (!mbar_wait_bounded(full_bar(stage), phase, abort_flag, args.limit_ns, args.err) ||
-            !mbar_wait_bounded(sfull_bar(stage), phase, abort_flag, args.limit_ns, args.err)) {
+            !mbar_wait_bounded(sfull_bar(sslot), sphase, abort_flag, args.limit_ns, args.err)) {
           ok = false;
           break;
         }
@@ -298,6 +317,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const uint64_t adesc = sdesc_k_sw128(sa);
         const uint64_t bdesc = sdesc_k_sw128(sa + A_BYTES);
         const uint32_t sfa = tmem_base + SF_COL0 + SF_SLOT * 2 * stage;
+        const uint32_t sf_src = sf_base + sslot * SF_BYTES;
+        tmem_cp_32x128b_x4(sfa, sdesc_rows16(sf_src));
+        tmem_cp_32x128b_x4(sfa + SF_SLOT, sdesc_rows16(sf_src + SF_A_BYTES));
+        tmem_cp_32x128b_x4(sfa + SF_SLOT + 4, sdesc_rows16(sf_src + SF_A_BYTES + 512));
 #pragma unroll
         for (int j = 0; j < BK / 32; ++j) {
           umma_mxf8f6f4(tmem_base, adesc + 2 * j, bdesc + 2 * j,
@@ -305,9 +328,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         sfa + SF_SLOT, (kb | j) != 0);
         }
         tc_commit(empty_bar(stage));
+        tc_commit(sempty_bar(sslot));
         if (++stage == STAGES) {
           stage = 0;
           phase ^= 1;
+        }
+        if (++sslot == SSLOTS) {
+          sslot = 0;
+          sphase ^= 1;
         }
       }
       if (!ok) break;
@@ -316,9 +344,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
     tc_commit(drain_bar);
     mbar_wait_bounded(drain_bar, 0, nullptr, args.limit_ns, args.err);
-  } else if (warp >= 6) {
+  } else if (warp >= EPI_WARP0) {
     // ------------------------------------------------------------ epilogue
-    const int q = warp & 3;
+    const int q = warp & 3;                         // TMEM lane quadrant
+    const int half = (warp - EPI_WARP0) >> 2;       // 128-column half of the tile
     const int row_in_tile = q * 32 + lane;
     int local = 0;
     for (int t = blockIdx.x; t < total; t += gridDim.x) {
@@ -332,27 +361,32 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       ok = __shfl_sync(0xffffffffu, ok, 0);
       if (!ok) break;
       tc_fence_after();
-      const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16);
+      const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + half * 128;
       const size_t row = (size_t)m_blk * BM + row_in_tile;
-      __nv_bfloat16* out_row = args.out + row * args.ldo + (size_t)n_tile * BN;
-      const int ncols = min(BN, N - n_tile * BN);    // 256, or 128 on a ragged last tile
-#pragma unroll 1
-      for (int c = 0; c < BN / 32; ++c) {
-        uint32_t r[32];
-        tmem_ld_32x32b_x32(taddr + c * 32, r);
-        tmem_ld_wait();
-        if (c * 32 >= ncols) continue;
-        uint4 pk[4];
-        __nv_bfloat16* pb = reinterpret_cast<__nv_bfloat16*>(pk);
+      __nv_bfloat16* out_row = args.out + row * args.ldo + (size_t)n_tile * BN + half * 128;
+      // 256 columns, or 128 on a ragged last tile
+      const bool store = half * 128 < N - n_tile * BN;
+      // read the whole 128-column slice, hand the accumulator back to the
+      // MMA thread, then convert and store
+      uint32_t r[4][32];
 #pragma unroll
-        for (int j = 0; j < 32; ++j) pb[j] = __float2bfloat16_rn(__uint_as_float(r[j]));
-        uint4* dst = reinterpret_cast<uint4*>(out_row + c * 32);
-#pragma unroll
-        for (int j = 0; j < 4; ++j) dst[j] = pk[j];
-      }
+      for (int c = 0; c < 4; ++c) tmem_ld_32x32b_x32(taddr + c * 32, r[c]);
+      tmem_ld_wait();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(tempty_bar);
+      if (store) {
+        uint4* dst = reinterpret_cast<uint4*>(out_row);
+#pragma unroll
+        for (int v = 0; v < 16; ++v) {
+          uint4 pk;
+          __nv_bfloat16* pb = reinterpret_cast<__nv_bfloat16*>(&pk);
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+            pb[j] = __float2bfloat16_rn(__uint_as_float(r[v >> 2][8 * (v & 3) + j]));
+          dst[v] = pk;
+        }
+      }
       ++local;
     }
   }

@@ -106,6 +106,38 @@ __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
 
+// 4-byte asynchronous copy global -> shared (no registers held while in
+// flight); completes by commit group.
+__device__ __forceinline__ void cp_async_4(uint32_t dst_smem, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst_smem), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+// Waits until at most N of this thread's most recent commit groups are pending.
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+__device__ __forceinline__ uint32_t ld_shared_u32(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_shared_u32(uint32_t addr, uint32_t v) {
+  asm volatile("st.shared.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+
+// Asks for a 2-D box of a tensor to be brought into L2 (no shared memory,
+// no completion to wait for); used ahead of the loads of a streamed operand.
+__device__ __forceinline__ void tma_prefetch_l2_2d(const CUtensorMap* map, int32_t c0,
+                                                   int32_t c1) {
+  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(c0), "r"(c1)
+               : "memory");
+}
+
 // 2-D tiled bulk tensor load global -> shared, completion counted in bytes on
 // `bar`.  c0 is the innermost (contiguous) coordinate in elements.
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
@@ -256,6 +288,29 @@ __device__ __forceinline__ uint64_t sdesc_k_sw128(uint32_t saddr) {
   d |= (uint64_t)1 << 46;
   d |= (uint64_t)2 << 61;
   return d;
+}
+
+// Descriptor of a 32-row x 16-byte shared-memory block stored row after row
+// (no swizzle: four 8-row core matrices of 128 contiguous bytes, 128 bytes
+// apart), the source shape of tmem_cp_32x128b_x4.
+__device__ __forceinline__ uint64_t sdesc_rows16(uint32_t saddr) {
+  uint64_t d = (uint64_t)((saddr & 0x3FFFFu) >> 4);
+  d |= (uint64_t)(16u >> 4) << 16;     // leading offset: the block is one core matrix wide
+  d |= (uint64_t)(128u >> 4) << 32;    // between 8-row core matrices
+  d |= (uint64_t)1 << 46;
+  return d;
+}
+// Asynchronous copy of 32 rows x 128 bits of shared memory into tensor
+// memory lanes 0-31 x 4 columns, repeated in all four 32-lane quadrants.
+// Issued by the MMA thread, it is ordered before that thread's later MMAs.
+__device__ __forceinline__ void tmem_cp_32x128b_x4(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc)
+               : "memory");
+}
+// Makes this thread's generic-proxy shared-memory writes visible to the async
+// proxy (TMA, tcgen05.cp, tcgen05.mma operand reads).
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
 // 32 lanes x 32 consecutive fp32 columns from tensor memory, one row per
