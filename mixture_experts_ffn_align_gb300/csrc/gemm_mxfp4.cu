@@ -23,9 +23,15 @@
 //    byte j of the word for K chunk j, which is the tensor-memory layout the
 //    block-scaled MMA reads (32 lanes x 4 columns, row r at lane r % 32,
 //    column r / 32, repeated in every lane quadrant; byte j picked by the
-//    scale-ID field of MMA j).  Scales are loaded 16 bytes (4 K blocks) at a
-//    time, one group ahead.  (4-byte cp.async copies straight into the
-//    packed places were slower: four times the L1 wavefronts.)
+//    scale-ID field of MMA j).  When K % 512 == 0 (weight-scale rows are
+//    16-byte multiples) the weight scales of 4 K blocks x the tile's 256 rows
+//    come in as one TMA box, two groups ahead, and are transposed from
+//    shared memory; otherwise every lane loads them 16 bytes (4 K blocks) at
+//    a time, one group ahead.  The staged form took the DeepSeek-shaped GEMM1
+//    from 1.08 to 0.88 ms: each weight-scale row is read once from HBM, and
+//    register loads one group ahead left that latency exposed.  (4-byte
+//    cp.async copies straight into the packed places were slower still:
+//    four times the L1 wavefronts.)
 //  * warp 1 lane 0: copies the K block's scale operands into tensor memory
 //    with tcgen05.cp (32x128b, repeated to the four lane quadrants), then
 //    issues four MMAs (M=128, N=256, K=32) into the 256-column accumulator
@@ -37,15 +43,17 @@
 //    scale slot (16-column aligned: an odd-column scale address raised a
 //    misaligned-address fault), rewritten only after the stage's producer
 //    wait has seen that slot's MMAs complete;
-//  * warps 4-11: epilogue, two warps per TMEM lane quadrant, 128 columns
-//    each: tcgen05.ld -> bf16 -> global.  Tensor memory holds one 256-column
+//  * warps 4-7: epilogue, one warp per TMEM lane quadrant, 128 columns at a
+//    time: tcgen05.ld -> bf16 -> global.  Tensor memory holds one 256-column
 //    accumulator plus the scale slots, so the next tile's MMAs wait for the
-//    epilogue; eight warps halve that wait.
+//    epilogue to have read it.  (Eight warps of 128 columns each measured
+//    slower on both GEMMs.)
 //  * a last column tile narrower than 256 (N % 256 == 128) is computed on
 //    whatever the weight box held above N and its upper half is not stored.
 //  * tiles walked expert by expert (tile_sched.cuh); every wait is bounded.
 #include <mutex>
 
+#include "../../include/moe_ffn.h"
 #include "moe_common.cuh"
 #include "moe_internal.h"
 #include "tile_sched.cuh"
@@ -56,10 +64,19 @@ bool make_tmap_k_sw128(CUtensorMap* map, const void* base, uint64_t rows, uint64
                        int elem_bytes, uint32_t box_rows);
 bool make_tmap_fp4_k_sw128(CUtensorMap* map, const void* base, uint64_t rows, uint64_t k_elems,
                            uint32_t box_rows);
+bool make_tmap_u8_rows(CUtensorMap* map, const void* base, uint64_t rows, uint64_t row_bytes,
+                       uint32_t box_bytes, uint32_t box_rows);
 
 namespace {
 
-constexpr int BM = 128, BN = 256, BK = 128, STAGES = 4, SSLOTS = 8;
+constexpr int BM = 128, BN = 256, BK = 128, STAGES = 4, SSLOTS = 4;
+// Staged weight scales (K % 512 == 0): 16 bytes = 4 K blocks of each of the
+// tile's 256 rows per TMA box, NSTG groups in flight.
+constexpr int NSTG = 2, STG_BYTES = 16 * BN;
+// Blocks the schedule can hold: M * topk + E * 127 rows at the boundary's limits.
+constexpr int kMaxBlocks = 3072;
+static_assert((MOE_MAX_TOKENS * MOE_MAX_TOPK + MOE_MAX_EXPERTS * 127) / 128 <= kMaxBlocks,
+              "schedule capacity");
 constexpr int A_BYTES = BM * BK;          // e4m3
 constexpr int B_BYTES = BN * BK;          // 4-bit values padded to one byte each in smem
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
@@ -69,10 +86,11 @@ constexpr int SF_BYTES = SF_A_BYTES + 2 * 512;    // + 256 columns x 4 K chunks
 constexpr int SF_COL0 = BN;               // tensor-memory scale slots after the accumulator
 constexpr int SF_SLOT = 16;               // stage s: A at SF_COL0 + 32 s, B at + 16
 constexpr int TMEM_COLS = 512;
-constexpr int NUM_EPI_WARPS = 8, EPI_WARP0 = 4;
+constexpr int NUM_EPI_WARPS = 4, EPI_WARP0 = 4;
 constexpr int NUM_THREADS = (EPI_WARP0 + NUM_EPI_WARPS) * 32;
-constexpr int SCHED_BYTES = 16 + 4 * kSchedMaxRuns + 4 * kSchedMaxBlocks;
-constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + SSLOTS * SF_BYTES + 1024 + 256 + SCHED_BYTES;
+constexpr int SCHED_BYTES = 16 + 4 * kSchedMaxRuns + 4 * kMaxBlocks;
+constexpr int SMEM_BYTES =
+    STAGES * STAGE_BYTES + SSLOTS * SF_BYTES + NSTG * STG_BYTES + 1024 + 256 + SCHED_BYTES;
 static_assert(SF_COL0 + SF_SLOT * (2 * STAGES - 1) + BN / 32 <= TMEM_COLS, "tensor memory");
 static_assert(SMEM_BYTES <= 232448, "shared memory");
 
@@ -94,18 +112,20 @@ struct Mx4Args {
   int* err;
 };
 
+template <bool STAGED>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     k_ggemm_mxfp4(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                  const Mx4Args args) {
+                  const __grid_constant__ CUtensorMap tmS, const Mx4Args args) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
   uint8_t* sf_ring = smem + STAGES * STAGE_BYTES;    // SSLOTS x SF_BYTES, 16-byte aligned
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sf_ring + SSLOTS * SF_BYTES);
-  // full[S], empty[S], sfull[SS], sempty[SS], tfull, tempty, drain
-  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 2 * SSLOTS + 3);
+  uint8_t* stg_ring = sf_ring + SSLOTS * SF_BYTES;     // NSTG x STG_BYTES (STAGED)
+  uint64_t* bars = reinterpret_cast<uint64_t*>(stg_ring + NSTG * STG_BYTES);
+  // full[S], empty[S], sfull[SS], sempty[SS], tfull, tempty, drain, stg_full[NSTG]
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 2 * SSLOTS + 3 + NSTG);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
-  int* s_nruns = reinterpret_cast<int*>(sf_ring + SSLOTS * SF_BYTES + 256);
+  int* s_nruns = reinterpret_cast<int*>(stg_ring + NSTG * STG_BYTES + 256);
   int* s_runs = s_nruns + 4;
   int* s_ids = s_runs + kSchedMaxRuns;
 
@@ -120,6 +140,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   const uint32_t tfull_bar = bar_base + 8u * (2 * STAGES + 2 * SSLOTS);
   const uint32_t tempty_bar = bar_base + 8u * (2 * STAGES + 2 * SSLOTS + 1);
   const uint32_t drain_bar = bar_base + 8u * (2 * STAGES + 2 * SSLOTS + 2);
+  auto stg_full = [&](int s) { return bar_base + 8u * (2 * STAGES + 2 * SSLOTS + 3 + s); };
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -132,6 +153,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
     mbar_init(tfull_bar, 1);
     mbar_init(tempty_bar, NUM_EPI_WARPS);
+    for (int s = 0; s < NSTG; ++s) mbar_init(stg_full(s), 1);
     mbar_init(drain_bar, 1);
     *abort_flag = 0;
     fence_barrier_init();
@@ -139,6 +161,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
+    if (STAGED) tma_prefetch_desc(&tmS);
   }
   if (warp == 1) {
     __syncwarp();
@@ -150,8 +173,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   tc_fence_after();
   const uint32_t tmem_base = *tmem_holder;
 
-  const int nb_valid =
-      min(min(*args.num_post_padded / BM, args.m_blocks_cap), kSchedMaxBlocks);
+  const int nb_valid = min(min(*args.num_post_padded / BM, args.m_blocks_cap), kMaxBlocks);
   const int total = nb_valid * args.n_tiles;
   TileSched sched;
   sched.nruns = sched_build(args.block_expert_ids, nb_valid, s_ids, s_runs, s_nruns);
@@ -202,57 +224,96 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         mbar_wait_bounded(full_bar(s), (issued_parity >> s) & 1, nullptr, args.limit_ns, args.err);
   } else if (warp == 2) {
     // ------------------------------------------------------------ scale writer
-    const int kq = args.num_kb * 4;            // E8M0 bytes per weight row
-    const bool vec = (args.num_kb & 3) == 0;   // rows 16-byte aligned: vector loads
+    // Packs K block j (0-3) of a group: A words from four fp32 scales of
+    // this lane's rows, B words as given; then hands the ring slot over.
     uint32_t sslot = 0, sphase = 0;
-    bool ok = true;
-    for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-      int m_blk, n_tile;
-      sched_tile(sched, t, m_blk, n_tile);
-      const int e = s_ids[m_blk];
-      if (e < 0 || e >= args.num_experts) continue;
-      // lane l builds rows l + 32 c of A (c < 4) and of B (c < 8); B rows
-      // past N (ragged last tile) read nothing
-      const float* sa_base = args.a_scale + ((size_t)m_blk * BM + lane) * args.num_kb;
-      const size_t sa_step = (size_t)32 * args.num_kb;             // floats per 32 rows
-      const uint8_t* sb_base = args.b_scale + ((size_t)e * N + (size_t)n_tile * BN + lane) * kq;
-      const size_t sb_step = (size_t)32 * kq;                      // bytes per 32 rows
-      const int n_valid = N - n_tile * BN - lane;                  // B row c valid if 32c < this
-      // scales of 4 K blocks per load, one group of 4 in flight ahead
-      auto load_group = [&](int g, float4 (&A)[4], uint4 (&B)[8]) {
-        const int n = args.num_kb - g;
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          const float* pa = sa_base + c * sa_step + g;
-          if (vec) {
-            A[c] = __ldg(reinterpret_cast<const float4*>(pa));
-          } else {
-            A[c] = make_float4(__ldg(pa), n > 1 ? __ldg(pa + 1) : 1.0f,
-                               n > 2 ? __ldg(pa + 2) : 1.0f, n > 3 ? __ldg(pa + 3) : 1.0f);
-          }
-        }
-#pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          const uint32_t* pb = reinterpret_cast<const uint32_t*>(sb_base + c * sb_step) + g;
-          if (32 * c >= n_valid) {
-            B[c] = make_uint4(0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu);
-          } else if (vec) {
-            B[c] = __ldg(reinterpret_cast<const uint4*>(pb));
-          } else {
-            B[c] = make_uint4(__ldg(pb), n > 1 ? __ldg(pb + 1) : 0u, n > 2 ? __ldg(pb + 2) : 0u,
-                              n > 3 ? __ldg(pb + 3) : 0u);
-          }
-        }
+    auto put_slot = [&](const uint32_t (&aw)[4], const uint32_t (&bw)[8]) {
+      int got = 1;
+      if (lane == 0)
+        got = mbar_wait_bounded(sempty_bar(sslot), sphase ^ 1, abort_flag, args.limit_ns,
+                                args.err);
+      got = __shfl_sync(0xffffffffu, got, 0);
+      if (!got) return false;
+      // lane l: 16 bytes at row l of the A block and of both B blocks
+      uint4* dst = reinterpret_cast<uint4*>(sf_ring + sslot * SF_BYTES) + lane;
+      dst[0] = make_uint4(aw[0], aw[1], aw[2], aw[3]);
+      dst[32] = make_uint4(bw[0], bw[1], bw[2], bw[3]);
+      dst[64] = make_uint4(bw[4], bw[5], bw[6], bw[7]);
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(sfull_bar(sslot));
+      if (++sslot == SSLOTS) {
+        sslot = 0;
+        sphase ^= 1;
+      }
+      return true;
+    };
+    if constexpr (STAGED) {
+      // The weight scales of 4 K blocks x the tile's 256 rows arrive as one
+      // TMA box (row n at byte 16 n) NSTG groups ahead; the activation
+      // scales (in L2: the permute/act kernel just wrote them) are loaded to
+      // registers one group ahead.
+      const int ngroups = args.num_kb / 4;
+      const uint64_t pol_s = l2_policy(MOE_GEMM_L2_B);
+      const uint32_t stg_base = smem_u32(stg_ring);
+      struct Cursor {
+        int t, g, m_blk, n_tile, e;
       };
+      auto seek = [&](Cursor& c) {             // first tile at or after c.t with a valid expert
+        for (; c.t < total; c.t += gridDim.x) {
+          sched_tile(sched, c.t, c.m_blk, c.n_tile);
+          c.e = s_ids[c.m_blk];
+          if (c.e >= 0 && c.e < args.num_experts) {
+            c.g = 0;
+            return true;
+          }
+        }
+        return false;
+      };
+      auto step = [&](Cursor& c) {
+        if (++c.g < ngroups) return true;
+        c.t += gridDim.x;
+        return seek(c);
+      };
+      auto stage_group = [&](const Cursor& c, int slot) {   // lane 0
+        mbar_arrive_expect_tx(stg_full(slot), STG_BYTES);
+        tma_load_2d(stg_base + slot * STG_BYTES, &tmS, stg_full(slot), 16 * c.g,
+                    c.e * N + c.n_tile * BN, pol_s);
+      };
+      auto load_a = [&](const Cursor& c, float4 (&A)[4]) {
+        const float* pa = args.a_scale + ((size_t)c.m_blk * BM + lane) * args.num_kb + 4 * c.g;
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+          A[i] = __ldg(reinterpret_cast<const float4*>(pa + (size_t)32 * i * args.num_kb));
+      };
+      Cursor fill{(int)blockIdx.x, 0, 0, 0, 0};
+      bool fill_ok = seek(fill);
+      Cursor use = fill, anext = fill;
+      bool use_ok = fill_ok, anext_ok = fill_ok;
+      int nfill = 0, nuse = 0;
+      for (; nfill < NSTG && fill_ok; ++nfill) {
+        if (lane == 0) stage_group(fill, nfill);
+        fill_ok = step(fill);
+      }
       float4 a_cur[4], a_nxt[4];
-      uint4 b_cur[8], b_nxt[8];
-      load_group(0, a_cur, b_cur);
-      if (args.num_kb > 4) load_group(4, a_nxt, b_nxt);
-      for (int kb0 = 0; kb0 < args.num_kb && ok; kb0 += 4) {
+      if (use_ok) {
+        load_a(use, a_cur);
+        anext_ok = step(anext);
+        if (anext_ok) load_a(anext, a_nxt);
+      }
+      bool ok = true;
+      while (use_ok && ok) {
+        const int slot = nuse % NSTG;
+        int got = 1;
+        if (lane == 0)
+          got = mbar_wait_bounded(stg_full(slot), (nuse / NSTG) & 1, abort_flag, args.limit_ns,
+                                  args.err);
+        got = __shfl_sync(0xffffffffu, got, 0);
+        if (!got) break;
+        const uint32_t stg = stg_base + slot * STG_BYTES;
+        const int n0 = use.n_tile * BN + lane;    // this lane's rows: n0 + 32 c
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-          const int kb = kb0 + j;
-          if (kb >= args.num_kb) break;
           uint32_t aw[4], bw[8];
 #pragma unroll
           for (int c = 0; c < 4; ++c) {
@@ -262,35 +323,109 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             aw[c] = ((__float_as_uint(av) >> 23) & 0xFFu) * 0x01010101u;
           }
 #pragma unroll
-          for (int c = 0; c < 8; ++c)
-            bw[c] = j == 0 ? b_cur[c].x : j == 1 ? b_cur[c].y : j == 2 ? b_cur[c].z : b_cur[c].w;
-          int got = 1;
-          if (lane == 0)
-            got = mbar_wait_bounded(sempty_bar(sslot), sphase ^ 1, abort_flag, args.limit_ns,
-                                    args.err);
-          got = __shfl_sync(0xffffffffu, got, 0);
-          if (!got) {
+          for (int c = 0; c < 8; ++c)   // rows past N (ragged last tile): 2^0
+            bw[c] = n0 + 32 * c < N ? ld_shared_u32(stg + 16 * (lane + 32 * c) + 4 * j)
+                                    : 0x7F7F7F7Fu;
+          if (!put_slot(aw, bw)) {
             ok = false;
             break;
           }
-          // lane l: 16 bytes at row l of the A block and of both B blocks
-          uint4* dst = reinterpret_cast<uint4*>(sf_ring + sslot * SF_BYTES) + lane;
-          dst[0] = make_uint4(aw[0], aw[1], aw[2], aw[3]);
-          dst[32] = make_uint4(bw[0], bw[1], bw[2], bw[3]);
-          dst[64] = make_uint4(bw[4], bw[5], bw[6], bw[7]);
-          fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(sfull_bar(sslot));
-          if (++sslot == SSLOTS) {
-            sslot = 0;
-            sphase ^= 1;
-          }
         }
+        if (!ok) break;
+        ++nuse;
+        // this warp's reads of the staging slot come before the copy that refills it
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (fill_ok) {
+          if (lane == 0) stage_group(fill, nfill % NSTG);
+          ++nfill;
+          fill_ok = step(fill);
+        }
+        use_ok = step(use);
 #pragma unroll
         for (int c = 0; c < 4; ++c) a_cur[c] = a_nxt[c];
-#pragma unroll
-        for (int c = 0; c < 8; ++c) b_cur[c] = b_nxt[c];
-        if (kb0 + 8 < args.num_kb) load_group(kb0 + 8, a_nxt, b_nxt);
+        if (anext_ok) {
+          anext_ok = step(anext);
+          if (anext_ok) load_a(anext, a_nxt);
+        }
+      }
+      // copies issued but not consumed (a wait ran out) land before the CTA exits
+      if (lane == 0)
+        for (int k = nuse; k < nfill; ++k)
+          mbar_wait_bounded(stg_full(k % NSTG), (k / NSTG) & 1, nullptr, args.limit_ns, args.err);
+    } else {
+      const int kq = args.num_kb * 4;            // E8M0 bytes per weight row
+      const bool vec = (args.num_kb & 3) == 0;   // rows 16-byte aligned: vector loads
+      bool ok = true;
+      for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+        int m_blk, n_tile;
+        sched_tile(sched, t, m_blk, n_tile);
+        const int e = s_ids[m_blk];
+        if (e < 0 || e >= args.num_experts) continue;
+        // lane l builds rows l + 32 c of A (c < 4) and of B (c < 8); B rows
+        // past N (ragged last tile) read nothing
+        const float* sa_base = args.a_scale + ((size_t)m_blk * BM + lane) * args.num_kb;
+        const size_t sa_step = (size_t)32 * args.num_kb;             // floats per 32 rows
+        const uint8_t* sb_base = args.b_scale + ((size_t)e * N + (size_t)n_tile * BN + lane) * kq;
+        const size_t sb_step = (size_t)32 * kq;                      // bytes per 32 rows
+        const int n_valid = N - n_tile * BN - lane;                  // B row c valid if 32c < this
+        // scales of 4 K blocks per load, one group of 4 in flight ahead
+        auto load_group = [&](int g, float4 (&A)[4], uint4 (&B)[8]) {
+          const int n = args.num_kb - g;
+  #pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            const float* pa = sa_base + c * sa_step + g;
+            if (vec) {
+              A[c] = __ldg(reinterpret_cast<const float4*>(pa));
+            } else {
+              A[c] = make_float4(__ldg(pa), n > 1 ? __ldg(pa + 1) : 1.0f,
+                                 n > 2 ? __ldg(pa + 2) : 1.0f, n > 3 ? __ldg(pa + 3) : 1.0f);
+            }
+          }
+  #pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            const uint32_t* pb = reinterpret_cast<const uint32_t*>(sb_base + c * sb_step) + g;
+            if (32 * c >= n_valid) {
+              B[c] = make_uint4(0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu);
+            } else if (vec) {
+              B[c] = __ldg(reinterpret_cast<const uint4*>(pb));
+            } else {
+              B[c] = make_uint4(__ldg(pb), n > 1 ? __ldg(pb + 1) : 0u, n > 2 ? __ldg(pb + 2) : 0u,
+                                n > 3 ? __ldg(pb + 3) : 0u);
+            }
+          }
+        };
+        float4 a_cur[4], a_nxt[4];
+        uint4 b_cur[8], b_nxt[8];
+        load_group(0, a_cur, b_cur);
+        if (args.num_kb > 4) load_group(4, a_nxt, b_nxt);
+        for (int kb0 = 0; kb0 < args.num_kb && ok; kb0 += 4) {
+  #pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const int kb = kb0 + j;
+            if (kb >= args.num_kb) break;
+            uint32_t aw[4], bw[8];
+  #pragma unroll
+            for (int c = 0; c < 4; ++c) {
+              const float av = j == 0 ? a_cur[c].x : j == 1 ? a_cur[c].y : j == 2 ? a_cur[c].z
+                                                                                  : a_cur[c].w;
+              // a power-of-two fp32 scale 2^(x-127) has biased exponent x = its E8M0 code
+              aw[c] = ((__float_as_uint(av) >> 23) & 0xFFu) * 0x01010101u;
+            }
+  #pragma unroll
+            for (int c = 0; c < 8; ++c)
+              bw[c] = j == 0 ? b_cur[c].x : j == 1 ? b_cur[c].y : j == 2 ? b_cur[c].z : b_cur[c].w;
+            if (!put_slot(aw, bw)) {
+              ok = false;
+              break;
+            }
+          }
+  #pragma unroll
+          for (int c = 0; c < 4; ++c) a_cur[c] = a_nxt[c];
+  #pragma unroll
+          for (int c = 0; c < 8; ++c) b_cur[c] = b_nxt[c];
+          if (kb0 + 8 < args.num_kb) load_group(kb0 + 8, a_nxt, b_nxt);
+        }
       }
     }
   } else if (warp == 1 && lane == 0) {
@@ -347,7 +482,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   } else if (warp >= EPI_WARP0) {
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;                         // TMEM lane quadrant
-    const int half = (warp - EPI_WARP0) >> 2;       // 128-column half of the tile
     const int row_in_tile = q * 32 + lane;
     int local = 0;
     for (int t = blockIdx.x; t < total; t += gridDim.x) {
@@ -361,30 +495,32 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       ok = __shfl_sync(0xffffffffu, ok, 0);
       if (!ok) break;
       tc_fence_after();
-      const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + half * 128;
       const size_t row = (size_t)m_blk * BM + row_in_tile;
-      __nv_bfloat16* out_row = args.out + row * args.ldo + (size_t)n_tile * BN + half * 128;
-      // 256 columns, or 128 on a ragged last tile
-      const bool store = half * 128 < N - n_tile * BN;
-      // read the whole 128-column slice, hand the accumulator back to the
-      // MMA thread, then convert and store
-      uint32_t r[4][32];
+#pragma unroll 1
+      for (int half = 0; half < 2; ++half) {        // 128 columns at a time
+        const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + half * 128;
+        __nv_bfloat16* out_row = args.out + row * args.ldo + (size_t)n_tile * BN + half * 128;
+        const bool store = half * 128 < N - n_tile * BN;   // 256 columns, or 128 if ragged
+        uint32_t r[4][32];
 #pragma unroll
-      for (int c = 0; c < 4; ++c) tmem_ld_32x32b_x32(taddr + c * 32, r[c]);
-      tmem_ld_wait();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(tempty_bar);
-      if (store) {
-        uint4* dst = reinterpret_cast<uint4*>(out_row);
+        for (int c = 0; c < 4; ++c) tmem_ld_32x32b_x32(taddr + c * 32, r[c]);
+        tmem_ld_wait();
+        if (half == 1) {                            // the accumulator is read: hand it back
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(tempty_bar);
+        }
+        if (store) {
+          uint4* dst = reinterpret_cast<uint4*>(out_row);
 #pragma unroll
-        for (int v = 0; v < 16; ++v) {
-          uint4 pk;
-          __nv_bfloat16* pb = reinterpret_cast<__nv_bfloat16*>(&pk);
+          for (int v = 0; v < 16; ++v) {
+            uint4 pk;
+            __nv_bfloat16* pb = reinterpret_cast<__nv_bfloat16*>(&pk);
 #pragma unroll
-          for (int j = 0; j < 8; ++j)
-            pb[j] = __float2bfloat16_rn(__uint_as_float(r[v >> 2][8 * (v & 3) + j]));
-          dst[v] = pk;
+            for (int j = 0; j < 8; ++j)
+              pb[j] = __float2bfloat16_rn(__uint_as_float(r[v >> 2][8 * (v & 3) + j]));
+            dst[v] = pk;
+          }
         }
       }
       ++local;
@@ -428,12 +564,24 @@ cudaError_t launch_ggemm_mxfp4(const void* A, const float* a_scale, int cap, int
   a.group_max = sched_group_max(K, 1);
   watchdog_params(&a.limit_ns, &a.never_arrive);
   a.err = dev_error_word();
+  // weight scales staged by TMA when their rows are 16-byte multiples
+  const bool staged = K % 512 == 0 && (reinterpret_cast<uintptr_t>(b_scale) & 15u) == 0;
+  CUtensorMap tmS = tmB;        // unused by the register form
+  if (staged && !make_tmap_u8_rows(&tmS, b_scale, (uint64_t)b_rows_total, (uint64_t)(K / 32), 16,
+                                   BN))
+    return cudaErrorInvalidValue;
   static bool attr_done = false;
   if (!attr_done) {
-    cudaFuncSetAttribute(k_ggemm_mxfp4, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    cudaFuncSetAttribute(k_ggemm_mxfp4<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         SMEM_BYTES);
+    cudaFuncSetAttribute(k_ggemm_mxfp4<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         SMEM_BYTES);
     attr_done = true;
   }
-  k_ggemm_mxfp4<<<num_sms(), NUM_THREADS, SMEM_BYTES, stream>>>(tmA, tmB, a);
+  if (staged)
+    k_ggemm_mxfp4<true><<<num_sms(), NUM_THREADS, SMEM_BYTES, stream>>>(tmA, tmB, tmS, a);
+  else
+    k_ggemm_mxfp4<false><<<num_sms(), NUM_THREADS, SMEM_BYTES, stream>>>(tmA, tmB, tmS, a);
   return cudaGetLastError();
 }
 

@@ -29,7 +29,11 @@ def _ragged(counts, H, I, seed):
 
 
 @pytest.mark.parametrize("counts,H,I", [([0, 1, 127, 128, 129, 300], 512, 256),
-                                        ([7, 0, 260], 384, 384)])
+                                        ([7, 0, 260], 384, 384),
+                                        # K % 512 == 0: weight scales staged by TMA (GEMM2
+                                        # here, with a ragged last column tile, N = 640)
+                                        ([0, 1, 127, 128, 129, 300], 640, 512),
+                                        ([5, 200, 0, 131], 1024, 512)])
 def test_mxfp4_stages_ragged(counts, H, I):
     cfg, d = _ragged(counts, H, I, 9)
     p = moe.Problem.from_config(cfg)
