@@ -25,9 +25,11 @@ Modules:
   experts  -- permute, activation quantisation, grouped GEMMs, SiLU-and-mul,
               unpermute-reduce, the whole forward (permuted form) and the
               per-token brute-force form.
+  router   -- the step before the path: softmax / sigmoid scores, top-k
+              selection, renormalisation and the expert-parallel expert map.
 
 Every function has a pin in ``tests/test_oracle_*.py`` (library routines,
 closed forms, invariants, brute force, hand-worked fixtures); none is marked
 "parity unpinned".
 """
-from . import codecs, routing, experts  # noqa: F401
+from . import codecs, routing, experts, router  # noqa: F401
