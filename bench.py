@@ -380,6 +380,33 @@ def run_ours(args):
     if moe.moe_sync_status(stream) != 0:
         raise RuntimeError("device error in the e2e region")
 
+    # the step before the path (not in the step): the router on logits of
+    # this workload's shape, softmax + renormalise
+    gen = torch.Generator(device=dev).manual_seed(cfg.seed)
+    logits = torch.randn(cfg.M, cfg.E, device=dev, generator=gen)
+    r_w = torch.empty(cfg.M, cfg.topk, dtype=torch.float32, device=dev)
+    r_ids = torch.empty(cfg.M, cfg.topk, dtype=torch.int32, device=dev)
+    for _ in range(3):
+        moe.moe_topk_router(logits, cfg.topk, r_w, r_ids, stream=stream)
+    barrier()
+    # a launch is a few microseconds of GPU work, less than its host-side
+    # call: time 20 launches captured in a CUDA graph
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):          # captured on torch's side stream
+        for _ in range(20):
+            moe.moe_topk_router(logits, cfg.topk, r_w, r_ids)
+    graph.replay()
+    barrier()
+    rs, re_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    r_reps = 10
+    rs.record(stream)
+    for _ in range(r_reps):
+        graph.replay()
+    re_.record(stream)
+    barrier()
+    router_ms = rs.elapsed_time(re_) / (20 * r_reps)
+    router_bytes = cfg.M * cfg.E * 4 + cfg.M * cfg.topk * 8
+
     # max over ranks
     elapsed_ms, e2e_s, fused_ms = max_over_ranks([elapsed_ms, e2e_s, fused_ms], world, dev)
     ms = elapsed_ms / args.steps
@@ -423,6 +450,10 @@ def run_ours(args):
                                peaks["hbm_gbs"]},
             "e2e": {"value": world * R / e2e_s, "unit": UNIT, "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "ms_per_step": e2e_s * 1e3},
+            "router": {"ms": router_ms, "bytes": router_bytes,
+                       "gbs": router_bytes / (router_ms * 1e-3) / 1e9,
+                       "note": "moe_topk_router on [M, E] fp32 logits (softmax, renormalise); "
+                               "the step before the path, not part of a step"},
             "gpu_launches": launches_per_step * args.steps,
             "clocks": clk.summary(),
         }

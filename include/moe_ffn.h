@@ -134,6 +134,32 @@ moe_status moe_align_permute(const moe_problem* p, const void* x, const int32_t*
                              float* x_perm_scale, void* workspace, size_t workspace_bytes,
                              void* stream);
 
+/* Router: the step before the path (page "fused_moe.py 分析", section
+ * "topk_ids, topk_weights 的由来以及内容": fused_topk with scoring_func softmax
+ * or sigmoid and renormalize; expert_map from the same page).  For each of M
+ * tokens (one row of logits[M, E], device, row-major, fp32 or bf16 with
+ * logits_bf16 != 0):
+ *  - the k experts with the largest logits -- the largest scores, since both
+ *    scores increase with the logit; equal logits in ascending expert order --
+ *    go to topk_ids[t, 0..k) in that order;
+ *  - their scores (softmax over the row's E logits, or sigmoid of the logit)
+ *    go to topk_weights[t, 0..k) (fp32), divided by the k scores' sum when
+ *    renormalize != 0;
+ *  - token_expert_indices[t, i] = t*k + i, the routed-item index (may be NULL);
+ *  - with expert_map (device, E int32: the expert's id on this expert-parallel
+ *    shard, or -1 when it lives elsewhere; may be NULL) the ids written are
+ *    expert_map[id]; -1 ids are skipped by every stage of the path.
+ * All outputs are device buffers of M*k elements, written on `stream`.
+ * Errors: MOE_ERR_INVALID_ARG when M < 0 or M > MOE_MAX_TOKENS, E < 1 or
+ * E > MOE_MAX_EXPERTS, topk < 1 or topk > min(E, MOE_MAX_TOPK), scoring is
+ * not a moe_scoring value, or logits / topk_weights / topk_ids is NULL with
+ * M > 0.  M = 0 returns MOE_OK without launching. */
+typedef enum { MOE_SCORE_SOFTMAX = 0, MOE_SCORE_SIGMOID = 1 } moe_scoring;
+moe_status moe_topk_router(int M, int E, int topk, const void* logits, int logits_bf16,
+                           int scoring, int renormalize, const int32_t* expert_map,
+                           float* topk_weights, int32_t* topk_ids,
+                           int32_t* token_expert_indices, void* stream);
+
 /* Stage 1 without a workspace, for callers that cannot allocate device memory
  * when they call the library -- for example a serving engine that reserves the
  * whole device for its own memory pool and does not let plug-ins call

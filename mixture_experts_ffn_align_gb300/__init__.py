@@ -30,7 +30,7 @@ EXPORTS = ["moe_m_sum_bound", "moe_align_workspace_bytes", "moe_workspace_bytes"
            "grouped_gemm_w2", "unpermute_reduce", "fused_experts", "fused_experts_from_host",
            "moe_sync_status", "moe_status_string", "moe_debug_set_watchdog",
            "moe_debug_set_bf16_gemm_form",
-           "moe_align_permute_noalloc", "moe_last_error_string"]
+           "moe_align_permute_noalloc", "moe_last_error_string", "moe_topk_router"]
 
 NOALLOC_SCRATCH_BYTES = 1 << 20   # MOE_NOALLOC_SCRATCH_BYTES in include/moe_ffn.h
 
@@ -100,6 +100,7 @@ def lib() -> ctypes.CDLL:
         L.fused_experts.argtypes = [P] + [vp] * 9 + [sz, vp]
         L.fused_experts_from_host.argtypes = [P] + [vp] * 9 + [sz, vp]
         L.moe_sync_status.argtypes = [vp]
+        L.moe_topk_router.argtypes = [i32, i32, i32, vp, i32, i32, i32, vp, vp, vp, vp, vp]
         L.moe_status_string.argtypes, L.moe_status_string.restype = [i32], ctypes.c_char_p
         L.moe_last_error_string.argtypes, L.moe_last_error_string.restype = [], ctypes.c_char_p
         L.moe_debug_set_watchdog.argtypes, L.moe_debug_set_watchdog.restype = \
@@ -108,7 +109,7 @@ def lib() -> ctypes.CDLL:
             [i32], None
         for n in ("moe_align_permute", "grouped_gemm_w13", "act_mul_quant", "grouped_gemm_w2",
                   "unpermute_reduce", "fused_experts", "fused_experts_from_host",
-                  "moe_sync_status"):
+                  "moe_sync_status", "moe_topk_router"):
             getattr(L, n).restype = i32
         _lib = L
     return _lib
@@ -203,6 +204,25 @@ def grouped_gemm_w2(p: Problem, z, z_scale, w2, w2_scale, block_expert_ids, num_
 def unpermute_reduce(p: Problem, y2, inv_perm, topk_weights, y, stream=None):
     _check(lib().unpermute_reduce(_cp(p), _p(y2), _p(inv_perm), _p(topk_weights), _p(y),
                                   _stream(stream)), "unpermute_reduce")
+
+
+SCORING = {"softmax": 0, "sigmoid": 1}
+
+
+def moe_topk_router(logits, topk, topk_weights, topk_ids, token_expert_indices=None,
+                    scoring="softmax", renormalize=True, expert_map=None, stream=None):
+    """Router (softmax or sigmoid scores, top-k, optional renormalisation and
+    expert map) into caller-allocated [M, topk] float32 / int32 tensors;
+    logits [M, E] float32 or bfloat16, all on the device."""
+    import torch
+    M, E = logits.shape
+    bf16 = logits.dtype == torch.bfloat16
+    if not bf16 and logits.dtype != torch.float32:
+        raise TypeError("logits must be float32 or bfloat16")
+    _check(lib().moe_topk_router(int(M), int(E), int(topk), _p(logits), int(bf16),
+                                 SCORING[scoring], int(bool(renormalize)), _p(expert_map),
+                                 _p(topk_weights), _p(topk_ids), _p(token_expert_indices),
+                                 _stream(stream)), "moe_topk_router")
 
 
 def fused_experts(p: Problem, x, w13, w13_scale, w2, w2_scale, topk_weights, topk_ids, y,

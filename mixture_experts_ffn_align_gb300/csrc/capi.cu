@@ -396,6 +396,22 @@ const char* moe_status_string(moe_status s) {
   return "MOE_ERR_UNKNOWN";
 }
 
+moe_status moe_topk_router(int M, int E, int topk, const void* logits, int logits_bf16,
+                           int scoring, int renormalize, const int32_t* expert_map,
+                           float* topk_weights, int32_t* topk_ids,
+                           int32_t* token_expert_indices, void* stream) {
+  if (M < 0 || M > MOE_MAX_TOKENS || E < 1 || E > MOE_MAX_EXPERTS || topk < 1 ||
+      topk > MOE_MAX_TOPK || topk > E ||
+      (scoring != MOE_SCORE_SOFTMAX && scoring != MOE_SCORE_SIGMOID))
+    return MOE_ERR_INVALID_ARG;
+  if (M == 0) return MOE_OK;
+  if (!logits || !topk_weights || !topk_ids) return MOE_ERR_INVALID_ARG;
+  return cuda_status(launch_topk_router(logits, logits_bf16 != 0, M, E, topk,
+                                        scoring == MOE_SCORE_SIGMOID, renormalize != 0,
+                                        expert_map, topk_weights, topk_ids,
+                                        token_expert_indices, static_cast<cudaStream_t>(stream)));
+}
+
 void moe_debug_set_watchdog(int64_t limit_ns, int never_arrive) {
   g_watchdog_ns = limit_ns > 0 ? limit_ns : 0;
   g_never_arrive = never_arrive != 0;

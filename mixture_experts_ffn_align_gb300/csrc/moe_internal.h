@@ -40,6 +40,11 @@ cudaError_t launch_unpermute_reduce(const void* y2, int H, int M, int topk,
                                     const int32_t* inv_perm, const float* topk_weights,
                                     bool unit_weights, void* y, cudaStream_t stream);
 
+// Router: softmax / sigmoid top-k per token, one warp per token.
+cudaError_t launch_topk_router(const void* logits, bool bf16, int M, int E, int k, bool sigmoid,
+                               bool renorm, const int32_t* expert_map, float* w, int32_t* ids,
+                               int32_t* tei, cudaStream_t stream);
+
 // bf16 grouped GEMM on tcgen05: out[row, n] = sum_k A[row, k] * B[e*b_rows + n, k].
 //   fuse_act: B tile = 128 gate rows + 128 up rows; writes SiLU(g)*u (bf16).
 cudaError_t launch_ggemm_bf16(const void* A, int cap, int K, const void* B, int b_rows_total,

@@ -95,6 +95,24 @@ def test_gemm_block_size_must_equal_tile_height():
     assert L.grouped_gemm_w13(ctypes.byref(p.c()), d, None, d, None, d, d, d, None, 1, None) == 2
 
 
+@pytest.mark.parametrize("M,E,k,scoring", [(-1, 8, 2, 0), (16385, 8, 2, 0), (4, 0, 1, 0),
+                                            (4, 1025, 2, 0), (4, 8, 0, 0), (4, 8, 9, 0),
+                                            (4, 64, 17, 0), (4, 8, 2, 2)])
+def test_router_invalid_arguments_rejected(M, E, k, scoring):
+    L = moe.lib()
+    dummy = ctypes.c_void_p(16)   # never dereferenced: validation fails first
+    st = L.moe_topk_router(M, E, k, dummy, 0, scoring, 1, None, dummy, dummy, None, None)
+    assert st == 1   # MOE_ERR_INVALID_ARG
+
+
+def test_router_empty_batch_and_null_outputs():
+    L = moe.lib()
+    assert L.moe_topk_router(0, 8, 2, None, 0, 0, 1, None, None, None, None, None) == 0
+    dummy = ctypes.c_void_p(16)
+    assert L.moe_topk_router(4, 8, 2, dummy, 0, 0, 1, None, None, dummy, None, None) == 1
+    assert L.moe_topk_router(4, 8, 2, None, 0, 0, 1, None, dummy, dummy, None, None) == 1
+
+
 def test_status_strings():
     for code, name in moe.STATUS.items():
         assert moe.moe_status_string(code) == name
