@@ -305,3 +305,28 @@ def _fp8_matvec(qa, sa, w_codes, w_scale):
     part = np.einsum("nbj,bj->nb", qb.reshape(N, K // 128, 128), qa.reshape(K // 128, 128))
     sb = np.repeat(np.asarray(w_scale, dtype=np.float64), 128, axis=0)[:N]   # [N, K/128]
     return (sa[None, :] * sb * part).sum(axis=1)
+
+
+def batched_experts(x_b, counts, w13, w2, w13_scale=None, w2_scale=None, *, quant="bf16",
+                    act_scale_fmt="fp32"):
+    """The BatchedExperts layout (page "fused_moe.py 分析", activation formats:
+    [E, max_tokens, K], one buffer per local expert; page "Blackwell 上的
+    DeepGEMM FusedMoE（vLLM）", §2.5: the per-expert counts come with the
+    dispatch and the experts run a masked grouped GEMM).
+
+    For each expert e and row r < clamp(counts[e], 0, T): y[e, r] = expert e's
+    MLP of x[e, r] with the path's roundings -- form 1 with a single slot of
+    weight 1 routed to e, whose bf16 output rounding leaves the bf16 W2 output
+    unchanged.  No router weight is applied.  Rows past a count are NaN (they
+    have no meaning).  Returns y [E, T, H]."""
+    x_b = np.asarray(x_b, dtype=np.float64)
+    E, T, H = x_b.shape
+    y = np.full((E, T, H), np.nan)
+    for e in range(E):
+        c = min(max(int(counts[e]), 0), T)
+        if c == 0:
+            continue
+        y[e, :c] = fused_experts_per_token(
+            x_b[e, :c], np.full((c, 1), e), np.ones((c, 1)), w13, w2, w13_scale, w2_scale,
+            quant=quant, act_scale_fmt=act_scale_fmt)
+    return y

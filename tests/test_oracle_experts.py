@@ -247,3 +247,29 @@ def test_planted_fp8_scale_mistake_is_caught(monkeypatch):
     monkeypatch.setattr(experts, "quant_act_1x128", wrong)
     with pytest.raises(AssertionError):
         test_activation_quant_against_torch_cast()
+
+
+@pytest.mark.parametrize("name", ["bf16", "fp8", "mxfp4"])
+def test_batched_layout_equals_permuted_form(name):
+    """The batched layout's rows through the permuted form (form 2) with one
+    slot of weight 1 routed to each row's expert give the same values; rows
+    past a count are NaN; counts are clamped to [0, T]."""
+    cfg = SMALL[name]
+    a = _inputs(cfg)
+    E, H, T = cfg.E, cfg.H, 5
+    rng = np.random.default_rng(2)
+    x_b = np.stack([a["x"][rng.integers(0, cfg.M, T)] for _ in range(E)])     # [E, T, H]
+    counts = np.array([T, 0, 3, 9][:E] + [1] * max(0, E - 4))                  # 9 > T: clamped
+    kw = dict(quant=cfg.quant, act_scale_fmt=cfg.act_scale_fmt)
+    y_b = experts.batched_experts(x_b, counts, a["w13"], a["w2"], a["w13_scale"], a["w2_scale"],
+                                  **kw)
+    rows, ids = [], []
+    for e in range(E):
+        c = min(max(int(counts[e]), 0), T)
+        rows += [x_b[e, r] for r in range(c)]
+        ids += [e] * c
+        assert np.all(np.isnan(y_b[e, c:]))
+    f2 = experts.fused_experts(np.array(rows), np.array(ids)[:, None], np.ones((len(ids), 1)),
+                               a["w13"], a["w2"], a["w13_scale"], a["w2_scale"], **kw)["y"]
+    got = np.concatenate([y_b[e, :min(int(counts[e]), T)] for e in range(E)])
+    np.testing.assert_array_equal(got, f2)
