@@ -134,6 +134,40 @@ moe_status moe_align_permute(const moe_problem* p, const void* x, const int32_t*
                              float* x_perm_scale, void* workspace, size_t workspace_bytes,
                              void* stream);
 
+/* The batched (masked) expert layout, for decode steps captured in CUDA
+ * graphs (page "fused_moe.py 分析", activation formats Standard [M, K] and
+ * BatchedExperts [E, max_tokens, K]; page "Blackwell 上的 DeepGEMM FusedMoE（vLLM）",
+ * §2.5: DeepEP low-latency dispatch hands over [E_local, max_tokens, K] with
+ * the per-expert token counts, and the experts run a masked grouped GEMM; the
+ * expected_m hint of the same pages).  For each expert e and each row
+ * r < expert_num_tokens[e]:
+ *   y[e, r, :] = W2_e( SiLU(W1gate_e x[e, r, :]) * (W1up_e x[e, r, :]) )
+ * with the path's roundings (bf16 GEMM outputs; in the quantised modes x and
+ * the activation are quantised per 1x128 group as in stages 1 and 3).  No
+ * router weight is applied (the combine after the experts applies it).
+ *  - p: E, H, I, block_size (must be 128), quant, act_scale_fmt as for
+ *    fused_experts; p->M, p->topk and apply_router_weight_on_input are ignored.
+ *  - x, y: device, [E, max_tokens, H] bf16, row-major; rows of y at or past a
+ *    count are left as they were or hold values of no meaning.
+ *  - expert_num_tokens: device, E int32, read on the device (a graph replay
+ *    sees the counts of the moment); each is clamped to [0, max_tokens].
+ *  - max_tokens: a positive multiple of 128, E * max_tokens <= MOE_MAX_TOKENS *
+ *    MOE_MAX_TOPK.
+ *  - expected_m: expected tokens per expert (0 if unknown); picks the tile
+ *    form of the bf16 GEMMs (SM pairs from 256 up), never the results.
+ *  - workspace: device, at least moe_batched_workspace_bytes(p, max_tokens).
+ * Nothing is allocated and the host never waits on the device, so a call can
+ * be captured in a CUDA graph once a first call has run outside capture.
+ * Errors: MOE_ERR_INVALID_ARG (bad sizes or NULL pointers),
+ * MOE_ERR_UNSUPPORTED (as for fused_experts), MOE_ERR_WORKSPACE_TOO_SMALL,
+ * MOE_ERR_CUDA. */
+size_t moe_batched_workspace_bytes(const moe_problem* p, int max_tokens);
+moe_status fused_experts_batched(const moe_problem* p, const void* x,
+                                 const int32_t* expert_num_tokens, int max_tokens,
+                                 int expected_m, const void* w13, const void* w13_scale,
+                                 const void* w2, const void* w2_scale, void* y, void* workspace,
+                                 size_t workspace_bytes, void* stream);
+
 /* Router: the step before the path (page "fused_moe.py 分析", section
  * "topk_ids, topk_weights 的由来以及内容": fused_topk with scoring_func softmax
  * or sigmoid and renormalize; expert_map from the same page).  For each of M

@@ -30,7 +30,8 @@ EXPORTS = ["moe_m_sum_bound", "moe_align_workspace_bytes", "moe_workspace_bytes"
            "grouped_gemm_w2", "unpermute_reduce", "fused_experts", "fused_experts_from_host",
            "moe_sync_status", "moe_status_string", "moe_debug_set_watchdog",
            "moe_debug_set_bf16_gemm_form",
-           "moe_align_permute_noalloc", "moe_last_error_string", "moe_topk_router"]
+           "moe_align_permute_noalloc", "moe_last_error_string", "moe_topk_router",
+           "moe_batched_workspace_bytes", "fused_experts_batched"]
 
 NOALLOC_SCRATCH_BYTES = 1 << 20   # MOE_NOALLOC_SCRATCH_BYTES in include/moe_ffn.h
 
@@ -101,6 +102,9 @@ def lib() -> ctypes.CDLL:
         L.fused_experts_from_host.argtypes = [P] + [vp] * 9 + [sz, vp]
         L.moe_sync_status.argtypes = [vp]
         L.moe_topk_router.argtypes = [i32, i32, i32, vp, i32, i32, i32, vp, vp, vp, vp, vp]
+        L.moe_batched_workspace_bytes.argtypes = [P, i32]
+        L.moe_batched_workspace_bytes.restype = sz
+        L.fused_experts_batched.argtypes = [P, vp, vp, i32, i32, vp, vp, vp, vp, vp, vp, sz, vp]
         L.moe_status_string.argtypes, L.moe_status_string.restype = [i32], ctypes.c_char_p
         L.moe_last_error_string.argtypes, L.moe_last_error_string.restype = [], ctypes.c_char_p
         L.moe_debug_set_watchdog.argtypes, L.moe_debug_set_watchdog.restype = \
@@ -109,7 +113,7 @@ def lib() -> ctypes.CDLL:
             [i32], None
         for n in ("moe_align_permute", "grouped_gemm_w13", "act_mul_quant", "grouped_gemm_w2",
                   "unpermute_reduce", "fused_experts", "fused_experts_from_host",
-                  "moe_sync_status", "moe_topk_router"):
+                  "moe_sync_status", "moe_topk_router", "fused_experts_batched"):
             getattr(L, n).restype = i32
         _lib = L
     return _lib
@@ -204,6 +208,21 @@ def grouped_gemm_w2(p: Problem, z, z_scale, w2, w2_scale, block_expert_ids, num_
 def unpermute_reduce(p: Problem, y2, inv_perm, topk_weights, y, stream=None):
     _check(lib().unpermute_reduce(_cp(p), _p(y2), _p(inv_perm), _p(topk_weights), _p(y),
                                   _stream(stream)), "unpermute_reduce")
+
+
+def moe_batched_workspace_bytes(p: Problem, max_tokens: int) -> int:
+    return int(lib().moe_batched_workspace_bytes(_cp(p), int(max_tokens)))
+
+
+def fused_experts_batched(p: Problem, x, expert_num_tokens, w13, w13_scale, w2, w2_scale, y,
+                          workspace, expected_m=0, stream=None):
+    """Expert MLPs on the batched layout x [E, max_tokens, H] (bf16) with
+    per-expert counts (int32 [E]) into y of the same shape."""
+    E, T, _ = x.shape
+    _check(lib().fused_experts_batched(
+        _cp(p), _p(x), _p(expert_num_tokens), int(T), int(expected_m), _p(w13), _p(w13_scale),
+        _p(w2), _p(w2_scale), _p(y), _p(workspace), workspace.numel() * workspace.element_size(),
+        _stream(stream)), "fused_experts_batched")
 
 
 SCORING = {"softmax": 0, "sigmoid": 1}

@@ -127,6 +127,45 @@ Layout layout(const moe_problem* p) {
   return L;
 }
 
+// The batched layout [E, T, H] (T = max_tokens): T a positive multiple of the
+// 128-row tile and E*T within the rows the GEMM schedules hold.
+bool valid_batched(const moe_problem* p, int max_tokens) {
+  if (p == nullptr || p->E < 1 || p->E > MOE_MAX_EXPERTS || p->H <= 0 || p->I <= 0 ||
+      p->block_size != 128 || max_tokens <= 0 || max_tokens % 128 != 0)
+    return false;
+  if (p->quant != MOE_Q_BF16 && p->quant != MOE_Q_FP8_BLOCK128 && p->quant != MOE_Q_MXFP4_W4A8)
+    return false;
+  if (p->act_scale_fmt != MOE_SCALE_FP32 && p->act_scale_fmt != MOE_SCALE_UE8M0) return false;
+  if (p->H % 128 != 0 || p->I % 128 != 0) return false;
+  return (int64_t)p->E * max_tokens <= (int64_t)MOE_MAX_TOKENS * MOE_MAX_TOPK;
+}
+
+struct BatchedLayout {
+  size_t blocks, npp, sorted, xq, xscale, h1, z, zscale, total;
+};
+
+BatchedLayout batched_layout(const moe_problem* p, int max_tokens) {
+  BatchedLayout L{};
+  const size_t rows = (size_t)p->E * max_tokens, H = p->H, I = p->I;
+  const bool q = quantised(p);
+  size_t o = 0;
+  auto take = [&](size_t bytes) {
+    const size_t at = o;
+    o = align_up(o + bytes);
+    return at;
+  };
+  L.blocks = take(rows / 128 * 4);
+  L.npp = take(4);
+  L.sorted = q ? take(rows * 4) : 0;
+  L.xq = q ? take(rows * H) : 0;
+  L.xscale = q ? take(rows * (H / 128) * 4) : 0;
+  L.h1 = q ? take(rows * 2 * I * 2) : 0;
+  L.z = take(rows * I * (q ? 1 : 2));
+  L.zscale = q ? take(rows * (I / 128) * 4) : 0;
+  L.total = o;
+  return L;
+}
+
 thread_local char g_last_error[256] = "";
 
 // Records the CUDA error of a failed call for moe_last_error_string.
@@ -206,12 +245,12 @@ namespace {
 // stages per MMA, which pays once the experts average two or more 128-row
 // blocks; below that most pairs would carry a lone block whose second half
 // repeats the first.
-cudaError_t launch_bf16_gemm(const moe_problem* p, const void* A, int cap, int K, const void* B,
-                             int b_rows_total, int b_rows_per_expert, int n_out,
+// rows_per_expert: the expected routed rows per expert.
+cudaError_t launch_bf16_gemm(int64_t rows_per_expert, const void* A, int cap, int K,
+                             const void* B, int b_rows_total, int b_rows_per_expert, int n_out,
                              const int32_t* block_expert_ids, const int32_t* num_post_padded,
                              void* out, bool fuse_act, cudaStream_t s) {
-  const bool pairs = g_bf16_form == 2 ||
-                     (g_bf16_form == 0 && (int64_t)p->M * p->topk >= 2LL * 128 * p->E);
+  const bool pairs = g_bf16_form == 2 || (g_bf16_form == 0 && rows_per_expert >= 2 * 128);
   return (pairs ? launch_ggemm_bf16_2sm : launch_ggemm_bf16)(
       A, cap, K, B, b_rows_total, b_rows_per_expert, n_out, block_expert_ids, num_post_padded,
       out, fuse_act, s);
@@ -232,9 +271,9 @@ moe_status grouped_gemm_w13(const moe_problem* p, const void* x_perm, const floa
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const int cap = (int)cap_rows(p);
   if (p->quant == MOE_Q_BF16) {
-    return cuda_status(launch_bf16_gemm(p, x_perm, cap, p->H, w13, p->E * 2 * p->I, 2 * p->I,
-                                         2 * p->I, block_expert_ids, num_post_padded, out,
-                                         fuse_act != 0, s));
+    return cuda_status(launch_bf16_gemm((int64_t)p->M * p->topk / p->E, x_perm, cap, p->H, w13,
+                                        p->E * 2 * p->I, 2 * p->I, 2 * p->I, block_expert_ids,
+                                        num_post_padded, out, fuse_act != 0, s));
   }
   if (fuse_act) return MOE_ERR_UNSUPPORTED;
   if (!x_scale || !w13_scale) return MOE_ERR_INVALID_ARG;
@@ -272,8 +311,9 @@ moe_status grouped_gemm_w2(const moe_problem* p, const void* z, const float* z_s
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const int cap = (int)cap_rows(p);
   if (p->quant == MOE_Q_BF16) {
-    return cuda_status(launch_bf16_gemm(p, z, cap, p->I, w2, p->E * p->H, p->H, p->H,
-                                         block_expert_ids, num_post_padded, y2, false, s));
+    return cuda_status(launch_bf16_gemm((int64_t)p->M * p->topk / p->E, z, cap, p->I, w2,
+                                        p->E * p->H, p->H, p->H, block_expert_ids,
+                                        num_post_padded, y2, false, s));
   }
   if (!z_scale || !w2_scale) return MOE_ERR_INVALID_ARG;
   if (p->quant == MOE_Q_MXFP4_W4A8)
@@ -394,6 +434,63 @@ const char* moe_status_string(moe_status s) {
     case MOE_ERR_DEVICE_BAD_INDEX: return "MOE_ERR_DEVICE_BAD_INDEX";
   }
   return "MOE_ERR_UNKNOWN";
+}
+
+size_t moe_batched_workspace_bytes(const moe_problem* p, int max_tokens) {
+  if (!valid_batched(p, max_tokens)) return 0;
+  return batched_layout(p, max_tokens).total;
+}
+
+moe_status fused_experts_batched(const moe_problem* p, const void* x,
+                                 const int32_t* expert_num_tokens, int max_tokens,
+                                 int expected_m, const void* w13, const void* w13_scale,
+                                 const void* w2, const void* w2_scale, void* y, void* workspace,
+                                 size_t workspace_bytes, void* stream) {
+  if (!valid_batched(p, max_tokens) || expected_m < 0) return MOE_ERR_INVALID_ARG;
+  if (!x || !expert_num_tokens || !w13 || !w2 || !y || !workspace) return MOE_ERR_INVALID_ARG;
+  if (quantised(p) && (!w13_scale || !w2_scale)) return MOE_ERR_INVALID_ARG;
+  if (!gemm_supported(p)) return MOE_ERR_UNSUPPORTED;
+  const BatchedLayout L = batched_layout(p, max_tokens);
+  if (workspace_bytes < L.total) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  int32_t* blocks = reinterpret_cast<int32_t*>(ws + L.blocks);
+  int32_t* npp = reinterpret_cast<int32_t*>(ws + L.npp);
+  int32_t* sorted = quantised(p) ? reinterpret_cast<int32_t*>(ws + L.sorted) : nullptr;
+  float* xscale = reinterpret_cast<float*>(ws + L.xscale);
+  float* zscale = reinterpret_cast<float*>(ws + L.zscale);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int rows = p->E * max_tokens, H = p->H, I = p->I, E = p->E;
+  const bool ue8m0 = p->act_scale_fmt == MOE_SCALE_UE8M0;
+  cudaError_t e = launch_batched_blocks(expert_num_tokens, E, max_tokens, blocks, npp, sorted, s);
+  if (e != cudaSuccess) return cuda_status(e);
+  if (!quantised(p)) {
+    // the layout's rows are GEMM1's rows as they are: no permute
+    e = launch_bf16_gemm(expected_m, x, rows, H, w13, E * 2 * I, 2 * I, 2 * I, blocks, npp,
+                         ws + L.z, true, s);
+    if (e == cudaSuccess)
+      e = launch_bf16_gemm(expected_m, ws + L.z, rows, I, w2, E * H, H, H, blocks, npp, y,
+                           false, s);
+    return cuda_status(e);
+  }
+  // quantised: per-row dynamic quantisation of the layout, then the same stages
+  e = launch_permute_rows(x, H, 1, rows, sorted, npp, nullptr, ws + L.xq, xscale, ue8m0, rows, s);
+  if (e != cudaSuccess) return cuda_status(e);
+  if (p->quant == MOE_Q_MXFP4_W4A8)
+    e = launch_ggemm_mxfp4(ws + L.xq, xscale, rows, H, w13, static_cast<const uint8_t*>(w13_scale),
+                           E * 2 * I, 2 * I, 2 * I, blocks, npp, ws + L.h1, s);
+  else
+    e = launch_ggemm_fp8(ws + L.xq, xscale, rows, H, w13, static_cast<const float*>(w13_scale),
+                         E * 2 * I, 2 * I, 2 * I, blocks, npp, ws + L.h1, s);
+  if (e != cudaSuccess) return cuda_status(e);
+  e = launch_act_mul(ws + L.h1, I, npp, ws + L.z, zscale, ue8m0, rows, s);
+  if (e != cudaSuccess) return cuda_status(e);
+  if (p->quant == MOE_Q_MXFP4_W4A8)
+    e = launch_ggemm_mxfp4(ws + L.z, zscale, rows, I, w2, static_cast<const uint8_t*>(w2_scale),
+                           E * H, H, H, blocks, npp, y, s);
+  else
+    e = launch_ggemm_fp8(ws + L.z, zscale, rows, I, w2, static_cast<const float*>(w2_scale),
+                         E * H, H, H, blocks, npp, y, s);
+  return cuda_status(e);
 }
 
 moe_status moe_topk_router(int M, int E, int topk, const void* logits, int logits_bf16,

@@ -40,6 +40,13 @@ cudaError_t launch_unpermute_reduce(const void* y2, int H, int M, int topk,
                                     const int32_t* inv_perm, const float* topk_weights,
                                     bool unit_weights, void* y, cudaStream_t stream);
 
+// Batched layout [E, T, H] (T % 128 == 0): per-expert counts -> block expert
+// ids of the E*T/128 row blocks (-1 past a count), num_post_padded = E*T, and
+// (if sorted_ids != nullptr) the identity row map with padding id E*T.
+cudaError_t launch_batched_blocks(const int32_t* counts, int E, int T, int32_t* block_expert_ids,
+                                  int32_t* num_post_padded, int32_t* sorted_ids,
+                                  cudaStream_t stream);
+
 // Router: softmax / sigmoid top-k per token, one warp per token.
 cudaError_t launch_topk_router(const void* logits, bool bf16, int M, int E, int k, bool sigmoid,
                                bool renorm, const int32_t* expert_map, float* w, int32_t* ids,
