@@ -55,7 +55,9 @@ _LABEL = {"mixtral": "Mixtral-8x7B-shaped prefill", "decode": "Mixtral-8x7B-shap
 
 def _workload(args):
     from moe_synth import get_config
-    cfg = get_config(args.workload)
+    # the batched layout runs the decode workload's rows (reference arm: the
+    # same per-row expert MLPs through the oracle)
+    cfg = get_config("decode" if args.workload == "decode_batched" else args.workload)
     if args.tokens:
         cfg = cfg.with_(M=args.tokens, name=f"{cfg.name}-M{args.tokens}")
     if args.experts:
@@ -216,6 +218,26 @@ def _traffic(cfg):
                 and r.get("source_sha") == kernel_source_sha(kind)):
             return r["dram_bytes_per_launch"]
     return None
+
+
+def _gemm1_roofline(cfg, peaks, peak, ratio, flops, w13_bytes, ms):
+    """Roofline object of GEMM1: tensor-bound when its FLOPs take at least as
+    long at the tensor peak as its weights at the HBM peak, else HBM-bound
+    (decode and the one-block-per-expert MXFP4 workload stream weights)."""
+    t_flop = flops / (peak * 1e12)
+    t_mem = w13_bytes / (peaks["hbm_gbs"] * 1e9)
+    tflops = flops / (ms * 1e-3) / 1e12
+    gbs = w13_bytes / (ms * 1e-3) / 1e9
+    common = {"kernel": gemm1_kernel(cfg)[1], "traffic": _traffic(cfg),
+              "tensor_frac": tflops / peak, "weight_hbm_frac": gbs / peaks["hbm_gbs"]}
+    if t_flop >= t_mem:
+        return {"bound": "tensor", "achieved": tflops, "peak": peak, "unit": "TFLOP/s",
+                "frac": tflops / peak,
+                "peak_source": f"bf16_tflops_sustained x {ratio:g} ({peaks['source']})",
+                "algorithmic_per_launch": f"2*R*H*2I = {flops:.4e} FLOP", **common}
+    return {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+            "frac": gbs / peaks["hbm_gbs"], "peak_source": f"hbm_gbs ({peaks['source']})",
+            "algorithmic_per_launch": f"w13 bytes E*2I*H*b = {w13_bytes:.4e} B", **common}
 
 
 def _cores():
@@ -437,13 +459,8 @@ def run_ours(args):
             "tflops": (gemm1_flops + gemm2_flops) / (ms * 1e-3) / 1e12,
             "stages_ms": stage_ms,
             "fused_call_ms": fused_ms,
-            "roofline": {"bound": "tensor", "kernel": gemm1_kernel(cfg)[1],
-                         "achieved": ach, "peak": peak, "unit": "TFLOP/s",
-                         "frac": ach / peak, "traffic": _traffic(cfg),
-                         "peak_source": (f"bf16_tflops_sustained x {ratio:g} ({peaks['source']})"),
-                         "algorithmic_per_launch": f"2*R*H*2I = {gemm1_flops:.4e} FLOP",
-                         "weight_hbm_frac": w13_bytes / (stage_ms[g1] * 1e-3) / 1e9 /
-                         peaks["hbm_gbs"]},
+            "roofline": _gemm1_roofline(cfg, peaks, peak, ratio, gemm1_flops, w13_bytes,
+                                        stage_ms[g1]),
             "gemm2_roofline": {"achieved": gemm2_flops / (stage_ms["gemm2"] * 1e-3) / 1e12,
                                "frac": gemm2_flops / (stage_ms["gemm2"] * 1e-3) / 1e12 / peak,
                                "weight_hbm_frac": w2_bytes / (stage_ms["gemm2"] * 1e-3) / 1e9 /
@@ -475,6 +492,135 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
+def run_batched(args):
+    """The batched expert layout at the Mixtral-shaped decode size: x [E, T, H]
+    with the decode routing's per-expert counts, T = 128; one step = one
+    fused_experts_batched call (count-to-block kernel, GEMM1 with SiLU-and-mul,
+    GEMM2), counts read on the device."""
+    import torch
+    import torch.distributed as dist
+
+    import mixture_experts_ffn_align_gb300 as moe
+    from moe_synth import get_config, make_inputs
+
+    world, rank, local = _dist()
+    if world > 1:
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    moe.lib()
+    cfg = get_config("decode")
+    if rank > 0:
+        cfg = cfg.with_(seed=cfg.seed + 100 * rank)
+    d = make_inputs(cfg, dev)
+    counts = torch.bincount(d["topk_ids"].reshape(-1).long(), minlength=cfg.E)
+    T = 128 * max(1, -(-int(counts.max()) // 128))
+    cnt = counts.to(torch.int32)
+    g = torch.Generator(device=dev).manual_seed(cfg.seed)
+    x_b = torch.randn(cfg.E, T, cfg.H, device=dev, generator=g).to(torch.bfloat16)
+    y_b = torch.empty_like(x_b)
+    p = moe.Problem.from_config(cfg)
+    ws = torch.empty(moe.moe_batched_workspace_bytes(p, T), dtype=torch.uint8, device=dev)
+    expected_m = (cfg.M * cfg.topk + cfg.E) // cfg.E      # the pages' expected_m, one dispatcher
+    stream = torch.cuda.current_stream(dev)
+    routed = int(counts.sum())
+
+    def step():
+        moe.fused_experts_batched(p, x_b, cnt, d["w13"], None, d["w2"], None, y_b, ws,
+                                  expected_m=expected_m, stream=stream)
+
+    def barrier():
+        torch.cuda.synchronize(dev)
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+
+    for _ in range(args.warmup):
+        step()
+    if moe.moe_sync_status(stream) != 0:
+        raise RuntimeError("device error in the warm-up")
+    barrier()
+    with ClockSampler(_gpu_id(dev)) as clk:
+        start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        start.record(stream)
+        for _ in range(args.steps):
+            step()
+        end.record(stream)
+        barrier()
+    elapsed_ms = start.elapsed_time(end)
+    if moe.moe_sync_status(stream) != 0:
+        raise RuntimeError("device error in the timed region")
+    # end to end: the layout and counts from pinned host memory, the result back
+    hx = x_b.cpu().pin_memory()
+    hc = cnt.cpu().pin_memory()
+    hy = torch.empty_like(hx).pin_memory()
+    e_steps = max(3, args.steps // 4)
+
+    def e2e_step():
+        x_b.copy_(hx, non_blocking=True)
+        cnt.copy_(hc, non_blocking=True)
+        step()
+        hy.copy_(y_b, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    barrier()
+    t0 = time.perf_counter()
+    for _ in range(e_steps):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    e2e_s = (time.perf_counter() - t0) / e_steps
+    elapsed_ms, e2e_s = max_over_ranks([elapsed_ms, e2e_s], world, dev)
+    ms = elapsed_ms / args.steps
+    if rank == 0:
+        peaks = _peaks()
+        used = int((counts > 0).sum())
+        wbytes = used * 3 * cfg.I * cfg.H * 2          # w13 + w2 of the experts with tokens
+        gbs = wbytes / (ms * 1e-3) / 1e9
+        out = {
+            "metric": METRIC, "value": world * routed / (ms * 1e-3), "unit": UNIT,
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic (seeded; random-init weights)",
+            "config": {"workload": f"decode_batched: Mixtral-8x7B-shaped decode in the batched "
+                                   f"layout [E={cfg.E}, T={T}, H={cfg.H}], I={cfg.I}, per-expert "
+                                   f"counts of M={cfg.M} top-{cfg.topk} routing",
+                       "E": cfg.E, "T": T, "H": cfg.H, "I": cfg.I, "routed_tokens_per_gpu": routed,
+                       "expected_m": expected_m, "quant": "bf16",
+                       "l2": "inputs larger than L2 (expert weights 2.8 GB per GPU), no flush",
+                       "parallelism": f"replicas x{world}"},
+            "roofline": {"bound": "hbm", "kernel": "fused_experts_batched step (the weights of "
+                                                   "every expert with tokens, once)",
+                         "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                         "frac": gbs / peaks["hbm_gbs"], "traffic": None,
+                         "peak_source": f"hbm_gbs ({peaks['source']})",
+                         "algorithmic_per_launch": f"3*I*H*2 B x {used} experts = {wbytes:.4e} B"},
+            "e2e": {"value": world * routed / e2e_s, "unit": UNIT,
+                    "h2d_bytes_per_step": hx.numel() * 2 + hc.numel() * 4,
+                    "d2h_bytes_per_step": hy.numel() * 2, "ms_per_step": e2e_s * 1e3},
+            "gpu_launches": 3 * args.steps,
+            "clocks": clk.summary(),
+        }
+        if world == 1 and not args.no_cpu_baseline:
+            # the same per-row expert MLPs: the decode workload's tokens through
+            # the per-token oracle (each routed item is one row of the layout)
+            arrs = _oracle_arrays(d, cfg)
+            t2 = _time_oracle(arrs, [0, 1], cfg)
+            n_tok = int(min(cfg.M - 2, max(4, round(15.0 / max(t2 / 2, 1e-3)))))
+            tokens = list(range(2, 2 + n_tok))
+            secs = _time_oracle(arrs, tokens, cfg)
+            out["cpu_baseline"] = {
+                "value": len(tokens) * cfg.topk / secs, "unit": UNIT, "cores": _cores(),
+                "kind": "oracle",
+                "sample": f"{len(tokens)} tokens ({len(tokens) * cfg.topk} routed rows) of the "
+                          f"decode workload through the per-token fp64 oracle, weights decoded "
+                          f"once outside timing; {secs:.1f} s"}
+        print(json.dumps(out), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -482,7 +628,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=WORKLOAD,
-                    choices=["mixtral", "decode", "dsfp8", "mxfp4", "tiny"])
+                    choices=["mixtral", "decode", "dsfp8", "mxfp4", "tiny", "decode_batched"])
     ap.add_argument("--tokens", type=int, default=0,
                     help="override M (smaller cases for profiling captures)")
     ap.add_argument("--experts", type=int, default=0,
@@ -493,6 +639,8 @@ def main():
         ap.error("--warmup must be >= 3")
     if args.impl == "reference":
         run_reference(args)
+    elif args.workload == "decode_batched":
+        run_batched(args)
     else:
         run_ours(args)
 
