@@ -156,13 +156,47 @@ def silu(g):
     return g / (1.0 + np.exp(-g))
 
 
-def act_mul(h1, I: int, exact: bool = False):
-    """SiLU-and-mul on the 2I outputs of GEMM1: z = SiLU(h[:, :I]) * h[:, I:].
-    Unless ``exact``, h1 is first rounded to bf16 (mm1_out is bf16)."""
+def gated(g, u, recipe=None):
+    """The gated activation of GEMM1's gate and up halves.  recipe None:
+    SiLU(g) * u.  recipe (alpha, beta, limit) -- the gemm1_alpha / gemm1_beta /
+    gemm1_clamp_limit recipe (page "Blackwell 上的 DeepGEMM FusedMoE（vLLM）",
+    §2.6.4; alpha = 1, beta = 0 is SiLU-and-mul): with limit > 0 the gate is
+    clamped from above and the up half to [-limit, limit], then
+    z = (u + beta) * g * sigmoid(alpha * g)."""
+    g = np.asarray(g, dtype=np.float64)
+    u = np.asarray(u, dtype=np.float64)
+    if recipe is None:
+        return silu(g) * u
+    alpha, beta, limit = (float(v) for v in recipe)
+    if limit > 0:
+        g = np.minimum(g, limit)
+        u = np.clip(u, -limit, limit)
+    return (u + beta) * g / (1.0 + np.exp(-alpha * g))
+
+
+def act_mul(h1, I: int, exact: bool = False, recipe=None):
+    """SiLU-and-mul on the 2I outputs of GEMM1: z = SiLU(h[:, :I]) * h[:, I:]
+    (or the gated recipe).  Unless ``exact``, h1 is first rounded to bf16
+    (mm1_out is bf16)."""
     h1 = np.asarray(h1, dtype=np.float64)
     if not exact:
         h1 = codecs.round_bf16(h1)
-    return silu(h1[:, :I]) * h1[:, I:]
+    return gated(h1[:, :I], h1[:, I:], recipe)
+
+
+def add_expert_bias(c, bias, route, block_size: int):
+    """c[row] += bias[e] for the rows of every used block of expert e (the
+    GEMM epilogue's bias, page "fused_moe.py 分析", fused_moe_kernel
+    post-processing: dequant -> bias -> router weight -> cast)."""
+    if bias is None:
+        return c
+    c = np.array(c, dtype=np.float64)
+    bias = np.asarray(bias, dtype=np.float64)
+    ids = route["block_expert_ids"]
+    for b in range(route["num_tokens_post_padded"] // block_size):
+        if ids[b] >= 0:
+            c[b * block_size:(b + 1) * block_size] += bias[ids[b]]
+    return c
 
 
 def unpermute_reduce(y2, inv_perm, topk_weights, apply_router_weight_on_input=False,
@@ -188,9 +222,13 @@ def _act_scale_fmt(quant: str, act_scale_fmt: str):
 
 def fused_experts(x, topk_ids, topk_weights, w13, w2, w13_scale=None, w2_scale=None, *,
                   quant="bf16", act_scale_fmt="fp32", block_size=128,
-                  apply_router_weight_on_input=False, exact=False):
+                  apply_router_weight_on_input=False, exact=False, w13_bias=None,
+                  w2_bias=None, router_weight_in_gemm2=False, act_recipe=None):
     """Form 2 (the pages' organisation): routing, permute, grouped GEMM1,
     SiLU-and-mul (+ quant), grouped GEMM2, weighted unpermute-reduce.
+    Epilogue variants: expert biases added to the GEMM sums before rounding,
+    the router weight applied to GEMM2's rows before their rounding (the
+    reduce then only sums), the gated activation recipe (see ``gated``).
     Returns a dict with every intermediate and ``y`` [M, H]."""
     x = np.asarray(x, dtype=np.float64)
     ids = np.asarray(topk_ids)
@@ -199,12 +237,15 @@ def fused_experts(x, topk_ids, topk_weights, w13, w2, w13_scale=None, w2_scale=N
     I = np.asarray(w2).shape[2] if quant != "mxfp4" else 2 * np.asarray(w2).shape[2]
     if apply_router_weight_on_input and k != 1:
         raise ValueError("apply_router_weight_on_input needs top-k = 1")
+    if apply_router_weight_on_input and router_weight_in_gemm2:
+        raise ValueError("the router weight is applied once")
     fmt = _act_scale_fmt(quant, act_scale_fmt)
     route = align_permute(ids, E, block_size)
     xp, xs = permute_rows(x, route, k,
                           topk_weights if apply_router_weight_on_input else None, fmt)
     h1 = grouped_gemm(xp, xs, w13, w13_scale, route, block_size, quant)
-    z = act_mul(h1, I, exact=exact)
+    h1 = add_expert_bias(h1, w13_bias, route, block_size)
+    z = act_mul(h1, I, exact=exact, recipe=act_recipe)
     if fmt is None:
         zq, zs = (z if exact else codecs.round_bf16(z)), None
     else:
@@ -213,10 +254,16 @@ def fused_experts(x, topk_ids, topk_weights, w13, w2, w13_scale=None, w2_scale=N
         zq[~live] = 0.0
         zs[~live] = 0.0
     y2 = grouped_gemm(zq, zs, w2, w2_scale, route, block_size, quant)
+    y2 = add_expert_bias(y2, w2_bias, route, block_size)
+    if router_weight_in_gemm2:
+        sid = route["sorted_token_ids"]
+        wflat = np.asarray(topk_weights, dtype=np.float64).reshape(-1)
+        row_w = np.where(sid < M * k, wflat[np.minimum(sid, M * k - 1)], 0.0)
+        y2 = y2 * row_w[:, None]
     if not exact:
         y2 = codecs.round_bf16(y2)
-    y = unpermute_reduce(y2, route["inv_perm"], topk_weights, apply_router_weight_on_input,
-                         exact=exact)
+    y = unpermute_reduce(y2, route["inv_perm"], topk_weights,
+                         apply_router_weight_on_input or router_weight_in_gemm2, exact=exact)
     return {"route": route, "x_perm": xp, "x_scale": xs, "h1": h1, "z": zq, "z_scale": zs,
             "y2": y2, "y": y}
 
@@ -224,7 +271,8 @@ def fused_experts(x, topk_ids, topk_weights, w13, w2, w13_scale=None, w2_scale=N
 def fused_experts_per_token(x, topk_ids, topk_weights, w13, w2, w13_scale=None,
                             w2_scale=None, *, quant="bf16", act_scale_fmt="fp32",
                             apply_router_weight_on_input=False, exact=False, tokens=None,
-                            return_items=False):
+                            return_items=False, w13_bias=None, w2_bias=None,
+                            router_weight_in_gemm2=False, act_recipe=None):
     """Form 1: brute-force loop over tokens and slots, no permutation.
 
     For each (t, i) with e = id[t, i] >= 0: quantise x_t (quantised modes),
@@ -267,9 +315,11 @@ def fused_experts_per_token(x, topk_ids, topk_weights, w13, w2, w13_scale=None,
                         h = _fp8_matvec(q[0], s[0], w13[e], np.asarray(w13_scale)[e])
                     else:
                         h = W13 @ (q[0] * np.repeat(s[0], 128))
+                if w13_bias is not None:
+                    h = h + np.asarray(w13_bias, dtype=np.float64)[e]
                 if not exact:
                     h = codecs.round_bf16(h)
-                z = silu(h[:I]) * h[I:]
+                z = gated(h[:I], h[I:], act_recipe)
                 if fmt is None:
                     if not exact:
                         z = codecs.round_bf16(z)
@@ -280,6 +330,10 @@ def fused_experts_per_token(x, topk_ids, topk_weights, w13, w2, w13_scale=None,
                         o = _fp8_matvec(q[0], s[0], w2[e], np.asarray(w2_scale)[e])
                     else:
                         o = W2 @ (q[0] * np.repeat(s[0], 128))
+                if w2_bias is not None:
+                    o = o + np.asarray(w2_bias, dtype=np.float64)[e]
+                if router_weight_in_gemm2:
+                    o = wts[t, i] * o
                 if not exact:
                     o = codecs.round_bf16(o)
                 outs[(t, i)] = o
@@ -290,7 +344,7 @@ def fused_experts_per_token(x, topk_ids, topk_weights, w13, w2, w13_scale=None,
         for i in range(k):                      # slot order
             if ids[t, i] < 0:
                 continue
-            wi = 1.0 if apply_router_weight_on_input else wts[t, i]
+            wi = 1.0 if (apply_router_weight_on_input or router_weight_in_gemm2) else wts[t, i]
             y[j] += wi * outs[(t, i)]
             items[j, i] = outs[(t, i)]
             used_w[j, i] = wi

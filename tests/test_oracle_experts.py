@@ -209,9 +209,9 @@ def _catches(monkeypatch, target, replacement):
 def test_planted_gate_up_swap_is_caught(monkeypatch):
     orig = experts.act_mul
 
-    def swapped(h1, I, exact=False):
+    def swapped(h1, I, exact=False, recipe=None):
         h1 = np.asarray(h1)
-        return orig(np.concatenate([h1[:, I:], h1[:, :I]], axis=1), I, exact)
+        return orig(np.concatenate([h1[:, I:], h1[:, :I]], axis=1), I, exact, recipe)
     assert _catches(monkeypatch, "act_mul", swapped)
 
 
@@ -273,3 +273,95 @@ def test_batched_layout_equals_permuted_form(name):
                                a["w13"], a["w2"], a["w13_scale"], a["w2_scale"], **kw)["y"]
     got = np.concatenate([y_b[e, :min(int(counts[e]), T)] for e in range(E)])
     np.testing.assert_array_equal(got, f2)
+
+
+# ---------------------------------------------------------------- epilogue variants
+RECIPE = (1.702, 1.0, 7.0)     # a swigluoai-style setting of the gemm1 recipe
+
+
+def test_recipe_identity_is_silu_and_clamp_closed_forms():
+    rng = np.random.default_rng(9)
+    g, u = rng.normal(size=(50, 16)) * 3, rng.normal(size=(50, 16)) * 3
+    np.testing.assert_allclose(experts.gated(g, u, (1.0, 0.0, 0.0)), experts.gated(g, u),
+                               rtol=1e-15, atol=0)
+    # closed forms: g = 0 gives 0; a clamped gate and up; beta shifts the up half
+    assert experts.gated(0.0, 5.0, RECIPE) == 0.0
+    v = experts.gated(100.0, -50.0, RECIPE)              # g' = 7, u' = -7
+    np.testing.assert_allclose(v, (-7.0 + 1.0) * 7.0 / (1.0 + np.exp(-1.702 * 7.0)), rtol=1e-15)
+    v = experts.gated(-3.0, 2.0, (2.0, 0.5, 0.0))        # no clamp
+    np.testing.assert_allclose(v, 2.5 * -3.0 * special_expit(2.0 * -3.0), rtol=1e-15)
+
+
+def special_expit(x):
+    from scipy import special
+    return special.expit(x)
+
+
+@pytest.mark.parametrize("name", ["bf16", "fp8", "mxfp4"])
+def test_router_weight_placement_in_gemm2_is_exact_by_linearity(name):
+    """exact mode: scaling GEMM2's rows by the router weight and summing gives
+    the default path's result (W2^T (a z) + a b = a (W2^T z + b)); both forms."""
+    cfg = SMALL[name]
+    a = _inputs(cfg)
+    kw = dict(quant=cfg.quant, act_scale_fmt=cfg.act_scale_fmt, exact=True)
+    rng = np.random.default_rng(4)
+    b2 = rng.normal(size=(cfg.E, cfg.H)) * 0.1
+    ref = experts.fused_experts(**a, w2_bias=b2, **kw)["y"]
+    f2 = experts.fused_experts(**a, w2_bias=b2, router_weight_in_gemm2=True, **kw)["y"]
+    f1 = experts.fused_experts_per_token(**a, w2_bias=b2, router_weight_in_gemm2=True, **kw)
+    np.testing.assert_allclose(f2, ref, rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(f1, ref, rtol=1e-12, atol=1e-12)
+
+
+@pytest.mark.parametrize("name", ["bf16", "fp8", "mxfp4"])
+def test_epilogue_variants_both_forms_agree(name):
+    cfg = SMALL[name]
+    a = _inputs(cfg)
+    rng = np.random.default_rng(5)
+    kw = dict(quant=cfg.quant, act_scale_fmt=cfg.act_scale_fmt,
+              w13_bias=codecs.round_bf16(rng.normal(size=(cfg.E, 2 * cfg.I)) * 0.5),
+              w2_bias=codecs.round_bf16(rng.normal(size=(cfg.E, cfg.H)) * 0.5),
+              router_weight_in_gemm2=True, act_recipe=RECIPE)
+    f2 = experts.fused_experts(**a, **kw)["y"]
+    f1 = experts.fused_experts_per_token(**a, **kw)
+    np.testing.assert_allclose(f1, f2, rtol=0, atol=1e-12 * np.sqrt(np.mean(f2 ** 2)))
+
+
+def test_biases_with_zero_weights_closed_form():
+    """W = 0: H1 = b13, so z = gated(b13 gate, b13 up) and y = sum_i w_i b2[e_i]."""
+    cfg = SMALL["bf16"]
+    a = _inputs(cfg)
+    a["w13"] = np.zeros_like(a["w13"])
+    a["w2"] = np.zeros_like(a["w2"])
+    rng = np.random.default_rng(6)
+    b13 = codecs.round_bf16(rng.normal(size=(cfg.E, 2 * cfg.I)))
+    b2 = codecs.round_bf16(rng.normal(size=(cfg.E, cfg.H)))
+    out = experts.fused_experts(**a, w13_bias=b13, w2_bias=b2, act_recipe=RECIPE)
+    ids, w = a["topk_ids"], a["topk_weights"]
+    want = np.zeros((cfg.M, cfg.H))
+    for t in range(cfg.M):
+        for i in range(cfg.topk):
+            want[t] += w[t, i] * b2[ids[t, i]]
+    np.testing.assert_allclose(out["y"], codecs.round_bf16(want), rtol=0, atol=0)
+    zb = codecs.round_bf16(experts.gated(b13[:, :cfg.I], b13[:, cfg.I:], RECIPE))
+    e0 = out["route"]["block_expert_ids"][0]
+    np.testing.assert_array_equal(out["z"][0], zb[e0])
+
+
+def test_dense_special_case_with_bias_and_recipe():
+    """E=1, k=1, w=1, exact: a dense gated MLP with biases, against torch."""
+    g = torch.Generator().manual_seed(8)
+    M, H, I = 6, 128, 128
+    x = torch.randn(M, H, generator=g, dtype=torch.float64)
+    w13 = torch.randn(1, 2 * I, H, generator=g, dtype=torch.float64) * 0.1
+    w2 = torch.randn(1, H, I, generator=g, dtype=torch.float64) * 0.1
+    b13 = torch.randn(1, 2 * I, generator=g, dtype=torch.float64)
+    b2 = torch.randn(1, H, generator=g, dtype=torch.float64)
+    h = x @ w13[0].T + b13[0]
+    gt, up = h[:, :I].clamp(max=7.0), h[:, I:].clamp(-7.0, 7.0)
+    z = (up + 1.0) * gt * torch.sigmoid(1.702 * gt)
+    ref = z @ w2[0].T + b2[0]
+    out = experts.fused_experts(x.numpy(), np.zeros((M, 1), np.int64), np.ones((M, 1)),
+                                w13.numpy(), w2.numpy(), exact=True, w13_bias=b13.numpy(),
+                                w2_bias=b2.numpy(), act_recipe=RECIPE)["y"]
+    np.testing.assert_allclose(out, ref.numpy(), rtol=1e-12, atol=1e-12)
