@@ -72,17 +72,33 @@ typedef enum { MOE_Q_BF16 = 0, MOE_Q_FP8_BLOCK128 = 1, MOE_Q_MXFP4_W4A8 = 2 } mo
 typedef enum { MOE_SCALE_FP32 = 0, MOE_SCALE_UE8M0 = 1 } moe_scale_fmt;
 
 /* The problem statement (page 1, "FusedMoEExpertsModular.apply" and
- * "moe_problem_size": E, M, N = 2I, K = H, topk).  Activation is SiLU-and-mul.
+ * "moe_problem_size": E, M, N = 2I, K = H, topk).
  *  block_size: padding granularity of each expert's rows (BLOCK_SIZE_M);
  *              one of 16, 32, 64, 128.  The grouped GEMMs need 128.
  *  apply_router_weight_on_input: multiply x_t by its router weight before
  *              GEMM1 and reduce with weight 1 (top-k must be 1).
+ *  router_weight_in_gemm2: GEMM2's epilogue multiplies each output row by its
+ *              routed item's weight (fp32, after the bias, before the bf16
+ *              cast) and the reduce only sums (page "fused_moe.py 分析",
+ *              fused_moe_kernel post-processing "optional router weight";
+ *              TopKWeightAndReduce when the experts already applied it).
+ *              Not together with apply_router_weight_on_input.
+ *  act_recipe: 0: z = SiLU(gate) * up.  1: the recipe of gemm1_alpha,
+ *              gemm1_beta and gemm1_clamp_limit (page "Blackwell 上的 DeepGEMM
+ *              FusedMoE（vLLM）", §2.6.4): with L = gemm1_clamp_limit,
+ *              g' = min(gate, L), u' = clamp(up, -L, L) (no clamp if L <= 0),
+ *              z = (u' + beta) * g' * sigmoid(alpha * g'); alpha = 1, beta = 0
+ *              and no clamp give SiLU-and-mul back.
+ * Zero-initialised trailing fields select the plain path.
  */
 typedef struct {
   int32_t M, H, I, E, topk, block_size;
   int32_t quant;          /* moe_quant */
   int32_t act_scale_fmt;  /* moe_scale_fmt */
   int32_t apply_router_weight_on_input;
+  int32_t router_weight_in_gemm2;
+  int32_t act_recipe;
+  float gemm1_alpha, gemm1_beta, gemm1_clamp_limit;
 } moe_problem;
 
 /* Limits checked by every entry point: 0 <= M <= MOE_MAX_TOKENS (the pages'
@@ -232,8 +248,8 @@ moe_status moe_align_permute_noalloc(const moe_problem* p, const void* x,
  *  in : x_perm [S,H] (+ x_scale [S,H/128] fp32 for quantised modes),
  *       w13 [E,2I,H] (+ w13_scale), block_expert_ids, num_post_padded (device).
  *  out: fuse_act == 0: h1 [S,2I] bf16.
- *       fuse_act == 1: the SiLU-and-mul result z written directly (MOE_Q_BF16:
- *       z [S,I] bf16).  Quantised modes currently need fuse_act == 0
+ *       fuse_act == 1: the gated activation (p->act_recipe) written directly
+ *       (MOE_Q_BF16: z [S,I] bf16).  Quantised modes currently need fuse_act == 0
  *       (MOE_ERR_UNSUPPORTED otherwise).
  *  Rows of blocks past num_post_padded are not written. */
 moe_status grouped_gemm_w13(const moe_problem* p, const void* x_perm, const float* x_scale,
@@ -241,9 +257,10 @@ moe_status grouped_gemm_w13(const moe_problem* p, const void* x_perm, const floa
                             const int32_t* block_expert_ids, const int32_t* num_post_padded,
                             void* out, float* out_scale, int fuse_act, void* stream);
 
-/* Stage 3: SiLU-and-mul, z = SiLU(h1[:, :I]) * h1[:, I:], computed in fp32
- * from the bf16 h1 (page "Blackwell 上的 DeepGEMM FusedMoE（vLLM）", §2.6.4;
- * page "fused_moe.py 分析", _silu_and_mul_kernel).  MOE_Q_BF16: z [S,I] bf16.
+/* Stage 3: SiLU-and-mul, z = SiLU(h1[:, :I]) * h1[:, I:] (or the recipe of
+ * p->act_recipe), computed in fp32 from the bf16 h1 (page "Blackwell 上的
+ * DeepGEMM FusedMoE（vLLM）", §2.6.4; page "fused_moe.py 分析",
+ * _silu_and_mul_kernel).  MOE_Q_BF16: z [S,I] bf16.
  * Quantised modes: z [S,I] e4m3fn codes + z_scale [S,I/128] fp32 (dynamic
  * per 1x128 group).  Only rows below num_post_padded are written. */
 moe_status act_mul_quant(const moe_problem* p, const void* h1, const int32_t* num_post_padded,
@@ -259,7 +276,8 @@ moe_status grouped_gemm_w2(const moe_problem* p, const void* z, const float* z_s
 /* Stage 5: weighted unpermute + top-k reduce (page "Blackwell 上的 DeepGEMM
  * FusedMoE（vLLM）", §2.6.5 ep_gather): y[t,:] = bf16( sum_{i, inv_perm[t,i] >= 0}
  * w'[t,i] * y2[inv_perm[t,i], :] ), fp32 accumulation in slot order,
- * w' = 1 when apply_router_weight_on_input.  y [M,H] bf16. */
+ * w' = 1 when apply_router_weight_on_input or router_weight_in_gemm2 (the
+ * weight is then already in y2).  y [M,H] bf16. */
 moe_status unpermute_reduce(const moe_problem* p, const void* y2, const int32_t* inv_perm,
                             const float* topk_weights, void* y, void* stream);
 
@@ -271,6 +289,34 @@ moe_status fused_experts(const moe_problem* p, const void* x, const void* w13,
                          const void* w13_scale, const void* w2, const void* w2_scale,
                          const float* topk_weights, const int32_t* topk_ids, void* y,
                          void* workspace, size_t workspace_bytes, void* stream);
+
+/* Stages 2 and 4 and the whole forward with per-expert biases (page
+ * "fused_moe.py 分析", fused_moe_kernel post-processing: dequant -> bias ->
+ * router weight -> cast; the pages' bias inputs of the expert GEMMs):
+ *  - w13_bias: device, [E, 2I] bf16 (gate columns then up columns), added in
+ *    fp32 to GEMM1's sums before H1 is rounded; may be NULL.
+ *  - w2_bias: device, [E, H] bf16, added to GEMM2's sums before the router
+ *    weight (router_weight_in_gemm2) and the bf16 cast; may be NULL.
+ *  - grouped_gemm_w2_ex also takes sorted_ids (from moe_align_permute) and
+ *    topk_weights [M, topk] fp32, used (and then required) only when
+ *    p->router_weight_in_gemm2 is set.
+ * Otherwise as grouped_gemm_w13 / grouped_gemm_w2 / fused_experts, which are
+ * these entry points with NULL biases. */
+moe_status grouped_gemm_w13_ex(const moe_problem* p, const void* x_perm, const float* x_scale,
+                               const void* w13, const void* w13_scale, const void* w13_bias,
+                               const int32_t* block_expert_ids,
+                               const int32_t* num_post_padded, void* out, float* out_scale,
+                               int fuse_act, void* stream);
+moe_status grouped_gemm_w2_ex(const moe_problem* p, const void* z, const float* z_scale,
+                              const void* w2, const void* w2_scale, const void* w2_bias,
+                              const int32_t* block_expert_ids, const int32_t* num_post_padded,
+                              const int32_t* sorted_ids, const float* topk_weights, void* y2,
+                              void* stream);
+moe_status fused_experts_ex(const moe_problem* p, const void* x, const void* w13,
+                            const void* w13_scale, const void* w13_bias, const void* w2,
+                            const void* w2_scale, const void* w2_bias,
+                            const float* topk_weights, const int32_t* topk_ids, void* y,
+                            void* workspace, size_t workspace_bytes, void* stream);
 
 /* fused_experts fed from host memory: copies x [M,H] bf16, topk_ids and
  * topk_weights from host (pinned memory gives asynchronous copies) into the

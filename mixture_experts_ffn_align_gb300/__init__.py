@@ -31,7 +31,8 @@ EXPORTS = ["moe_m_sum_bound", "moe_align_workspace_bytes", "moe_workspace_bytes"
            "moe_sync_status", "moe_status_string", "moe_debug_set_watchdog",
            "moe_debug_set_bf16_gemm_form",
            "moe_align_permute_noalloc", "moe_last_error_string", "moe_topk_router",
-           "moe_batched_workspace_bytes", "fused_experts_batched"]
+           "moe_batched_workspace_bytes", "fused_experts_batched", "grouped_gemm_w13_ex",
+           "grouped_gemm_w2_ex", "fused_experts_ex"]
 
 NOALLOC_SCRATCH_BYTES = 1 << 20   # MOE_NOALLOC_SCRATCH_BYTES in include/moe_ffn.h
 
@@ -45,7 +46,8 @@ class MoEError(RuntimeError):
 class CProblem(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in
                 ("M", "H", "I", "E", "topk", "block_size", "quant", "act_scale_fmt",
-                 "apply_router_weight_on_input")]
+                 "apply_router_weight_on_input", "router_weight_in_gemm2", "act_recipe")] + \
+               [(n, ctypes.c_float) for n in ("gemm1_alpha", "gemm1_beta", "gemm1_clamp_limit")]
 
 
 @dataclass(frozen=True)
@@ -60,11 +62,17 @@ class Problem:
     quant: str = "bf16"
     act_scale_fmt: str = "fp32"
     apply_router_weight_on_input: bool = False
+    router_weight_in_gemm2: bool = False
+    # None: SiLU(gate) * up; else (alpha, beta, clamp_limit) of the gemm1 recipe
+    act_recipe: tuple | None = None
 
     def c(self) -> CProblem:
+        a, b, lim = self.act_recipe if self.act_recipe is not None else (0.0, 0.0, 0.0)
         return CProblem(self.M, self.H, self.I, self.E, self.topk, self.block_size,
                         QUANT[self.quant], SCALE_FMT[self.act_scale_fmt],
-                        int(self.apply_router_weight_on_input))
+                        int(self.apply_router_weight_on_input),
+                        int(self.router_weight_in_gemm2), int(self.act_recipe is not None),
+                        float(a), float(b), float(lim))
 
     @classmethod
     def from_config(cls, cfg, **kw):
@@ -105,6 +113,9 @@ def lib() -> ctypes.CDLL:
         L.moe_batched_workspace_bytes.argtypes = [P, i32]
         L.moe_batched_workspace_bytes.restype = sz
         L.fused_experts_batched.argtypes = [P, vp, vp, i32, i32, vp, vp, vp, vp, vp, vp, sz, vp]
+        L.grouped_gemm_w13_ex.argtypes = [P, vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, vp]
+        L.grouped_gemm_w2_ex.argtypes = [P, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
+        L.fused_experts_ex.argtypes = [P] + [vp] * 11 + [sz, vp]
         L.moe_status_string.argtypes, L.moe_status_string.restype = [i32], ctypes.c_char_p
         L.moe_last_error_string.argtypes, L.moe_last_error_string.restype = [], ctypes.c_char_p
         L.moe_debug_set_watchdog.argtypes, L.moe_debug_set_watchdog.restype = \
@@ -113,7 +124,8 @@ def lib() -> ctypes.CDLL:
             [i32], None
         for n in ("moe_align_permute", "grouped_gemm_w13", "act_mul_quant", "grouped_gemm_w2",
                   "unpermute_reduce", "fused_experts", "fused_experts_from_host",
-                  "moe_sync_status", "moe_topk_router", "fused_experts_batched"):
+                  "moe_sync_status", "moe_topk_router", "fused_experts_batched",
+                  "grouped_gemm_w13_ex", "grouped_gemm_w2_ex", "fused_experts_ex"):
             getattr(L, n).restype = i32
         _lib = L
     return _lib
@@ -208,6 +220,30 @@ def grouped_gemm_w2(p: Problem, z, z_scale, w2, w2_scale, block_expert_ids, num_
 def unpermute_reduce(p: Problem, y2, inv_perm, topk_weights, y, stream=None):
     _check(lib().unpermute_reduce(_cp(p), _p(y2), _p(inv_perm), _p(topk_weights), _p(y),
                                   _stream(stream)), "unpermute_reduce")
+
+
+def grouped_gemm_w13_ex(p: Problem, x_perm, x_scale, w13, w13_scale, w13_bias, block_expert_ids,
+                        num_post_padded, out, out_scale=None, fuse_act=False, stream=None):
+    _check(lib().grouped_gemm_w13_ex(
+        _cp(p), _p(x_perm), _p(x_scale), _p(w13), _p(w13_scale), _p(w13_bias),
+        _p(block_expert_ids), _p(num_post_padded), _p(out), _p(out_scale), int(bool(fuse_act)),
+        _stream(stream)), "grouped_gemm_w13_ex")
+
+
+def grouped_gemm_w2_ex(p: Problem, z, z_scale, w2, w2_scale, w2_bias, block_expert_ids,
+                       num_post_padded, sorted_ids, topk_weights, y2, stream=None):
+    _check(lib().grouped_gemm_w2_ex(
+        _cp(p), _p(z), _p(z_scale), _p(w2), _p(w2_scale), _p(w2_bias), _p(block_expert_ids),
+        _p(num_post_padded), _p(sorted_ids), _p(topk_weights), _p(y2), _stream(stream)),
+        "grouped_gemm_w2_ex")
+
+
+def fused_experts_ex(p: Problem, x, w13, w13_scale, w13_bias, w2, w2_scale, w2_bias,
+                     topk_weights, topk_ids, y, workspace, stream=None):
+    _check(lib().fused_experts_ex(
+        _cp(p), _p(x), _p(w13), _p(w13_scale), _p(w13_bias), _p(w2), _p(w2_scale), _p(w2_bias),
+        _p(topk_weights), _p(topk_ids), _p(y), _p(workspace),
+        workspace.numel() * workspace.element_size(), _stream(stream)), "fused_experts_ex")
 
 
 def moe_batched_workspace_bytes(p: Problem, max_tokens: int) -> int:

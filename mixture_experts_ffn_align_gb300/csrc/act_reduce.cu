@@ -21,10 +21,11 @@ namespace moe {
 constexpr int ACT_U = 4;             // 16-byte vectors of g (and of u) per lane in flight
 constexpr int ACT_THREADS = 256;
 
-// z[row, :] = bf16(SiLU(bf16 g) * bf16 u) for rows below num_post_padded.
+// z[row, :] = bf16(act(bf16 g, bf16 u)) for rows below num_post_padded;
+// act = SiLU(g) * u, or the gemm1 alpha / beta / clamp recipe.
 __global__ void __launch_bounds__(ACT_THREADS)
     k_act_mul_bf16(const __nv_bfloat16* __restrict__ h1, int I, const int32_t* __restrict__ npp,
-                   __nv_bfloat16* __restrict__ z) {
+                   __nv_bfloat16* __restrict__ z, const Epilogue act) {
   const int lane = threadIdx.x & 31;
   const int wpc = blockDim.x >> 5;
   const int rows = *npp;
@@ -53,7 +54,8 @@ __global__ void __launch_bounds__(ACT_THREADS)
         __nv_bfloat16* ob = reinterpret_cast<__nv_bfloat16*>(&out);
 #pragma unroll
         for (int j = 0; j < 8; ++j)
-          ob[j] = __float2bfloat16_rn(silu_fast(__bfloat162float(gb[j])) * __bfloat162float(ub[j]));
+          ob[j] = __float2bfloat16_rn(
+              act_glu(act, __bfloat162float(gb[j]), __bfloat162float(ub[j])));
         z4[v] = out;
       }
     }
@@ -64,7 +66,8 @@ __global__ void __launch_bounds__(ACT_THREADS)
 // scale -> e4m3 with one reciprocal per group.
 __global__ void __launch_bounds__(ACT_THREADS)
     k_act_mul_fp8(const __nv_bfloat16* __restrict__ h1, int I, const int32_t* __restrict__ npp,
-                  uint8_t* __restrict__ zq, float* __restrict__ zs, int ue8m0) {
+                  uint8_t* __restrict__ zq, float* __restrict__ zs, int ue8m0,
+                  const Epilogue recipe) {
   const int lane = threadIdx.x & 31;
   const int wpc = blockDim.x >> 5;
   const int rows = *npp;
@@ -95,7 +98,7 @@ __global__ void __launch_bounds__(ACT_THREADS)
           const __nv_bfloat16* ub = reinterpret_cast<const __nv_bfloat16*>(&uv[k]);
 #pragma unroll
           for (int j = 0; j < 8; ++j) {
-            f[j] = silu_fast(__bfloat162float(gb[j])) * __bfloat162float(ub[j]);
+            f[j] = act_glu(recipe, __bfloat162float(gb[j]), __bfloat162float(ub[j]));
             amax = fmaxf(amax, fabsf(f[j]));
           }
         }
@@ -121,18 +124,19 @@ __global__ void __launch_bounds__(ACT_THREADS)
 }
 
 cudaError_t launch_act_mul(const void* h1, int I, const int32_t* num_post_padded, void* z,
-                           float* z_scale, bool ue8m0, int cap, cudaStream_t stream) {
+                           float* z_scale, bool ue8m0, int cap, const Epilogue& act,
+                           cudaStream_t stream) {
   if (cap <= 0) return cudaSuccess;
   const int wpc = ACT_THREADS / 32;
   const int grid = min((cap + wpc - 1) / wpc, num_sms() * 8);
   if (z_scale == nullptr) {
     k_act_mul_bf16<<<grid, ACT_THREADS, 0, stream>>>(static_cast<const __nv_bfloat16*>(h1), I,
                                                      num_post_padded,
-                                                     static_cast<__nv_bfloat16*>(z));
+                                                     static_cast<__nv_bfloat16*>(z), act);
   } else {
     k_act_mul_fp8<<<grid, ACT_THREADS, 0, stream>>>(static_cast<const __nv_bfloat16*>(h1), I,
                                                     num_post_padded, static_cast<uint8_t*>(z),
-                                                    z_scale, ue8m0);
+                                                    z_scale, ue8m0, act);
   }
   return cudaGetLastError();
 }

@@ -8,6 +8,7 @@
 // taller than the padding granularity reads another expert's id (so the
 // GEMMs demand block_size == 128 here), and M == 0 returning early (page 1,
 // FusedMoEKernelModularImpl._fused_experts, "M_full == 0").
+#include <cmath>
 #include <cstdio>
 #include <cstring>
 #include <mutex>
@@ -82,7 +83,31 @@ bool valid_problem(const moe_problem* p) {
   if (p->quant < MOE_Q_BF16 || p->quant > MOE_Q_MXFP4_W4A8) return false;
   if (p->act_scale_fmt != MOE_SCALE_FP32 && p->act_scale_fmt != MOE_SCALE_UE8M0) return false;
   if (p->apply_router_weight_on_input && p->topk != 1) return false;
+  if (p->router_weight_in_gemm2 != 0 && p->router_weight_in_gemm2 != 1) return false;
+  if (p->router_weight_in_gemm2 && p->apply_router_weight_on_input) return false;
+  if (p->act_recipe != 0 && p->act_recipe != 1) return false;
+  if (p->act_recipe &&
+      !(std::isfinite(p->gemm1_alpha) && std::isfinite(p->gemm1_beta) &&
+        std::isfinite(p->gemm1_clamp_limit)))
+    return false;
   return true;
+}
+
+// Epilogue work of one GEMM of problem p: the activation recipe, a bias and
+// (GEMM2 with router_weight_in_gemm2) the router weight per row.
+Epilogue make_epilogue(const moe_problem* p, const void* bias, int n_bias,
+                       const int32_t* sorted_ids, const float* item_weights) {
+  Epilogue ep{};
+  ep.bias = static_cast<const __nv_bfloat16*>(bias);
+  ep.n_bias = n_bias;
+  ep.sorted_ids = item_weights != nullptr ? sorted_ids : nullptr;
+  ep.item_weights = sorted_ids != nullptr ? item_weights : nullptr;
+  ep.R = p->M * p->topk;
+  ep.recipe = p->act_recipe;
+  ep.alpha = p->act_recipe ? p->gemm1_alpha : 1.0f;
+  ep.beta = p->act_recipe ? p->gemm1_beta : 0.0f;
+  ep.limit = p->act_recipe ? p->gemm1_clamp_limit : 0.0f;
+  return ep;
 }
 
 bool quantised(const moe_problem* p) { return p->quant != MOE_Q_BF16; }
@@ -249,20 +274,21 @@ namespace {
 cudaError_t launch_bf16_gemm(int64_t rows_per_expert, const void* A, int cap, int K,
                              const void* B, int b_rows_total, int b_rows_per_expert, int n_out,
                              const int32_t* block_expert_ids, const int32_t* num_post_padded,
-                             void* out, bool fuse_act, cudaStream_t s) {
+                             void* out, bool fuse_act, const Epilogue& ep, cudaStream_t s) {
   const bool pairs = g_bf16_form == 2 || (g_bf16_form == 0 && rows_per_expert >= 2 * 128);
   return (pairs ? launch_ggemm_bf16_2sm : launch_ggemm_bf16)(
       A, cap, K, B, b_rows_total, b_rows_per_expert, n_out, block_expert_ids, num_post_padded,
-      out, fuse_act, s);
+      out, fuse_act, ep, s);
 }
 }  // namespace
 
 extern "C" {
 
-moe_status grouped_gemm_w13(const moe_problem* p, const void* x_perm, const float* x_scale,
-                            const void* w13, const void* w13_scale,
-                            const int32_t* block_expert_ids, const int32_t* num_post_padded,
-                            void* out, float* out_scale, int fuse_act, void* stream) {
+moe_status grouped_gemm_w13_ex(const moe_problem* p, const void* x_perm, const float* x_scale,
+                               const void* w13, const void* w13_scale, const void* w13_bias,
+                               const int32_t* block_expert_ids,
+                               const int32_t* num_post_padded, void* out, float* out_scale,
+                               int fuse_act, void* stream) {
   (void)out_scale;
   if (!valid_problem(p)) return MOE_ERR_INVALID_ARG;
   if (p->M == 0) return MOE_OK;
@@ -270,10 +296,11 @@ moe_status grouped_gemm_w13(const moe_problem* p, const void* x_perm, const floa
   if (!gemm_supported(p)) return MOE_ERR_UNSUPPORTED;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const int cap = (int)cap_rows(p);
+  const Epilogue ep = make_epilogue(p, w13_bias, 2 * p->I, nullptr, nullptr);
   if (p->quant == MOE_Q_BF16) {
     return cuda_status(launch_bf16_gemm((int64_t)p->M * p->topk / p->E, x_perm, cap, p->H, w13,
                                         p->E * 2 * p->I, 2 * p->I, 2 * p->I, block_expert_ids,
-                                        num_post_padded, out, fuse_act != 0, s));
+                                        num_post_padded, out, fuse_act != 0, ep, s));
   }
   if (fuse_act) return MOE_ERR_UNSUPPORTED;
   if (!x_scale || !w13_scale) return MOE_ERR_INVALID_ARG;
@@ -281,11 +308,19 @@ moe_status grouped_gemm_w13(const moe_problem* p, const void* x_perm, const floa
     return cuda_status(launch_ggemm_mxfp4(x_perm, x_scale, cap, p->H, w13,
                                           static_cast<const uint8_t*>(w13_scale),
                                           p->E * 2 * p->I, 2 * p->I, 2 * p->I, block_expert_ids,
-                                          num_post_padded, out, s));
+                                          num_post_padded, out, ep, s));
   return cuda_status(launch_ggemm_fp8(x_perm, x_scale, cap, p->H, w13,
                                       static_cast<const float*>(w13_scale), p->E * 2 * p->I,
                                       2 * p->I, 2 * p->I, block_expert_ids, num_post_padded, out,
-                                      s));
+                                      ep, s));
+}
+
+moe_status grouped_gemm_w13(const moe_problem* p, const void* x_perm, const float* x_scale,
+                            const void* w13, const void* w13_scale,
+                            const int32_t* block_expert_ids, const int32_t* num_post_padded,
+                            void* out, float* out_scale, int fuse_act, void* stream) {
+  return grouped_gemm_w13_ex(p, x_perm, x_scale, w13, w13_scale, nullptr, block_expert_ids,
+                             num_post_padded, out, out_scale, fuse_act, stream);
 }
 
 moe_status act_mul_quant(const moe_problem* p, const void* h1, const int32_t* num_post_padded,
@@ -297,32 +332,48 @@ moe_status act_mul_quant(const moe_problem* p, const void* h1, const int32_t* nu
   return cuda_status(launch_act_mul(h1, p->I, num_post_padded, z,
                                     quantised(p) ? z_scale : nullptr,
                                     p->act_scale_fmt == MOE_SCALE_UE8M0, (int)cap_rows(p),
+                                    make_epilogue(p, nullptr, 0, nullptr, nullptr),
                                     static_cast<cudaStream_t>(stream)));
+}
+
+moe_status grouped_gemm_w2_ex(const moe_problem* p, const void* z, const float* z_scale,
+                              const void* w2, const void* w2_scale, const void* w2_bias,
+                              const int32_t* block_expert_ids, const int32_t* num_post_padded,
+                              const int32_t* sorted_ids, const float* topk_weights, void* y2,
+                              void* stream) {
+  if (!valid_problem(p)) return MOE_ERR_INVALID_ARG;
+  if (p->M == 0) return MOE_OK;
+  if (!z || !w2 || !block_expert_ids || !num_post_padded || !y2) return MOE_ERR_INVALID_ARG;
+  if (p->router_weight_in_gemm2 && (!sorted_ids || !topk_weights)) return MOE_ERR_INVALID_ARG;
+  if (!gemm_supported(p)) return MOE_ERR_UNSUPPORTED;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int cap = (int)cap_rows(p);
+  const Epilogue ep =
+      p->router_weight_in_gemm2 ? make_epilogue(p, w2_bias, p->H, sorted_ids, topk_weights)
+                                : make_epilogue(p, w2_bias, p->H, nullptr, nullptr);
+  if (p->quant == MOE_Q_BF16) {
+    return cuda_status(launch_bf16_gemm((int64_t)p->M * p->topk / p->E, z, cap, p->I, w2,
+                                        p->E * p->H, p->H, p->H, block_expert_ids,
+                                        num_post_padded, y2, false, ep, s));
+  }
+  if (!z_scale || !w2_scale) return MOE_ERR_INVALID_ARG;
+  if (p->quant == MOE_Q_MXFP4_W4A8)
+    return cuda_status(launch_ggemm_mxfp4(z, z_scale, cap, p->I, w2,
+                                          static_cast<const uint8_t*>(w2_scale), p->E * p->H,
+                                          p->H, p->H, block_expert_ids, num_post_padded, y2, ep,
+                                          s));
+  return cuda_status(launch_ggemm_fp8(z, z_scale, cap, p->I, w2,
+                                      static_cast<const float*>(w2_scale), p->E * p->H, p->H,
+                                      p->H, block_expert_ids, num_post_padded, y2, ep, s));
 }
 
 moe_status grouped_gemm_w2(const moe_problem* p, const void* z, const float* z_scale,
                            const void* w2, const void* w2_scale,
                            const int32_t* block_expert_ids, const int32_t* num_post_padded,
                            void* y2, void* stream) {
-  if (!valid_problem(p)) return MOE_ERR_INVALID_ARG;
-  if (p->M == 0) return MOE_OK;
-  if (!z || !w2 || !block_expert_ids || !num_post_padded || !y2) return MOE_ERR_INVALID_ARG;
-  if (!gemm_supported(p)) return MOE_ERR_UNSUPPORTED;
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  const int cap = (int)cap_rows(p);
-  if (p->quant == MOE_Q_BF16) {
-    return cuda_status(launch_bf16_gemm((int64_t)p->M * p->topk / p->E, z, cap, p->I, w2,
-                                        p->E * p->H, p->H, p->H, block_expert_ids,
-                                        num_post_padded, y2, false, s));
-  }
-  if (!z_scale || !w2_scale) return MOE_ERR_INVALID_ARG;
-  if (p->quant == MOE_Q_MXFP4_W4A8)
-    return cuda_status(launch_ggemm_mxfp4(z, z_scale, cap, p->I, w2,
-                                          static_cast<const uint8_t*>(w2_scale), p->E * p->H,
-                                          p->H, p->H, block_expert_ids, num_post_padded, y2, s));
-  return cuda_status(launch_ggemm_fp8(z, z_scale, cap, p->I, w2,
-                                      static_cast<const float*>(w2_scale), p->E * p->H, p->H,
-                                      p->H, block_expert_ids, num_post_padded, y2, s));
+  if (p != nullptr && p->router_weight_in_gemm2) return MOE_ERR_INVALID_ARG;   // needs _ex
+  return grouped_gemm_w2_ex(p, z, z_scale, w2, w2_scale, nullptr, block_expert_ids,
+                            num_post_padded, nullptr, nullptr, y2, stream);
 }
 
 moe_status unpermute_reduce(const moe_problem* p, const void* y2, const int32_t* inv_perm,
@@ -330,16 +381,17 @@ moe_status unpermute_reduce(const moe_problem* p, const void* y2, const int32_t*
   if (!valid_problem(p)) return MOE_ERR_INVALID_ARG;
   if (p->M == 0) return MOE_OK;
   if (!y2 || !inv_perm || !y) return MOE_ERR_INVALID_ARG;
-  if (!p->apply_router_weight_on_input && !topk_weights) return MOE_ERR_INVALID_ARG;
+  const bool unit = p->apply_router_weight_on_input || p->router_weight_in_gemm2;
+  if (!unit && !topk_weights) return MOE_ERR_INVALID_ARG;
   return cuda_status(launch_unpermute_reduce(y2, p->H, p->M, p->topk, inv_perm, topk_weights,
-                                             p->apply_router_weight_on_input != 0, y,
-                                             static_cast<cudaStream_t>(stream)));
+                                             unit, y, static_cast<cudaStream_t>(stream)));
 }
 
-moe_status fused_experts(const moe_problem* p, const void* x, const void* w13,
-                         const void* w13_scale, const void* w2, const void* w2_scale,
-                         const float* topk_weights, const int32_t* topk_ids, void* y,
-                         void* workspace, size_t workspace_bytes, void* stream) {
+moe_status fused_experts_ex(const moe_problem* p, const void* x, const void* w13,
+                            const void* w13_scale, const void* w13_bias, const void* w2,
+                            const void* w2_scale, const void* w2_bias,
+                            const float* topk_weights, const int32_t* topk_ids, void* y,
+                            void* workspace, size_t workspace_bytes, void* stream) {
   if (!valid_problem(p)) return MOE_ERR_INVALID_ARG;
   if (p->M == 0) return MOE_OK;
   if (!x || !w13 || !w2 || !topk_ids || !y || !workspace || !topk_weights)
@@ -358,21 +410,30 @@ moe_status fused_experts(const moe_problem* p, const void* x, const void* w13,
                                     ws + L.hist, L.sorted - L.hist, stream);
   if (st != MOE_OK) return st;
   if (!quantised(p)) {
-    st = grouped_gemm_w13(p, ws + L.xperm, nullptr, w13, nullptr, blocks, npp, ws + L.z, nullptr,
-                          1, stream);
+    st = grouped_gemm_w13_ex(p, ws + L.xperm, nullptr, w13, nullptr, w13_bias, blocks, npp,
+                             ws + L.z, nullptr, 1, stream);
     if (st != MOE_OK) return st;
-    st = grouped_gemm_w2(p, ws + L.z, nullptr, w2, nullptr, blocks, npp, ws + L.y2, stream);
+    st = grouped_gemm_w2_ex(p, ws + L.z, nullptr, w2, nullptr, w2_bias, blocks, npp, sorted,
+                            topk_weights, ws + L.y2, stream);
   } else {
-    st = grouped_gemm_w13(p, ws + L.xperm, f32(L.xscale), w13, w13_scale, blocks, npp,
-                          ws + L.h1, nullptr, 0, stream);
+    st = grouped_gemm_w13_ex(p, ws + L.xperm, f32(L.xscale), w13, w13_scale, w13_bias, blocks,
+                             npp, ws + L.h1, nullptr, 0, stream);
     if (st != MOE_OK) return st;
     st = act_mul_quant(p, ws + L.h1, npp, ws + L.z, f32(L.zscale), stream);
     if (st != MOE_OK) return st;
-    st = grouped_gemm_w2(p, ws + L.z, f32(L.zscale), w2, w2_scale, blocks, npp, ws + L.y2,
-                         stream);
+    st = grouped_gemm_w2_ex(p, ws + L.z, f32(L.zscale), w2, w2_scale, w2_bias, blocks, npp,
+                            sorted, topk_weights, ws + L.y2, stream);
   }
   if (st != MOE_OK) return st;
   return unpermute_reduce(p, ws + L.y2, inv, topk_weights, y, stream);
+}
+
+moe_status fused_experts(const moe_problem* p, const void* x, const void* w13,
+                         const void* w13_scale, const void* w2, const void* w2_scale,
+                         const float* topk_weights, const int32_t* topk_ids, void* y,
+                         void* workspace, size_t workspace_bytes, void* stream) {
+  return fused_experts_ex(p, x, w13, w13_scale, nullptr, w2, w2_scale, nullptr, topk_weights,
+                          topk_ids, y, workspace, workspace_bytes, stream);
 }
 
 moe_status fused_experts_from_host(const moe_problem* p, const void* host_x,
@@ -447,6 +508,8 @@ moe_status fused_experts_batched(const moe_problem* p, const void* x,
                                  const void* w2, const void* w2_scale, void* y, void* workspace,
                                  size_t workspace_bytes, void* stream) {
   if (!valid_batched(p, max_tokens) || expected_m < 0) return MOE_ERR_INVALID_ARG;
+  if (p->router_weight_in_gemm2 || p->act_recipe < 0 || p->act_recipe > 1)
+    return MOE_ERR_INVALID_ARG;   // the layout carries no router weights
   if (!x || !expert_num_tokens || !w13 || !w2 || !y || !workspace) return MOE_ERR_INVALID_ARG;
   if (quantised(p) && (!w13_scale || !w2_scale)) return MOE_ERR_INVALID_ARG;
   if (!gemm_supported(p)) return MOE_ERR_UNSUPPORTED;
@@ -461,15 +524,16 @@ moe_status fused_experts_batched(const moe_problem* p, const void* x,
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const int rows = p->E * max_tokens, H = p->H, I = p->I, E = p->E;
   const bool ue8m0 = p->act_scale_fmt == MOE_SCALE_UE8M0;
+  const Epilogue ep = make_epilogue(p, nullptr, 0, nullptr, nullptr);
   cudaError_t e = launch_batched_blocks(expert_num_tokens, E, max_tokens, blocks, npp, sorted, s);
   if (e != cudaSuccess) return cuda_status(e);
   if (!quantised(p)) {
     // the layout's rows are GEMM1's rows as they are: no permute
     e = launch_bf16_gemm(expected_m, x, rows, H, w13, E * 2 * I, 2 * I, 2 * I, blocks, npp,
-                         ws + L.z, true, s);
+                         ws + L.z, true, ep, s);
     if (e == cudaSuccess)
       e = launch_bf16_gemm(expected_m, ws + L.z, rows, I, w2, E * H, H, H, blocks, npp, y,
-                           false, s);
+                           false, ep, s);
     return cuda_status(e);
   }
   // quantised: per-row dynamic quantisation of the layout, then the same stages
@@ -477,19 +541,19 @@ moe_status fused_experts_batched(const moe_problem* p, const void* x,
   if (e != cudaSuccess) return cuda_status(e);
   if (p->quant == MOE_Q_MXFP4_W4A8)
     e = launch_ggemm_mxfp4(ws + L.xq, xscale, rows, H, w13, static_cast<const uint8_t*>(w13_scale),
-                           E * 2 * I, 2 * I, 2 * I, blocks, npp, ws + L.h1, s);
+                           E * 2 * I, 2 * I, 2 * I, blocks, npp, ws + L.h1, ep, s);
   else
     e = launch_ggemm_fp8(ws + L.xq, xscale, rows, H, w13, static_cast<const float*>(w13_scale),
-                         E * 2 * I, 2 * I, 2 * I, blocks, npp, ws + L.h1, s);
+                         E * 2 * I, 2 * I, 2 * I, blocks, npp, ws + L.h1, ep, s);
   if (e != cudaSuccess) return cuda_status(e);
-  e = launch_act_mul(ws + L.h1, I, npp, ws + L.z, zscale, ue8m0, rows, s);
+  e = launch_act_mul(ws + L.h1, I, npp, ws + L.z, zscale, ue8m0, rows, ep, s);
   if (e != cudaSuccess) return cuda_status(e);
   if (p->quant == MOE_Q_MXFP4_W4A8)
     e = launch_ggemm_mxfp4(ws + L.z, zscale, rows, I, w2, static_cast<const uint8_t*>(w2_scale),
-                           E * H, H, H, blocks, npp, y, s);
+                           E * H, H, H, blocks, npp, y, ep, s);
   else
     e = launch_ggemm_fp8(ws + L.z, zscale, rows, I, w2, static_cast<const float*>(w2_scale),
-                         E * H, H, H, blocks, npp, y, s);
+                         E * H, H, H, blocks, npp, y, ep, s);
   return cuda_status(e);
 }
 

@@ -59,6 +59,7 @@ struct GemmArgs {
   uint64_t limit_ns;
   int never_arrive;
   int* err;
+  Epilogue ep;            // bias, router weight, activation recipe
 };
 
 template <bool FUSE>
@@ -230,37 +231,24 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const size_t row = (size_t)m_blk * BM + row_in_tile;
       __nv_bfloat16* out_row = args.out + row * args.ldo + (size_t)n_tile * args.out_cols_per_tile;
       if (FUSE) {
+        const int gcol = n_tile * 128;          // gate columns of the tile; up at + I
 #pragma unroll 1
         for (int c = 0; c < 4; ++c) {
           uint32_t g[32], u[32];
           tmem_ld_32x32b_x32(taddr + c * 32, g);
           tmem_ld_32x32b_x32(taddr + 128 + c * 32, u);
           tmem_ld_wait();
-          uint4 pk[4];
-          __nv_bfloat16* pb = reinterpret_cast<__nv_bfloat16*>(pk);
-#pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            const float gv = bf16_round(__uint_as_float(g[j]));
-            const float uv = bf16_round(__uint_as_float(u[j]));
-            pb[j] = __float2bfloat16_rn(silu_fast(gv) * uv);
-          }
-          uint4* dst = reinterpret_cast<uint4*>(out_row + c * 32);
-#pragma unroll
-          for (int j = 0; j < 4; ++j) dst[j] = pk[j];
+          epi_glu_store32(args.ep, e, gcol + c * 32, args.ldo + gcol + c * 32, g, u,
+                          out_row + c * 32);
         }
       } else {
+        const float w = epi_row_weight(args.ep, row);
 #pragma unroll 1
         for (int c = 0; c < BN / 32; ++c) {
           uint32_t r[32];
           tmem_ld_32x32b_x32(taddr + c * 32, r);
           tmem_ld_wait();
-          uint4 pk[4];
-          __nv_bfloat16* pb = reinterpret_cast<__nv_bfloat16*>(pk);
-#pragma unroll
-          for (int j = 0; j < 32; ++j) pb[j] = __float2bfloat16_rn(__uint_as_float(r[j]));
-          uint4* dst = reinterpret_cast<uint4*>(out_row + c * 32);
-#pragma unroll
-          for (int j = 0; j < 4; ++j) dst[j] = pk[j];
+          epi_store32(args.ep, e, n_tile * BN + c * 32, w, r, out_row + c * 32);
         }
       }
       tc_fence_before();
@@ -357,7 +345,7 @@ bool make_tmap_u8_rows(CUtensorMap* map, const void* base, uint64_t rows, uint64
 cudaError_t launch_ggemm_bf16(const void* A, int cap, int K, const void* B, int b_rows_total,
                               int b_rows_per_expert, int n_out, const int32_t* block_expert_ids,
                               const int32_t* num_post_padded, void* out, bool fuse_act,
-                              cudaStream_t stream) {
+                              const Epilogue& ep, cudaStream_t stream) {
   if (cap <= 0) return cudaSuccess;
   CUtensorMap tmA, tmB;
   if (!make_tmap_k_sw128(&tmA, A, (uint64_t)cap, (uint64_t)K, 2, 128) ||
@@ -388,6 +376,7 @@ cudaError_t launch_ggemm_bf16(const void* A, int cap, int K, const void* B, int 
   }
   watchdog_params(&a.limit_ns, &a.never_arrive);
   a.err = dev_error_word();
+  a.ep = ep;
   const int grid = num_sms();
   if (fuse_act) {
     static bool attr_done = false;

@@ -79,6 +79,7 @@ struct Fp8Args {
   uint64_t limit_ns;
   int never_arrive;
   int* err;
+  Epilogue ep;            // bias, router weight
 };
 
 __global__ void __launch_bounds__(NUM_THREADS, 1)
@@ -292,12 +293,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       if (!ok) break;
       if (active) {
         uint4* dst = reinterpret_cast<uint4*>(args.out + row * args.ldo + (size_t)nblk * 128);
+        const float w = epi_row_weight(args.ep, row);
+        const bool bias = args.ep.bias != nullptr;
 #pragma unroll
         for (int v = 0; v < 16; ++v) {
           uint4 pk;
           __nv_bfloat16* pb = reinterpret_cast<__nv_bfloat16*>(&pk);
 #pragma unroll
-          for (int j = 0; j < 8; ++j) pb[j] = __float2bfloat16_rn(acc[v * 8 + j]);
+          for (int j = 0; j < 8; ++j) {
+            float x = acc[v * 8 + j];
+            if (bias) x += epi_bias(args.ep, e, nblk * 128 + v * 8 + j);
+            pb[j] = __float2bfloat16_rn(x * w);
+          }
           dst[v] = pk;
         }
       }
@@ -318,13 +325,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 cudaError_t launch_ggemm_fp8(const void* A, const float* a_scale, int cap, int K, const void* B,
                              const float* b_scale, int b_rows_total, int b_rows_per_expert,
                              int n_out, const int32_t* block_expert_ids,
-                             const int32_t* num_post_padded, void* out, cudaStream_t stream) {
+                             const int32_t* num_post_padded, void* out, const Epilogue& ep,
+                             cudaStream_t stream) {
   if (cap <= 0) return cudaSuccess;
   CUtensorMap tmA, tmB;
   if (!make_tmap_k_sw128(&tmA, A, (uint64_t)cap, (uint64_t)K, 1, 128) ||
       !make_tmap_k_sw128(&tmB, B, (uint64_t)b_rows_total, (uint64_t)K, 1, 128))
     return cudaErrorInvalidValue;
   Fp8Args a;
+  a.ep = ep;
   a.block_expert_ids = block_expert_ids;
   a.num_post_padded = num_post_padded;
   a.a_scale = a_scale;

@@ -110,6 +110,7 @@ struct Mx4Args {
   uint64_t limit_ns;
   int never_arrive;
   int* err;
+  Epilogue ep;              // bias, router weight
 };
 
 template <bool STAGED>
@@ -496,6 +497,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       if (!ok) break;
       tc_fence_after();
       const size_t row = (size_t)m_blk * BM + row_in_tile;
+      const float w = epi_row_weight(args.ep, row);
+      const bool bias = args.ep.bias != nullptr;
 #pragma unroll 1
       for (int half = 0; half < 2; ++half) {        // 128 columns at a time
         const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + half * 128;
@@ -512,13 +515,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
         if (store) {
           uint4* dst = reinterpret_cast<uint4*>(out_row);
+          const int col0 = n_tile * BN + half * 128;
 #pragma unroll
           for (int v = 0; v < 16; ++v) {
             uint4 pk;
             __nv_bfloat16* pb = reinterpret_cast<__nv_bfloat16*>(&pk);
 #pragma unroll
-            for (int j = 0; j < 8; ++j)
-              pb[j] = __float2bfloat16_rn(__uint_as_float(r[v >> 2][8 * (v & 3) + j]));
+            for (int j = 0; j < 8; ++j) {
+              float x = __uint_as_float(r[v >> 2][8 * (v & 3) + j]);
+              if (bias) x += epi_bias(args.ep, e, col0 + 8 * v + j);
+              pb[j] = __float2bfloat16_rn(x * w);
+            }
             dst[v] = pk;
           }
         }
@@ -541,7 +548,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 cudaError_t launch_ggemm_mxfp4(const void* A, const float* a_scale, int cap, int K, const void* B,
                                const uint8_t* b_scale, int b_rows_total, int b_rows_per_expert,
                                int n_out, const int32_t* block_expert_ids,
-                               const int32_t* num_post_padded, void* out, cudaStream_t stream) {
+                               const int32_t* num_post_padded, void* out, const Epilogue& ep,
+                               cudaStream_t stream) {
   if (cap <= 0) return cudaSuccess;
   if ((reinterpret_cast<uintptr_t>(B) & 31u) != 0 || (reinterpret_cast<uintptr_t>(b_scale) & 3u))
     return cudaErrorInvalidValue;
@@ -550,6 +558,7 @@ cudaError_t launch_ggemm_mxfp4(const void* A, const float* a_scale, int cap, int
       !make_tmap_fp4_k_sw128(&tmB, B, (uint64_t)b_rows_total, (uint64_t)K, 128))
     return cudaErrorInvalidValue;
   Mx4Args a;
+  a.ep = ep;
   a.block_expert_ids = block_expert_ids;
   a.num_post_padded = num_post_padded;
   a.a_scale = a_scale;

@@ -434,6 +434,82 @@ __device__ __forceinline__ float bf16_round(float v) {
 // the power cap).  g -> -inf gives -0, g -> +inf gives g.
 __device__ __forceinline__ float silu_fast(float g) { return __fdividef(g, 1.0f + __expf(-g)); }
 
+// Optional epilogue work of the grouped GEMMs, in the order of the pages'
+// GEMM post-processing (page "fused_moe.py 分析", fused_moe_kernel "后处理":
+// dequant -> bias -> router weight -> cast to the output type), plus the
+// gated activation recipe of the fused GEMM1 (page "Blackwell 上的 DeepGEMM
+// FusedMoE（vLLM）", §2.6.4: gemm1_alpha / gemm1_beta / gemm1_clamp_limit).
+struct Epilogue {
+  const __nv_bfloat16* bias;   // [E, n_bias] bf16 added in fp32, or null
+  int n_bias;                  // bias columns per expert (2I for GEMM1, H for GEMM2)
+  const int32_t* sorted_ids;   // row -> routed item, with item_weights for the
+  const float* item_weights;   //   router weight of the row (null: none)
+  int R;                       // routed items; rows holding ids >= R are padding
+  int recipe;                  // 0: SiLU(g) * u; 1: the alpha / beta / limit recipe
+  float alpha, beta, limit;    // z = (clamp(u, -limit, limit) + beta) * g' * sigmoid(alpha g'),
+                               // g' = min(g, limit); limit <= 0: no clamping
+};
+
+// Router weight of output row `row` (1 without one; 0 for a padding row).
+__device__ __forceinline__ float epi_row_weight(const Epilogue& ep, size_t row) {
+  if (ep.item_weights == nullptr) return 1.0f;
+  const int sid = ep.sorted_ids[row];
+  return sid < ep.R ? ep.item_weights[sid] : 0.0f;
+}
+// Bias of expert e at column col (0 without a bias).
+__device__ __forceinline__ float epi_bias(const Epilogue& ep, int e, int col) {
+  return ep.bias == nullptr ? 0.0f
+                            : __bfloat162float(ep.bias[(size_t)e * ep.n_bias + col]);
+}
+// The gated activation of one (gate, up) pair.
+__device__ __forceinline__ float act_glu(const Epilogue& ep, float g, float u) {
+  if (ep.recipe == 0) return silu_fast(g) * u;
+  if (ep.limit > 0.0f) {
+    g = fminf(g, ep.limit);
+    u = fminf(fmaxf(u, -ep.limit), ep.limit);
+  }
+  return __fdividef(g, 1.0f + __expf(-ep.alpha * g)) * (u + ep.beta);
+}
+
+// Fused GEMM1 epilogue for 32 columns of one row: the gate and up sums
+// (plus bias), each rounded to bf16 as a stored H1 would be, through the gated
+// activation, as 32 bf16 values at dst (16-byte aligned).
+__device__ __forceinline__ void epi_glu_store32(const Epilogue& ep, int e, int gcol0, int ucol0,
+                                                const uint32_t (&g)[32], const uint32_t (&u)[32],
+                                                __nv_bfloat16* dst) {
+  uint4 pk[4];
+  __nv_bfloat16* pb = reinterpret_cast<__nv_bfloat16*>(pk);
+  const bool bias = ep.bias != nullptr;
+#pragma unroll
+  for (int j = 0; j < 32; ++j) {
+    float gs = __uint_as_float(g[j]), us = __uint_as_float(u[j]);
+    if (bias) {
+      gs += epi_bias(ep, e, gcol0 + j);
+      us += epi_bias(ep, e, ucol0 + j);
+    }
+    pb[j] = __float2bfloat16_rn(act_glu(ep, bf16_round(gs), bf16_round(us)));
+  }
+  uint4* d = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+  for (int j = 0; j < 4; ++j) d[j] = pk[j];
+}
+// Plain epilogue for 32 columns of one row: bf16((acc + bias) * w) at dst.
+__device__ __forceinline__ void epi_store32(const Epilogue& ep, int e, int col0, float w,
+                                            const uint32_t (&r)[32], __nv_bfloat16* dst) {
+  uint4 pk[4];
+  __nv_bfloat16* pb = reinterpret_cast<__nv_bfloat16*>(pk);
+  const bool bias = ep.bias != nullptr;
+#pragma unroll
+  for (int j = 0; j < 32; ++j) {
+    float v = __uint_as_float(r[j]);
+    if (bias) v += epi_bias(ep, e, col0 + j);
+    pb[j] = __float2bfloat16_rn(v * w);
+  }
+  uint4* d = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+  for (int j = 0; j < 4; ++j) d[j] = pk[j];
+}
+
 // fp32 -> e4m3fn, round to nearest even, saturating to +-448.
 __device__ __forceinline__ uint8_t f32_to_e4m3(float v) {
   return static_cast<uint8_t>(__nv_cvt_float_to_fp8(v, __NV_SATFINITE, __NV_E4M3));

@@ -9,6 +9,8 @@
 
 namespace moe {
 
+struct Epilogue;   // optional GEMM epilogue work (moe_common.cuh)
+
 constexpr int kRouteSeg = 512;        // routed items handled by one warp
 constexpr int kRouteWarps = 8;        // warps per routing CTA
 
@@ -32,8 +34,10 @@ cudaError_t launch_permute_rows(const void* x, int H, int topk, int R, const int
                                 cudaStream_t stream);
 
 // SiLU-and-mul over h1 [rows, 2I] bf16 -> z bf16, or e4m3 + scales.
+// act: the gated activation recipe (recipe / alpha / beta / limit fields).
 cudaError_t launch_act_mul(const void* h1, int I, const int32_t* num_post_padded, void* z,
-                           float* z_scale, bool ue8m0, int cap, cudaStream_t stream);
+                           float* z_scale, bool ue8m0, int cap, const Epilogue& act,
+                           cudaStream_t stream);
 
 // Weighted top-k gather-reduce into y [M, H] bf16.
 cudaError_t launch_unpermute_reduce(const void* y2, int H, int M, int topk,
@@ -57,26 +61,28 @@ cudaError_t launch_topk_router(const void* logits, bool bf16, int M, int E, int 
 cudaError_t launch_ggemm_bf16(const void* A, int cap, int K, const void* B, int b_rows_total,
                               int b_rows_per_expert, int n_out, const int32_t* block_expert_ids,
                               const int32_t* num_post_padded, void* out, bool fuse_act,
-                              cudaStream_t stream);
+                              const Epilogue& ep, cudaStream_t stream);
 // The same GEMM issued on SM pairs (cta_group::2, 256 x 256 tiles).
 cudaError_t launch_ggemm_bf16_2sm(const void* A, int cap, int K, const void* B,
                                   int b_rows_total, int b_rows_per_expert, int n_out,
                                   const int32_t* block_expert_ids,
                                   const int32_t* num_post_padded, void* out, bool fuse_act,
-                                  cudaStream_t stream);
+                                  const Epilogue& ep, cudaStream_t stream);
 
 // FP8 (e4m3) grouped GEMM with fp32 1x128 activation scales and 128x128
 // weight block scales: out = sum_kb sa*sb*partial_kb (bf16 output).
 cudaError_t launch_ggemm_fp8(const void* A, const float* a_scale, int cap, int K, const void* B,
                              const float* b_scale, int b_rows_total, int b_rows_per_expert,
                              int n_out, const int32_t* block_expert_ids,
-                             const int32_t* num_post_padded, void* out, cudaStream_t stream);
+                             const int32_t* num_post_padded, void* out, const Epilogue& ep,
+                             cudaStream_t stream);
 
 // MXFP4 (E2M1 + E8M0 per 32) weights x e4m3 activations with power-of-two
 // 1x128 scales, block-scaled tensor-core MMA (bf16 output).
 cudaError_t launch_ggemm_mxfp4(const void* A, const float* a_scale, int cap, int K, const void* B,
                                const uint8_t* b_scale, int b_rows_total, int b_rows_per_expert,
                                int n_out, const int32_t* block_expert_ids,
-                               const int32_t* num_post_padded, void* out, cudaStream_t stream);
+                               const int32_t* num_post_padded, void* out, const Epilogue& ep,
+                               cudaStream_t stream);
 
 }  // namespace moe
