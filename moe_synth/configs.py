@@ -2,7 +2,8 @@
 
 Shapes: Mixtral-8x7B-class experts (H=4096, I=14336, E=8, top-2) at prefill and
 decode token counts, a DeepSeek-class FP8 layer (H=7168, I=2048, E=256, top-8)
-with skewed routing, and the same DeepSeek-class shape with MXFP4 weights.
+with skewed routing, the same DeepSeek-class shape with MXFP4 weights, and
+with MXFP8 (1x32) weights and activations.
 """
 from __future__ import annotations
 
@@ -17,7 +18,7 @@ class MoEConfig:
     I: int            # expert intermediate size (GEMM1 N = 2I)
     E: int            # experts
     topk: int
-    quant: str        # "bf16" | "fp8" | "mxfp4"
+    quant: str        # "bf16" | "fp8" | "mxfp4" | "mxfp8"
     routing: str      # "softmax" | "skew" | "uniform"
     seed: int
     block_size: int = 128
@@ -45,6 +46,8 @@ CONFIGS = {
     "mxfp4": MoEConfig("mxfp4", M=2048, H=7168, I=2048, E=256, topk=8,
                        quant="mxfp4", routing="uniform", seed=5,
                        act_scale_fmt="ue8m0"),
+    "mxfp8": MoEConfig("mxfp8", M=8192, H=7168, I=2048, E=256, topk=8, quant="mxfp8",
+                       routing="skew", seed=6, act_scale_fmt="ue8m0"),
 }
 
 

@@ -106,6 +106,22 @@ def _mxfp4_weights(E, N, K, g, device):
     return packed, scales
 
 
+def _mxfp8_weights(E, N, K, g, device):
+    """N(0,0.02) weights cast to e4m3fn with one E8M0 scale per 1x32 group
+    along K: 2^ceil(log2(amax / 448)), stored as the biased exponent byte."""
+    codes = torch.empty(E, N, K, dtype=torch.uint8, device=device)
+    scales = torch.empty(E, N, K // 32, dtype=torch.uint8, device=device)
+    for e in range(E):
+        w = (torch.randn(N, K, generator=g, device=device) * 0.02).view(N, K // 32, 32)
+        amax = w.abs().amax(dim=-1).clamp_min(1e-30)
+        ex = torch.ceil(torch.log2(amax / 448.0)).clamp_(-127, 127)
+        s = torch.exp2(ex)
+        q = (w / s[..., None]).clamp_(-448.0, 448.0).to(torch.float8_e4m3fn)
+        codes[e] = q.view(torch.uint8).view(N, K)
+        scales[e] = (ex + 127).to(torch.uint8)
+    return codes, scales
+
+
 def make_inputs(cfg: MoEConfig, device="cpu", weights: bool = True):
     """All inputs of one workload as torch tensors on ``device``.
 
@@ -132,6 +148,9 @@ def make_inputs(cfg: MoEConfig, device="cpu", weights: bool = True):
     elif cfg.quant == "mxfp4":
         out["w13"], out["w13_scale"] = _mxfp4_weights(E, 2 * I, H, gw, device)
         out["w2"], out["w2_scale"] = _mxfp4_weights(E, H, I, gw, device)
+    elif cfg.quant == "mxfp8":
+        out["w13"], out["w13_scale"] = _mxfp8_weights(E, 2 * I, H, gw, device)
+        out["w2"], out["w2_scale"] = _mxfp8_weights(E, H, I, gw, device)
     else:
         raise ValueError(cfg.quant)
     return out

@@ -38,15 +38,16 @@ EPS32 = float(np.float32(1e-10))
 
 
 # ----------------------------------------------------------------- quantisation
-def quant_act_1x128(v, scale_fmt: str = "fp32"):
-    """Dynamic per-(row, 128-column group) FP8 quantisation.
+def quant_act_1x128(v, scale_fmt: str = "fp32", group: int = 128):
+    """Dynamic per-(row, column group) FP8 quantisation, groups of 128 (the
+    FP8 block and W4A8 recipes) or 32 (MXFP8, always with UE8M0 scales).
 
-    v: [R, K] fp64 (K % 128 == 0).  Returns (q values [R, K] fp64 on the e4m3
-    grid, s [R, K/128] fp64 holding fp32 (or power-of-two) scales)."""
+    v: [R, K] fp64 (K % group == 0).  Returns (q values [R, K] fp64 on the
+    e4m3 grid, s [R, K/group] fp64 holding fp32 (or power-of-two) scales)."""
     v = np.asarray(v, dtype=np.float64)
     R, K = v.shape
-    g = v.reshape(R, K // 128, 128)
-    amax = np.abs(g).max(axis=-1) if R else np.zeros((0, K // 128))
+    g = v.reshape(R, K // group, group)
+    amax = np.abs(g).max(axis=-1) if R else np.zeros((0, K // group))
     s = codecs.round_fp32(np.maximum(amax, EPS32) / codecs.E4M3_MAX)
     if scale_fmt == "ue8m0":
         s = codecs.ceil_pow2(s)
@@ -61,6 +62,7 @@ def dequant_weights(w, w_scale, quant: str):
 
     bf16: values as given.  fp8: e4m3 codes * fp32 128x128 block scale.
     mxfp4: E2M1 codes (packed, low nibble even k) * E8M0 scale per 32 along K.
+    mxfp8: e4m3 codes * E8M0 scale per 32 along K.
     """
     if quant == "bf16":
         return np.asarray(w, dtype=np.float64)
@@ -74,11 +76,20 @@ def dequant_weights(w, w_scale, quant: str):
         q = codecs.e2m1_decode(codecs.unpack_fp4(w, 2 * Kh))
         s = codecs.e8m0_decode(w_scale)
         return q * np.repeat(s, 32, axis=2)
+    if quant == "mxfp8":
+        q = codecs.e4m3_decode(w)
+        return q * np.repeat(codecs.e8m0_decode(w_scale), 32, axis=2)
     raise ValueError(quant)
 
 
+def act_group(quant: str) -> int:
+    """Activation quantisation group along K: 32 for MXFP8 (recipe (1, 32)),
+    else 128."""
+    return 32 if quant == "mxfp8" else 128
+
+
 # ------------------------------------------------------------------ the stages
-def permute_rows(x, route, topk: int, topk_weights=None, scale_fmt=None):
+def permute_rows(x, route, topk: int, topk_weights=None, scale_fmt=None, group: int = 128):
     """Data half of the permute: x_perm[row] = x[sorted_token_ids[row] // k].
 
     Padding rows are zero.  With ``topk_weights`` (apply_router_weight_on_input)
@@ -98,7 +109,7 @@ def permute_rows(x, route, topk: int, topk_weights=None, scale_fmt=None):
         xp[live] = codecs.round_bf16(codecs.round_fp32(xp[live] * w[sid[live]][:, None]))
     if scale_fmt is None:
         return xp, None
-    q, s = quant_act_1x128(xp, scale_fmt)
+    q, s = quant_act_1x128(xp, scale_fmt, group)
     q[~live] = 0.0
     s[~live] = 0.0
     return q, s
@@ -111,6 +122,7 @@ def grouped_gemm(a, a_scale, w, w_scale, route, block_size: int, quant: str):
     bf16: plain fp64 product.  fp8 (block 128x128 weight scales, 1x128
     activation scales): C = sum_kb sa[row, kb] * sb[e, n/128, kb] *
     sum_{k in kb} qa * qb.  mxfp4: A = qa * sa (per 128), W dequantised.
+    mxfp8: A = qa * sa (per 32), W dequantised (E8M0 per 32).
     Returns fp64 [cap, N] (not rounded)."""
     a = np.asarray(a, dtype=np.float64)
     cap, K = a.shape
@@ -141,9 +153,9 @@ def grouped_gemm(a, a_scale, w, w_scale, route, block_size: int, quant: str):
                 sb_n = np.repeat(sb[:, kb], 128)[:N]
                 acc += a_scale[rows, kb][:, None] * sb_n[None, :] * part
             out[rows] = acc
-        elif quant == "mxfp4":
-            wd = dequant_weights(np.asarray(w[e])[None], np.asarray(w_scale[e])[None], "mxfp4")[0]
-            ad = a[rows] * np.repeat(a_scale[rows], 128, axis=1)
+        elif quant in ("mxfp4", "mxfp8"):
+            wd = dequant_weights(np.asarray(w[e])[None], np.asarray(w_scale[e])[None], quant)[0]
+            ad = a[rows] * np.repeat(a_scale[rows], act_group(quant), axis=1)
             out[rows] = ad @ wd.T
         else:
             raise ValueError(quant)
@@ -217,6 +229,8 @@ def unpermute_reduce(y2, inv_perm, topk_weights, apply_router_weight_on_input=Fa
 
 # ------------------------------------------------------------- whole forward
 def _act_scale_fmt(quant: str, act_scale_fmt: str):
+    if quant == "mxfp8" and act_scale_fmt != "ue8m0":
+        raise ValueError("MXFP8 activations take UE8M0 scales")
     return None if quant == "bf16" else act_scale_fmt
 
 
@@ -242,14 +256,15 @@ def fused_experts(x, topk_ids, topk_weights, w13, w2, w13_scale=None, w2_scale=N
     fmt = _act_scale_fmt(quant, act_scale_fmt)
     route = align_permute(ids, E, block_size)
     xp, xs = permute_rows(x, route, k,
-                          topk_weights if apply_router_weight_on_input else None, fmt)
+                          topk_weights if apply_router_weight_on_input else None, fmt,
+                          act_group(quant))
     h1 = grouped_gemm(xp, xs, w13, w13_scale, route, block_size, quant)
     h1 = add_expert_bias(h1, w13_bias, route, block_size)
     z = act_mul(h1, I, exact=exact, recipe=act_recipe)
     if fmt is None:
         zq, zs = (z if exact else codecs.round_bf16(z)), None
     else:
-        zq, zs = quant_act_1x128(z, fmt)
+        zq, zs = quant_act_1x128(z, fmt, act_group(quant))
         live = route["sorted_token_ids"] < M * k
         zq[~live] = 0.0
         zs[~live] = 0.0
@@ -310,11 +325,11 @@ def fused_experts_per_token(x, topk_ids, topk_weights, w13, w2, w13_scale=None,
                 if fmt is None:
                     h = W13 @ xt
                 else:
-                    q, s = quant_act_1x128(xt[None], fmt)
+                    q, s = quant_act_1x128(xt[None], fmt, act_group(quant))
                     if quant == "fp8":
                         h = _fp8_matvec(q[0], s[0], w13[e], np.asarray(w13_scale)[e])
                     else:
-                        h = W13 @ (q[0] * np.repeat(s[0], 128))
+                        h = W13 @ (q[0] * np.repeat(s[0], act_group(quant)))
                 if w13_bias is not None:
                     h = h + np.asarray(w13_bias, dtype=np.float64)[e]
                 if not exact:
@@ -325,11 +340,11 @@ def fused_experts_per_token(x, topk_ids, topk_weights, w13, w2, w13_scale=None,
                         z = codecs.round_bf16(z)
                     o = W2 @ z
                 else:
-                    q, s = quant_act_1x128(z[None], fmt)
+                    q, s = quant_act_1x128(z[None], fmt, act_group(quant))
                     if quant == "fp8":
                         o = _fp8_matvec(q[0], s[0], w2[e], np.asarray(w2_scale)[e])
                     else:
-                        o = W2 @ (q[0] * np.repeat(s[0], 128))
+                        o = W2 @ (q[0] * np.repeat(s[0], act_group(quant)))
                 if w2_bias is not None:
                     o = o + np.asarray(w2_bias, dtype=np.float64)[e]
                 if router_weight_in_gemm2:

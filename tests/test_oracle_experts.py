@@ -41,6 +41,8 @@ SMALL = {
                        routing="uniform", seed=13, act_scale_fmt="ue8m0"),
     "invalid": MoEConfig("t_inv", M=20, H=128, I=128, E=6, topk=3, quant="bf16",
                          routing="softmax", seed=14, invalid_frac=0.3),
+    "mxfp8": MoEConfig("t_mx8", M=10, H=256, I=128, E=4, topk=3, quant="mxfp8",
+                       routing="uniform", seed=15, act_scale_fmt="ue8m0"),
 }
 
 
@@ -218,14 +220,14 @@ def test_planted_gate_up_swap_is_caught(monkeypatch):
 def test_planted_token_index_mistake_is_caught(monkeypatch):
     orig = experts.permute_rows
 
-    def wrong(x, route, topk, topk_weights=None, scale_fmt=None):
+    def wrong(x, route, topk, topk_weights=None, scale_fmt=None, group=128):
         r2 = dict(route)
         sid = route["sorted_token_ids"].copy()
         R = route["inv_perm"].size
         live = sid < R
         sid[live] = (sid[live] % topk) * topk + (sid[live] // topk) % topk  # r % k for r // k
         r2["sorted_token_ids"] = sid
-        return orig(x, r2, topk, topk_weights, scale_fmt)
+        return orig(x, r2, topk, topk_weights, scale_fmt, group)
     assert _catches(monkeypatch, "permute_rows", wrong)
 
 
@@ -365,3 +367,51 @@ def test_dense_special_case_with_bias_and_recipe():
                                 w13.numpy(), w2.numpy(), exact=True, w13_bias=b13.numpy(),
                                 w2_bias=b2.numpy(), act_recipe=RECIPE)["y"]
     np.testing.assert_allclose(out, ref.numpy(), rtol=1e-12, atol=1e-12)
+
+
+# ---------------------------------------------------------------- MXFP8 (1x32)
+def test_mxfp8_activation_quant_against_torch_cast():
+    """1x32 groups with UE8M0 scales: scale 2^ceil(log2(amax/448)), codes by
+    torch's float8 cast."""
+    rng = np.random.default_rng(11)
+    v = codecs.round_bf16(rng.normal(0, 1, (32, 256)) * rng.uniform(0.01, 100, (32, 1)))
+    q, s = experts.quant_act_1x128(v, "ue8m0", 32)
+    vt = torch.from_numpy(v.astype(np.float32)).view(32, 8, 32).double()
+    st = torch.exp2(torch.ceil(torch.log2(vt.abs().amax(-1) / 448.0)))
+    qt = (vt / st[..., None]).float().to(torch.float8_e4m3fn).double().view(32, 256)
+    assert np.array_equal(s, st.numpy())
+    assert np.array_equal(q, qt.numpy())
+    assert np.all(np.abs(q) <= 448.0) and s.shape == (32, 8)
+
+
+def test_mxfp8_weight_dequant_against_torch():
+    rng = np.random.default_rng(12)
+    codes = rng.integers(0, 256, (2, 8, 64), dtype=np.uint8)
+    codes[(codes & 0x7F) == 0x7F] = 0          # the two NaN codes of e4m3fn are never stored
+    sc = rng.integers(120, 135, (2, 8, 2), dtype=np.uint8)
+    want = (torch.from_numpy(codes).view(torch.float8_e4m3fn).double() *
+            torch.exp2(torch.from_numpy(sc.astype(np.float64) - 127.0)).repeat_interleave(32, -1))
+    assert np.array_equal(experts.dequant_weights(codes, sc, "mxfp8"), want.numpy())
+
+
+def test_mxfp8_gemm_is_the_dequantised_product():
+    cfg = SMALL["mxfp8"]
+    a = _inputs(cfg)
+    out = experts.fused_experts(**a, quant="mxfp8", act_scale_fmt="ue8m0", exact=True)
+    route = out["route"]
+    h1 = experts.grouped_gemm(out["x_perm"], out["x_scale"], a["w13"], a["w13_scale"], route, 128,
+                              "mxfp8")
+    wd = experts.dequant_weights(a["w13"], a["w13_scale"], "mxfp8")
+    xd = out["x_perm"] * np.repeat(out["x_scale"], 32, axis=1)
+    ids = route["block_expert_ids"]
+    for b in range(route["num_tokens_post_padded"] // 128):
+        r = slice(b * 128, b * 128 + 128)
+        np.testing.assert_allclose(h1[r], xd[r] @ torch.from_numpy(wd[ids[b]]).numpy().T,
+                                   rtol=1e-13, atol=1e-13)
+
+
+def test_mxfp8_needs_ue8m0_activation_scales():
+    cfg = SMALL["mxfp8"]
+    a = _inputs(cfg)
+    with pytest.raises(ValueError):
+        experts.fused_experts(**a, quant="mxfp8", act_scale_fmt="fp32")
