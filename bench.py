@@ -50,7 +50,8 @@ def _peaks():
 
 _LABEL = {"mixtral": "Mixtral-8x7B-shaped prefill", "decode": "Mixtral-8x7B-shaped decode",
           "dsfp8": "DeepSeek-class FP8 (128x128 block scales, skewed routing)",
-          "mxfp4": "DeepSeek-class MXFP4 W4A8", "tiny": "tiny"}
+          "mxfp4": "DeepSeek-class MXFP4 W4A8", "mxfp8": "DeepSeek-class MXFP8 (1x32)",
+          "tiny": "tiny"}
 
 
 def _workload(args):
@@ -178,6 +179,7 @@ _KERNEL_SOURCES = {
     "bf16_2sm": ["gemm_bf16_2sm.cu", "moe_common.cuh", "tile_sched.cuh"],
     "fp8": ["gemm_fp8.cu", "moe_common.cuh", "tile_sched.cuh"],
     "mxfp4": ["gemm_mxfp4.cu", "moe_common.cuh", "tile_sched.cuh"],
+    "mxfp8": ["gemm_mxfp4.cu", "moe_common.cuh", "tile_sched.cuh"],
 }
 
 
@@ -188,6 +190,8 @@ def gemm1_kernel(cfg):
         return "fp8", "k_ggemm_fp8 (GEMM1)"
     if cfg.quant == "mxfp4":
         return "mxfp4", "k_ggemm_mxfp4 (GEMM1)"
+    if cfg.quant == "mxfp8":
+        return "mxfp8", "k_ggemm_mxfp4<MX8> (GEMM1, e4m3 weights)"
     if cfg.M * cfg.topk >= 2 * 128 * cfg.E:
         return "bf16_2sm", "k_ggemm_bf16_2sm<fused SiLU-and-mul> (GEMM1, SM pairs)"
     return "bf16", "k_ggemm_bf16<fused SiLU-and-mul> (GEMM1)"
@@ -445,7 +449,7 @@ def run_ours(args):
         ratio = 2.0 if q else 1.0
         peak = peaks["bf16_tflops_sustained"] * ratio
         ach = gemm1_flops / (stage_ms[g1] * 1e-3) / 1e12
-        wbytes = {"bf16": 2.0, "fp8": 1.0, "mxfp4": 0.5}[cfg.quant]
+        wbytes = {"bf16": 2.0, "fp8": 1.0, "mxfp4": 0.5, "mxfp8": 1.0}[cfg.quant]
         w13_bytes = cfg.E * 2 * cfg.I * cfg.H * wbytes
         w2_bytes = cfg.E * cfg.H * cfg.I * wbytes
         out = {
@@ -453,7 +457,7 @@ def run_ours(args):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": {"bf16": "bf16", "fp8": "e4m3 (fp32 accumulate)",
-                      "mxfp4": "e2m1 x e4m3"}[cfg.quant],
+                      "mxfp4": "e2m1 x e4m3", "mxfp8": "e4m3 x e4m3 (E8M0 / 32)"}[cfg.quant],
             "data": "synthetic (seeded; random-init weights)",
             "config": _config_dict(cfg, world),
             "tflops": (gemm1_flops + gemm2_flops) / (ms * 1e-3) / 1e12,
@@ -628,7 +632,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=WORKLOAD,
-                    choices=["mixtral", "decode", "dsfp8", "mxfp4", "tiny", "decode_batched"])
+                    choices=["mixtral", "decode", "dsfp8", "mxfp4", "mxfp8", "tiny",
+                             "decode_batched"])
     ap.add_argument("--tokens", type=int, default=0,
                     help="override M (smaller cases for profiling captures)")
     ap.add_argument("--experts", type=int, default=0,

@@ -62,8 +62,19 @@ typedef enum {
  *  MOE_Q_MXFP4_W4A8:    w13/w2 E2M1 codes packed two per byte ([E, N, K/2],
  *                       low nibble = even k) with E8M0 scales per 32 along K
  *                       ([E, N, K/32] uint8); activations e4m3fn per 1x128.
+ *  MOE_Q_MXFP8_1X32:    w13/w2 e4m3fn codes ([E, N, K] uint8) with E8M0
+ *                       scales per 1x32 along K ([E, N, K/32] uint8);
+ *                       activations e4m3fn per 1x32 group with UE8M0 scales
+ *                       (act_scale_fmt must be MOE_SCALE_UE8M0), stored as
+ *                       fp32 powers of two [S, K/32] (MXFP8 1x32 row of the
+ *                       same table).
  */
-typedef enum { MOE_Q_BF16 = 0, MOE_Q_FP8_BLOCK128 = 1, MOE_Q_MXFP4_W4A8 = 2 } moe_quant;
+typedef enum {
+  MOE_Q_BF16 = 0,
+  MOE_Q_FP8_BLOCK128 = 1,
+  MOE_Q_MXFP4_W4A8 = 2,
+  MOE_Q_MXFP8_1X32 = 3
+} moe_quant;
 
 /* Activation scale format of the quantised modes: fp32 amax/448, or that
  * value rounded up to a power of two (UE8M0; page "Blackwell 上的 DeepGEMM
@@ -245,7 +256,8 @@ moe_status moe_align_permute_noalloc(const moe_problem* p, const void* x,
 /* Stage 2: grouped GEMM1, H1[row, n] = sum_k x_perm[row, k] * w13[e, n, k] for
  * every used block (page "fused_moe.py 分析", §1.3 routed GEMM and
  * "fused_moe_kernel 的核心原理"; FP8 blocks: "FP8 W8A8").  fp32 accumulation.
- *  in : x_perm [S,H] (+ x_scale [S,H/128] fp32 for quantised modes),
+ *  in : x_perm [S,H] (+ x_scale [S,H/128] fp32 for quantised modes; [S,H/32]
+ *       for MOE_Q_MXFP8_1X32),
  *       w13 [E,2I,H] (+ w13_scale), block_expert_ids, num_post_padded (device).
  *  out: fuse_act == 0: h1 [S,2I] bf16.
  *       fuse_act == 1: the gated activation (p->act_recipe) written directly
@@ -262,7 +274,8 @@ moe_status grouped_gemm_w13(const moe_problem* p, const void* x_perm, const floa
  * DeepGEMM FusedMoE（vLLM）", §2.6.4; page "fused_moe.py 分析",
  * _silu_and_mul_kernel).  MOE_Q_BF16: z [S,I] bf16.
  * Quantised modes: z [S,I] e4m3fn codes + z_scale [S,I/128] fp32 (dynamic
- * per 1x128 group).  Only rows below num_post_padded are written. */
+ * per 1x128 group; [S,I/32] per 1x32 for MOE_Q_MXFP8_1X32).  Only rows below
+ * num_post_padded are written. */
 moe_status act_mul_quant(const moe_problem* p, const void* h1, const int32_t* num_post_padded,
                          void* z, float* z_scale, void* stream);
 

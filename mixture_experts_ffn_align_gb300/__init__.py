@@ -18,7 +18,7 @@ from dataclasses import dataclass
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libmoe_ffn.so")
 
-QUANT = {"bf16": 0, "fp8": 1, "mxfp4": 2}
+QUANT = {"bf16": 0, "fp8": 1, "mxfp4": 2, "mxfp8": 3}
 SCALE_FMT = {"fp32": 0, "ue8m0": 1}
 
 STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED", 3: "MOE_ERR_CUDA",
@@ -329,6 +329,7 @@ def stage_buffers(p: Problem, device="cuda"):
     import torch
     cap = moe_m_sum_bound(p)
     q = p.quant != "bf16"
+    g = 32 if p.quant == "mxfp8" else 128      # activation quantisation group
     xb = torch.uint8 if q else torch.bfloat16
     i32 = dict(dtype=torch.int32, device=device)
     return {
@@ -338,11 +339,11 @@ def stage_buffers(p: Problem, device="cuda"):
         "num_post_padded": torch.empty(1, **i32),
         "inv_perm": torch.empty(p.M, p.topk, **i32),
         "x_perm": torch.empty(cap, p.H, dtype=xb, device=device),
-        "x_perm_scale": torch.empty(cap, p.H // 128, dtype=torch.float32, device=device)
+        "x_perm_scale": torch.empty(cap, p.H // g, dtype=torch.float32, device=device)
         if q else None,
         "h1": torch.empty(cap, 2 * p.I, dtype=torch.bfloat16, device=device),
         "z": torch.empty(cap, p.I, dtype=xb, device=device),
-        "z_scale": torch.empty(cap, p.I // 128, dtype=torch.float32, device=device)
+        "z_scale": torch.empty(cap, p.I // g, dtype=torch.float32, device=device)
         if q else None,
         "y2": torch.empty(cap, p.H, dtype=torch.bfloat16, device=device),
         "y": torch.empty(p.M, p.H, dtype=torch.bfloat16, device=device),

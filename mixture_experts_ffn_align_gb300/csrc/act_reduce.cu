@@ -62,8 +62,10 @@ __global__ void __launch_bounds__(ACT_THREADS)
   }
 }
 
-// Quantised variant: z in fp32, then per 1x128 group (one half-warp) amax ->
-// scale -> e4m3 with one reciprocal per group.
+// Quantised variant: z in fp32, then per group of LPG lanes x 8 values
+// (16 lanes: 1x128; 4 lanes: the 1x32 groups of MXFP8) amax -> scale -> e4m3
+// with one reciprocal per group.
+template <int LPG>
 __global__ void __launch_bounds__(ACT_THREADS)
     k_act_mul_fp8(const __nv_bfloat16* __restrict__ h1, int I, const int32_t* __restrict__ npp,
                   uint8_t* __restrict__ zq, float* __restrict__ zs, int ue8m0,
@@ -71,12 +73,12 @@ __global__ void __launch_bounds__(ACT_THREADS)
   const int lane = threadIdx.x & 31;
   const int wpc = blockDim.x >> 5;
   const int rows = *npp;
-  const int nv = I / 8;   // multiple of 16: a half-warp is one 1x128 group
+  const int nv = I / 8;   // a multiple of LPG: groups never straddle rows
   for (int row = blockIdx.x * wpc + (threadIdx.x >> 5); row < rows; row += gridDim.x * wpc) {
     const uint4* g4 = reinterpret_cast<const uint4*>(h1 + (size_t)row * 2 * I);
     const uint4* u4 = reinterpret_cast<const uint4*>(h1 + (size_t)row * 2 * I + I);
     uint2* q2 = reinterpret_cast<uint2*>(zq + (size_t)row * I);
-    float* srow = zs + (size_t)row * (I / 128);
+    float* srow = zs + (size_t)row * (nv / LPG);
     for (int base = 0; base < nv; base += 32 * ACT_U) {
       uint4 gv[ACT_U], uv[ACT_U];
 #pragma unroll
@@ -103,7 +105,7 @@ __global__ void __launch_bounds__(ACT_THREADS)
           }
         }
 #pragma unroll
-        for (int o = 8; o >= 1; o >>= 1)
+        for (int o = LPG / 2; o >= 1; o >>= 1)
           amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
         if (act) {
           const float s = act_scale(amax, ue8m0 != 0);
@@ -116,7 +118,7 @@ __global__ void __launch_bounds__(ACT_THREADS)
           for (int j = 0; j < 4; ++j)
             hi |= (uint32_t)f32_to_e4m3(div_rn_shared(f[4 + j], s, r)) << (8 * j);
           q2[v] = make_uint2(lo, hi);
-          if ((v & 15) == 0) srow[v >> 4] = s;
+          if (v % LPG == 0) srow[v / LPG] = s;
         }
       }
     }
@@ -124,8 +126,8 @@ __global__ void __launch_bounds__(ACT_THREADS)
 }
 
 cudaError_t launch_act_mul(const void* h1, int I, const int32_t* num_post_padded, void* z,
-                           float* z_scale, bool ue8m0, int cap, const Epilogue& act,
-                           cudaStream_t stream) {
+                           float* z_scale, bool ue8m0, int group, int cap,
+                           const Epilogue& act, cudaStream_t stream) {
   if (cap <= 0) return cudaSuccess;
   const int wpc = ACT_THREADS / 32;
   const int grid = min((cap + wpc - 1) / wpc, num_sms() * 8);
@@ -134,9 +136,14 @@ cudaError_t launch_act_mul(const void* h1, int I, const int32_t* num_post_padded
                                                      num_post_padded,
                                                      static_cast<__nv_bfloat16*>(z), act);
   } else {
-    k_act_mul_fp8<<<grid, ACT_THREADS, 0, stream>>>(static_cast<const __nv_bfloat16*>(h1), I,
-                                                    num_post_padded, static_cast<uint8_t*>(z),
-                                                    z_scale, ue8m0, act);
+    if (group == 32)
+      k_act_mul_fp8<4><<<grid, ACT_THREADS, 0, stream>>>(
+          static_cast<const __nv_bfloat16*>(h1), I, num_post_padded, static_cast<uint8_t*>(z),
+          z_scale, ue8m0, act);
+    else
+      k_act_mul_fp8<16><<<grid, ACT_THREADS, 0, stream>>>(
+          static_cast<const __nv_bfloat16*>(h1), I, num_post_padded, static_cast<uint8_t*>(z),
+          z_scale, ue8m0, act);
   }
   return cudaGetLastError();
 }

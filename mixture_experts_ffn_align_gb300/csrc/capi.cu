@@ -80,7 +80,7 @@ bool valid_problem(const moe_problem* p) {
   if (p->block_size != 16 && p->block_size != 32 && p->block_size != 64 &&
       p->block_size != 128)
     return false;
-  if (p->quant < MOE_Q_BF16 || p->quant > MOE_Q_MXFP4_W4A8) return false;
+  if (p->quant < MOE_Q_BF16 || p->quant > MOE_Q_MXFP8_1X32) return false;
   if (p->act_scale_fmt != MOE_SCALE_FP32 && p->act_scale_fmt != MOE_SCALE_UE8M0) return false;
   if (p->apply_router_weight_on_input && p->topk != 1) return false;
   if (p->router_weight_in_gemm2 != 0 && p->router_weight_in_gemm2 != 1) return false;
@@ -111,6 +111,12 @@ Epilogue make_epilogue(const moe_problem* p, const void* bias, int n_bias,
 }
 
 bool quantised(const moe_problem* p) { return p->quant != MOE_Q_BF16; }
+// Activation quantisation group along K: 32 for MXFP8 (1x32), else 128.
+int act_group(const moe_problem* p) { return p->quant == MOE_Q_MXFP8_1X32 ? 32 : 128; }
+// The block-scaled (E8M0 per 32) GEMM serves MXFP4 and MXFP8 weights.
+bool block_scaled(const moe_problem* p) {
+  return p->quant == MOE_Q_MXFP4_W4A8 || p->quant == MOE_Q_MXFP8_1X32;
+}
 
 size_t cap_rows(const moe_problem* p) {
   const size_t R = (size_t)p->M * p->topk;
@@ -144,10 +150,10 @@ Layout layout(const moe_problem* p) {
   // x_perm is dead once GEMM1 has run, so GEMM2's output reuses its storage
   L.xperm = take(std::max(cap * H * xb, cap * H * 2));
   L.y2 = L.xperm;
-  L.xscale = quantised(p) ? take(cap * (H / 128) * 4) : 0;
+  L.xscale = quantised(p) ? take(cap * (H / act_group(p)) * 4) : 0;
   L.h1 = quantised(p) ? take(cap * 2 * I * 2) : 0;
   L.z = take(cap * I * (quantised(p) ? 1 : 2));
-  L.zscale = quantised(p) ? take(cap * (I / 128) * 4) : 0;
+  L.zscale = quantised(p) ? take(cap * (I / act_group(p)) * 4) : 0;
   L.total = o;
   return L;
 }
@@ -158,8 +164,7 @@ bool valid_batched(const moe_problem* p, int max_tokens) {
   if (p == nullptr || p->E < 1 || p->E > MOE_MAX_EXPERTS || p->H <= 0 || p->I <= 0 ||
       p->block_size != 128 || max_tokens <= 0 || max_tokens % 128 != 0)
     return false;
-  if (p->quant != MOE_Q_BF16 && p->quant != MOE_Q_FP8_BLOCK128 && p->quant != MOE_Q_MXFP4_W4A8)
-    return false;
+  if (p->quant < MOE_Q_BF16 || p->quant > MOE_Q_MXFP8_1X32) return false;
   if (p->act_scale_fmt != MOE_SCALE_FP32 && p->act_scale_fmt != MOE_SCALE_UE8M0) return false;
   if (p->H % 128 != 0 || p->I % 128 != 0) return false;
   return (int64_t)p->E * max_tokens <= (int64_t)MOE_MAX_TOKENS * MOE_MAX_TOPK;
@@ -183,10 +188,10 @@ BatchedLayout batched_layout(const moe_problem* p, int max_tokens) {
   L.npp = take(4);
   L.sorted = q ? take(rows * 4) : 0;
   L.xq = q ? take(rows * H) : 0;
-  L.xscale = q ? take(rows * (H / 128) * 4) : 0;
+  L.xscale = q ? take(rows * (H / act_group(p)) * 4) : 0;
   L.h1 = q ? take(rows * 2 * I * 2) : 0;
   L.z = take(rows * I * (q ? 1 : 2));
-  L.zscale = q ? take(rows * (I / 128) * 4) : 0;
+  L.zscale = q ? take(rows * (I / act_group(p)) * 4) : 0;
   L.total = o;
   return L;
 }
@@ -207,7 +212,7 @@ moe_status cuda_status(cudaError_t e) {
 bool gemm_supported(const moe_problem* p) {
   if (p->block_size != 128) return false;
   if (p->quant == MOE_Q_BF16) return p->H % 256 == 0;
-  if (p->quant == MOE_Q_MXFP4_W4A8) return p->act_scale_fmt == MOE_SCALE_UE8M0;
+  if (block_scaled(p)) return p->act_scale_fmt == MOE_SCALE_UE8M0;
   return p->quant == MOE_Q_FP8_BLOCK128;
 }
 
@@ -258,7 +263,7 @@ moe_status moe_align_permute(const moe_problem* p, const void* x, const int32_t*
     e = launch_permute_rows(x, p->H, p->topk, R, sorted_ids, num_post_padded,
                             p->apply_router_weight_on_input ? topk_weights : nullptr, x_perm,
                             quantised(p) ? x_perm_scale : nullptr,
-                            p->act_scale_fmt == MOE_SCALE_UE8M0, cap, s);
+                            p->act_scale_fmt == MOE_SCALE_UE8M0, act_group(p), cap, s);
   }
   return cuda_status(e);
 }
@@ -304,11 +309,12 @@ moe_status grouped_gemm_w13_ex(const moe_problem* p, const void* x_perm, const f
   }
   if (fuse_act) return MOE_ERR_UNSUPPORTED;
   if (!x_scale || !w13_scale) return MOE_ERR_INVALID_ARG;
-  if (p->quant == MOE_Q_MXFP4_W4A8)
+  if (block_scaled(p))
     return cuda_status(launch_ggemm_mxfp4(x_perm, x_scale, cap, p->H, w13,
                                           static_cast<const uint8_t*>(w13_scale),
                                           p->E * 2 * p->I, 2 * p->I, 2 * p->I, block_expert_ids,
-                                          num_post_padded, out, ep, s));
+                                          num_post_padded, out,
+                                          p->quant == MOE_Q_MXFP8_1X32, ep, s));
   return cuda_status(launch_ggemm_fp8(x_perm, x_scale, cap, p->H, w13,
                                       static_cast<const float*>(w13_scale), p->E * 2 * p->I,
                                       2 * p->I, 2 * p->I, block_expert_ids, num_post_padded, out,
@@ -331,7 +337,8 @@ moe_status act_mul_quant(const moe_problem* p, const void* h1, const int32_t* nu
   if (quantised(p) && !z_scale) return MOE_ERR_INVALID_ARG;
   return cuda_status(launch_act_mul(h1, p->I, num_post_padded, z,
                                     quantised(p) ? z_scale : nullptr,
-                                    p->act_scale_fmt == MOE_SCALE_UE8M0, (int)cap_rows(p),
+                                    p->act_scale_fmt == MOE_SCALE_UE8M0, act_group(p),
+                                    (int)cap_rows(p),
                                     make_epilogue(p, nullptr, 0, nullptr, nullptr),
                                     static_cast<cudaStream_t>(stream)));
 }
@@ -357,11 +364,11 @@ moe_status grouped_gemm_w2_ex(const moe_problem* p, const void* z, const float* 
                                         num_post_padded, y2, false, ep, s));
   }
   if (!z_scale || !w2_scale) return MOE_ERR_INVALID_ARG;
-  if (p->quant == MOE_Q_MXFP4_W4A8)
+  if (block_scaled(p))
     return cuda_status(launch_ggemm_mxfp4(z, z_scale, cap, p->I, w2,
                                           static_cast<const uint8_t*>(w2_scale), p->E * p->H,
-                                          p->H, p->H, block_expert_ids, num_post_padded, y2, ep,
-                                          s));
+                                          p->H, p->H, block_expert_ids, num_post_padded, y2,
+                                          p->quant == MOE_Q_MXFP8_1X32, ep, s));
   return cuda_status(launch_ggemm_fp8(z, z_scale, cap, p->I, w2,
                                       static_cast<const float*>(w2_scale), p->E * p->H, p->H,
                                       p->H, block_expert_ids, num_post_padded, y2, ep, s));
@@ -537,20 +544,22 @@ moe_status fused_experts_batched(const moe_problem* p, const void* x,
     return cuda_status(e);
   }
   // quantised: per-row dynamic quantisation of the layout, then the same stages
-  e = launch_permute_rows(x, H, 1, rows, sorted, npp, nullptr, ws + L.xq, xscale, ue8m0, rows, s);
+  e = launch_permute_rows(x, H, 1, rows, sorted, npp, nullptr, ws + L.xq, xscale, ue8m0,
+                          act_group(p), rows, s);
   if (e != cudaSuccess) return cuda_status(e);
-  if (p->quant == MOE_Q_MXFP4_W4A8)
+  if (block_scaled(p))
     e = launch_ggemm_mxfp4(ws + L.xq, xscale, rows, H, w13, static_cast<const uint8_t*>(w13_scale),
-                           E * 2 * I, 2 * I, 2 * I, blocks, npp, ws + L.h1, ep, s);
+                           E * 2 * I, 2 * I, 2 * I, blocks, npp, ws + L.h1,
+                           p->quant == MOE_Q_MXFP8_1X32, ep, s);
   else
     e = launch_ggemm_fp8(ws + L.xq, xscale, rows, H, w13, static_cast<const float*>(w13_scale),
                          E * 2 * I, 2 * I, 2 * I, blocks, npp, ws + L.h1, ep, s);
   if (e != cudaSuccess) return cuda_status(e);
-  e = launch_act_mul(ws + L.h1, I, npp, ws + L.z, zscale, ue8m0, rows, ep, s);
+  e = launch_act_mul(ws + L.h1, I, npp, ws + L.z, zscale, ue8m0, act_group(p), rows, ep, s);
   if (e != cudaSuccess) return cuda_status(e);
-  if (p->quant == MOE_Q_MXFP4_W4A8)
+  if (block_scaled(p))
     e = launch_ggemm_mxfp4(ws + L.z, zscale, rows, I, w2, static_cast<const uint8_t*>(w2_scale),
-                           E * H, H, H, blocks, npp, y, ep, s);
+                           E * H, H, H, blocks, npp, y, p->quant == MOE_Q_MXFP8_1X32, ep, s);
   else
     e = launch_ggemm_fp8(ws + L.z, zscale, rows, I, w2, static_cast<const float*>(w2_scale),
                          E * H, H, H, blocks, npp, y, ep, s);

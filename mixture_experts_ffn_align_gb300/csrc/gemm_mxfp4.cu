@@ -1,4 +1,12 @@
-// MXFP4 x FP8 (W4A8) grouped GEMM (stages 2 and 4 of MOE_Q_MXFP4_W4A8).
+// Block-scaled (E8M0 per 32) grouped GEMM: MXFP4 x FP8 (W4A8, stages 2 and 4 of
+// MOE_Q_MXFP4_W4A8) and MXFP8 x MXFP8 (MOE_Q_MXFP8_1X32: e4m3 weights with an
+// E8M0 scale per 1x32, activations e4m3 with a UE8M0 scale per 1x32 -- page
+// "Blackwell 上的 DeepGEMM FusedMoE（vLLM）", TL;DR table, MXFP8 (1x32) row and
+// §2.9: the same GEMM with recipe (1, 32)).  The MXFP8 form (template MX8)
+// loads the weights with the ordinary byte tensor map (one e4m3 per byte, the
+// same smem footprint as the padded E2M1 tile), tells the MMA that B is e4m3,
+// and builds each activation scale word from four 1x32 exponents instead of
+// one 1x128 exponent repeated.
 //
 // What it computes: page "Blackwell 上的 DeepGEMM FusedMoE（vLLM）", TL;DR table,
 // W4A8 MXFP4 row: weights E2M1 with one E8M0 scale per 32 along K, activations
@@ -113,7 +121,52 @@ struct Mx4Args {
   Epilogue ep;              // bias, router weight
 };
 
-template <bool STAGED>
+// Activation scales of 4 K blocks for this lane's rows (lane + 32 c):
+// W4A8: one fp32 per K block (a 1x128 group covers the 4 chunks of 32);
+// MXFP8: four fp32 per K block (one per 1x32 chunk).
+template <bool MX8>
+struct AGroup {
+  float4 v[4][MX8 ? 4 : 1];
+};
+// Loads the scales of K blocks g .. g+3 (those past num_kb read as 2^0).
+template <bool MX8>
+__device__ __forceinline__ void load_ascales(AGroup<MX8>& A, const float* a_scale, size_t row0,
+                                             int num_kb, int g) {
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    const size_t row = row0 + 32 * c;
+    if constexpr (MX8) {
+      const float* pa = a_scale + row * (size_t)(4 * num_kb);
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        A.v[c][j] = g + j < num_kb ? __ldg(reinterpret_cast<const float4*>(pa + 4 * (g + j)))
+                                   : make_float4(1.0f, 1.0f, 1.0f, 1.0f);
+    } else {
+      const float* pa = a_scale + row * (size_t)num_kb + g;
+      const int n = num_kb - g;
+      if ((num_kb & 3) == 0)
+        A.v[c][0] = __ldg(reinterpret_cast<const float4*>(pa));
+      else
+        A.v[c][0] = make_float4(__ldg(pa), n > 1 ? __ldg(pa + 1) : 1.0f,
+                                n > 2 ? __ldg(pa + 2) : 1.0f, n > 3 ? __ldg(pa + 3) : 1.0f);
+    }
+  }
+}
+// a power-of-two fp32 scale 2^(x-127) has biased exponent x = its E8M0 code
+__device__ __forceinline__ uint32_t e8m0_of(float s) { return (__float_as_uint(s) >> 23) & 0xFFu; }
+// The scale word of row c for K block j of the group: byte q for chunk q.
+template <bool MX8>
+__device__ __forceinline__ uint32_t a_word(const AGroup<MX8>& A, int c, int j) {
+  if constexpr (MX8) {
+    const float4 f = A.v[c][j];
+    return e8m0_of(f.x) | e8m0_of(f.y) << 8 | e8m0_of(f.z) << 16 | e8m0_of(f.w) << 24;
+  } else {
+    const float4 f = A.v[c][0];
+    return e8m0_of(j == 0 ? f.x : j == 1 ? f.y : j == 2 ? f.z : f.w) * 0x01010101u;
+  }
+}
+
+template <bool STAGED, bool MX8>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     k_ggemm_mxfp4(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                   const __grid_constant__ CUtensorMap tmS, const Mx4Args args) {
@@ -205,7 +258,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           skip_first = false;
         } else {
           const uint32_t sa = smem_base + stage * STAGE_BYTES;
-          mbar_arrive_expect_tx(full_bar(stage), TX_BYTES);
+          mbar_arrive_expect_tx(full_bar(stage), MX8 ? A_BYTES + B_BYTES : TX_BYTES);
           tma_load_2d(sa, &tmA, full_bar(stage), kb * BK, m_blk * BM, pol_a);
           tma_load_2d(sa + A_BYTES, &tmB, full_bar(stage), kb * BK, brow, pol_b);
           tma_load_2d(sa + A_BYTES + B_BYTES / 2, &tmB, full_bar(stage), kb * BK, brow + 128,
@@ -281,11 +334,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         tma_load_2d(stg_base + slot * STG_BYTES, &tmS, stg_full(slot), 16 * c.g,
                     c.e * N + c.n_tile * BN, pol_s);
       };
-      auto load_a = [&](const Cursor& c, float4 (&A)[4]) {
-        const float* pa = args.a_scale + ((size_t)c.m_blk * BM + lane) * args.num_kb + 4 * c.g;
-#pragma unroll
-        for (int i = 0; i < 4; ++i)
-          A[i] = __ldg(reinterpret_cast<const float4*>(pa + (size_t)32 * i * args.num_kb));
+      auto load_a = [&](const Cursor& c, AGroup<MX8>& A) {
+        load_ascales<MX8>(A, args.a_scale, (size_t)c.m_blk * BM + lane, args.num_kb, 4 * c.g);
       };
       Cursor fill{(int)blockIdx.x, 0, 0, 0, 0};
       bool fill_ok = seek(fill);
@@ -296,7 +346,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         if (lane == 0) stage_group(fill, nfill);
         fill_ok = step(fill);
       }
-      float4 a_cur[4], a_nxt[4];
+      AGroup<MX8> a_cur, a_nxt;
       if (use_ok) {
         load_a(use, a_cur);
         anext_ok = step(anext);
@@ -317,12 +367,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         for (int j = 0; j < 4; ++j) {
           uint32_t aw[4], bw[8];
 #pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            const float av = j == 0 ? a_cur[c].x : j == 1 ? a_cur[c].y : j == 2 ? a_cur[c].z
-                                                                                : a_cur[c].w;
-            // a power-of-two fp32 scale 2^(x-127) has biased exponent x = its E8M0 code
-            aw[c] = ((__float_as_uint(av) >> 23) & 0xFFu) * 0x01010101u;
-          }
+          for (int c = 0; c < 4; ++c) aw[c] = a_word<MX8>(a_cur, c, j);
 #pragma unroll
           for (int c = 0; c < 8; ++c)   // rows past N (ragged last tile): 2^0
             bw[c] = n0 + 32 * c < N ? ld_shared_u32(stg + 16 * (lane + 32 * c) + 4 * j)
@@ -343,8 +388,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           fill_ok = step(fill);
         }
         use_ok = step(use);
-#pragma unroll
-        for (int c = 0; c < 4; ++c) a_cur[c] = a_nxt[c];
+        a_cur = a_nxt;
         if (anext_ok) {
           anext_ok = step(anext);
           if (anext_ok) load_a(anext, a_nxt);
@@ -365,24 +409,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         if (e < 0 || e >= args.num_experts) continue;
         // lane l builds rows l + 32 c of A (c < 4) and of B (c < 8); B rows
         // past N (ragged last tile) read nothing
-        const float* sa_base = args.a_scale + ((size_t)m_blk * BM + lane) * args.num_kb;
-        const size_t sa_step = (size_t)32 * args.num_kb;             // floats per 32 rows
         const uint8_t* sb_base = args.b_scale + ((size_t)e * N + (size_t)n_tile * BN + lane) * kq;
         const size_t sb_step = (size_t)32 * kq;                      // bytes per 32 rows
         const int n_valid = N - n_tile * BN - lane;                  // B row c valid if 32c < this
         // scales of 4 K blocks per load, one group of 4 in flight ahead
-        auto load_group = [&](int g, float4 (&A)[4], uint4 (&B)[8]) {
+        // (MXFP8 loads its 4x larger activation scales at the group's start
+        // instead: two groups of them in registers would spill)
+        auto load_group = [&](int g, AGroup<MX8>& A, uint4 (&B)[8]) {
           const int n = args.num_kb - g;
-  #pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            const float* pa = sa_base + c * sa_step + g;
-            if (vec) {
-              A[c] = __ldg(reinterpret_cast<const float4*>(pa));
-            } else {
-              A[c] = make_float4(__ldg(pa), n > 1 ? __ldg(pa + 1) : 1.0f,
-                                 n > 2 ? __ldg(pa + 2) : 1.0f, n > 3 ? __ldg(pa + 3) : 1.0f);
-            }
-          }
+          if constexpr (!MX8)
+            load_ascales<MX8>(A, args.a_scale, (size_t)m_blk * BM + lane, args.num_kb, g);
   #pragma unroll
           for (int c = 0; c < 8; ++c) {
             const uint32_t* pb = reinterpret_cast<const uint32_t*>(sb_base + c * sb_step) + g;
@@ -396,23 +432,20 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             }
           }
         };
-        float4 a_cur[4], a_nxt[4];
+        AGroup<MX8> a_cur, a_nxt;
         uint4 b_cur[8], b_nxt[8];
         load_group(0, a_cur, b_cur);
         if (args.num_kb > 4) load_group(4, a_nxt, b_nxt);
         for (int kb0 = 0; kb0 < args.num_kb && ok; kb0 += 4) {
+          if constexpr (MX8)
+            load_ascales<MX8>(a_cur, args.a_scale, (size_t)m_blk * BM + lane, args.num_kb, kb0);
   #pragma unroll
           for (int j = 0; j < 4; ++j) {
             const int kb = kb0 + j;
             if (kb >= args.num_kb) break;
             uint32_t aw[4], bw[8];
   #pragma unroll
-            for (int c = 0; c < 4; ++c) {
-              const float av = j == 0 ? a_cur[c].x : j == 1 ? a_cur[c].y : j == 2 ? a_cur[c].z
-                                                                                  : a_cur[c].w;
-              // a power-of-two fp32 scale 2^(x-127) has biased exponent x = its E8M0 code
-              aw[c] = ((__float_as_uint(av) >> 23) & 0xFFu) * 0x01010101u;
-            }
+            for (int c = 0; c < 4; ++c) aw[c] = a_word<MX8>(a_cur, c, j);
   #pragma unroll
             for (int c = 0; c < 8; ++c)
               bw[c] = j == 0 ? b_cur[c].x : j == 1 ? b_cur[c].y : j == 2 ? b_cur[c].z : b_cur[c].w;
@@ -421,8 +454,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
               break;
             }
           }
-  #pragma unroll
-          for (int c = 0; c < 4; ++c) a_cur[c] = a_nxt[c];
+          if constexpr (!MX8) a_cur = a_nxt;
   #pragma unroll
           for (int c = 0; c < 8; ++c) b_cur[c] = b_nxt[c];
           if (kb0 + 8 < args.num_kb) load_group(kb0 + 8, a_nxt, b_nxt);
@@ -460,7 +492,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
         for (int j = 0; j < BK / 32; ++j) {
           umma_mxf8f6f4(tmem_base, adesc + 2 * j, bdesc + 2 * j,
-                        make_idesc_block_scaled(kFmtE4M3, kFmtE2M1, BM, BN, j), sfa,
+                        make_idesc_block_scaled(kFmtE4M3, MX8 ? kFmtE4M3 : kFmtE2M1, BM, BN, j),
+                        sfa,
                         sfa + SF_SLOT, (kb | j) != 0);
         }
         tc_commit(empty_bar(stage));
@@ -545,17 +578,34 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
 }  // namespace
 
+namespace {
+template <bool STAGED, bool MX8>
+void launch_form(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmS,
+                 const Mx4Args& a, cudaStream_t stream) {
+  static bool attr_done = false;
+  if (!attr_done) {
+    cudaFuncSetAttribute(k_ggemm_mxfp4<STAGED, MX8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         SMEM_BYTES);
+    attr_done = true;
+  }
+  k_ggemm_mxfp4<STAGED, MX8><<<num_sms(), NUM_THREADS, SMEM_BYTES, stream>>>(tmA, tmB, tmS, a);
+}
+}  // namespace
+
 cudaError_t launch_ggemm_mxfp4(const void* A, const float* a_scale, int cap, int K, const void* B,
                                const uint8_t* b_scale, int b_rows_total, int b_rows_per_expert,
                                int n_out, const int32_t* block_expert_ids,
-                               const int32_t* num_post_padded, void* out, const Epilogue& ep,
-                               cudaStream_t stream) {
+                               const int32_t* num_post_padded, void* out, bool b_e4m3,
+                               const Epilogue& ep, cudaStream_t stream) {
   if (cap <= 0) return cudaSuccess;
-  if ((reinterpret_cast<uintptr_t>(B) & 31u) != 0 || (reinterpret_cast<uintptr_t>(b_scale) & 3u))
+  // packed E2M1 tensor maps want 32-byte aligned bases, byte maps 16
+  if ((reinterpret_cast<uintptr_t>(B) & (b_e4m3 ? 15u : 31u)) != 0 ||
+      (reinterpret_cast<uintptr_t>(b_scale) & 3u))
     return cudaErrorInvalidValue;
   CUtensorMap tmA, tmB;
   if (!make_tmap_k_sw128(&tmA, A, (uint64_t)cap, (uint64_t)K, 1, 128) ||
-      !make_tmap_fp4_k_sw128(&tmB, B, (uint64_t)b_rows_total, (uint64_t)K, 128))
+      !(b_e4m3 ? make_tmap_k_sw128(&tmB, B, (uint64_t)b_rows_total, (uint64_t)K, 1, 128)
+               : make_tmap_fp4_k_sw128(&tmB, B, (uint64_t)b_rows_total, (uint64_t)K, 128)))
     return cudaErrorInvalidValue;
   Mx4Args a;
   a.ep = ep;
@@ -579,18 +629,12 @@ cudaError_t launch_ggemm_mxfp4(const void* A, const float* a_scale, int cap, int
   if (staged && !make_tmap_u8_rows(&tmS, b_scale, (uint64_t)b_rows_total, (uint64_t)(K / 32), 16,
                                    BN))
     return cudaErrorInvalidValue;
-  static bool attr_done = false;
-  if (!attr_done) {
-    cudaFuncSetAttribute(k_ggemm_mxfp4<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                         SMEM_BYTES);
-    cudaFuncSetAttribute(k_ggemm_mxfp4<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                         SMEM_BYTES);
-    attr_done = true;
-  }
   if (staged)
-    k_ggemm_mxfp4<true><<<num_sms(), NUM_THREADS, SMEM_BYTES, stream>>>(tmA, tmB, tmS, a);
+    b_e4m3 ? launch_form<true, true>(tmA, tmB, tmS, a, stream)
+           : launch_form<true, false>(tmA, tmB, tmS, a, stream);
   else
-    k_ggemm_mxfp4<false><<<num_sms(), NUM_THREADS, SMEM_BYTES, stream>>>(tmA, tmB, tmS, a);
+    b_e4m3 ? launch_form<false, true>(tmA, tmB, tmS, a, stream)
+           : launch_form<false, false>(tmA, tmB, tmS, a, stream);
   return cudaGetLastError();
 }
 

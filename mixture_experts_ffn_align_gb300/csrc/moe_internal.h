@@ -28,15 +28,16 @@ cudaError_t launch_route(const int32_t* topk_ids, int R, int E, int block_size, 
 
 // Data half: gather x rows into the padded layout (bf16 copy, or fused
 // dynamic 1x128 e4m3 quantisation when x_scale != nullptr).
+// group: the quantisation group along H (128, or 32 for MXFP8).
 cudaError_t launch_permute_rows(const void* x, int H, int topk, int R, const int32_t* sorted_ids,
                                 const int32_t* num_post_padded, const float* row_weights,
-                                void* x_perm, float* x_scale, bool ue8m0, int cap,
+                                void* x_perm, float* x_scale, bool ue8m0, int group, int cap,
                                 cudaStream_t stream);
 
 // SiLU-and-mul over h1 [rows, 2I] bf16 -> z bf16, or e4m3 + scales.
 // act: the gated activation recipe (recipe / alpha / beta / limit fields).
 cudaError_t launch_act_mul(const void* h1, int I, const int32_t* num_post_padded, void* z,
-                           float* z_scale, bool ue8m0, int cap, const Epilogue& act,
+                           float* z_scale, bool ue8m0, int group, int cap, const Epilogue& act,
                            cudaStream_t stream);
 
 // Weighted top-k gather-reduce into y [M, H] bf16.
@@ -82,7 +83,7 @@ cudaError_t launch_ggemm_fp8(const void* A, const float* a_scale, int cap, int K
 cudaError_t launch_ggemm_mxfp4(const void* A, const float* a_scale, int cap, int K, const void* B,
                                const uint8_t* b_scale, int b_rows_total, int b_rows_per_expert,
                                int n_out, const int32_t* block_expert_ids,
-                               const int32_t* num_post_padded, void* out, const Epilogue& ep,
-                               cudaStream_t stream);
+                               const int32_t* num_post_padded, void* out, bool b_e4m3,
+                               const Epilogue& ep, cudaStream_t stream);
 
 }  // namespace moe

@@ -210,9 +210,11 @@ __global__ void __launch_bounds__(PERMUTE_THREADS)
   }
 }
 
-// FP8 variant: each half-warp (16 lanes x 8 values) is one 1x128 group; the
-// lanes of a group share one scale, so the quotient uses one reciprocal and
-// a correction step instead of a division per value.
+// FP8 variant: LPG lanes x 8 values form one quantisation group (16 lanes:
+// a 1x128 group; 4 lanes: the 1x32 groups of MXFP8); the lanes of a group
+// share one scale, so the quotient uses one reciprocal and a correction step
+// instead of a division per value.
+template <int LPG>
 __global__ void __launch_bounds__(PERMUTE_THREADS)
     k_permute_fp8(const __nv_bfloat16* __restrict__ x, int H, int topk, int R,
                   const int32_t* __restrict__ sorted_ids, const int32_t* __restrict__ npp,
@@ -221,15 +223,15 @@ __global__ void __launch_bounds__(PERMUTE_THREADS)
   const int lane = threadIdx.x & 31;
   const int wpc = blockDim.x >> 5;
   const int rows = *npp;
-  const int nv = H / 8;          // 8-element vectors per row; a multiple of 16
+  const int nv = H / 8;          // 8-element vectors per row; a multiple of LPG
   for (int row = blockIdx.x * wpc + (threadIdx.x >> 5); row < rows; row += gridDim.x * wpc) {
     const int sid = sorted_ids[row];
     uint2* dst = reinterpret_cast<uint2*>(xq + (size_t)row * H);
-    float* srow = xs + (size_t)row * (H / 128);
+    float* srow = xs + (size_t)row * (nv / LPG);
     if (sid >= R) {
       for (int v = lane; v < nv; v += 32) {
         dst[v] = make_uint2(0, 0);
-        if ((v & 15) == 0) srow[v >> 4] = 0.0f;
+        if (v % LPG == 0) srow[v / LPG] = 0.0f;
       }
       continue;
     }
@@ -245,7 +247,7 @@ __global__ void __launch_bounds__(PERMUTE_THREADS)
 #pragma unroll
       for (int u = 0; u < PERMUTE_U; ++u) {
         const int v = base + 32 * u + lane;
-        // a half-warp is wholly inside or outside the row (nv % 16 == 0), but
+        // a group is wholly inside or outside the row (nv % LPG == 0), but
         // every lane takes part in the shuffles
         const bool act = v < nv;
         float f[8];
@@ -260,7 +262,7 @@ __global__ void __launch_bounds__(PERMUTE_THREADS)
           }
         }
 #pragma unroll
-        for (int o = 8; o >= 1; o >>= 1)
+        for (int o = LPG / 2; o >= 1; o >>= 1)
           amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
         if (act) {
           const float s = act_scale(amax, ue8m0 != 0);
@@ -273,7 +275,7 @@ __global__ void __launch_bounds__(PERMUTE_THREADS)
           for (int j = 0; j < 4; ++j)
             hi |= (uint32_t)f32_to_e4m3(div_rn_shared(f[4 + j], s, r)) << (8 * j);
           dst[v] = make_uint2(lo, hi);
-          if ((v & 15) == 0) srow[v >> 4] = s;
+          if (v % LPG == 0) srow[v / LPG] = s;
         }
       }
     }
@@ -282,7 +284,7 @@ __global__ void __launch_bounds__(PERMUTE_THREADS)
 
 cudaError_t launch_permute_rows(const void* x, int H, int topk, int R, const int32_t* sorted_ids,
                                 const int32_t* num_post_padded, const float* row_weights,
-                                void* x_perm, float* x_scale, bool ue8m0, int cap,
+                                void* x_perm, float* x_scale, bool ue8m0, int group, int cap,
                                 cudaStream_t stream) {
   if (cap <= 0) return cudaSuccess;
   const int wpc = PERMUTE_THREADS / 32;
@@ -292,9 +294,14 @@ cudaError_t launch_permute_rows(const void* x, int H, int topk, int R, const int
         static_cast<const __nv_bfloat16*>(x), H, topk, R, sorted_ids, num_post_padded,
         row_weights, static_cast<__nv_bfloat16*>(x_perm));
   } else {
-    k_permute_fp8<<<grid, PERMUTE_THREADS, 0, stream>>>(
-        static_cast<const __nv_bfloat16*>(x), H, topk, R, sorted_ids, num_post_padded,
-        row_weights, static_cast<uint8_t*>(x_perm), x_scale, ue8m0);
+    if (group == 32)
+      k_permute_fp8<4><<<grid, PERMUTE_THREADS, 0, stream>>>(
+          static_cast<const __nv_bfloat16*>(x), H, topk, R, sorted_ids, num_post_padded,
+          row_weights, static_cast<uint8_t*>(x_perm), x_scale, ue8m0);
+    else
+      k_permute_fp8<16><<<grid, PERMUTE_THREADS, 0, stream>>>(
+          static_cast<const __nv_bfloat16*>(x), H, topk, R, sorted_ids, num_post_padded,
+          row_weights, static_cast<uint8_t*>(x_perm), x_scale, ue8m0);
   }
   return cudaGetLastError();
 }
