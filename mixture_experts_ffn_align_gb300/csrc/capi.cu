@@ -259,7 +259,11 @@ moe_status moe_align_permute(const moe_problem* p, const void* x, const int32_t*
                                static_cast<int32_t*>(workspace), sorted_ids, block_expert_ids,
                                expert_offsets, num_post_padded, inv_perm, s);
   if (e != cudaSuccess) return cuda_status(e);
-  if (x) {
+  if (x && quantised(p) && !p->apply_router_weight_on_input) {
+    e = launch_permute_tokens(x, p->H, p->M, p->topk, R, inv_perm, sorted_ids, num_post_padded,
+                              x_perm, x_perm_scale, p->act_scale_fmt == MOE_SCALE_UE8M0,
+                              act_group(p), cap, s);
+  } else if (x) {
     e = launch_permute_rows(x, p->H, p->topk, R, sorted_ids, num_post_padded,
                             p->apply_router_weight_on_input ? topk_weights : nullptr, x_perm,
                             quantised(p) ? x_perm_scale : nullptr,

@@ -282,6 +282,117 @@ __global__ void __launch_bounds__(PERMUTE_THREADS)
   }
 }
 
+// Token-major FP8 variant for the routed layout: one warp per token reads
+// the row of x once, quantises it once and stores the codes and scales into
+// each of the token's k destination rows (inv_perm); the gather form above
+// reads and quantises each routed copy again (k = 8 on the DeepSeek-class
+// shapes).  Each lane holds 16 consecutive values (two 16-byte loads, one
+// 16-byte store of codes); LPG lanes form one quantisation group (8 lanes:
+// 1x128, 2 lanes: 1x32).  Padding rows (sorted id >= R) below the used row
+// count are zeroed by the same warps afterwards, 32 rows per ballot.
+template <int LPG>
+__global__ void __launch_bounds__(PERMUTE_THREADS)
+    k_permute_fp8_tok(const __nv_bfloat16* __restrict__ x, int H, int M, int topk, int R,
+                      const int32_t* __restrict__ inv_perm,
+                      const int32_t* __restrict__ sorted_ids, const int32_t* __restrict__ npp,
+                      uint8_t* __restrict__ xq, float* __restrict__ xs, int ue8m0) {
+  constexpr int U = 2;           // 16-value chunks per lane in flight
+  const int lane = threadIdx.x & 31;
+  const int gw = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  const int nw = gridDim.x * (blockDim.x >> 5);
+  const int nv = H / 16;         // 16-value chunks per row; a multiple of LPG
+  const int gpr = nv / LPG;      // scale groups per row
+  for (int t = gw; t < M; t += nw) {
+    // lane i < topk holds the destination row of routed item (t, i)
+    const int my_dst = lane < topk ? inv_perm[(size_t)t * topk + lane] : -1;
+    const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)t * H);
+    for (int base = 0; base < nv; base += 32 * U) {
+      uint4 buf[2 * U];
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int v = base + 32 * u + lane;
+        if (v < nv) {
+          buf[2 * u] = __ldg(src + 2 * v);
+          buf[2 * u + 1] = __ldg(src + 2 * v + 1);
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int v = base + 32 * u + lane;
+        const bool act = v < nv;   // groups lie wholly inside or outside the row
+        float f[16];
+        float amax = 0.0f;
+        if (act) {
+          const __nv_bfloat16* b = reinterpret_cast<const __nv_bfloat16*>(&buf[2 * u]);
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            f[j] = __bfloat162float(b[j]);
+            amax = fmaxf(amax, fabsf(f[j]));
+          }
+        }
+#pragma unroll
+        for (int o = LPG / 2; o >= 1; o >>= 1)
+          amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+        const float s = act_scale(amax, ue8m0 != 0);
+        uint4 code = make_uint4(0, 0, 0, 0);
+        if (act) {
+          const float r = __frcp_rn(s);
+          uint32_t w[4];
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            uint32_t word = 0;
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+              word |= (uint32_t)f32_to_e4m3(div_rn_shared(f[4 * q + j], s, r)) << (8 * j);
+            w[q] = word;
+          }
+          code = make_uint4(w[0], w[1], w[2], w[3]);
+        }
+        for (int i = 0; i < topk; ++i) {
+          const int row = __shfl_sync(0xffffffffu, my_dst, i);
+          if (row < 0 || !act) continue;
+          reinterpret_cast<uint4*>(xq + (size_t)row * H)[v] = code;
+          if (lane % LPG == 0) xs[(size_t)row * gpr + v / LPG] = s;
+        }
+      }
+    }
+  }
+  // padding rows of the used blocks: codes and scales zero
+  const int rows = *npp;
+  for (int c = gw; c * 32 < rows; c += nw) {
+    const int row = c * 32 + lane;
+    const bool pad = row < rows && sorted_ids[row] >= R;
+    unsigned m = __ballot_sync(0xffffffffu, pad);
+    while (m) {
+      const int j = __ffs(m) - 1;
+      m &= m - 1;
+      const size_t prow = (size_t)c * 32 + j;
+      uint4* dst = reinterpret_cast<uint4*>(xq + prow * H);
+      for (int v = lane; v < nv; v += 32) dst[v] = make_uint4(0, 0, 0, 0);
+      for (int g = lane; g < gpr; g += 32) xs[prow * gpr + g] = 0.0f;
+    }
+  }
+}
+
+cudaError_t launch_permute_tokens(const void* x, int H, int M, int topk, int R,
+                                  const int32_t* inv_perm, const int32_t* sorted_ids,
+                                  const int32_t* num_post_padded, void* x_perm, float* x_scale,
+                                  bool ue8m0, int group, int cap, cudaStream_t stream) {
+  const int wpc = PERMUTE_THREADS / 32;
+  const int work = max(M, (cap + 31) / 32);
+  if (work <= 0) return cudaSuccess;
+  const int grid = min((work + wpc - 1) / wpc, num_sms() * 8);
+  if (group == 32)
+    k_permute_fp8_tok<2><<<grid, PERMUTE_THREADS, 0, stream>>>(
+        static_cast<const __nv_bfloat16*>(x), H, M, topk, R, inv_perm, sorted_ids,
+        num_post_padded, static_cast<uint8_t*>(x_perm), x_scale, ue8m0);
+  else
+    k_permute_fp8_tok<8><<<grid, PERMUTE_THREADS, 0, stream>>>(
+        static_cast<const __nv_bfloat16*>(x), H, M, topk, R, inv_perm, sorted_ids,
+        num_post_padded, static_cast<uint8_t*>(x_perm), x_scale, ue8m0);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_permute_rows(const void* x, int H, int topk, int R, const int32_t* sorted_ids,
                                 const int32_t* num_post_padded, const float* row_weights,
                                 void* x_perm, float* x_scale, bool ue8m0, int group, int cap,

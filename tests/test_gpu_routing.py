@@ -138,3 +138,37 @@ def test_permute_fp8_codes_bit_exact(name, fmt):
     codes_gpu = np32(b["x_perm"])[rows]
     assert np.array_equal(codes_gpu, codecs.e4m3_encode(q))
     assert np.array_equal(np32(b["x_perm_scale"])[rows].astype(np.float64), s)
+
+
+QPERM = [  # (M, k, E, H, kind, quant, fmt)
+    (300, 3, 16, 384, "invalid", "fp8", "fp32"),      # 40% of the slots skipped, H/16 < 32 lanes
+    (300, 3, 16, 384, "invalid", "mxfp8", "ue8m0"),
+    (257, 8, 64, 1152, "rand", "fp8", "ue8m0"),       # top-8, ragged tail of 16-value chunks
+    (257, 8, 64, 1152, "hot1", "mxfp8", "ue8m0"),     # one hot expert, many padded experts
+    (64, 2, 64, 256, "invalid_all", "fp8", "fp32"),   # no routed row at all
+    (1, 16, 32, 7168, "rand", "fp8", "fp32"),         # one token, the maximum top-k
+]
+
+
+@pytest.mark.parametrize("M,k,E,H,kind,quant,fmt", QPERM)
+def test_permute_quant_every_row_bit_exact(M, k, E, H, kind, quant, fmt):
+    """The quantising permute stores each token's codes into all of its routed
+    rows and zeroes the padding rows: every row below num_post_padded is
+    compared with the oracle (output buffers pre-filled with 0xFF so a row the
+    kernel never writes shows up)."""
+    ids = _edge_ids(M, k, E, kind, seed=M + k)
+    g = torch.Generator().manual_seed(11)
+    x = torch.randn(M, H, generator=g).to(torch.bfloat16)
+    p = moe.Problem(M=M, H=H, I=128, E=E, topk=k, quant=quant, act_scale_fmt=fmt)
+    b = moe.stage_buffers(p)
+    b["x_perm"].fill_(0xFF)
+    b["x_perm_scale"].fill_(float("nan"))
+    moe.moe_align_permute(p, x.cuda(), ids.cuda(), None, b["sorted_ids"], b["block_expert_ids"],
+                          b["expert_offsets"], b["num_post_padded"], b["inv_perm"], b["x_perm"],
+                          b["x_perm_scale"], b["align_ws"])
+    assert moe.moe_sync_status() == 0
+    ref = _check_routing(b, ids.numpy(), E, 128)
+    n = ref["num_tokens_post_padded"]
+    q, s = experts.permute_rows(x.float().numpy(), ref, k, None, fmt, experts.act_group(quant))
+    assert np.array_equal(np32(b["x_perm"])[:n], codecs.e4m3_encode(q[:n]))
+    assert np.array_equal(np32(b["x_perm_scale"])[:n].astype(np.float64), s[:n])
