@@ -50,67 +50,109 @@ __global__ void __launch_bounds__(kRouteWarps * 32)
     for (int e = lane; e < E; e += 32) hist[(size_t)g * E + e] = h[e];
 }
 
-// One CTA of 1024 threads; thread e owns expert e (E <= 1024).
+// One CTA of 1024 threads.  Thread t works on expert e = t % E and on part
+// t / E of the segments (P = 1024 / E parts, rounded down to a power of two),
+// so each thread walks G / P segments instead of all G: (1) per-part sums,
+// (2) per-expert counts, padded exclusive scan over experts, (3) each part
+// rewrites its segments' counts as the running start row of the segment.
 __global__ void __launch_bounds__(1024)
     k_route_scan(int32_t* __restrict__ hist, int G, int E, int A, int R, int cap,
                  int32_t* __restrict__ expert_offsets, int32_t* __restrict__ num_post_padded,
                  int32_t* __restrict__ block_ids, int32_t* __restrict__ sorted_ids) {
+  __shared__ int32_t part_sum[1024];
+  __shared__ int32_t s_off[1025];
+  __shared__ int32_t s_cnt[1024];
   __shared__ int32_t warp_sums[32];
-  __shared__ int32_t s_total;
-  const int e = threadIdx.x, lane = e & 31, warp = e >> 5;
-  int count = 0;
-  if (e < E) {
-    int g = 0;
-    for (; g + 4 <= G; g += 4) {   // exclusive scan over segments, 4 loads in flight
-      int v0 = hist[(size_t)(g + 0) * E + e], v1 = hist[(size_t)(g + 1) * E + e];
-      int v2 = hist[(size_t)(g + 2) * E + e], v3 = hist[(size_t)(g + 3) * E + e];
-      hist[(size_t)(g + 0) * E + e] = count; count += v0;
-      hist[(size_t)(g + 1) * E + e] = count; count += v1;
-      hist[(size_t)(g + 2) * E + e] = count; count += v2;
-      hist[(size_t)(g + 3) * E + e] = count; count += v3;
-    }
-    for (; g < G; ++g) {
-      int v = hist[(size_t)g * E + e];
-      hist[(size_t)g * E + e] = count;
-      count += v;
-    }
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  int P = 1;
+  while (P * 2 * E <= 1024) P *= 2;
+  const int e = tid % E, part = tid / E;
+  const bool worker = part < P;
+  const int per = (G + P - 1) / P;
+  const int g0 = min(G, part * per), g1 = min(G, g0 + per);
+  // (1) sum of this part's segments
+  if (worker) {
+    int sum = 0, g = g0;
+    for (; g + 4 <= g1; g += 4)
+      sum += hist[(size_t)g * E + e] + hist[(size_t)(g + 1) * E + e] +
+             hist[(size_t)(g + 2) * E + e] + hist[(size_t)(g + 3) * E + e];
+    for (; g < g1; ++g) sum += hist[(size_t)g * E + e];
+    part_sum[part * E + e] = sum;
   }
+  __syncthreads();
+  // (2) expert counts and the padded exclusive scan over experts
+  int count = 0;
+  if (tid < E)
+    for (int q = 0; q < P; ++q) count += part_sum[q * E + tid];
   const int padded = (count + A - 1) / A * A;
-  // block-wide exclusive scan of padded counts (expert order)
   int incl = padded;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
-    int v = __shfl_up_sync(0xffffffffu, incl, o);
+    const int v = __shfl_up_sync(0xffffffffu, incl, o);
     if (lane >= o) incl += v;
   }
   if (lane == 31) warp_sums[warp] = incl;
   __syncthreads();
   if (warp == 0) {
-    int w = warp_sums[lane];
+    const int w = warp_sums[lane];
     int wi = w;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-      int v = __shfl_up_sync(0xffffffffu, wi, o);
+      const int v = __shfl_up_sync(0xffffffffu, wi, o);
       if (lane >= o) wi += v;
     }
     warp_sums[lane] = wi - w;   // exclusive prefix of warp totals
-    if (lane == 31) s_total = wi;
+    if (lane == 31) s_off[1024] = wi;
   }
   __syncthreads();
-  const int off = incl - padded + warp_sums[warp];
-  const int total = s_total;
-  if (e < E) {
-    expert_offsets[e] = off;
-    for (int g = 0; g < G; ++g) hist[(size_t)g * E + e] += off;
-    for (int b = off / A; b < (off + padded) / A; ++b) block_ids[b] = e;
-    for (int j = off + count; j < off + padded; ++j) sorted_ids[j] = R;
+  if (tid < E) {
+    s_off[tid] = incl - padded + warp_sums[warp];
+    s_cnt[tid] = count;
   }
-  if (e == 0) {
+  __syncthreads();
+  const int total = s_off[1024];
+  // (3) start row of each segment's first item of expert e
+  if (worker) {
+    int run = s_off[e];
+    for (int q = 0; q < part; ++q) run += part_sum[q * E + e];
+    int g = g0;
+    for (; g + 4 <= g1; g += 4) {
+      const int v0 = hist[(size_t)g * E + e], v1 = hist[(size_t)(g + 1) * E + e];
+      const int v2 = hist[(size_t)(g + 2) * E + e], v3 = hist[(size_t)(g + 3) * E + e];
+      hist[(size_t)g * E + e] = run; run += v0;
+      hist[(size_t)(g + 1) * E + e] = run; run += v1;
+      hist[(size_t)(g + 2) * E + e] = run; run += v2;
+      hist[(size_t)(g + 3) * E + e] = run; run += v3;
+    }
+    for (; g < g1; ++g) {
+      const int v = hist[(size_t)g * E + e];
+      hist[(size_t)g * E + e] = run;
+      run += v;
+    }
+    // padding entries at the end of expert e's segment
+    for (int j = s_off[e] + s_cnt[e] + part; j < s_off[e] + (s_cnt[e] + A - 1) / A * A; j += P)
+      sorted_ids[j] = R;
+  }
+  if (tid < E) expert_offsets[tid] = s_off[tid];
+  if (tid == 0) {
     expert_offsets[E] = total;
     num_post_padded[0] = total;
   }
-  for (int b = total / A + e; b < cap / A; b += blockDim.x) block_ids[b] = -1;
-  for (int j = total + e; j < cap; j += blockDim.x) sorted_ids[j] = R;
+  // block expert ids: the expert whose padded range holds the block (binary
+  // search over the offsets), -1 past the used blocks
+  for (int b = tid; b < cap / A; b += blockDim.x) {
+    int id = -1;
+    if (b * A < total) {
+      int lo = 0, hi = E - 1;   // last expert with s_off <= b * A and a non-empty range
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (s_off[mid] <= b * A) lo = mid; else hi = mid - 1;
+      }
+      id = lo;
+    }
+    block_ids[b] = id;
+  }
+  for (int j = total + tid; j < cap; j += blockDim.x) sorted_ids[j] = R;
 }
 
 __global__ void __launch_bounds__(kRouteWarps * 32)
