@@ -189,9 +189,9 @@ def gemm1_kernel(cfg):
     if cfg.quant == "fp8":
         return "fp8", "k_ggemm_fp8 (GEMM1)"
     if cfg.quant == "mxfp4":
-        return "mxfp4", "k_ggemm_mxfp4 (GEMM1)"
+        return "mxfp4", "k_ggemm_mxfp4<fused act + e4m3 quant> (GEMM1)"
     if cfg.quant == "mxfp8":
-        return "mxfp8", "k_ggemm_mxfp4<MX8> (GEMM1, e4m3 weights)"
+        return "mxfp8", "k_ggemm_mxfp4<MX8, fused act + 1x32 quant> (GEMM1, e4m3 weights)"
     if cfg.M * cfg.topk >= 2 * 128 * cfg.E:
         return "bf16_2sm", "k_ggemm_bf16_2sm<fused SiLU-and-mul> (GEMM1, SM pairs)"
     return "bf16", "k_ggemm_bf16<fused SiLU-and-mul> (GEMM1)"
@@ -297,6 +297,11 @@ def _stage_plan(moe, p, cfg, d, b, stream):
         plan.append(("gemm1_silu_mul", lambda: moe.grouped_gemm_w13(
             p, b["x_perm"], None, w13, None, b["block_expert_ids"], b["num_post_padded"],
             b["z"], None, fuse_act=True, stream=stream)))
+    elif cfg.quant in ("mxfp4", "mxfp8"):
+        # the block-scaled GEMM1 writes the quantised activation itself
+        plan.append(("gemm1_act_quant", lambda: moe.grouped_gemm_w13(
+            p, b["x_perm"], b["x_perm_scale"], w13, d["w13_scale"], b["block_expert_ids"],
+            b["num_post_padded"], b["z"], b["z_scale"], fuse_act=True, stream=stream)))
     else:
         plan.append(("gemm1", lambda: moe.grouped_gemm_w13(
             p, b["x_perm"], b["x_perm_scale"], w13, d["w13_scale"], b["block_expert_ids"],
@@ -444,7 +449,7 @@ def run_ours(args):
         q = cfg.quant != "bf16"
         gemm1_flops = 2.0 * R * cfg.H * 2 * cfg.I      # padding rows not counted
         gemm2_flops = 2.0 * R * cfg.I * cfg.H
-        g1 = "gemm1" if q else "gemm1_silu_mul"
+        g1 = [n for n, _ in plan if n.startswith("gemm1")][0]
         # a contraction takes the peak of its own dtype: FP8 = bf16 x 2 (4.5 / 2.25 nominal)
         ratio = 2.0 if q else 1.0
         peak = peaks["bf16_tflops_sustained"] * ratio

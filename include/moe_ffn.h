@@ -261,8 +261,14 @@ moe_status moe_align_permute_noalloc(const moe_problem* p, const void* x,
  *       w13 [E,2I,H] (+ w13_scale), block_expert_ids, num_post_padded (device).
  *  out: fuse_act == 0: h1 [S,2I] bf16.
  *       fuse_act == 1: the gated activation (p->act_recipe) written directly
- *       (MOE_Q_BF16: z [S,I] bf16).  Quantised modes currently need fuse_act == 0
- *       (MOE_ERR_UNSUPPORTED otherwise).
+ *       (MOE_Q_BF16: z [S,I] bf16; quantised modes: out = z [S,I] e4m3fn
+ *       codes and out_scale = z_scale [S,I/group] fp32, exactly as
+ *       act_mul_quant would write them from h1; MOE_Q_FP8_BLOCK128 and
+ *       MOE_Q_MXFP4_W4A8: 1x128 groups, MOE_Q_MXFP8_1X32: 1x32).  out_scale
+ *       is only read when a quantised mode fuses the activation (then
+ *       required).  fused_experts runs GEMM1 this way except for
+ *       MOE_Q_FP8_BLOCK128, whose promotion epilogue bounds the GEMM (two
+ *       steps measured faster there).
  *  Rows of blocks past num_post_padded are not written. */
 moe_status grouped_gemm_w13(const moe_problem* p, const void* x_perm, const float* x_scale,
                             const void* w13, const void* w13_scale,

@@ -13,6 +13,7 @@
 // loads issued in batches ahead of the arithmetic so each warp keeps several
 // KB in flight; the reduce issues all k gathers of a vector pair before it
 // accumulates.
+#include "e4m3_pack.cuh"
 #include "moe_common.cuh"
 #include "moe_internal.h"
 
@@ -64,12 +65,13 @@ __global__ void __launch_bounds__(ACT_THREADS)
 
 // Quantised variant: z in fp32, then per group of LPG lanes x 8 values
 // (16 lanes: 1x128; 4 lanes: the 1x32 groups of MXFP8) amax -> scale -> e4m3
-// with one reciprocal per group.
-template <int LPG>
+// with one reciprocal per group.  With power-of-two scales (UE8M0) the
+// reciprocal is exact and v * r is the correctly rounded quotient, so the
+// correction step is skipped.
+template <int LPG, bool UE8M0>
 __global__ void __launch_bounds__(ACT_THREADS)
     k_act_mul_fp8(const __nv_bfloat16* __restrict__ h1, int I, const int32_t* __restrict__ npp,
-                  uint8_t* __restrict__ zq, float* __restrict__ zs, int ue8m0,
-                  const Epilogue recipe) {
+                  uint8_t* __restrict__ zq, float* __restrict__ zs, const Epilogue recipe) {
   const int lane = threadIdx.x & 31;
   const int wpc = blockDim.x >> 5;
   const int rows = *npp;
@@ -108,16 +110,11 @@ __global__ void __launch_bounds__(ACT_THREADS)
         for (int o = LPG / 2; o >= 1; o >>= 1)
           amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
         if (act) {
-          const float s = act_scale(amax, ue8m0 != 0);
+          const float s = act_scale(amax, UE8M0);
           const float r = __frcp_rn(s);
-          uint32_t lo = 0, hi = 0;
 #pragma unroll
-          for (int j = 0; j < 4; ++j)
-            lo |= (uint32_t)f32_to_e4m3(div_rn_shared(f[j], s, r)) << (8 * j);
-#pragma unroll
-          for (int j = 0; j < 4; ++j)
-            hi |= (uint32_t)f32_to_e4m3(div_rn_shared(f[4 + j], s, r)) << (8 * j);
-          q2[v] = make_uint2(lo, hi);
+          for (int j = 0; j < 8; ++j) f[j] = UE8M0 ? f[j] * r : quot_rn(f[j], s, r);
+          q2[v] = make_uint2(e4m3x4(f[0], f[1], f[2], f[3]), e4m3x4(f[4], f[5], f[6], f[7]));
           if (v % LPG == 0) srow[v / LPG] = s;
         }
       }
@@ -136,14 +133,20 @@ cudaError_t launch_act_mul(const void* h1, int I, const int32_t* num_post_padded
                                                      num_post_padded,
                                                      static_cast<__nv_bfloat16*>(z), act);
   } else {
-    if (group == 32)
-      k_act_mul_fp8<4><<<grid, ACT_THREADS, 0, stream>>>(
-          static_cast<const __nv_bfloat16*>(h1), I, num_post_padded, static_cast<uint8_t*>(z),
-          z_scale, ue8m0, act);
+    const auto* hp = static_cast<const __nv_bfloat16*>(h1);
+    auto* zp = static_cast<uint8_t*>(z);
+    if (group == 32 && ue8m0)
+      k_act_mul_fp8<4, true><<<grid, ACT_THREADS, 0, stream>>>(hp, I, num_post_padded, zp,
+                                                                z_scale, act);
+    else if (group == 32)
+      k_act_mul_fp8<4, false><<<grid, ACT_THREADS, 0, stream>>>(hp, I, num_post_padded, zp,
+                                                                 z_scale, act);
+    else if (ue8m0)
+      k_act_mul_fp8<16, true><<<grid, ACT_THREADS, 0, stream>>>(hp, I, num_post_padded, zp,
+                                                                 z_scale, act);
     else
-      k_act_mul_fp8<16><<<grid, ACT_THREADS, 0, stream>>>(
-          static_cast<const __nv_bfloat16*>(h1), I, num_post_padded, static_cast<uint8_t*>(z),
-          z_scale, ue8m0, act);
+      k_act_mul_fp8<16, false><<<grid, ACT_THREADS, 0, stream>>>(hp, I, num_post_padded, zp,
+                                                                  z_scale, act);
   }
   return cudaGetLastError();
 }

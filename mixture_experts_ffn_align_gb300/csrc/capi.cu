@@ -151,7 +151,9 @@ Layout layout(const moe_problem* p) {
   L.xperm = take(std::max(cap * H * xb, cap * H * 2));
   L.y2 = L.xperm;
   L.xscale = quantised(p) ? take(cap * (H / act_group(p)) * 4) : 0;
-  L.h1 = quantised(p) ? take(cap * 2 * I * 2) : 0;
+  // bf16 and block-scaled GEMM1s write z (activation, and its quantisation,
+  // fused); FP8 block scales keep H1
+  L.h1 = p->quant == MOE_Q_FP8_BLOCK128 ? take(cap * 2 * I * 2) : 0;
   L.z = take(cap * I * (quantised(p) ? 1 : 2));
   L.zscale = quantised(p) ? take(cap * (I / act_group(p)) * 4) : 0;
   L.total = o;
@@ -189,7 +191,7 @@ BatchedLayout batched_layout(const moe_problem* p, int max_tokens) {
   L.sorted = q ? take(rows * 4) : 0;
   L.xq = q ? take(rows * H) : 0;
   L.xscale = q ? take(rows * (H / act_group(p)) * 4) : 0;
-  L.h1 = q ? take(rows * 2 * I * 2) : 0;
+  L.h1 = p->quant == MOE_Q_FP8_BLOCK128 ? take(rows * 2 * I * 2) : 0;
   L.z = take(rows * I * (q ? 1 : 2));
   L.zscale = q ? take(rows * (I / act_group(p)) * 4) : 0;
   L.total = o;
@@ -298,7 +300,6 @@ moe_status grouped_gemm_w13_ex(const moe_problem* p, const void* x_perm, const f
                                const int32_t* block_expert_ids,
                                const int32_t* num_post_padded, void* out, float* out_scale,
                                int fuse_act, void* stream) {
-  (void)out_scale;
   if (!valid_problem(p)) return MOE_ERR_INVALID_ARG;
   if (p->M == 0) return MOE_OK;
   if (!x_perm || !w13 || !block_expert_ids || !num_post_padded || !out) return MOE_ERR_INVALID_ARG;
@@ -311,18 +312,19 @@ moe_status grouped_gemm_w13_ex(const moe_problem* p, const void* x_perm, const f
                                         p->E * 2 * p->I, 2 * p->I, 2 * p->I, block_expert_ids,
                                         num_post_padded, out, fuse_act != 0, ep, s));
   }
-  if (fuse_act) return MOE_ERR_UNSUPPORTED;
   if (!x_scale || !w13_scale) return MOE_ERR_INVALID_ARG;
+  if (fuse_act && !out_scale) return MOE_ERR_INVALID_ARG;
   if (block_scaled(p))
-    return cuda_status(launch_ggemm_mxfp4(x_perm, x_scale, cap, p->H, w13,
-                                          static_cast<const uint8_t*>(w13_scale),
-                                          p->E * 2 * p->I, 2 * p->I, 2 * p->I, block_expert_ids,
-                                          num_post_padded, out,
-                                          p->quant == MOE_Q_MXFP8_1X32, ep, s));
+    return cuda_status(launch_ggemm_mxfp4(
+        x_perm, x_scale, cap, p->H, w13, static_cast<const uint8_t*>(w13_scale), p->E * 2 * p->I,
+        2 * p->I, 2 * p->I, block_expert_ids, num_post_padded, out,
+        p->quant == MOE_Q_MXFP8_1X32, ep, s, out_scale, fuse_act != 0,
+        p->act_scale_fmt == MOE_SCALE_UE8M0));
   return cuda_status(launch_ggemm_fp8(x_perm, x_scale, cap, p->H, w13,
                                       static_cast<const float*>(w13_scale), p->E * 2 * p->I,
                                       2 * p->I, 2 * p->I, block_expert_ids, num_post_padded, out,
-                                      ep, s));
+                                      ep, s, out_scale, fuse_act != 0,
+                                      p->act_scale_fmt == MOE_SCALE_UE8M0));
 }
 
 moe_status grouped_gemm_w13(const moe_problem* p, const void* x_perm, const float* x_scale,
@@ -426,7 +428,17 @@ moe_status fused_experts_ex(const moe_problem* p, const void* x, const void* w13
     if (st != MOE_OK) return st;
     st = grouped_gemm_w2_ex(p, ws + L.z, nullptr, w2, nullptr, w2_bias, blocks, npp, sorted,
                             topk_weights, ws + L.y2, stream);
+  } else if (block_scaled(p)) {
+    // GEMM1 writes the quantised activation directly (act_mul_quant fused)
+    st = grouped_gemm_w13_ex(p, ws + L.xperm, f32(L.xscale), w13, w13_scale, w13_bias, blocks,
+                             npp, ws + L.z, f32(L.zscale), 1, stream);
+    if (st != MOE_OK) return st;
+    st = grouped_gemm_w2_ex(p, ws + L.z, f32(L.zscale), w2, w2_scale, w2_bias, blocks, npp,
+                            sorted, topk_weights, ws + L.y2, stream);
   } else {
+    // FP8 block scales: the promotion epilogue bounds this GEMM, and the
+    // activation at the end of each tile lengthened it by more than the
+    // separate pass costs, so H1 goes through HBM
     st = grouped_gemm_w13_ex(p, ws + L.xperm, f32(L.xscale), w13, w13_scale, w13_bias, blocks,
                              npp, ws + L.h1, nullptr, 0, stream);
     if (st != MOE_OK) return st;
@@ -551,15 +563,17 @@ moe_status fused_experts_batched(const moe_problem* p, const void* x,
   e = launch_permute_rows(x, H, 1, rows, sorted, npp, nullptr, ws + L.xq, xscale, ue8m0,
                           act_group(p), rows, s);
   if (e != cudaSuccess) return cuda_status(e);
-  if (block_scaled(p))
+  if (block_scaled(p)) {
+    // GEMM1 with the activation and its quantisation in the epilogue
     e = launch_ggemm_mxfp4(ws + L.xq, xscale, rows, H, w13, static_cast<const uint8_t*>(w13_scale),
-                           E * 2 * I, 2 * I, 2 * I, blocks, npp, ws + L.h1,
-                           p->quant == MOE_Q_MXFP8_1X32, ep, s);
-  else
+                           E * 2 * I, 2 * I, 2 * I, blocks, npp, ws + L.z,
+                           p->quant == MOE_Q_MXFP8_1X32, ep, s, zscale, true, ue8m0);
+  } else {   // FP8 block scales: two steps (see fused_experts_ex)
     e = launch_ggemm_fp8(ws + L.xq, xscale, rows, H, w13, static_cast<const float*>(w13_scale),
                          E * 2 * I, 2 * I, 2 * I, blocks, npp, ws + L.h1, ep, s);
-  if (e != cudaSuccess) return cuda_status(e);
-  e = launch_act_mul(ws + L.h1, I, npp, ws + L.z, zscale, ue8m0, act_group(p), rows, ep, s);
+    if (e == cudaSuccess)
+      e = launch_act_mul(ws + L.h1, I, npp, ws + L.z, zscale, ue8m0, act_group(p), rows, ep, s);
+  }
   if (e != cudaSuccess) return cuda_status(e);
   if (block_scaled(p))
     e = launch_ggemm_mxfp4(ws + L.z, zscale, rows, I, w2, static_cast<const uint8_t*>(w2_scale),

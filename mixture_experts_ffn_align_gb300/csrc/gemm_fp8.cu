@@ -32,6 +32,7 @@
 //  * every wait is bounded, as in the bf16 kernel.
 #include <mutex>
 
+#include "e4m3_pack.cuh"
 #include "moe_common.cuh"
 #include "moe_internal.h"
 #include "tile_sched.cuh"
@@ -60,7 +61,9 @@ static_assert(128 * CTRL_REGS + 256 * EPI_REGS <= NUM_THREADS * LAUNCH_REGS,
               "register split exceeds the launch allocation");
 static_assert(32 * (CTRL_REGS + 2 * EPI_REGS) <= 16384, "register-file partition");
 constexpr int SCHED_BYTES = 16 + 4 * kSchedMaxRuns + 4 * kSchedMaxBlocks;
-constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + 256 + SCHED_BYTES;
+constexpr int AMAX_BYTES = 2 * 2 * BM * 4;      // fused epilogue: [tile parity][half][row]
+constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + 256 + SCHED_BYTES + AMAX_BYTES;
+static_assert(SMEM_BYTES <= 232448, "shared memory");
 
 struct Fp8Args {
   const int32_t* block_expert_ids;
@@ -79,9 +82,15 @@ struct Fp8Args {
   uint64_t limit_ns;
   int never_arrive;
   int* err;
-  Epilogue ep;            // bias, router weight
+  Epilogue ep;            // bias, router weight, gated activation recipe
+  // fused GEMM1 epilogue (FUSE): z codes [cap, I] e4m3, scales [cap, I/128]
+  uint8_t* zq;
+  float* zs;
+  int I;
+  int ue8m0;
 };
 
+template <bool FUSE>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     k_ggemm_fp8(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const Fp8Args args) {
@@ -89,7 +98,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
-  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 2 * NPART + 1);
+  // full[S], empty[S], pfull[P], pempty[P], drain, amax exchange[4]
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 2 * NPART + 1 + 4);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
   int* s_nruns = reinterpret_cast<int*>(smem + STAGES * STAGE_BYTES + 256);
   int* s_runs = s_nruns + 4;
@@ -103,6 +113,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   auto pfull_bar = [&](int b) { return bar_base + 8u * (2 * STAGES + b); };
   auto pempty_bar = [&](int b) { return bar_base + 8u * (2 * STAGES + NPART + b); };
   const uint32_t drain_bar = bar_base + 8u * (2 * STAGES + 2 * NPART);
+  auto amax_bar = [&](int q) { return bar_base + 8u * (2 * STAGES + 2 * NPART + 1 + q); };
+  float* s_amax = reinterpret_cast<float*>(smem + STAGES * STAGE_BYTES + 1024 + 256 + SCHED_BYTES);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -114,6 +126,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       mbar_init(pempty_bar(b), NUM_EPI_WARPS);
     }
     mbar_init(drain_bar, 1);
+    for (int qq = 0; qq < 4; ++qq) mbar_init(amax_bar(qq), 2);   // the two halves' lane 0
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -153,7 +166,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       sched_tile(sched, t, m_blk, n_tile);
       const int e = s_ids[m_blk];
       if (e < 0 || e >= args.num_experts) continue;
-      const int brow = e * args.b_rows_per_expert + n_tile * BN;
+      // B tile: 256 consecutive weight rows, or (FUSE) gate rows
+      // [128 j, 128 j + 128) and the matching up rows I + 128 j ...
+      const int brow = FUSE ? e * args.b_rows_per_expert + n_tile * 128
+                            : e * args.b_rows_per_expert + n_tile * BN;
+      const int brow2 = FUSE ? brow + args.I : brow + 128;
       bool ok = true;
       for (int kb = 0; kb < args.num_kb; ++kb) {
         if (!mbar_wait_bounded(empty_bar(stage), phase ^ 1, abort_flag, args.limit_ns, args.err)) {
@@ -167,7 +184,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           mbar_arrive_expect_tx(full_bar(stage), STAGE_BYTES);
           tma_load_2d(sa, &tmA, full_bar(stage), kb * BK, m_blk * BM, pol_a);
           tma_load_2d(sa + A_BYTES, &tmB, full_bar(stage), kb * BK, brow, pol_b);
-          tma_load_2d(sa + A_BYTES + 128 * BK, &tmB, full_bar(stage), kb * BK, brow + 128, pol_b);
+          tma_load_2d(sa + A_BYTES + 128 * BK, &tmB, full_bar(stage), kb * BK, brow2, pol_b);
           issued_mask |= 1u << stage;
           issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
         }
@@ -222,28 +239,33 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const int q = warp & 3;               // TMEM lane quadrant
     const int half = (warp - EPI_WARP0) >> 2;   // 128-column half of the tile
     const int row_in_tile = q * 32 + lane;
-    uint32_t pc = 0;
+    uint32_t pc = 0, xpar = 0;
     bool ok = true;
     for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
       int m_blk, n_tile;
       sched_tile(sched, t, m_blk, n_tile);
       const int e = s_ids[m_blk];
       if (e < 0 || e >= args.num_experts) continue;
-      const int nblk = 2 * n_tile + half;            // weight-scale block of this warp
-      const bool active = nblk < args.n_blocks;      // false: past N on a ragged last tile
+      // weight-scale block of this warp's columns (FUSE: its 64 gate columns
+      // lie in block n_tile, the matching up columns in block I/128 + n_tile)
+      const int nblk = FUSE ? n_tile : 2 * n_tile + half;
+      const bool active = FUSE || nblk < args.n_blocks;   // false: past N on a ragged last tile
       const size_t row = (size_t)m_blk * BM + row_in_tile;
       const float* sa_row = args.a_scale + row * args.num_kb;
       const float* sb_blk =
           args.b_scale + ((size_t)e * args.n_blocks + (active ? nblk : 0)) * (size_t)args.num_kb;
+      const float* sb_up =
+          FUSE ? sb_blk + (size_t)(args.I / 128) * args.num_kb : sb_blk;
       float acc[128];
 #pragma unroll
       for (int j = 0; j < 128; ++j) acc[j] = 0.0f;
-      constexpr int SCALE_AHEAD = 4;
-      float ra[SCALE_AHEAD], rb[SCALE_AHEAD];
+      constexpr int SCALE_AHEAD = FUSE ? 2 : 4;   // FUSE holds two weight-scale streams
+      float ra[SCALE_AHEAD], rb[SCALE_AHEAD], ru[SCALE_AHEAD];
 #pragma unroll
       for (int j = 0; j < SCALE_AHEAD; ++j) {
         ra[j] = j < args.num_kb ? __ldg(sa_row + j) : 0.0f;
         rb[j] = j < args.num_kb ? __ldg(sb_blk + j) : 0.0f;
+        ru[j] = FUSE && j < args.num_kb ? __ldg(sb_up + j) : 0.0f;
       }
       for (int kb0 = 0; kb0 < args.num_kb && ok; kb0 += SCALE_AHEAD) {
 #pragma unroll
@@ -251,9 +273,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           const int kb = kb0 + j;
           if (kb >= args.num_kb) break;
           const float s = ra[j] * rb[j];
+          const float su = FUSE ? ra[j] * ru[j] : s;       // up columns' scale product
           if (kb + SCALE_AHEAD < args.num_kb) {
             ra[j] = __ldg(sa_row + kb + SCALE_AHEAD);
             rb[j] = __ldg(sb_blk + kb + SCALE_AHEAD);
+            if (FUSE) ru[j] = __ldg(sb_up + kb + SCALE_AHEAD);
           }
           const uint32_t buf = pc % NPART, pphase = (pc / NPART) & 1;
           int got = 0;
@@ -265,14 +289,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             break;
           }
           tc_fence_after();
-          const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + buf * BN + half * 128;
+          // FUSE: columns [64 half, +64) of the gate half, then of the up half
+          const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + buf * BN +
+                                 (FUSE ? half * 64 : half * 128);
 #pragma unroll
           for (int c = 0; c < 2; ++c) {     // two rounds of four 16-column loads
             uint32_t p0[16], p1[16], p2[16], p3[16];
-            tmem_ld_32x32b_x16(taddr + c * 64, p0);
-            tmem_ld_32x32b_x16(taddr + c * 64 + 16, p1);
-            tmem_ld_32x32b_x16(taddr + c * 64 + 32, p2);
-            tmem_ld_32x32b_x16(taddr + c * 64 + 48, p3);
+            const uint32_t tc = taddr + (FUSE ? c * 128 : c * 64);
+            const float sc = c == 0 ? s : su;
+            tmem_ld_32x32b_x16(tc, p0);
+            tmem_ld_32x32b_x16(tc + 16, p1);
+            tmem_ld_32x32b_x16(tc + 32, p2);
+            tmem_ld_32x32b_x16(tc + 48, p3);
             tmem_ld_wait();
             if (c == 1) {     // every read of this buffer by this warp is done
               tc_fence_before();
@@ -281,17 +309,70 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             }
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
-              acc[c * 64 + i] = fmaf(s, __uint_as_float(p0[i]), acc[c * 64 + i]);
-              acc[c * 64 + 16 + i] = fmaf(s, __uint_as_float(p1[i]), acc[c * 64 + 16 + i]);
-              acc[c * 64 + 32 + i] = fmaf(s, __uint_as_float(p2[i]), acc[c * 64 + 32 + i]);
-              acc[c * 64 + 48 + i] = fmaf(s, __uint_as_float(p3[i]), acc[c * 64 + 48 + i]);
+              acc[c * 64 + i] = fmaf(sc, __uint_as_float(p0[i]), acc[c * 64 + i]);
+              acc[c * 64 + 16 + i] = fmaf(sc, __uint_as_float(p1[i]), acc[c * 64 + 16 + i]);
+              acc[c * 64 + 32 + i] = fmaf(sc, __uint_as_float(p2[i]), acc[c * 64 + 32 + i]);
+              acc[c * 64 + 48 + i] = fmaf(sc, __uint_as_float(p3[i]), acc[c * 64 + 48 + i]);
             }
           }
           ++pc;
         }
       }
       if (!ok) break;
-      if (active) {
+      if (FUSE) {
+        // acc[0, 64): gate sums, acc[64, 128): up sums of columns 64 half ..
+        // of n-block n_tile.  z = act(bf16 g, bf16 u) in fp32 as act_mul_quant
+        // computes it from a stored H1; the 1x128 group's amax is combined
+        // with the other half's warp through shared memory.
+        const int gcol0 = n_tile * 128 + half * 64, ucol0 = args.I + gcol0;
+        const bool bias = args.ep.bias != nullptr;
+        float amax = 0.0f;
+#pragma unroll
+        for (int j = 0; j < 64; ++j) {
+          float gs = acc[j], us = acc[64 + j];
+          if (bias) {
+            gs += epi_bias(args.ep, e, gcol0 + j);
+            us += epi_bias(args.ep, e, ucol0 + j);
+          }
+          acc[j] = act_glu(args.ep, bf16_round(gs), bf16_round(us));
+          amax = fmaxf(amax, fabsf(acc[j]));
+        }
+        const uint32_t par = xpar & 1;
+        float* sx = s_amax + (par * 2) * BM;
+        sx[half * BM + row_in_tile] = amax;
+        __syncwarp();
+        int got = 1;
+        if (lane == 0) {
+          mbar_arrive(amax_bar(q));
+          got = mbar_wait_bounded(amax_bar(q), par, abort_flag, args.limit_ns, args.err);
+        }
+        got = __shfl_sync(0xffffffffu, got, 0);
+        __syncwarp();                                 // lane 0's acquire covers the warp
+        ++xpar;
+        if (!got) {
+          ok = false;
+          break;
+        }
+        amax = fmaxf(sx[row_in_tile], sx[BM + row_in_tile]);
+        const float sc = act_scale(amax, args.ue8m0 != 0);
+        const float rc = __frcp_rn(sc);
+        uint4* zdst = reinterpret_cast<uint4*>(args.zq + row * (size_t)args.I + (size_t)gcol0);
+#pragma unroll
+        for (int v = 0; v < 4; ++v) {
+          uint32_t wd[4];
+#pragma unroll
+          for (int qd = 0; qd < 4; ++qd) {
+            uint32_t word = 0;
+#pragma unroll
+            for (int bb = 0; bb < 4; ++bb)
+              word |= (uint32_t)f32_to_e4m3(quot_rn(acc[16 * v + 4 * qd + bb], sc, rc))
+                      << (8 * bb);
+            wd[qd] = word;
+          }
+          zdst[v] = make_uint4(wd[0], wd[1], wd[2], wd[3]);
+        }
+        if (half == 0) args.zs[row * (size_t)(args.I / 128) + n_tile] = sc;
+      } else if (active) {
         uint4* dst = reinterpret_cast<uint4*>(args.out + row * args.ldo + (size_t)nblk * 128);
         const float w = epi_row_weight(args.ep, row);
         const bool bias = args.ep.bias != nullptr;
@@ -322,12 +403,37 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
 }  // namespace
 
+namespace {
+template <bool FUSE>
+cudaError_t launch_fp8_form(const CUtensorMap& tmA, const CUtensorMap& tmB, const Fp8Args& a,
+                            cudaStream_t stream) {
+  static bool attr_done = false;
+  static bool regs_ok = false;
+  if (!attr_done) {
+    cudaFuncSetAttribute(k_ggemm_fp8<FUSE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         SMEM_BYTES);
+    // the register split above is only safe at exactly LAUNCH_REGS a thread
+    cudaFuncAttributes fa;
+    regs_ok = cudaFuncGetAttributes(&fa, k_ggemm_fp8<FUSE>) == cudaSuccess &&
+              fa.numRegs == LAUNCH_REGS;
+    attr_done = true;
+  }
+  if (!regs_ok) return cudaErrorInvalidConfiguration;
+  k_ggemm_fp8<FUSE><<<num_sms(), NUM_THREADS, SMEM_BYTES, stream>>>(tmA, tmB, a);
+  return cudaGetLastError();
+}
+}  // namespace
+
 cudaError_t launch_ggemm_fp8(const void* A, const float* a_scale, int cap, int K, const void* B,
                              const float* b_scale, int b_rows_total, int b_rows_per_expert,
                              int n_out, const int32_t* block_expert_ids,
                              const int32_t* num_post_padded, void* out, const Epilogue& ep,
-                             cudaStream_t stream) {
+                             cudaStream_t stream, float* z_scale, bool fuse_act, bool ue8m0) {
   if (cap <= 0) return cudaSuccess;
+  // fused GEMM1: B rows per expert = 2I (gate then up), I a multiple of 128
+  if (fuse_act && (z_scale == nullptr || b_rows_per_expert % 256 != 0 ||
+                   n_out != b_rows_per_expert))
+    return cudaErrorInvalidValue;
   CUtensorMap tmA, tmB;
   if (!make_tmap_k_sw128(&tmA, A, (uint64_t)cap, (uint64_t)K, 1, 128) ||
       !make_tmap_k_sw128(&tmB, B, (uint64_t)b_rows_total, (uint64_t)K, 1, 128))
@@ -342,25 +448,20 @@ cudaError_t launch_ggemm_fp8(const void* A, const float* a_scale, int cap, int K
   a.ldo = n_out;
   a.num_kb = K / BK;
   a.n_blocks = n_out / 128;
-  a.n_tiles = (n_out + BN - 1) / BN;
+  a.I = b_rows_per_expert / 2;
+  // fused: one tile per 128-column block of z (gate rows j + up rows I + j)
+  a.n_tiles = fuse_act ? a.I / 128 : (n_out + BN - 1) / BN;
+  a.zq = fuse_act ? static_cast<uint8_t*>(out) : nullptr;
+  a.zs = z_scale;
+  a.ue8m0 = ue8m0 ? 1 : 0;
   a.b_rows_per_expert = b_rows_per_expert;
   a.m_blocks_cap = cap / BM;
   a.num_experts = b_rows_total / b_rows_per_expert;
   a.group_max = sched_group_max(K, 1);
   watchdog_params(&a.limit_ns, &a.never_arrive);
   a.err = dev_error_word();
-  static bool attr_done = false;
-  static bool regs_ok = false;
-  if (!attr_done) {
-    cudaFuncSetAttribute(k_ggemm_fp8, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
-    // the register split above is only safe at exactly LAUNCH_REGS a thread
-    cudaFuncAttributes fa;
-    regs_ok = cudaFuncGetAttributes(&fa, k_ggemm_fp8) == cudaSuccess && fa.numRegs == LAUNCH_REGS;
-    attr_done = true;
-  }
-  if (!regs_ok) return cudaErrorInvalidConfiguration;
-  k_ggemm_fp8<<<num_sms(), NUM_THREADS, SMEM_BYTES, stream>>>(tmA, tmB, a);
-  return cudaGetLastError();
+  return fuse_act ? launch_fp8_form<true>(tmA, tmB, a, stream)
+                  : launch_fp8_form<false>(tmA, tmB, a, stream);
 }
 
 }  // namespace moe

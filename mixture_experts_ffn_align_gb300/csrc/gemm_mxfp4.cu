@@ -23,7 +23,10 @@
 //    padded 4-bit TMA type (each 16 values -> 8 bytes + 8-byte gap, so a row
 //    of 128 values fills one 128-byte swizzled smem row; the copy counts the
 //    packed bytes toward the barrier), 128-byte swizzle;
-//  * warp 2: scale writer.  Per K block it builds the two scale operands in
+//  * warps 2 and 3: scale writers (warp 2 the A operand, warp 3 the B
+//    operand; one warp doing both measured busy ~90 % of the kernel and
+//    stalled the MMA issuer ~27 % of the DeepSeek-shaped MXFP8 GEMM1).  Per
+//    K block they build the two scale operands in
 //    a shared-memory ring of SSLOTS slots: the A operand (each row's UE8M0
 //    exponent in all 4 bytes: one scale covers 128 = 4 x 32) and the B
 //    operand (the 4 E8M0 bytes of each column's 4 K chunks), each 128-row
@@ -62,6 +65,7 @@
 #include <mutex>
 
 #include "../../include/moe_ffn.h"
+#include "e4m3_pack.cuh"
 #include "moe_common.cuh"
 #include "moe_internal.h"
 #include "tile_sched.cuh"
@@ -118,7 +122,13 @@ struct Mx4Args {
   uint64_t limit_ns;
   int never_arrive;
   int* err;
-  Epilogue ep;              // bias, router weight
+  Epilogue ep;              // bias, router weight, gated activation recipe
+  // fused GEMM1 epilogue (FUSE): z codes [cap, I] e4m3 and z scales
+  // [cap, I / group] fp32 (powers of two when ue8m0)
+  uint8_t* zq;
+  float* zs;
+  int I;
+  int ue8m0;
 };
 
 // Activation scales of 4 K blocks for this lane's rows (lane + 32 c):
@@ -166,7 +176,7 @@ __device__ __forceinline__ uint32_t a_word(const AGroup<MX8>& A, int c, int j) {
   }
 }
 
-template <bool STAGED, bool MX8>
+template <bool STAGED, bool MX8, bool FUSE>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     k_ggemm_mxfp4(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                   const __grid_constant__ CUtensorMap tmS, const Mx4Args args) {
@@ -202,7 +212,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       mbar_init(empty_bar(s), 1);
     }
     for (int s = 0; s < SSLOTS; ++s) {
-      mbar_init(sfull_bar(s), 1);
+      mbar_init(sfull_bar(s), MX8 ? 2 : 1);   // one arrival per scale writer
       mbar_init(sempty_bar(s), 1);
     }
     mbar_init(tfull_bar, 1);
@@ -247,7 +257,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       sched_tile(sched, t, m_blk, n_tile);
       const int e = s_ids[m_blk];
       if (e < 0 || e >= args.num_experts) continue;
-      const int brow = e * N + n_tile * BN;
+      // B tile: 256 consecutive weight rows, or (FUSE) gate rows
+      // [128 j, 128 j + 128) and the matching up rows I + 128 j ...
+      const int brow = FUSE ? e * N + n_tile * 128 : e * N + n_tile * BN;
+      const int brow2 = FUSE ? brow + args.I : brow + 128;
       bool ok = true;
       for (int kb = 0; kb < args.num_kb; ++kb) {
         if (!mbar_wait_bounded(empty_bar(stage), phase ^ 1, abort_flag, args.limit_ns, args.err)) {
@@ -261,8 +274,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           mbar_arrive_expect_tx(full_bar(stage), MX8 ? A_BYTES + B_BYTES : TX_BYTES);
           tma_load_2d(sa, &tmA, full_bar(stage), kb * BK, m_blk * BM, pol_a);
           tma_load_2d(sa + A_BYTES, &tmB, full_bar(stage), kb * BK, brow, pol_b);
-          tma_load_2d(sa + A_BYTES + B_BYTES / 2, &tmB, full_bar(stage), kb * BK, brow + 128,
-                      pol_b);
+          tma_load_2d(sa + A_BYTES + B_BYTES / 2, &tmB, full_bar(stage), kb * BK, brow2, pol_b);
           issued_mask |= 1u << stage;
           issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
         }
@@ -276,23 +288,32 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     for (int s = 0; s < STAGES; ++s)
       if (issued_mask & (1u << s))
         mbar_wait_bounded(full_bar(s), (issued_parity >> s) & 1, nullptr, args.limit_ns, args.err);
-  } else if (warp == 2) {
-    // ------------------------------------------------------------ scale writer
-    // Packs K block j (0-3) of a group: A words from four fp32 scales of
-    // this lane's rows, B words as given; then hands the ring slot over.
+  } else if ((MX8 && warp == 2) || warp == 3) {
+    // ------------------------------------------------------------ scale writers
+    // Warp 3 builds the weight-scale operand of each K block (the E8M0 bytes
+    // as given).  MXFP8: warp 2 builds the activation-scale operand (A words
+    // from four 1x32 fp32 scales of each of this lane's rows); each writes its
+    // part of the ring slot and arrives on the slot's full barrier.  (One warp
+    // doing both was busy ~90 % of the MXFP8 GEMM1 and held the MMA issuer
+    // back.)  W4A8: one 1x128 scale per row and K block is little work, a
+    // second writer measured 3-5 % slower, so warp 3 writes both parts.
+    const bool wa = warp == 2;
     uint32_t sslot = 0, sphase = 0;
-    auto put_slot = [&](const uint32_t (&aw)[4], const uint32_t (&bw)[8]) {
+    // lane l: 16 bytes at row l of the A block (warp 2; W4A8: aw from warp
+    // 3) or of both B blocks (warp 3)
+    auto put_slot = [&](const uint32_t (&w)[8], const uint32_t (&aw)[4]) {
       int got = 1;
       if (lane == 0)
         got = mbar_wait_bounded(sempty_bar(sslot), sphase ^ 1, abort_flag, args.limit_ns,
                                 args.err);
       got = __shfl_sync(0xffffffffu, got, 0);
       if (!got) return false;
-      // lane l: 16 bytes at row l of the A block and of both B blocks
       uint4* dst = reinterpret_cast<uint4*>(sf_ring + sslot * SF_BYTES) + lane;
-      dst[0] = make_uint4(aw[0], aw[1], aw[2], aw[3]);
-      dst[32] = make_uint4(bw[0], bw[1], bw[2], bw[3]);
-      dst[64] = make_uint4(bw[4], bw[5], bw[6], bw[7]);
+      if (wa || !MX8) dst[0] = make_uint4(aw[0], aw[1], aw[2], aw[3]);
+      if (!wa) {
+        dst[32] = make_uint4(w[0], w[1], w[2], w[3]);
+        dst[64] = make_uint4(w[4], w[5], w[6], w[7]);
+      }
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(sfull_bar(sslot));
@@ -303,10 +324,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       return true;
     };
     if constexpr (STAGED) {
-      // The weight scales of 4 K blocks x the tile's 256 rows arrive as one
-      // TMA box (row n at byte 16 n) NSTG groups ahead; the activation
-      // scales (in L2: the permute/act kernel just wrote them) are loaded to
-      // registers one group ahead.
+      // Warp 3: the weight scales of 4 K blocks x the tile's 256 rows arrive
+      // as one TMA box (row n at byte 16 n) NSTG groups ahead.  Warp 2: the
+      // activation scales (in L2: the permute/act kernel just wrote them)
+      // are loaded to registers one group ahead.
       const int ngroups = args.num_kb / 4;
       const uint64_t pol_s = l2_policy(MOE_GEMM_L2_B);
       const uint32_t stg_base = smem_u32(stg_ring);
@@ -329,75 +350,125 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         c.t += gridDim.x;
         return seek(c);
       };
-      auto stage_group = [&](const Cursor& c, int slot) {   // lane 0
-        mbar_arrive_expect_tx(stg_full(slot), STG_BYTES);
-        tma_load_2d(stg_base + slot * STG_BYTES, &tmS, stg_full(slot), 16 * c.g,
-                    c.e * N + c.n_tile * BN, pol_s);
-      };
-      auto load_a = [&](const Cursor& c, AGroup<MX8>& A) {
-        load_ascales<MX8>(A, args.a_scale, (size_t)c.m_blk * BM + lane, args.num_kb, 4 * c.g);
-      };
-      Cursor fill{(int)blockIdx.x, 0, 0, 0, 0};
-      bool fill_ok = seek(fill);
-      Cursor use = fill, anext = fill;
-      bool use_ok = fill_ok, anext_ok = fill_ok;
-      int nfill = 0, nuse = 0;
-      for (; nfill < NSTG && fill_ok; ++nfill) {
-        if (lane == 0) stage_group(fill, nfill);
-        fill_ok = step(fill);
-      }
-      AGroup<MX8> a_cur, a_nxt;
-      if (use_ok) {
-        load_a(use, a_cur);
-        anext_ok = step(anext);
-        if (anext_ok) load_a(anext, a_nxt);
-      }
+      Cursor use{(int)blockIdx.x, 0, 0, 0, 0};
+      bool use_ok = seek(use);
       bool ok = true;
-      while (use_ok && ok) {
-        const int slot = nuse % NSTG;
-        int got = 1;
-        if (lane == 0)
-          got = mbar_wait_bounded(stg_full(slot), (nuse / NSTG) & 1, abort_flag, args.limit_ns,
-                                  args.err);
-        got = __shfl_sync(0xffffffffu, got, 0);
-        if (!got) break;
-        const uint32_t stg = stg_base + slot * STG_BYTES;
-        const int n0 = use.n_tile * BN + lane;    // this lane's rows: n0 + 32 c
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          uint32_t aw[4], bw[8];
-#pragma unroll
-          for (int c = 0; c < 4; ++c) aw[c] = a_word<MX8>(a_cur, c, j);
-#pragma unroll
-          for (int c = 0; c < 8; ++c)   // rows past N (ragged last tile): 2^0
-            bw[c] = n0 + 32 * c < N ? ld_shared_u32(stg + 16 * (lane + 32 * c) + 4 * j)
-                                    : 0x7F7F7F7Fu;
-          if (!put_slot(aw, bw)) {
-            ok = false;
-            break;
-          }
-        }
-        if (!ok) break;
-        ++nuse;
-        // this warp's reads of the staging slot come before the copy that refills it
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (fill_ok) {
-          if (lane == 0) stage_group(fill, nfill % NSTG);
-          ++nfill;
-          fill_ok = step(fill);
-        }
-        use_ok = step(use);
-        a_cur = a_nxt;
-        if (anext_ok) {
+      if (wa) {
+        auto load_a = [&](const Cursor& c, AGroup<MX8>& A) {
+          load_ascales<MX8>(A, args.a_scale, (size_t)c.m_blk * BM + lane, args.num_kb, 4 * c.g);
+        };
+        Cursor anext = use;
+        bool anext_ok = use_ok;
+        AGroup<MX8> a_cur, a_nxt;
+        if (use_ok) {
+          load_a(use, a_cur);
           anext_ok = step(anext);
           if (anext_ok) load_a(anext, a_nxt);
         }
+        while (use_ok && ok) {
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            uint32_t w[8] = {}, aw[4];
+#pragma unroll
+            for (int c = 0; c < 4; ++c) aw[c] = a_word<MX8>(a_cur, c, j);
+            if (!put_slot(w, aw)) {
+              ok = false;
+              break;
+            }
+          }
+          if (!ok) break;
+          use_ok = step(use);
+          a_cur = a_nxt;
+          if (anext_ok) {
+            anext_ok = step(anext);
+            if (anext_ok) load_a(anext, a_nxt);
+          }
+        }
+      } else {
+        auto stage_group = [&](const Cursor& c, int slot) {   // lane 0
+          mbar_arrive_expect_tx(stg_full(slot), STG_BYTES);
+          if (FUSE) {   // gate rows, then the matching up rows (128-row boxes)
+            tma_load_2d(stg_base + slot * STG_BYTES, &tmS, stg_full(slot), 16 * c.g,
+                        c.e * N + c.n_tile * 128, pol_s);
+            tma_load_2d(stg_base + slot * STG_BYTES + STG_BYTES / 2, &tmS, stg_full(slot),
+                        16 * c.g, c.e * N + args.I + c.n_tile * 128, pol_s);
+          } else {
+            tma_load_2d(stg_base + slot * STG_BYTES, &tmS, stg_full(slot), 16 * c.g,
+                        c.e * N + c.n_tile * BN, pol_s);
+          }
+        };
+        Cursor fill = use;
+        bool fill_ok = use_ok;
+        int nfill = 0, nuse = 0;
+        for (; nfill < NSTG && fill_ok; ++nfill) {
+          if (lane == 0) stage_group(fill, nfill);
+          fill_ok = step(fill);
+        }
+        // W4A8: this warp also builds the A words, scales one group ahead
+        AGroup<MX8> a_cur, a_nxt;
+        Cursor anext = use;
+        bool anext_ok = use_ok;
+        auto load_a = [&](const Cursor& c, AGroup<MX8>& A) {
+          load_ascales<MX8>(A, args.a_scale, (size_t)c.m_blk * BM + lane, args.num_kb, 4 * c.g);
+        };
+        if constexpr (!MX8) {
+          if (use_ok) {
+            load_a(use, a_cur);
+            anext_ok = step(anext);
+            if (anext_ok) load_a(anext, a_nxt);
+          }
+        }
+        while (use_ok && ok) {
+          const int slot = nuse % NSTG;
+          int got = 1;
+          if (lane == 0)
+            got = mbar_wait_bounded(stg_full(slot), (nuse / NSTG) & 1, abort_flag, args.limit_ns,
+                                    args.err);
+          got = __shfl_sync(0xffffffffu, got, 0);
+          if (!got) break;
+          const uint32_t stg = stg_base + slot * STG_BYTES;
+          const int n0 = use.n_tile * BN + lane;    // this lane's rows: n0 + 32 c
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            uint32_t w[8], aw[4] = {};
+#pragma unroll
+            for (int c = 0; c < 8; ++c)   // rows past N (ragged last tile): 2^0
+              w[c] = FUSE || n0 + 32 * c < N ? ld_shared_u32(stg + 16 * (lane + 32 * c) + 4 * j)
+                                              : 0x7F7F7F7Fu;
+            if constexpr (!MX8) {
+#pragma unroll
+              for (int c = 0; c < 4; ++c) aw[c] = a_word<MX8>(a_cur, c, j);
+            }
+            if (!put_slot(w, aw)) {
+              ok = false;
+              break;
+            }
+          }
+          if (!ok) break;
+          ++nuse;
+          // this warp's reads of the staging slot come before the copy that refills it
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (fill_ok) {
+            if (lane == 0) stage_group(fill, nfill % NSTG);
+            ++nfill;
+            fill_ok = step(fill);
+          }
+          use_ok = step(use);
+          if constexpr (!MX8) {
+            a_cur = a_nxt;
+            if (anext_ok) {
+              anext_ok = step(anext);
+              if (anext_ok) load_a(anext, a_nxt);
+            }
+          }
+        }
+        // copies issued but not consumed (a wait ran out) land before the CTA exits
+        if (lane == 0)
+          for (int k = nuse; k < nfill; ++k)
+            mbar_wait_bounded(stg_full(k % NSTG), (k / NSTG) & 1, nullptr, args.limit_ns,
+                              args.err);
       }
-      // copies issued but not consumed (a wait ran out) land before the CTA exits
-      if (lane == 0)
-        for (int k = nuse; k < nfill; ++k)
-          mbar_wait_bounded(stg_full(k % NSTG), (k / NSTG) & 1, nullptr, args.limit_ns, args.err);
     } else {
       const int kq = args.num_kb * 4;            // E8M0 bytes per weight row
       const bool vec = (args.num_kb & 3) == 0;   // rows 16-byte aligned: vector loads
@@ -407,57 +478,87 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         sched_tile(sched, t, m_blk, n_tile);
         const int e = s_ids[m_blk];
         if (e < 0 || e >= args.num_experts) continue;
-        // lane l builds rows l + 32 c of A (c < 4) and of B (c < 8); B rows
-        // past N (ragged last tile) read nothing
-        const uint8_t* sb_base = args.b_scale + ((size_t)e * N + (size_t)n_tile * BN + lane) * kq;
-        const size_t sb_step = (size_t)32 * kq;                      // bytes per 32 rows
-        const int n_valid = N - n_tile * BN - lane;                  // B row c valid if 32c < this
-        // scales of 4 K blocks per load, one group of 4 in flight ahead
-        // (MXFP8 loads its 4x larger activation scales at the group's start
-        // instead: two groups of them in registers would spill)
-        auto load_group = [&](int g, AGroup<MX8>& A, uint4 (&B)[8]) {
-          const int n = args.num_kb - g;
-          if constexpr (!MX8)
-            load_ascales<MX8>(A, args.a_scale, (size_t)m_blk * BM + lane, args.num_kb, g);
-  #pragma unroll
-          for (int c = 0; c < 8; ++c) {
-            const uint32_t* pb = reinterpret_cast<const uint32_t*>(sb_base + c * sb_step) + g;
-            if (32 * c >= n_valid) {
-              B[c] = make_uint4(0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu);
-            } else if (vec) {
-              B[c] = __ldg(reinterpret_cast<const uint4*>(pb));
-            } else {
-              B[c] = make_uint4(__ldg(pb), n > 1 ? __ldg(pb + 1) : 0u, n > 2 ? __ldg(pb + 2) : 0u,
-                                n > 3 ? __ldg(pb + 3) : 0u);
-            }
-          }
-        };
+        // activation scales of 4 K blocks per load (W4A8, built by warp 3
+        // with the weight operand: one group ahead; MXFP8, warp 2: its 4x
+        // larger scales at the group's start)
         AGroup<MX8> a_cur, a_nxt;
-        uint4 b_cur[8], b_nxt[8];
-        load_group(0, a_cur, b_cur);
-        if (args.num_kb > 4) load_group(4, a_nxt, b_nxt);
-        for (int kb0 = 0; kb0 < args.num_kb && ok; kb0 += 4) {
-          if constexpr (MX8)
+        if constexpr (!MX8) {
+          load_ascales<MX8>(a_cur, args.a_scale, (size_t)m_blk * BM + lane, args.num_kb, 0);
+          if (args.num_kb > 4)
+            load_ascales<MX8>(a_nxt, args.a_scale, (size_t)m_blk * BM + lane, args.num_kb, 4);
+        }
+        if (wa) {
+          for (int kb0 = 0; kb0 < args.num_kb && ok; kb0 += 4) {
             load_ascales<MX8>(a_cur, args.a_scale, (size_t)m_blk * BM + lane, args.num_kb, kb0);
-  #pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const int kb = kb0 + j;
-            if (kb >= args.num_kb) break;
-            uint32_t aw[4], bw[8];
-  #pragma unroll
-            for (int c = 0; c < 4; ++c) aw[c] = a_word<MX8>(a_cur, c, j);
-  #pragma unroll
-            for (int c = 0; c < 8; ++c)
-              bw[c] = j == 0 ? b_cur[c].x : j == 1 ? b_cur[c].y : j == 2 ? b_cur[c].z : b_cur[c].w;
-            if (!put_slot(aw, bw)) {
-              ok = false;
-              break;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              if (kb0 + j >= args.num_kb) break;
+              uint32_t w[8] = {}, aw[4];
+#pragma unroll
+              for (int c = 0; c < 4; ++c) aw[c] = a_word<MX8>(a_cur, c, j);
+              if (!put_slot(w, aw)) {
+                ok = false;
+                break;
+              }
             }
           }
-          if constexpr (!MX8) a_cur = a_nxt;
-  #pragma unroll
-          for (int c = 0; c < 8; ++c) b_cur[c] = b_nxt[c];
-          if (kb0 + 8 < args.num_kb) load_group(kb0 + 8, a_nxt, b_nxt);
+        } else {
+          // lane l builds rows l + 32 c (c < 8) of the weight operand; rows
+          // past N (ragged last tile) read nothing.  Scales of 4 K blocks per
+          // load, one group of 4 in flight ahead.
+          const size_t row0 = FUSE ? (size_t)e * N + (size_t)n_tile * 128 + lane
+                                   : (size_t)e * N + (size_t)n_tile * BN + lane;
+          const uint8_t* sb_base = args.b_scale + row0 * kq;
+          const size_t sb_step = (size_t)32 * kq;                    // bytes per 32 rows
+          // FUSE: operand rows 128..255 are the up rows, I - 128 further on
+          const size_t sb_up = FUSE ? (size_t)(args.I - 128) * kq : 0;
+          const int n_valid = FUSE ? 256 : N - n_tile * BN - lane;   // row c valid if 32c < this
+          auto load_b = [&](int g, uint4 (&B)[8]) {
+            const int n = args.num_kb - g;
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+              const uint32_t* pb =
+                  reinterpret_cast<const uint32_t*>(sb_base + c * sb_step + (c >= 4 ? sb_up : 0)) + g;
+              if (32 * c >= n_valid) {
+                B[c] = make_uint4(0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu);
+              } else if (vec) {
+                B[c] = __ldg(reinterpret_cast<const uint4*>(pb));
+              } else {
+                B[c] = make_uint4(__ldg(pb), n > 1 ? __ldg(pb + 1) : 0u,
+                                  n > 2 ? __ldg(pb + 2) : 0u, n > 3 ? __ldg(pb + 3) : 0u);
+              }
+            }
+          };
+          uint4 b_cur[8], b_nxt[8];
+          load_b(0, b_cur);
+          if (args.num_kb > 4) load_b(4, b_nxt);
+          for (int kb0 = 0; kb0 < args.num_kb && ok; kb0 += 4) {
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              if (kb0 + j >= args.num_kb) break;
+              uint32_t w[8], aw[4] = {};
+#pragma unroll
+              for (int c = 0; c < 8; ++c)
+                w[c] = j == 0 ? b_cur[c].x : j == 1 ? b_cur[c].y : j == 2 ? b_cur[c].z : b_cur[c].w;
+              if constexpr (!MX8) {
+#pragma unroll
+                for (int c = 0; c < 4; ++c) aw[c] = a_word<MX8>(a_cur, c, j);
+              }
+              if (!put_slot(w, aw)) {
+                ok = false;
+                break;
+              }
+            }
+#pragma unroll
+            for (int c = 0; c < 8; ++c) b_cur[c] = b_nxt[c];
+            if (kb0 + 8 < args.num_kb) load_b(kb0 + 8, b_nxt);
+            if constexpr (!MX8) {
+              a_cur = a_nxt;
+              if (kb0 + 8 < args.num_kb)
+                load_ascales<MX8>(a_nxt, args.a_scale, (size_t)m_blk * BM + lane, args.num_kb,
+                                  kb0 + 8);
+            }
+          }
         }
       }
     }
@@ -530,6 +631,86 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       if (!ok) break;
       tc_fence_after();
       const size_t row = (size_t)m_blk * BM + row_in_tile;
+      if constexpr (FUSE) {
+        // Gated activation + dynamic quantisation of z (as act_mul_quant
+        // does from a stored H1): columns [0, 128) hold this row's gate sums
+        // of n-block n_tile, [128, 256) the matching up sums; each is rounded
+        // to bf16 as H1 would be, z = act(g, u) in fp32, then e4m3 codes with
+        // one scale per group of 32 (MXFP8) or 128 columns.
+        const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16);
+        const int gcol0 = n_tile * 128, ucol0 = args.I + n_tile * 128;
+        const bool bias = args.ep.bias != nullptr;
+        uint4* zdst = reinterpret_cast<uint4*>(args.zq + row * (size_t)args.I + (size_t)gcol0);
+        constexpr int ZG = MX8 ? 32 : 128;                  // quantisation group
+        float* zs_row = args.zs + row * (size_t)(args.I / ZG) + (size_t)n_tile * (128 / ZG);
+        auto zval = [&](uint32_t g, uint32_t u, int col) {
+          float gs = __uint_as_float(g), us = __uint_as_float(u);
+          if (bias) {
+            gs += epi_bias(args.ep, e, gcol0 + col);
+            us += epi_bias(args.ep, e, ucol0 + col);
+          }
+          return act_glu(args.ep, bf16_round(gs), bf16_round(us));
+        };
+        // 16 codes -> uint4; power-of-two scales: v * (1/s) is the exact quotient
+        const bool p2 = args.ue8m0 != 0;
+        auto quant16 = [&](const float* z, float sc, float rc) {
+          float qv[16];
+#pragma unroll
+          for (int b = 0; b < 16; ++b) qv[b] = p2 ? z[b] * rc : quot_rn(z[b], sc, rc);
+          return make_uint4(e4m3x4(qv[0], qv[1], qv[2], qv[3]), e4m3x4(qv[4], qv[5], qv[6], qv[7]),
+                            e4m3x4(qv[8], qv[9], qv[10], qv[11]),
+                            e4m3x4(qv[12], qv[13], qv[14], qv[15]));
+        };
+        if constexpr (MX8) {
+#pragma unroll 1
+          for (int c = 0; c < 4; ++c) {                    // one 1x32 group per chunk
+            uint32_t g[32], u[32];
+            tmem_ld_32x32b_x32(taddr + c * 32, g);
+            tmem_ld_32x32b_x32(taddr + 128 + c * 32, u);
+            tmem_ld_wait();
+            if (c == 3) {                                  // the accumulator is read
+              tc_fence_before();
+              __syncwarp();
+              if (lane == 0) mbar_arrive(tempty_bar);
+            }
+            float z[32];
+            float amax = 0.0f;
+#pragma unroll
+            for (int jj = 0; jj < 32; ++jj) {
+              z[jj] = zval(g[jj], u[jj], c * 32 + jj);
+              amax = fmaxf(amax, fabsf(z[jj]));
+            }
+            const float sc = act_scale(amax, args.ue8m0 != 0);
+            const float rc = __frcp_rn(sc);
+            zdst[2 * c] = quant16(z, sc, rc);
+            zdst[2 * c + 1] = quant16(z + 16, sc, rc);
+            zs_row[c] = sc;
+          }
+        } else {
+          float z[128];
+          float amax = 0.0f;
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            uint32_t g[32], u[32];
+            tmem_ld_32x32b_x32(taddr + c * 32, g);
+            tmem_ld_32x32b_x32(taddr + 128 + c * 32, u);
+            tmem_ld_wait();
+#pragma unroll
+            for (int jj = 0; jj < 32; ++jj) {
+              z[c * 32 + jj] = zval(g[jj], u[jj], c * 32 + jj);
+              amax = fmaxf(amax, fabsf(z[c * 32 + jj]));
+            }
+          }
+          tc_fence_before();                               // the accumulator is read
+          __syncwarp();
+          if (lane == 0) mbar_arrive(tempty_bar);
+          const float sc = act_scale(amax, args.ue8m0 != 0);
+          const float rc = __frcp_rn(sc);
+#pragma unroll
+          for (int v = 0; v < 8; ++v) zdst[v] = quant16(z + 16 * v, sc, rc);
+          zs_row[0] = sc;
+        }
+      } else {
       const float w = epi_row_weight(args.ep, row);
       const bool bias = args.ep.bias != nullptr;
 #pragma unroll 1
@@ -563,6 +744,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           }
         }
       }
+      }
       ++local;
     }
   }
@@ -579,16 +761,27 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 }  // namespace
 
 namespace {
-template <bool STAGED, bool MX8>
+template <bool STAGED, bool MX8, bool FUSE>
 void launch_form(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmS,
                  const Mx4Args& a, cudaStream_t stream) {
   static bool attr_done = false;
   if (!attr_done) {
-    cudaFuncSetAttribute(k_ggemm_mxfp4<STAGED, MX8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                         SMEM_BYTES);
+    cudaFuncSetAttribute(k_ggemm_mxfp4<STAGED, MX8, FUSE>,
+                         cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
     attr_done = true;
   }
-  k_ggemm_mxfp4<STAGED, MX8><<<num_sms(), NUM_THREADS, SMEM_BYTES, stream>>>(tmA, tmB, tmS, a);
+  k_ggemm_mxfp4<STAGED, MX8, FUSE><<<num_sms(), NUM_THREADS, SMEM_BYTES, stream>>>(tmA, tmB, tmS,
+                                                                                  a);
+}
+template <bool FUSE>
+void launch_forms(bool staged, bool mx8, const CUtensorMap& tmA, const CUtensorMap& tmB,
+                  const CUtensorMap& tmS, const Mx4Args& a, cudaStream_t stream) {
+  if (staged)
+    mx8 ? launch_form<true, true, FUSE>(tmA, tmB, tmS, a, stream)
+        : launch_form<true, false, FUSE>(tmA, tmB, tmS, a, stream);
+  else
+    mx8 ? launch_form<false, true, FUSE>(tmA, tmB, tmS, a, stream)
+        : launch_form<false, false, FUSE>(tmA, tmB, tmS, a, stream);
 }
 }  // namespace
 
@@ -596,11 +789,16 @@ cudaError_t launch_ggemm_mxfp4(const void* A, const float* a_scale, int cap, int
                                const uint8_t* b_scale, int b_rows_total, int b_rows_per_expert,
                                int n_out, const int32_t* block_expert_ids,
                                const int32_t* num_post_padded, void* out, bool b_e4m3,
-                               const Epilogue& ep, cudaStream_t stream) {
+                               const Epilogue& ep, cudaStream_t stream, float* z_scale,
+                               bool fuse_act, bool ue8m0) {
   if (cap <= 0) return cudaSuccess;
   // packed E2M1 tensor maps want 32-byte aligned bases, byte maps 16
   if ((reinterpret_cast<uintptr_t>(B) & (b_e4m3 ? 15u : 31u)) != 0 ||
       (reinterpret_cast<uintptr_t>(b_scale) & 3u))
+    return cudaErrorInvalidValue;
+  // fused GEMM1: B rows per expert = 2I (gate then up), I a multiple of 128
+  if (fuse_act && (z_scale == nullptr || b_rows_per_expert % 256 != 0 ||
+                   n_out != b_rows_per_expert))
     return cudaErrorInvalidValue;
   CUtensorMap tmA, tmB;
   if (!make_tmap_k_sw128(&tmA, A, (uint64_t)cap, (uint64_t)K, 1, 128) ||
@@ -616,7 +814,12 @@ cudaError_t launch_ggemm_mxfp4(const void* A, const float* a_scale, int cap, int
   a.out = static_cast<__nv_bfloat16*>(out);
   a.ldo = n_out;
   a.num_kb = K / BK;
-  a.n_tiles = (n_out + BN - 1) / BN;
+  a.I = b_rows_per_expert / 2;
+  // fused: one tile per 128-column block of z (gate rows j + up rows I + j)
+  a.n_tiles = fuse_act ? a.I / 128 : (n_out + BN - 1) / BN;
+  a.zq = fuse_act ? static_cast<uint8_t*>(out) : nullptr;
+  a.zs = z_scale;
+  a.ue8m0 = ue8m0 ? 1 : 0;
   a.b_rows_per_expert = b_rows_per_expert;
   a.m_blocks_cap = cap / BM;
   a.num_experts = b_rows_total / b_rows_per_expert;
@@ -627,14 +830,12 @@ cudaError_t launch_ggemm_mxfp4(const void* A, const float* a_scale, int cap, int
   const bool staged = K % 512 == 0 && (reinterpret_cast<uintptr_t>(b_scale) & 15u) == 0;
   CUtensorMap tmS = tmB;        // unused by the register form
   if (staged && !make_tmap_u8_rows(&tmS, b_scale, (uint64_t)b_rows_total, (uint64_t)(K / 32), 16,
-                                   BN))
+                                   fuse_act ? 128 : BN))
     return cudaErrorInvalidValue;
-  if (staged)
-    b_e4m3 ? launch_form<true, true>(tmA, tmB, tmS, a, stream)
-           : launch_form<true, false>(tmA, tmB, tmS, a, stream);
+  if (fuse_act)
+    launch_forms<true>(staged, b_e4m3, tmA, tmB, tmS, a, stream);
   else
-    b_e4m3 ? launch_form<false, true>(tmA, tmB, tmS, a, stream)
-           : launch_form<false, false>(tmA, tmB, tmS, a, stream);
+    launch_forms<false>(staged, b_e4m3, tmA, tmB, tmS, a, stream);
   return cudaGetLastError();
 }
 

@@ -514,17 +514,6 @@ __device__ __forceinline__ void epi_store32(const Epilogue& ep, int e, int col0,
 __device__ __forceinline__ uint8_t f32_to_e4m3(float v) {
   return static_cast<uint8_t>(__nv_cvt_float_to_fp8(v, __NV_SATFINITE, __NV_E4M3));
 }
-// v / s rounded to nearest fp32, for many v sharing one divisor s with
-// r = __frcp_rn(s): q0 = v*r is within an ulp or two of v/s, the remainder
-// v - s*q0 is exact under an FMA, and one correction step q0 + rem*r rounds to
-// the correctly rounded quotient (Markstein's division correction).  s is a
-// positive normal fp32 and v finite, so no step overflows or underflows
-// except for tiny v, whose e4m3 code is 0 either way.
-__device__ __forceinline__ float div_rn_shared(float v, float s, float r) {
-  const float q0 = v * r;
-  const float rem = fmaf(-q0, s, v);
-  return fmaf(rem, r, q0);
-}
 
 // Dynamic 1x128 scale: max(amax, 1e-10) / 448 in fp32 (IEEE division); with
 // ue8m0, rounded up to a power of two.

@@ -80,18 +80,26 @@ cudaError_t launch_ggemm_bf16_2sm(const void* A, int cap, int K, const void* B,
 
 // FP8 (e4m3) grouped GEMM with fp32 1x128 activation scales and 128x128
 // weight block scales: out = sum_kb sa*sb*partial_kb (bf16 output).
+// fuse_act (GEMM1 only, n_out = b_rows_per_expert = 2I): the gated
+// activation quantised to e4m3 codes in out [cap, I], 1x128 scales in z_scale.
 cudaError_t launch_ggemm_fp8(const void* A, const float* a_scale, int cap, int K, const void* B,
                              const float* b_scale, int b_rows_total, int b_rows_per_expert,
                              int n_out, const int32_t* block_expert_ids,
                              const int32_t* num_post_padded, void* out, const Epilogue& ep,
-                             cudaStream_t stream);
+                             cudaStream_t stream, float* z_scale = nullptr,
+                             bool fuse_act = false, bool ue8m0 = false);
 
 // MXFP4 (E2M1 + E8M0 per 32) weights x e4m3 activations with power-of-two
-// 1x128 scales, block-scaled tensor-core MMA (bf16 output).
+// 1x128 scales (or MXFP8: e4m3 weights, b_e4m3, with 1x32 scales),
+// block-scaled tensor-core MMA (bf16 output).  fuse_act (GEMM1 only, n_out =
+// b_rows_per_expert = 2I): the gated activation quantised to e4m3 codes in
+// out [cap, I] with scales in z_scale (1x128 groups, 1x32 for MXFP8).
 cudaError_t launch_ggemm_mxfp4(const void* A, const float* a_scale, int cap, int K, const void* B,
                                const uint8_t* b_scale, int b_rows_total, int b_rows_per_expert,
                                int n_out, const int32_t* block_expert_ids,
                                const int32_t* num_post_padded, void* out, bool b_e4m3,
-                               const Epilogue& ep, cudaStream_t stream);
+                               const Epilogue& ep, cudaStream_t stream,
+                               float* z_scale = nullptr, bool fuse_act = false,
+                               bool ue8m0 = true);
 
 }  // namespace moe

@@ -20,6 +20,7 @@
 // The data gather (k_permute_*) runs one warp per destination row with
 // 16-byte vector loads batched ahead of the stores; the FP8 variant fuses the
 // dynamic 1x128 quantisation.
+#include "e4m3_pack.cuh"
 #include "moe_common.cuh"
 #include "moe_internal.h"
 
@@ -312,10 +313,10 @@ __global__ void __launch_bounds__(PERMUTE_THREADS)
           uint32_t lo = 0, hi = 0;
 #pragma unroll
           for (int j = 0; j < 4; ++j)
-            lo |= (uint32_t)f32_to_e4m3(div_rn_shared(f[j], s, r)) << (8 * j);
+            lo |= (uint32_t)f32_to_e4m3(quot_rn(f[j], s, r)) << (8 * j);
 #pragma unroll
           for (int j = 0; j < 4; ++j)
-            hi |= (uint32_t)f32_to_e4m3(div_rn_shared(f[4 + j], s, r)) << (8 * j);
+            hi |= (uint32_t)f32_to_e4m3(quot_rn(f[4 + j], s, r)) << (8 * j);
           dst[v] = make_uint2(lo, hi);
           if (v % LPG == 0) srow[v / LPG] = s;
         }
@@ -331,13 +332,15 @@ __global__ void __launch_bounds__(PERMUTE_THREADS)
 // shapes).  Each lane holds 16 consecutive values (two 16-byte loads, one
 // 16-byte store of codes); LPG lanes form one quantisation group (8 lanes:
 // 1x128, 2 lanes: 1x32).  Padding rows (sorted id >= R) below the used row
-// count are zeroed by the same warps afterwards, 32 rows per ballot.
-template <int LPG>
+// count are zeroed by the same warps afterwards, 32 rows per ballot.  With
+// power-of-two scales (UE8M0) v * (1/s) is already the correctly rounded
+// quotient.
+template <int LPG, bool UE8M0>
 __global__ void __launch_bounds__(PERMUTE_THREADS)
     k_permute_fp8_tok(const __nv_bfloat16* __restrict__ x, int H, int M, int topk, int R,
                       const int32_t* __restrict__ inv_perm,
                       const int32_t* __restrict__ sorted_ids, const int32_t* __restrict__ npp,
-                      uint8_t* __restrict__ xq, float* __restrict__ xs, int ue8m0) {
+                      uint8_t* __restrict__ xq, float* __restrict__ xs) {
   constexpr int U = 2;           // 16-value chunks per lane in flight
   const int lane = threadIdx.x & 31;
   const int gw = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
@@ -375,20 +378,14 @@ __global__ void __launch_bounds__(PERMUTE_THREADS)
 #pragma unroll
         for (int o = LPG / 2; o >= 1; o >>= 1)
           amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-        const float s = act_scale(amax, ue8m0 != 0);
+        const float s = act_scale(amax, UE8M0);
         uint4 code = make_uint4(0, 0, 0, 0);
         if (act) {
           const float r = __frcp_rn(s);
-          uint32_t w[4];
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            uint32_t word = 0;
-#pragma unroll
-            for (int j = 0; j < 4; ++j)
-              word |= (uint32_t)f32_to_e4m3(div_rn_shared(f[4 * q + j], s, r)) << (8 * j);
-            w[q] = word;
-          }
-          code = make_uint4(w[0], w[1], w[2], w[3]);
+          for (int j = 0; j < 16; ++j) f[j] = UE8M0 ? f[j] * r : quot_rn(f[j], s, r);
+          code = make_uint4(e4m3x4(f[0], f[1], f[2], f[3]), e4m3x4(f[4], f[5], f[6], f[7]),
+                            e4m3x4(f[8], f[9], f[10], f[11]), e4m3x4(f[12], f[13], f[14], f[15]));
         }
         for (int i = 0; i < topk; ++i) {
           const int row = __shfl_sync(0xffffffffu, my_dst, i);
@@ -424,14 +421,20 @@ cudaError_t launch_permute_tokens(const void* x, int H, int M, int topk, int R,
   const int work = max(M, (cap + 31) / 32);
   if (work <= 0) return cudaSuccess;
   const int grid = min((work + wpc - 1) / wpc, num_sms() * 8);
-  if (group == 32)
-    k_permute_fp8_tok<2><<<grid, PERMUTE_THREADS, 0, stream>>>(
-        static_cast<const __nv_bfloat16*>(x), H, M, topk, R, inv_perm, sorted_ids,
-        num_post_padded, static_cast<uint8_t*>(x_perm), x_scale, ue8m0);
+  const auto* xp = static_cast<const __nv_bfloat16*>(x);
+  auto* q = static_cast<uint8_t*>(x_perm);
+  if (group == 32 && ue8m0)
+    k_permute_fp8_tok<2, true><<<grid, PERMUTE_THREADS, 0, stream>>>(
+        xp, H, M, topk, R, inv_perm, sorted_ids, num_post_padded, q, x_scale);
+  else if (group == 32)
+    k_permute_fp8_tok<2, false><<<grid, PERMUTE_THREADS, 0, stream>>>(
+        xp, H, M, topk, R, inv_perm, sorted_ids, num_post_padded, q, x_scale);
+  else if (ue8m0)
+    k_permute_fp8_tok<8, true><<<grid, PERMUTE_THREADS, 0, stream>>>(
+        xp, H, M, topk, R, inv_perm, sorted_ids, num_post_padded, q, x_scale);
   else
-    k_permute_fp8_tok<8><<<grid, PERMUTE_THREADS, 0, stream>>>(
-        static_cast<const __nv_bfloat16*>(x), H, M, topk, R, inv_perm, sorted_ids,
-        num_post_padded, static_cast<uint8_t*>(x_perm), x_scale, ue8m0);
+    k_permute_fp8_tok<8, false><<<grid, PERMUTE_THREADS, 0, stream>>>(
+        xp, H, M, topk, R, inv_perm, sorted_ids, num_post_padded, q, x_scale);
   return cudaGetLastError();
 }
 

@@ -125,6 +125,32 @@ def test_act_mul_quant_fp8():
         assert codes_equal > 0.999, codes_equal
 
 
+@pytest.mark.parametrize("quant,fmt", [("fp8", "fp32"), ("fp8", "ue8m0"), ("mxfp8", "ue8m0")])
+def test_act_quant_keeps_the_sign_of_zero(quant, fmt):
+    """z = SiLU(g) * u is exactly -0 where u = +0 and g < 0 (or u = -0 and
+    g > 0): its code is the negative zero 0x80, as the IEEE quotient -0 / s
+    and the oracle give; +0 gives 0x00."""
+    I, rows = 256, 64
+    g = torch.Generator().manual_seed(4)
+    h1 = (torch.randn(rows, 2 * I, generator=g) * 3).to(torch.bfloat16)
+    h1[:, I:I + 32] = 0.0                                    # u = +0
+    h1[:, I + 32:I + 64] = -0.0                              # u = -0
+    p = moe.Problem(M=rows, H=256, I=I, E=1, topk=1, quant=quant, act_scale_fmt=fmt)
+    grp = experts.act_group(quant)
+    z = torch.empty(moe.moe_m_sum_bound(p), I, dtype=torch.uint8, device="cuda")
+    zs = torch.empty(moe.moe_m_sum_bound(p), I // grp, dtype=torch.float32, device="cuda")
+    moe.act_mul_quant(p, h1.cuda(), torch.tensor([rows], dtype=torch.int32).cuda(), z, zs)
+    assert moe.moe_sync_status() == 0
+    gate = np32(h1)[:, :64]
+    want = np.where(np.concatenate([gate[:, :32] < 0, gate[:, 32:] > 0], axis=1), 0x80, 0x00)
+    zero_g = gate == 0                                      # SiLU(0) * u = +0 * u
+    got = np32(z)[:rows, :64]
+    assert np.array_equal(got[~zero_g], want[~zero_g])
+    zr = experts.act_mul(np32(h1), I)
+    q, _ = experts.quant_act_1x128(zr, fmt, grp)
+    assert np.array_equal(codecs.e4m3_encode(q[:, :64]), np.where(zero_g, got, want))
+
+
 def test_reduce_skips_invalid_slots():
     H, M, k = 1024, 77, 4
     g = torch.Generator().manual_seed(9)
