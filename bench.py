@@ -475,7 +475,10 @@ def run_ours(args):
                                "weight_hbm_frac": w2_bytes / (stage_ms["gemm2"] * 1e-3) / 1e9 /
                                peaks["hbm_gbs"]},
             "e2e": {"value": world * R / e2e_s, "unit": UNIT, "h2d_bytes_per_step": h2d,
-                    "d2h_bytes_per_step": d2h, "ms_per_step": e2e_s * 1e3},
+                    "d2h_bytes_per_step": d2h, "ms_per_step": e2e_s * 1e3,
+                    "path": "fused_experts_from_host on pinned host buffers: topk ids/weights "
+                            "copied in; x read and y written in place in host memory by the "
+                            "permute and reduce kernels (each row once, over the host link)"},
             "router": {"ms": router_ms, "bytes": router_bytes,
                        "gbs": router_bytes / (router_ms * 1e-3) / 1e9,
                        "note": "moe_topk_router on [M, E] fp32 logits (softmax, renormalise); "

@@ -337,11 +337,16 @@ moe_status fused_experts_ex(const moe_problem* p, const void* x, const void* w13
                             const float* topk_weights, const int32_t* topk_ids, void* y,
                             void* workspace, size_t workspace_bytes, void* stream);
 
-/* fused_experts fed from host memory: copies x [M,H] bf16, topk_ids and
- * topk_weights from host (pinned memory gives asynchronous copies) into the
- * staging part of `workspace`, runs fused_experts, and copies y [M,H] bf16
- * back to host_y, all on `stream`.  Weights stay device pointers.
- * workspace: >= moe_host_workspace_bytes(p) device bytes. */
+/* fused_experts fed from host memory, all on `stream`; weights stay device
+ * pointers.  topk_ids and topk_weights are copied into the staging part of
+ * `workspace`.  x [M,H] bf16 and y [M,H] bf16: when a buffer is page-locked
+ * host memory mapped for the device (cudaHostAlloc / cudaHostRegister, as
+ * torch's pin_memory gives) and 16-byte aligned, the permute kernel reads
+ * x and the reduce kernel writes y in place over the host link, each row
+ * once; otherwise x is copied in and y copied out through the workspace.
+ * host_x and host_y must stay valid and untouched until `stream` has
+ * finished this call.  workspace: >= moe_host_workspace_bytes(p) device
+ * bytes. */
 size_t moe_host_workspace_bytes(const moe_problem* p);
 moe_status fused_experts_from_host(const moe_problem* p, const void* host_x,
                                    const int32_t* host_topk_ids,

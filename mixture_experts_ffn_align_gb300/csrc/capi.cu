@@ -198,6 +198,21 @@ BatchedLayout batched_layout(const moe_problem* p, int max_tokens) {
   return L;
 }
 
+// Device address through which kernels on the current device may read and
+// write a host buffer in place: page-locked (pinned or registered) host
+// memory mapped into the device's address space, 16-byte aligned for the
+// kernels' vector accesses.  nullptr for any other memory.
+void* device_view(const void* host) {
+  cudaPointerAttributes a;
+  if (cudaPointerGetAttributes(&a, host) != cudaSuccess) {
+    cudaGetLastError();   // clear the (non-sticky) error an unregistered pointer may leave
+    return nullptr;
+  }
+  if (a.type != cudaMemoryTypeHost || a.devicePointer == nullptr) return nullptr;
+  if (reinterpret_cast<uintptr_t>(a.devicePointer) & 15u) return nullptr;
+  return a.devicePointer;
+}
+
 thread_local char g_last_error[256] = "";
 
 // Records the CUDA error of a failed call for moe_last_error_string.
@@ -265,6 +280,9 @@ moe_status moe_align_permute(const moe_problem* p, const void* x, const int32_t*
     e = launch_permute_tokens(x, p->H, p->M, p->topk, R, inv_perm, sorted_ids, num_post_padded,
                               x_perm, x_perm_scale, p->act_scale_fmt == MOE_SCALE_UE8M0,
                               act_group(p), cap, s);
+  } else if (x && !p->apply_router_weight_on_input) {
+    e = launch_permute_bf16_tokens(x, p->H, p->M, p->topk, R, inv_perm, sorted_ids,
+                                   num_post_padded, x_perm, cap, s);
   } else if (x) {
     e = launch_permute_rows(x, p->H, p->topk, R, sorted_ids, num_post_padded,
                             p->apply_router_weight_on_input ? topk_weights : nullptr, x_perm,
@@ -473,18 +491,27 @@ moe_status fused_experts_from_host(const moe_problem* p, const void* host_x,
   const size_t base = layout(p).total;
   const size_t MH = (size_t)p->M * p->H * 2, Mk = (size_t)p->M * p->topk * 4;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
-  void* d_x = ws + base;
   int32_t* d_ids = reinterpret_cast<int32_t*>(ws + base + align_up(MH));
   float* d_w = reinterpret_cast<float*>(ws + base + align_up(MH) + align_up(Mk));
-  void* d_y = ws + base + align_up(MH) + 2 * align_up(Mk);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (cudaMemcpyAsync(d_x, host_x, MH, cudaMemcpyHostToDevice, s) != cudaSuccess ||
-      cudaMemcpyAsync(d_ids, host_topk_ids, Mk, cudaMemcpyHostToDevice, s) != cudaSuccess ||
+  // x and y in page-locked host memory are read and written in place by the
+  // permute and reduce kernels (each x row is read once, each y row written
+  // once, over the host link); other host memory is staged with copies.
+  const void* x_in = device_view(host_x);
+  void* y_out = device_view(host_y);
+  void* d_x = ws + base;
+  void* d_y = ws + base + align_up(MH) + 2 * align_up(Mk);
+  if (x_in == nullptr) {
+    if (cudaMemcpyAsync(d_x, host_x, MH, cudaMemcpyHostToDevice, s) != cudaSuccess)
+      return cuda_status(cudaGetLastError());
+    x_in = d_x;
+  }
+  if (cudaMemcpyAsync(d_ids, host_topk_ids, Mk, cudaMemcpyHostToDevice, s) != cudaSuccess ||
       cudaMemcpyAsync(d_w, host_topk_weights, Mk, cudaMemcpyHostToDevice, s) != cudaSuccess)
-    return MOE_ERR_CUDA;
-  moe_status st = fused_experts(p, d_x, w13, w13_scale, w2, w2_scale, d_w, d_ids, d_y, workspace,
-                                base, stream);
-  if (st != MOE_OK) return st;
+    return cuda_status(cudaGetLastError());
+  moe_status st = fused_experts(p, x_in, w13, w13_scale, w2, w2_scale, d_w, d_ids,
+                                y_out ? y_out : d_y, workspace, base, stream);
+  if (st != MOE_OK || y_out != nullptr) return st;
   return cuda_status(cudaMemcpyAsync(host_y, d_y, MH, cudaMemcpyDeviceToHost, s));
 }
 

@@ -42,6 +42,13 @@ cudaError_t launch_permute_tokens(const void* x, int H, int M, int topk, int R,
                                   const int32_t* num_post_padded, void* x_perm, float* x_scale,
                                   bool ue8m0, int group, int cap, cudaStream_t stream);
 
+// Token-major bf16 permute (a copy of each token's row into its k rows, read
+// once); padding rows below num_post_padded are zeroed.
+cudaError_t launch_permute_bf16_tokens(const void* x, int H, int M, int topk, int R,
+                                       const int32_t* inv_perm, const int32_t* sorted_ids,
+                                       const int32_t* num_post_padded, void* x_perm, int cap,
+                                       cudaStream_t stream);
+
 // SiLU-and-mul over h1 [rows, 2I] bf16 -> z bf16, or e4m3 + scales.
 // act: the gated activation recipe (recipe / alpha / beta / limit fields).
 cudaError_t launch_act_mul(const void* h1, int I, const int32_t* num_post_padded, void* z,

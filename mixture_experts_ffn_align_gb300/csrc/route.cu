@@ -332,7 +332,7 @@ __global__ void __launch_bounds__(PERMUTE_THREADS)
 // shapes).  Each lane holds 16 consecutive values (two 16-byte loads, one
 // 16-byte store of codes); LPG lanes form one quantisation group (8 lanes:
 // 1x128, 2 lanes: 1x32).  Padding rows (sorted id >= R) below the used row
-// count are zeroed by the same warps afterwards, 32 rows per ballot.  With
+// count are zeroed by the same warps afterwards, one warp per row.  With
 // power-of-two scales (UE8M0) v * (1/s) is already the correctly rounded
 // quotient.
 template <int LPG, bool UE8M0>
@@ -396,21 +396,72 @@ __global__ void __launch_bounds__(PERMUTE_THREADS)
       }
     }
   }
-  // padding rows of the used blocks: codes and scales zero
+  // padding rows of the used blocks (one warp per row): codes and scales zero
   const int rows = *npp;
-  for (int c = gw; c * 32 < rows; c += nw) {
-    const int row = c * 32 + lane;
-    const bool pad = row < rows && sorted_ids[row] >= R;
-    unsigned m = __ballot_sync(0xffffffffu, pad);
-    while (m) {
-      const int j = __ffs(m) - 1;
-      m &= m - 1;
-      const size_t prow = (size_t)c * 32 + j;
-      uint4* dst = reinterpret_cast<uint4*>(xq + prow * H);
-      for (int v = lane; v < nv; v += 32) dst[v] = make_uint4(0, 0, 0, 0);
-      for (int g = lane; g < gpr; g += 32) xs[prow * gpr + g] = 0.0f;
+  for (int row = gw; row < rows; row += nw) {
+    if (sorted_ids[row] < R) continue;
+    uint4* dst = reinterpret_cast<uint4*>(xq + (size_t)row * H);
+    for (int v = lane; v < nv; v += 32) dst[v] = make_uint4(0, 0, 0, 0);
+    for (int g = lane; g < gpr; g += 32) xs[(size_t)row * gpr + g] = 0.0f;
+  }
+}
+
+// Token-major bf16 form: one warp per token reads its row once (16-byte
+// loads, PERMUTE_U per lane in flight) and stores it to each of its k
+// destination rows; padding rows below the used count are zeroed as in the
+// FP8 form.  The row is read exactly once, also when x lives in host memory
+// that the kernel reads in place (fused_experts_from_host).
+__global__ void __launch_bounds__(PERMUTE_THREADS)
+    k_permute_bf16_tok(const __nv_bfloat16* __restrict__ x, int H, int M, int topk, int R,
+                       const int32_t* __restrict__ inv_perm,
+                       const int32_t* __restrict__ sorted_ids, const int32_t* __restrict__ npp,
+                       __nv_bfloat16* __restrict__ xp) {
+  const int lane = threadIdx.x & 31;
+  const int gw = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  const int nw = gridDim.x * (blockDim.x >> 5);
+  const int nv = H / 8;          // 16-byte vectors per row
+  for (int t = gw; t < M; t += nw) {
+    const int my_dst = lane < topk ? inv_perm[(size_t)t * topk + lane] : -1;
+    const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)t * H);
+    for (int base = 0; base < nv; base += 32 * PERMUTE_U) {
+      uint4 buf[PERMUTE_U];
+#pragma unroll
+      for (int u = 0; u < PERMUTE_U; ++u) {
+        const int v = base + 32 * u + lane;
+        if (v < nv) buf[u] = __ldg(src + v);
+      }
+      for (int i = 0; i < topk; ++i) {
+        const int row = __shfl_sync(0xffffffffu, my_dst, i);
+        if (row < 0) continue;
+        uint4* dst = reinterpret_cast<uint4*>(xp + (size_t)row * H);
+#pragma unroll
+        for (int u = 0; u < PERMUTE_U; ++u) {
+          const int v = base + 32 * u + lane;
+          if (v < nv) dst[v] = buf[u];
+        }
+      }
     }
   }
+  const int rows = *npp;
+  for (int row = gw; row < rows; row += nw) {   // padding rows, one warp per row
+    if (sorted_ids[row] < R) continue;
+    uint4* dst = reinterpret_cast<uint4*>(xp + (size_t)row * H);
+    for (int v = lane; v < nv; v += 32) dst[v] = make_uint4(0, 0, 0, 0);
+  }
+}
+
+cudaError_t launch_permute_bf16_tokens(const void* x, int H, int M, int topk, int R,
+                                       const int32_t* inv_perm, const int32_t* sorted_ids,
+                                       const int32_t* num_post_padded, void* x_perm, int cap,
+                                       cudaStream_t stream) {
+  const int wpc = PERMUTE_THREADS / 32;
+  const int work = max(M, cap);
+  if (work <= 0) return cudaSuccess;
+  const int grid = min((work + wpc - 1) / wpc, num_sms() * 8);
+  k_permute_bf16_tok<<<grid, PERMUTE_THREADS, 0, stream>>>(
+      static_cast<const __nv_bfloat16*>(x), H, M, topk, R, inv_perm, sorted_ids,
+      num_post_padded, static_cast<__nv_bfloat16*>(x_perm));
+  return cudaGetLastError();
 }
 
 cudaError_t launch_permute_tokens(const void* x, int H, int M, int topk, int R,
@@ -418,7 +469,7 @@ cudaError_t launch_permute_tokens(const void* x, int H, int M, int topk, int R,
                                   const int32_t* num_post_padded, void* x_perm, float* x_scale,
                                   bool ue8m0, int group, int cap, cudaStream_t stream) {
   const int wpc = PERMUTE_THREADS / 32;
-  const int work = max(M, (cap + 31) / 32);
+  const int work = max(M, cap);
   if (work <= 0) return cudaSuccess;
   const int grid = min((work + wpc - 1) / wpc, num_sms() * 8);
   const auto* xp = static_cast<const __nv_bfloat16*>(x);

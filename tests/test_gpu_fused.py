@@ -88,6 +88,16 @@ def test_fused_experts_inplace_and_host_entry():
     moe.fused_experts_from_host(p, hx, hid, hw, hy, d["w13"], None, d["w2"], None, ws)
     assert moe.moe_sync_status() == 0
     assert torch.equal(hy, y.cpu())
+    # pageable host buffers take the staged-copy path; a pinned x with a
+    # pageable y mixes the two
+    px, py = d["x"].cpu(), torch.zeros_like(hx)
+    moe.fused_experts_from_host(p, px, hid, hw, py, d["w13"], None, d["w2"], None, ws)
+    assert moe.moe_sync_status() == 0
+    assert torch.equal(py, y.cpu())
+    py2 = torch.zeros_like(hx)
+    moe.fused_experts_from_host(p, hx, hid, hw, py2, d["w13"], None, d["w2"], None, ws)
+    assert moe.moe_sync_status() == 0
+    assert torch.equal(py2, y.cpu())
 
 
 @pytest.mark.parametrize("name", ["mixtral"])
