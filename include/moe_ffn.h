@@ -300,6 +300,38 @@ moe_status grouped_gemm_w2(const moe_problem* p, const void* z, const float* z_s
 moe_status unpermute_reduce(const moe_problem* p, const void* y2, const int32_t* inv_perm,
                             const float* topk_weights, void* y, void* stream);
 
+/* Stages 4 and 5 in K slices (decode-sized bf16 problems; no counterpart on
+ * the pages, which run one program per output block).  With few routed rows
+ * per expert, GEMM2's 128 x 256 output tiles (used blocks x H/256) number
+ * fewer than the SMs; cutting K into `splits` slices gives every SM work.
+ *  - moe_gemm2_splits(p): the slice count fused_experts uses for p on the
+ *    current device: 1 (no slicing: bf16 SM-pair form, quantised modes,
+ *    H % 256 != 0, or enough tiles) up to 8.  0 for an invalid problem.
+ *  - moe_gemm2_partial_bytes(p, splits): bytes of `partial`,
+ *    splits * M * topk * H * 4.
+ *  - grouped_gemm_w2_split: z [S,I] bf16 (MOE_Q_BF16 only, as from
+ *    grouped_gemm_w13 with fuse_act), w2 [E,H,I], block ids,
+ *    num_post_padded and sorted_ids from moe_align_permute; writes the fp32
+ *    sums of slice s for routed item r = sorted_ids[row] < M*topk at
+ *    partial[(s * M*topk + r) * H + h] (padding rows are not written).
+ *    `splits` must be one that leaves no slice empty, as moe_gemm2_splits
+ *    returns (else MOE_ERR_INVALID_ARG); splits == 1 is allowed.
+ *  - unpermute_reduce_split: y[t,:] = bf16( sum_i w[t,i] * bf16( sum_s
+ *    partial[s, t*topk+i, :] ) ), fp32, slices and slots in order; slots
+ *    with inv_perm < 0 are skipped.  The bf16 rounding of the slice sum is
+ *    the rounding of the stored Y2 of the unsliced form.  Not for
+ *    apply_router_weight_on_input or router_weight_in_gemm2
+ *    (MOE_ERR_INVALID_ARG). */
+int moe_gemm2_splits(const moe_problem* p);
+size_t moe_gemm2_partial_bytes(const moe_problem* p, int splits);
+moe_status grouped_gemm_w2_split(const moe_problem* p, const void* z, const void* w2,
+                                 const int32_t* block_expert_ids,
+                                 const int32_t* num_post_padded, const int32_t* sorted_ids,
+                                 int splits, float* partial, void* stream);
+moe_status unpermute_reduce_split(const moe_problem* p, const float* partial, int splits,
+                                  const int32_t* inv_perm, const float* topk_weights, void* y,
+                                  void* stream);
+
 /* All five stages (page 1, FusedMoEKernelModularImpl.apply: prepare ->
  * experts -> finalize; inplace when y == x, page "fused_moe.py 分析",
  * "对外入口").  Weights as described for moe_quant; w13_scale/w2_scale NULL

@@ -32,7 +32,8 @@ EXPORTS = ["moe_m_sum_bound", "moe_align_workspace_bytes", "moe_workspace_bytes"
            "moe_debug_set_bf16_gemm_form",
            "moe_align_permute_noalloc", "moe_last_error_string", "moe_topk_router",
            "moe_batched_workspace_bytes", "fused_experts_batched", "grouped_gemm_w13_ex",
-           "grouped_gemm_w2_ex", "fused_experts_ex"]
+           "grouped_gemm_w2_ex", "fused_experts_ex", "moe_gemm2_splits",
+           "moe_gemm2_partial_bytes", "grouped_gemm_w2_split", "unpermute_reduce_split"]
 
 NOALLOC_SCRATCH_BYTES = 1 << 20   # MOE_NOALLOC_SCRATCH_BYTES in include/moe_ffn.h
 
@@ -116,6 +117,10 @@ def lib() -> ctypes.CDLL:
         L.grouped_gemm_w13_ex.argtypes = [P, vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, vp]
         L.grouped_gemm_w2_ex.argtypes = [P, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
         L.fused_experts_ex.argtypes = [P] + [vp] * 11 + [sz, vp]
+        L.moe_gemm2_splits.argtypes, L.moe_gemm2_splits.restype = [P], i32
+        L.moe_gemm2_partial_bytes.argtypes, L.moe_gemm2_partial_bytes.restype = [P, i32], sz
+        L.grouped_gemm_w2_split.argtypes = [P, vp, vp, vp, vp, vp, i32, vp, vp]
+        L.unpermute_reduce_split.argtypes = [P, vp, i32, vp, vp, vp, vp]
         L.moe_status_string.argtypes, L.moe_status_string.restype = [i32], ctypes.c_char_p
         L.moe_last_error_string.argtypes, L.moe_last_error_string.restype = [], ctypes.c_char_p
         L.moe_debug_set_watchdog.argtypes, L.moe_debug_set_watchdog.restype = \
@@ -125,7 +130,8 @@ def lib() -> ctypes.CDLL:
         for n in ("moe_align_permute", "grouped_gemm_w13", "act_mul_quant", "grouped_gemm_w2",
                   "unpermute_reduce", "fused_experts", "fused_experts_from_host",
                   "moe_sync_status", "moe_topk_router", "fused_experts_batched",
-                  "grouped_gemm_w13_ex", "grouped_gemm_w2_ex", "fused_experts_ex"):
+                  "grouped_gemm_w13_ex", "grouped_gemm_w2_ex", "fused_experts_ex",
+                  "grouped_gemm_w2_split", "unpermute_reduce_split"):
             getattr(L, n).restype = i32
         _lib = L
     return _lib
@@ -295,6 +301,27 @@ def fused_experts_from_host(p: Problem, host_x, host_topk_ids, host_topk_weights
         _p(w13_scale), _p(w2), _p(w2_scale), _p(workspace),
         workspace.numel() * workspace.element_size(), _stream(stream)),
         "fused_experts_from_host")
+
+
+def moe_gemm2_splits(p: Problem) -> int:
+    return int(lib().moe_gemm2_splits(_cp(p)))
+
+
+def moe_gemm2_partial_bytes(p: Problem, splits: int) -> int:
+    return int(lib().moe_gemm2_partial_bytes(_cp(p), int(splits)))
+
+
+def grouped_gemm_w2_split(p: Problem, z, w2, block_expert_ids, num_post_padded, sorted_ids,
+                          splits, partial, stream=None):
+    _check(lib().grouped_gemm_w2_split(
+        _cp(p), _p(z), _p(w2), _p(block_expert_ids), _p(num_post_padded), _p(sorted_ids),
+        int(splits), _p(partial), _stream(stream)), "grouped_gemm_w2_split")
+
+
+def unpermute_reduce_split(p: Problem, partial, splits, inv_perm, topk_weights, y, stream=None):
+    _check(lib().unpermute_reduce_split(
+        _cp(p), _p(partial), int(splits), _p(inv_perm), _p(topk_weights), _p(y),
+        _stream(stream)), "unpermute_reduce_split")
 
 
 def moe_sync_status(stream=None) -> int:

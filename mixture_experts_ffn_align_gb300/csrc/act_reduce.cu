@@ -237,6 +237,62 @@ __global__ void __launch_bounds__(REDUCE_THREADS)
   }
 }
 
+// Split-K form: GEMM2 left one fp32 partial per K slice for every routed
+// item r = t * k + i (part[(s * R + r) * H + col]).  Each (token, 256-column
+// segment) is one warp's work item, lane l owning 8 columns: the slices are
+// summed in order, rounded to bf16 where Y2 would have been stored, and the
+// weighted sum over the slots runs in fp32 as in k_unpermute_reduce.
+__global__ void __launch_bounds__(REDUCE_THREADS)
+    k_unpermute_reduce_split(const float* __restrict__ part, int S, int H, int M, int topk,
+                             const int32_t* __restrict__ inv_perm, const float* __restrict__ w,
+                             __nv_bfloat16* __restrict__ y) {
+  const int lane = threadIdx.x & 31;
+  const int gw = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  const int nw = gridDim.x * (blockDim.x >> 5);
+  const int segs = H / 256;
+  const size_t R = (size_t)M * topk;
+  for (int item = gw; item < M * segs; item += nw) {
+    const int t = item / segs, col = (item - t * segs) * 256 + lane * 8;
+    float acc[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) acc[j] = 0.0f;
+    for (int i = 0; i < topk; ++i) {
+      const size_t r = (size_t)t * topk + i;
+      if (__ldg(inv_perm + r) < 0) continue;       // skipped slot (same for the whole warp)
+      const float wi = __ldg(w + r);
+      float v[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) v[j] = 0.0f;
+      for (int sl = 0; sl < S; ++sl) {
+        const float4* src = reinterpret_cast<const float4*>(part + (sl * R + r) * H + col);
+        const float4 a = __ldg(src), b = __ldg(src + 1);
+        v[0] += a.x; v[1] += a.y; v[2] += a.z; v[3] += a.w;
+        v[4] += b.x; v[5] += b.y; v[6] += b.z; v[7] += b.w;
+      }
+#pragma unroll
+      for (int j = 0; j < 8; ++j) acc[j] = fmaf(wi, bf16_round(v[j]), acc[j]);
+    }
+    uint4 o;
+    __nv_bfloat16* ob = reinterpret_cast<__nv_bfloat16*>(&o);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) ob[j] = __float2bfloat16_rn(acc[j]);
+    *reinterpret_cast<uint4*>(y + (size_t)t * H + col) = o;
+  }
+}
+
+cudaError_t launch_unpermute_reduce_split(const float* part, int splits, int H, int M, int topk,
+                                          const int32_t* inv_perm, const float* topk_weights,
+                                          void* y, cudaStream_t stream) {
+  if (M <= 0) return cudaSuccess;
+  if (H % 256 != 0 || splits < 1) return cudaErrorInvalidValue;
+  const int wpc = REDUCE_THREADS / 32;
+  const int items = M * (H / 256);
+  const int grid = min((items + wpc - 1) / wpc, num_sms() * 8);
+  k_unpermute_reduce_split<<<grid, REDUCE_THREADS, 0, stream>>>(
+      part, splits, H, M, topk, inv_perm, topk_weights, static_cast<__nv_bfloat16*>(y));
+  return cudaGetLastError();
+}
+
 cudaError_t launch_unpermute_reduce(const void* y2, int H, int M, int topk,
                                     const int32_t* inv_perm, const float* topk_weights,
                                     bool unit_weights, void* y, cudaStream_t stream) {

@@ -125,8 +125,39 @@ size_t cap_rows(const moe_problem* p) {
   return (raw + A - 1) / A * A;
 }
 
+// K slices of the bf16 GEMM2 in fused_experts.  With few routed rows per
+// expert (decode) its 128 x 256 tiles -- the used blocks x H / 256 -- number
+// fewer than the SMs, and each SM streams weights at a bounded rate, so SMs
+// would sit idle; cutting K s ways makes s x tiles work units.  s in [1, 8]
+// minimises the rounds per unit of work, ceil(tiles s / SMs) / s, on the
+// expected block count (every expert that receives rows fills its blocks
+// evenly).  1 for the SM-pair form, the quantised modes and H % 256 != 0.
+int gemm2_splits(const moe_problem* p) {
+  if (p->quant != MOE_Q_BF16 || p->H % 256 != 0 || g_bf16_form == 2) return 1;
+  const int64_t R = (int64_t)p->M * p->topk;
+  if (R <= 0 || (g_bf16_form == 0 && R / p->E >= 2 * 128)) return 1;
+  const int64_t experts = std::min<int64_t>(p->E, R);
+  const int64_t blocks = experts * ((R / experts + 127) / 128);
+  const int64_t tiles = blocks * (p->H / 256);
+  const int64_t sms = num_sms();
+  if (tiles >= sms) return 1;
+  int best = 1;
+  double best_cost = 1.0;
+  for (int sp = 2; sp <= 8; ++sp) {
+    const double cost = (double)((tiles * sp + sms - 1) / sms) / sp;
+    if (cost < best_cost - 1e-9) {
+      best = sp;
+      best_cost = cost;
+    }
+  }
+  // slices of whole 64-deep K steps, none empty: the count the GEMM runs
+  const int num_kb = p->I / 64;
+  const int per = (num_kb + best - 1) / best;
+  return (num_kb + per - 1) / per;
+}
+
 struct Layout {
-  size_t hist, sorted, blocks, offsets, npp, inv, xperm, xscale, h1, z, zscale, y2, total;
+  size_t hist, sorted, blocks, offsets, npp, inv, xperm, xscale, h1, z, zscale, y2, part, total;
 };
 
 Layout layout(const moe_problem* p) {
@@ -156,6 +187,9 @@ Layout layout(const moe_problem* p) {
   L.h1 = p->quant == MOE_Q_FP8_BLOCK128 ? take(cap * 2 * I * 2) : 0;
   L.z = take(cap * I * (quantised(p) ? 1 : 2));
   L.zscale = quantised(p) ? take(cap * (I / act_group(p)) * 4) : 0;
+  // split-K GEMM2 partials: fp32 per K slice and routed item
+  const int sp = gemm2_splits(p);
+  L.part = sp > 1 ? take((size_t)sp * R * H * 4) : 0;
   L.total = o;
   return L;
 }
@@ -305,9 +339,11 @@ cudaError_t launch_bf16_gemm(int64_t rows_per_expert, const void* A, int cap, in
                              const int32_t* block_expert_ids, const int32_t* num_post_padded,
                              void* out, bool fuse_act, const Epilogue& ep, cudaStream_t s) {
   const bool pairs = g_bf16_form == 2 || (g_bf16_form == 0 && rows_per_expert >= 2 * 128);
-  return (pairs ? launch_ggemm_bf16_2sm : launch_ggemm_bf16)(
-      A, cap, K, B, b_rows_total, b_rows_per_expert, n_out, block_expert_ids, num_post_padded,
-      out, fuse_act, ep, s);
+  if (pairs)
+    return launch_ggemm_bf16_2sm(A, cap, K, B, b_rows_total, b_rows_per_expert, n_out,
+                                 block_expert_ids, num_post_padded, out, fuse_act, ep, s);
+  return launch_ggemm_bf16(A, cap, K, B, b_rows_total, b_rows_per_expert, n_out,
+                           block_expert_ids, num_post_padded, out, fuse_act, ep, s);
 }
 }  // namespace
 
@@ -418,6 +454,44 @@ moe_status unpermute_reduce(const moe_problem* p, const void* y2, const int32_t*
                                              unit, y, static_cast<cudaStream_t>(stream)));
 }
 
+int moe_gemm2_splits(const moe_problem* p) { return valid_problem(p) ? gemm2_splits(p) : 0; }
+
+size_t moe_gemm2_partial_bytes(const moe_problem* p, int splits) {
+  if (!valid_problem(p) || splits < 1) return 0;
+  return (size_t)splits * p->M * p->topk * p->H * 4;
+}
+
+moe_status grouped_gemm_w2_split(const moe_problem* p, const void* z, const void* w2,
+                                 const int32_t* block_expert_ids,
+                                 const int32_t* num_post_padded, const int32_t* sorted_ids,
+                                 int splits, float* partial, void* stream) {
+  if (!valid_problem(p) || p->quant != MOE_Q_BF16 || p->H % 256 != 0) return MOE_ERR_INVALID_ARG;
+  if (p->M == 0) return MOE_OK;
+  if (!z || !w2 || !block_expert_ids || !num_post_padded || !sorted_ids || !partial ||
+      splits < 1 || splits > p->I / 64)
+    return MOE_ERR_INVALID_ARG;
+  if (!gemm_supported(p)) return MOE_ERR_UNSUPPORTED;
+  const Epilogue ep = make_epilogue(p, nullptr, p->H, nullptr, nullptr);
+  const cudaError_t e = launch_ggemm_bf16(z, (int)cap_rows(p), p->I, w2, p->E * p->H, p->H, p->H,
+                                          block_expert_ids, num_post_padded, nullptr, false, ep,
+                                          static_cast<cudaStream_t>(stream), splits, partial,
+                                          sorted_ids, p->M * p->topk);
+  return e == cudaErrorInvalidValue ? MOE_ERR_INVALID_ARG : cuda_status(e);
+}
+
+moe_status unpermute_reduce_split(const moe_problem* p, const float* partial, int splits,
+                                  const int32_t* inv_perm, const float* topk_weights, void* y,
+                                  void* stream) {
+  if (!valid_problem(p) || p->H % 256 != 0 || p->apply_router_weight_on_input ||
+      p->router_weight_in_gemm2)
+    return MOE_ERR_INVALID_ARG;
+  if (p->M == 0) return MOE_OK;
+  if (!partial || !inv_perm || !topk_weights || !y || splits < 1) return MOE_ERR_INVALID_ARG;
+  return cuda_status(launch_unpermute_reduce_split(partial, splits, p->H, p->M, p->topk, inv_perm,
+                                                   topk_weights, y,
+                                                   static_cast<cudaStream_t>(stream)));
+}
+
 moe_status fused_experts_ex(const moe_problem* p, const void* x, const void* w13,
                             const void* w13_scale, const void* w13_bias, const void* w2,
                             const void* w2_scale, const void* w2_bias,
@@ -440,6 +514,18 @@ moe_status fused_experts_ex(const moe_problem* p, const void* x, const void* w13
                                     ws + L.xperm, quantised(p) ? f32(L.xscale) : nullptr,
                                     ws + L.hist, L.sorted - L.hist, stream);
   if (st != MOE_OK) return st;
+  const int splits = gemm2_splits(p);
+  if (!quantised(p) && splits > 1 && !w2_bias && !p->router_weight_in_gemm2 &&
+      !p->apply_router_weight_on_input) {
+    // decode-sized: GEMM2 in K slices over all SMs, the reduce sums them
+    st = grouped_gemm_w13_ex(p, ws + L.xperm, nullptr, w13, nullptr, w13_bias, blocks, npp,
+                             ws + L.z, nullptr, 1, stream);
+    if (st != MOE_OK) return st;
+    st = grouped_gemm_w2_split(p, ws + L.z, w2, blocks, npp, sorted, splits, f32(L.part),
+                               stream);
+    if (st != MOE_OK) return st;
+    return unpermute_reduce_split(p, f32(L.part), splits, inv, topk_weights, y, stream);
+  }
   if (!quantised(p)) {
     st = grouped_gemm_w13_ex(p, ws + L.xperm, nullptr, w13, nullptr, w13_bias, blocks, npp,
                              ws + L.z, nullptr, 1, stream);

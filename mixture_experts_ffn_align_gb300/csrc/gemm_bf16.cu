@@ -60,6 +60,14 @@ struct GemmArgs {
   int never_arrive;
   int* err;
   Epilogue ep;            // bias, router weight, activation recipe
+  // split-K (GEMM2 when its tiles would leave SMs idle): unit u is K slice
+  // u % splits of tile u / splits; part != nullptr stores each live row's raw
+  // fp32 sums at part[(slice * part_R + routed item) * ldo + column]
+  int splits;
+  int kb_per_split;
+  float* part;
+  const int32_t* part_ids;   // row -> routed item (sorted ids); >= part_R: padding
+  int part_R;
 };
 
 template <bool FUSE>
@@ -116,7 +124,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   // never walk past the buffers, whatever the routing wrote
   const int nb_valid =
       min(min(*args.num_post_padded / BM, args.m_blocks_cap), kSchedMaxBlocks);
-  const int total = nb_valid * args.n_tiles;
+  const int total = nb_valid * args.n_tiles * args.splits;   // work units
   TileSched sched;
   sched.nruns = sched_build(args.block_expert_ids, nb_valid, s_ids, s_runs, s_nruns);
   sched.runs = s_runs;
@@ -130,14 +138,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     uint32_t stage = 0, phase = 0;
     uint32_t issued_mask = 0, issued_parity = 0;
     bool skip_first = args.never_arrive != 0;
-    for (int t = blockIdx.x; t < total; t += gridDim.x) {
+    for (int u = blockIdx.x; u < total; u += gridDim.x) {
+      const int t = u / args.splits, ks = u - t * args.splits;
       int m_blk, n_tile;
       sched_tile(sched, t, m_blk, n_tile);
       const int e = s_ids[m_blk];
       if (e < 0 || e >= args.num_experts) continue;
       const int brow = e * args.b_rows_per_expert + n_tile * args.n_tile_rows;
+      const int kb0 = ks * args.kb_per_split;
+      const int kb1 = min(args.num_kb, kb0 + args.kb_per_split);
       bool ok = true;
-      for (int kb = 0; kb < args.num_kb; ++kb) {
+      for (int kb = kb0; kb < kb1; ++kb) {
         if (!mbar_wait_bounded(empty_bar(stage), phase ^ 1, abort_flag, args.limit_ns, args.err)) {
           ok = false;
           break;
@@ -171,7 +182,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     constexpr uint32_t idesc = make_idesc(kFmtBF16, kFmtBF16, BM, BN);
     uint32_t stage = 0, phase = 0;
     int local = 0;
-    for (int t = blockIdx.x; t < total; t += gridDim.x) {
+    for (int u = blockIdx.x; u < total; u += gridDim.x) {
+      const int t = u / args.splits, ks = u - t * args.splits;
       int m_blk, n_tile;
       sched_tile(sched, t, m_blk, n_tile);
       const int e = s_ids[m_blk];
@@ -181,8 +193,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       if (!mbar_wait_bounded(tempty_bar(acc), acc_phase ^ 1, abort_flag, args.limit_ns, args.err)) break;
       tc_fence_after();
       const uint32_t d_tmem = tmem_base + acc * BN;
+      const int kb0 = ks * args.kb_per_split;
+      const int kb1 = min(args.num_kb, kb0 + args.kb_per_split);
       bool ok = true;
-      for (int kb = 0; kb < args.num_kb; ++kb) {
+      for (int kb = kb0; kb < kb1; ++kb) {
         if (!mbar_wait_bounded(full_bar(stage), phase, abort_flag, args.limit_ns, args.err)) {
           ok = false;
           break;
@@ -195,7 +209,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         for (int k = 0; k < BK / 16; ++k) {
           // +32 bytes along K inside the 128-byte swizzled row = +2 in the
           // (address >> 4) field of the descriptor
-          umma_f16(d_tmem, adesc + 2 * k, bdesc + 2 * k, idesc, (kb | k) != 0);
+          umma_f16(d_tmem, adesc + 2 * k, bdesc + 2 * k, idesc, (kb != kb0) || k != 0);
         }
         tc_commit(empty_bar(stage));
         if (++stage == STAGES) {
@@ -215,7 +229,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const int q = warp & 3;   // TMEM lane quadrant this warp may access
     const int row_in_tile = q * 32 + lane;
     int local = 0;
-    for (int t = blockIdx.x; t < total; t += gridDim.x) {
+    for (int u = blockIdx.x; u < total; u += gridDim.x) {
+      const int t = u / args.splits, ks = u - t * args.splits;
       int m_blk, n_tile;
       sched_tile(sched, t, m_blk, n_tile);
       const int e = s_ids[m_blk];
@@ -240,6 +255,24 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           tmem_ld_wait();
           epi_glu_store32(args.ep, e, gcol + c * 32, args.ldo + gcol + c * 32, g, u,
                           out_row + c * 32);
+        }
+      } else if (args.part != nullptr) {
+        // split-K slice: raw fp32 sums of live rows, by routed item
+        const int item = args.part_ids[row];
+        float* prow = args.part + ((size_t)ks * args.part_R + (item < args.part_R ? item : 0)) *
+                                      args.ldo + (size_t)n_tile * BN;
+#pragma unroll 1
+        for (int c = 0; c < BN / 32; ++c) {
+          uint32_t r[32];
+          tmem_ld_32x32b_x32(taddr + c * 32, r);
+          tmem_ld_wait();
+          if (item < args.part_R) {
+            float4* d4 = reinterpret_cast<float4*>(prow + c * 32);
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+              d4[j] = make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
+                                  __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
+          }
         }
       } else {
         const float w = epi_row_weight(args.ep, row);
@@ -345,8 +378,13 @@ bool make_tmap_u8_rows(CUtensorMap* map, const void* base, uint64_t rows, uint64
 cudaError_t launch_ggemm_bf16(const void* A, int cap, int K, const void* B, int b_rows_total,
                               int b_rows_per_expert, int n_out, const int32_t* block_expert_ids,
                               const int32_t* num_post_padded, void* out, bool fuse_act,
-                              const Epilogue& ep, cudaStream_t stream) {
+                              const Epilogue& ep, cudaStream_t stream, int splits, float* part,
+                              const int32_t* part_ids, int part_R) {
   if (cap <= 0) return cudaSuccess;
+  // partial mode (part != nullptr): fp32 slice sums instead of bf16 out
+  if ((part != nullptr && (fuse_act || part_ids == nullptr || part_R <= 0)) ||
+      (part == nullptr && (splits > 1 || out == nullptr)))
+    return cudaErrorInvalidValue;
   CUtensorMap tmA, tmB;
   if (!make_tmap_k_sw128(&tmA, A, (uint64_t)cap, (uint64_t)K, 2, 128) ||
       !make_tmap_k_sw128(&tmB, B, (uint64_t)b_rows_total, (uint64_t)K, 2, 128))
@@ -377,6 +415,15 @@ cudaError_t launch_ggemm_bf16(const void* A, int cap, int K, const void* B, int 
   watchdog_params(&a.limit_ns, &a.never_arrive);
   a.err = dev_error_word();
   a.ep = ep;
+  // K slices of kb_per_split steps each; the caller sizes and reads the
+  // partials by `splits`, so a count that would leave a slice empty is an
+  // error rather than silently reduced
+  a.splits = splits > 1 ? splits : 1;
+  a.kb_per_split = (a.num_kb + a.splits - 1) / a.splits;
+  if ((a.num_kb + a.kb_per_split - 1) / a.kb_per_split != a.splits) return cudaErrorInvalidValue;
+  a.part = part;
+  a.part_ids = part_ids;
+  a.part_R = part_R;
   const int grid = num_sms();
   if (fuse_act) {
     static bool attr_done = false;

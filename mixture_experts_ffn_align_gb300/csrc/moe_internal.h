@@ -74,10 +74,23 @@ cudaError_t launch_topk_router(const void* logits, bool bf16, int M, int E, int 
 
 // bf16 grouped GEMM on tcgen05: out[row, n] = sum_k A[row, k] * B[e*b_rows + n, k].
 //   fuse_act: B tile = 128 gate rows + 128 up rows; writes SiLU(g)*u (bf16).
+//   part != nullptr (not with fuse_act): K is cut into `splits` slices (a
+//   count that would leave a slice empty is an error) and each live row's
+//   fp32 slice sums go to part[(slice * part_R + part_ids[row]) * n_out + n]
+//   instead of out.
 cudaError_t launch_ggemm_bf16(const void* A, int cap, int K, const void* B, int b_rows_total,
                               int b_rows_per_expert, int n_out, const int32_t* block_expert_ids,
                               const int32_t* num_post_padded, void* out, bool fuse_act,
-                              const Epilogue& ep, cudaStream_t stream);
+                              const Epilogue& ep, cudaStream_t stream, int splits = 1,
+                              float* part = nullptr, const int32_t* part_ids = nullptr,
+                              int part_R = 0);
+
+// Weighted top-k reduce of split-K GEMM2 partials: y[t, :] = bf16( sum_i w[t,i] *
+// bf16( sum_s part[s, t*k + i, :] ) ), fp32, slots and slices in order; slots
+// with inv_perm < 0 are skipped.  H % 256 == 0.
+cudaError_t launch_unpermute_reduce_split(const float* part, int splits, int H, int M, int topk,
+                                          const int32_t* inv_perm, const float* topk_weights,
+                                          void* y, cudaStream_t stream);
 // The same GEMM issued on SM pairs (cta_group::2, 256 x 256 tiles).
 cudaError_t launch_ggemm_bf16_2sm(const void* A, int cap, int K, const void* B,
                                   int b_rows_total, int b_rows_per_expert, int n_out,

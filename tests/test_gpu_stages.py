@@ -100,6 +100,84 @@ def test_stages_bf16_ragged(counts, H, I, fuse, form):
                 allow=flip_allowance(ref["y"], items, np32(d["w"])))
 
 
+SPLIT_CASES = [  # (counts, H, I, topk): ragged loads, top-1 and top-3 with skipped slots
+    ([0, 1, 127, 128, 129, 300], 256, 512, 1),
+    ([16, 16, 16, 16, 16, 16, 16, 16], 512, 896, 1),
+    (None, 512, 640, 3),
+]
+
+
+@pytest.mark.parametrize("counts,H,I,topk", SPLIT_CASES)
+def test_gemm2_split_k_stages(counts, H, I, topk):
+    """GEMM2 in K slices: each live routed item's slice sums add up to its
+    fp32 GEMM2 row (isolated on the GPU's own z), the sliced reduce matches
+    the oracle's reduce of the bf16-rounded sums, and both match the unsliced
+    stages; every slice count from 1 to the K steps that leaves no slice
+    empty is accepted, others are rejected."""
+    if counts is None:           # top-3, random experts, a quarter of the slots skipped
+        g = torch.Generator().manual_seed(2)
+        M, E = 40, 6
+        ids = torch.randint(0, E, (M, topk), generator=g, dtype=torch.int32)
+        ids[torch.rand(M, topk, generator=g) < 0.25] = -1
+        d = _ragged_problem([1] * E, H, I, seed=3)
+        d.update(ids=ids, M=M, x=torch.randn(M, H, generator=g).to(torch.bfloat16),
+                 w=torch.rand(M, topk, generator=g))
+    else:
+        d = _ragged_problem(counts, H, I, seed=5)
+    p = moe.Problem(M=d["M"], H=H, I=I, E=d["E"], topk=topk)
+    b = moe.stage_buffers(p)
+    dev = {k: v.cuda() for k, v in d.items() if isinstance(v, torch.Tensor)}
+    moe.moe_align_permute(p, dev["x"], dev["ids"], None, b["sorted_ids"], b["block_expert_ids"],
+                          b["expert_offsets"], b["num_post_padded"], b["inv_perm"], b["x_perm"],
+                          None, b["align_ws"])
+    moe.grouped_gemm_w13(p, b["x_perm"], None, dev["w13"], None, b["block_expert_ids"],
+                         b["num_post_padded"], b["z"], None, fuse_act=True)
+    moe.grouped_gemm_w2(p, b["z"], None, dev["w2"], None, b["block_expert_ids"],
+                        b["num_post_padded"], b["y2"])
+    moe.unpermute_reduce(p, b["y2"], b["inv_perm"], dev["w"], b["y"])
+    assert moe.moe_sync_status() == 0
+    ids = d["ids"].numpy()
+    route = routing.align_permute(ids, d["E"], 128)
+    n = route["num_tokens_post_padded"]
+    R = d["M"] * topk
+    sid = route["sorted_token_ids"][:n]
+    live = sid < R
+    zg = np.zeros((len(route["sorted_token_ids"]), I))
+    zg[:n] = np32(b["z"])[:n]
+    y2_iso = experts.grouped_gemm(zg, None, np32(d["w2"]), None, route, 128, "bf16")
+    num_kb = I // 64
+    valid = sorted({-(-num_kb // (-(-num_kb // s))) for s in range(1, num_kb + 1)})
+    assert moe.moe_gemm2_splits(p) in valid or moe.moe_gemm2_splits(p) == 1
+    for splits in sorted({1, 2, valid[len(valid) // 2], valid[-1]}):
+        part = torch.full((moe.moe_gemm2_partial_bytes(p, splits) // 4,), float("nan"),
+                          device="cuda")
+        moe.grouped_gemm_w2_split(p, b["z"], dev["w2"], b["block_expert_ids"],
+                                  b["num_post_padded"], b["sorted_ids"], splits, part)
+        y = torch.empty_like(b["y"])
+        moe.unpermute_reduce_split(p, part, splits, b["inv_perm"], dev["w"], y)
+        assert moe.moe_sync_status() == 0
+        ps = np32(part).reshape(splits, R, H).astype(np.float64).sum(axis=0)
+        # slice sums of each live routed item against its GEMM2 row
+        check_close(ps[sid[live]], y2_iso[:n][live], BF16_TOL, f"slice sums s={splits}")
+        # the sliced reduce = the oracle's reduce of the bf16-rounded slice sums
+        y2_pad = np.zeros((len(route["sorted_token_ids"]), H))
+        y2_pad[:n][live] = codecs.round_bf16(ps[sid[live]])
+        inv = route["inv_perm"]
+        y_iso = experts.unpermute_reduce(y2_pad, inv, np32(d["w"]))
+        check_close(np32(y), y_iso, BF16_TOL, f"split reduce s={splits}")
+        # and the unsliced stages, up to one flip of each stored Y2 row
+        items = np.where((inv >= 0)[..., None], np32(b["y2"])[np.maximum(inv, 0)], 0.0)
+        check_close(np32(y), np32(b["y"]).astype(np.float64), BF16_TOL,
+                    f"split vs unsplit s={splits}",
+                    allow=flip_allowance(np32(b["y"]), items, np32(d["w"])))
+    bad = [s for s in range(2, num_kb + 2) if s not in valid][:1]
+    for splits in bad:
+        part = torch.empty(moe.moe_gemm2_partial_bytes(p, splits) // 4, device="cuda")
+        with pytest.raises(moe.MoEError):
+            moe.grouped_gemm_w2_split(p, b["z"], dev["w2"], b["block_expert_ids"],
+                                      b["num_post_padded"], b["sorted_ids"], splits, part)
+
+
 def test_act_mul_quant_fp8():
     """Stage 3 with dynamic 1x128 FP8 output on random bf16 h1 rows."""
     I, rows = 512, 384
