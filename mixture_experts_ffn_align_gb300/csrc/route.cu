@@ -17,6 +17,8 @@
 //   k_route_scatter one warp per segment: __match_any_sync ranks items of the
 //                   same expert within 32-item chunks; a per-warp running
 //                   count in shared memory carries the rank across chunks.
+//   k_route_small   up to 2048 items (decode): the same three phases in one
+//                   CTA, histograms in shared memory (one launch, not three).
 // The data gather (k_permute_*) runs one warp per destination row with
 // 16-byte vector loads batched ahead of the stores; the FP8 variant fuses the
 // dynamic 1x128 quantisation.
@@ -187,10 +189,121 @@ __global__ void __launch_bounds__(kRouteWarps * 32)
   }
 }
 
+// Small batches (decode): the three routing phases in one CTA of 1024
+// threads, the per-segment histograms in shared memory.  Warp g < G handles
+// items [g S, (g + 1) S) (S a multiple of 32, G <= 32); the outputs are the
+// same as the three-kernel form's, bit for bit (same segments' order, same
+// ranks inside a segment).
+constexpr int kSmallThreads = 1024;
+constexpr int kSmallHistInts = 12000;   // G * E counters (static shared memory <= 48 KB)
+
+__global__ void __launch_bounds__(kSmallThreads)
+    k_route_small(const int32_t* __restrict__ ids, int R, int E, int A, int cap, int S, int G,
+                  int32_t* __restrict__ expert_offsets, int32_t* __restrict__ num_post_padded,
+                  int32_t* __restrict__ block_ids, int32_t* __restrict__ sorted_ids,
+                  int32_t* __restrict__ inv_perm, int* err) {
+  __shared__ int32_t hist[kSmallHistInts];
+  __shared__ int32_t warp_sums[32];
+  __shared__ int32_t s_total;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  // (1) per-segment histograms
+  if (warp < G) {
+    int32_t* h = hist + warp * E;
+    for (int e = lane; e < E; e += 32) h[e] = 0;
+    __syncwarp();
+    const int end = min(R, (warp + 1) * S);
+    for (int r = warp * S + lane; r < end; r += 32) {
+      const int e = __ldg(ids + r);
+      if (e >= E) {
+        set_dev_error(err, kDevErrBadIndex);
+      } else if (e >= 0) {
+        atomicAdd(h + e, 1);
+      }
+    }
+  }
+  __syncthreads();
+  // (2) per-expert counts, padded exclusive scan over experts, segment starts
+  int count = 0;
+  if (tid < E)
+    for (int g = 0; g < G; ++g) {
+      const int v = hist[g * E + tid];
+      hist[g * E + tid] = count;
+      count += v;
+    }
+  const int padded = (count + A - 1) / A * A;
+  int incl = padded;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int v = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += v;
+  }
+  if (lane == 31) warp_sums[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    const int w = warp_sums[lane];
+    int wi = w;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, wi, o);
+      if (lane >= o) wi += v;
+    }
+    warp_sums[lane] = wi - w;
+    if (lane == 31) s_total = wi;
+  }
+  __syncthreads();
+  const int total = s_total;
+  if (tid < E) {
+    const int off = incl - padded + warp_sums[warp];
+    expert_offsets[tid] = off;
+    for (int g = 0; g < G; ++g) hist[g * E + tid] += off;
+    for (int b = off / A; b < (off + padded) / A; ++b) block_ids[b] = tid;
+    for (int j = off + count; j < off + padded; ++j) sorted_ids[j] = R;
+  }
+  if (tid == 0) {
+    expert_offsets[E] = total;
+    num_post_padded[0] = total;
+  }
+  for (int b = total / A + tid; b < cap / A; b += kSmallThreads) block_ids[b] = -1;
+  for (int j = total + tid; j < cap; j += kSmallThreads) sorted_ids[j] = R;
+  __syncthreads();
+  // (3) stable scatter, ascending item index inside each expert
+  if (warp < G) {
+    int32_t* cnt = hist + warp * E;
+    const unsigned lt_mask = (1u << lane) - 1u;
+    const int end = min(R, (warp + 1) * S);
+    for (int base = warp * S; base < end; base += 32) {
+      const int r = base + lane;
+      const bool in = r < end;
+      const int e = in ? __ldg(ids + r) : -1;
+      const bool valid = in && e >= 0 && e < E;
+      const unsigned peers = __match_any_sync(0xffffffffu, valid ? e : -1);
+      int pos = -1;
+      if (valid) pos = cnt[e] + __popc(peers & lt_mask);
+      __syncwarp();
+      if (valid) {
+        sorted_ids[pos] = r;
+        if (lane == __ffs(peers) - 1) cnt[e] += __popc(peers);
+      }
+      if (in) inv_perm[r] = pos;
+      __syncwarp();
+    }
+  }
+}
+
 cudaError_t launch_route(const int32_t* topk_ids, int R, int E, int block_size, int cap,
                          int32_t* hist, int32_t* sorted_ids, int32_t* block_expert_ids,
                          int32_t* expert_offsets, int32_t* num_post_padded, int32_t* inv_perm,
                          cudaStream_t stream) {
+  // small batches: one CTA, histograms in shared memory
+  const int S = 32 * ((R + 32 * 32 - 1) / (32 * 32));   // items per warp, a multiple of 32
+  const int Gs = R > 0 ? (R + S - 1) / S : 0;
+  if (R <= 2048 && (size_t)Gs * E <= (size_t)kSmallHistInts) {
+    k_route_small<<<1, kSmallThreads, 0, stream>>>(topk_ids, R, E, block_size, cap, S, Gs,
+                                                   expert_offsets, num_post_padded,
+                                                   block_expert_ids, sorted_ids, inv_perm,
+                                                   dev_error_word());
+    return cudaGetLastError();
+  }
   const int G = route_segments(R);
   const int ctas = (G + kRouteWarps - 1) / kRouteWarps;
   const size_t sh = (size_t)kRouteWarps * E * sizeof(int32_t);

@@ -79,9 +79,12 @@ def test_routing_bit_exact_edge_cases(M, k, E, A, kind):
     _check_routing(b, ids.numpy(), E, A)
 
 
-def test_routing_bad_index_reported():
-    ids = torch.tensor([[0, 1], [2, 8]], dtype=torch.int32)
-    p = moe.Problem(M=2, H=128, I=128, E=8, topk=2)
+@pytest.mark.parametrize("M", [2, 2048])   # one-CTA small-batch form, three-kernel form
+def test_routing_bad_index_reported(M):
+    ids = torch.zeros(M, 2, dtype=torch.int32)
+    ids[0] = torch.tensor([0, 1])
+    ids[1] = torch.tensor([2, 8])
+    p = moe.Problem(M=M, H=128, I=128, E=8, topk=2)
     b = moe.stage_buffers(p)
     moe.moe_align_permute(p, None, ids.cuda(), None, b["sorted_ids"], b["block_expert_ids"],
                           b["expert_offsets"], b["num_post_padded"], b["inv_perm"], None, None,
