@@ -17,11 +17,13 @@
 //   k_route_scatter one warp per segment: __match_any_sync ranks items of the
 //                   same expert within 32-item chunks; a per-warp running
 //                   count in shared memory carries the rank across chunks.
-//   k_route_small   up to 2048 items (decode): the same three phases in one
-//                   CTA, histograms in shared memory (one launch, not three).
+//   k_route_small   small batches (decode, and the Mixtral-shaped prefill):
+//                   the same three phases in one CTA, histograms in shared
+//                   memory (one launch, not three).
 // The data gather (k_permute_*) runs one warp per destination row with
 // 16-byte vector loads batched ahead of the stores; the FP8 variant fuses the
 // dynamic 1x128 quantisation.
+#include "../../include/moe_ffn.h"
 #include "e4m3_pack.cuh"
 #include "moe_common.cuh"
 #include "moe_internal.h"
@@ -195,14 +197,18 @@ __global__ void __launch_bounds__(kRouteWarps * 32)
 // same as the three-kernel form's, bit for bit (same segments' order, same
 // ranks inside a segment).
 constexpr int kSmallThreads = 1024;
-constexpr int kSmallHistInts = 12000;   // G * E counters (static shared memory <= 48 KB)
+// One CTA routes up to 2048 items, or up to 8192 with at most 64 experts
+// (measured on GB300, routing alone: Mixtral-shaped 8192 items over 8
+// experts 10.9 vs 20.9 us for the three kernels; 16384 items over 256 experts
+// 34.6 vs 31.0 us and 65536 over 256 experts 91.5 vs 37.2 us favour them).
+inline bool route_in_one_cta(int R, int E) { return R <= 2048 || (R <= 8192 && E <= 64); }
 
 __global__ void __launch_bounds__(kSmallThreads)
     k_route_small(const int32_t* __restrict__ ids, int R, int E, int A, int cap, int S, int G,
                   int32_t* __restrict__ expert_offsets, int32_t* __restrict__ num_post_padded,
                   int32_t* __restrict__ block_ids, int32_t* __restrict__ sorted_ids,
                   int32_t* __restrict__ inv_perm, int* err) {
-  __shared__ int32_t hist[kSmallHistInts];
+  extern __shared__ int32_t hist[];     // [G][E]
   __shared__ int32_t warp_sums[32];
   __shared__ int32_t s_total;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -297,11 +303,17 @@ cudaError_t launch_route(const int32_t* topk_ids, int R, int E, int block_size, 
   // small batches: one CTA, histograms in shared memory
   const int S = 32 * ((R + 32 * 32 - 1) / (32 * 32));   // items per warp, a multiple of 32
   const int Gs = R > 0 ? (R + S - 1) / S : 0;
-  if (R <= 2048 && (size_t)Gs * E <= (size_t)kSmallHistInts) {
-    k_route_small<<<1, kSmallThreads, 0, stream>>>(topk_ids, R, E, block_size, cap, S, Gs,
-                                                   expert_offsets, num_post_padded,
-                                                   block_expert_ids, sorted_ids, inv_perm,
-                                                   dev_error_word());
+  if (route_in_one_cta(R, E)) {
+    const size_t sh_small = (size_t)Gs * E * sizeof(int32_t);   // <= 32 x 1024 x 4 B
+    static bool attr_done = false;
+    if (!attr_done) {
+      cudaFuncSetAttribute(k_route_small, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           32 * MOE_MAX_EXPERTS * (int)sizeof(int32_t));
+      attr_done = true;
+    }
+    k_route_small<<<1, kSmallThreads, sh_small, stream>>>(
+        topk_ids, R, E, block_size, cap, S, Gs, expert_offsets, num_post_padded,
+        block_expert_ids, sorted_ids, inv_perm, dev_error_word());
     return cudaGetLastError();
   }
   const int G = route_segments(R);

@@ -79,7 +79,7 @@ def test_routing_bit_exact_edge_cases(M, k, E, A, kind):
     _check_routing(b, ids.numpy(), E, A)
 
 
-@pytest.mark.parametrize("M", [2, 2048])   # one-CTA small-batch form, three-kernel form
+@pytest.mark.parametrize("M", [2, 8192])   # one-CTA small-batch form, three-kernel form
 def test_routing_bad_index_reported(M):
     ids = torch.zeros(M, 2, dtype=torch.int32)
     ids[0] = torch.tensor([0, 1])
