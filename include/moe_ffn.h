@@ -13,9 +13,14 @@
  *   1. block-aligned routing + permute  (moe_align_permute)
  *   2. grouped GEMM1 over w13           (grouped_gemm_w13)
  *   3. SiLU-and-mul (+ dynamic FP8)     (act_mul_quant, or fused into 2)
- *   4. grouped GEMM2 over w2            (grouped_gemm_w2)
- *   5. weighted unpermute + reduce      (unpermute_reduce)
- * and fused_experts runs all five.
+ *   4. grouped GEMM2 over w2            (grouped_gemm_w2, or in K slices:
+ *                                        grouped_gemm_w2_split)
+ *   5. weighted unpermute + reduce      (unpermute_reduce, or
+ *                                        unpermute_reduce_split)
+ * and fused_experts runs all five (fused_experts_ex with expert biases and
+ * epilogue options, fused_experts_from_host from host buffers,
+ * fused_experts_batched on the batched [E, T, H] layout).  moe_topk_router
+ * is the step before: logits -> topk_ids / topk_weights.
  *
  * Conventions for every entry point:
  *  - Pointers named as device pointers must point to device memory of the
