@@ -116,3 +116,31 @@ def test_router_empty_batch_and_null_outputs():
 def test_status_strings():
     for code, name in moe.STATUS.items():
         assert moe.moe_status_string(code) == name
+
+
+def test_gemm2_split_sizes_and_argument_checks():
+    """Sizing of the K-sliced GEMM2 and the checks made before any launch
+    (no GPU needed: invalid calls return before touching the device)."""
+    p = moe.Problem.from_config(CONFIGS["decode"])
+    R = p.M * p.topk
+    assert moe.moe_gemm2_partial_bytes(p, 7) == 7 * R * p.H * 4
+    assert moe.moe_gemm2_partial_bytes(p, 0) == 0
+    bad = moe.Problem(M=16, H=100, I=128, E=8, topk=2)
+    assert moe.moe_gemm2_splits(bad) == 0 and moe.moe_gemm2_partial_bytes(bad, 2) == 0
+    # any valid problem gets a count in [1, 8]; quantised modes never slice
+    assert 1 <= moe.moe_gemm2_splits(p) <= 8
+    assert moe.moe_gemm2_splits(moe.Problem.from_config(CONFIGS["dsfp8"])) == 1
+    L = moe.lib()
+    c = ctypes.byref(p.c())
+    # null pointers, a slice count above the K steps, a quantised problem
+    assert L.grouped_gemm_w2_split(c, None, None, None, None, None, 2, None, None) == 1
+    fake = ctypes.c_void_p(0x1000)
+    assert L.grouped_gemm_w2_split(c, fake, fake, fake, fake, fake, p.I // 64 + 1, fake,
+                                   None) == 1
+    q = ctypes.byref(moe.Problem.from_config(CONFIGS["dsfp8"]).c())
+    assert L.grouped_gemm_w2_split(q, fake, fake, fake, fake, fake, 2, fake, None) == 1
+    # the sliced reduce takes no router weight on the input or in GEMM2
+    w = ctypes.byref(moe.Problem(M=16, H=256, I=128, E=8, topk=1,
+                                 apply_router_weight_on_input=True).c())
+    assert L.unpermute_reduce_split(w, fake, 2, fake, fake, fake, None) == 1
+    assert L.unpermute_reduce_split(c, None, 2, None, None, None, None) == 1
