@@ -319,8 +319,8 @@ moe_status unpermute_reduce(const moe_problem* p, const void* y2, const int32_t*
  *    num_post_padded and sorted_ids from moe_align_permute; writes the fp32
  *    sums of slice s for routed item r = sorted_ids[row] < M*topk at
  *    partial[(s * M*topk + r) * H + h] (padding rows are not written).
- *    `splits` must be one that leaves no slice empty, as moe_gemm2_splits
- *    returns (else MOE_ERR_INVALID_ARG); splits == 1 is allowed.
+ *    `splits` (1 to 8) must leave no slice empty, as the counts
+ *    moe_gemm2_splits returns do (else MOE_ERR_INVALID_ARG).
  *  - unpermute_reduce_split: y[t,:] = bf16( sum_i w[t,i] * bf16( sum_s
  *    partial[s, t*topk+i, :] ) ), fp32, slices and slots in order; slots
  *    with inv_perm < 0 are skipped.  The bf16 rounding of the slice sum is

@@ -242,6 +242,32 @@ __global__ void __launch_bounds__(REDUCE_THREADS)
 // segment) is one warp's work item, lane l owning 8 columns: the slices are
 // summed in order, rounded to bf16 where Y2 would have been stored, and the
 // weighted sum over the slots runs in fp32 as in k_unpermute_reduce.
+constexpr int kMaxSlices = 8;
+
+// The slices of 8 columns of one routed item, summed in slice order; all
+// loads are issued before the first add.
+__device__ __forceinline__ void sum_slices(const float* __restrict__ part, int S, size_t stride,
+                                           size_t off, float (&v)[8]) {
+  float4 a[kMaxSlices], b[kMaxSlices];
+#pragma unroll
+  for (int sl = 0; sl < kMaxSlices; ++sl) {
+    if (sl < S) {
+      const float4* src = reinterpret_cast<const float4*>(part + sl * stride + off);
+      a[sl] = __ldg(src);
+      b[sl] = __ldg(src + 1);
+    }
+  }
+#pragma unroll
+  for (int j = 0; j < 8; ++j) v[j] = 0.0f;
+#pragma unroll
+  for (int sl = 0; sl < kMaxSlices; ++sl) {
+    if (sl < S) {
+      v[0] += a[sl].x; v[1] += a[sl].y; v[2] += a[sl].z; v[3] += a[sl].w;
+      v[4] += b[sl].x; v[5] += b[sl].y; v[6] += b[sl].z; v[7] += b[sl].w;
+    }
+  }
+}
+
 __global__ void __launch_bounds__(REDUCE_THREADS)
     k_unpermute_reduce_split(const float* __restrict__ part, int S, int H, int M, int topk,
                              const int32_t* __restrict__ inv_perm, const float* __restrict__ w,
@@ -261,14 +287,7 @@ __global__ void __launch_bounds__(REDUCE_THREADS)
       if (__ldg(inv_perm + r) < 0) continue;       // skipped slot (same for the whole warp)
       const float wi = __ldg(w + r);
       float v[8];
-#pragma unroll
-      for (int j = 0; j < 8; ++j) v[j] = 0.0f;
-      for (int sl = 0; sl < S; ++sl) {
-        const float4* src = reinterpret_cast<const float4*>(part + (sl * R + r) * H + col);
-        const float4 a = __ldg(src), b = __ldg(src + 1);
-        v[0] += a.x; v[1] += a.y; v[2] += a.z; v[3] += a.w;
-        v[4] += b.x; v[5] += b.y; v[6] += b.z; v[7] += b.w;
-      }
+      sum_slices(part, S, R * H, r * H + col, v);
 #pragma unroll
       for (int j = 0; j < 8; ++j) acc[j] = fmaf(wi, bf16_round(v[j]), acc[j]);
     }
@@ -284,7 +303,7 @@ cudaError_t launch_unpermute_reduce_split(const float* part, int splits, int H, 
                                           const int32_t* inv_perm, const float* topk_weights,
                                           void* y, cudaStream_t stream) {
   if (M <= 0) return cudaSuccess;
-  if (H % 256 != 0 || splits < 1) return cudaErrorInvalidValue;
+  if (H % 256 != 0 || splits < 1 || splits > kMaxSlices) return cudaErrorInvalidValue;
   const int wpc = REDUCE_THREADS / 32;
   const int items = M * (H / 256);
   const int grid = min((items + wpc - 1) / wpc, num_sms() * 8);

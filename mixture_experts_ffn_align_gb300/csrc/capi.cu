@@ -132,13 +132,19 @@ size_t cap_rows(const moe_problem* p) {
 // minimises the rounds per unit of work, ceil(tiles s / SMs) / s, on the
 // expected block count (every expert that receives rows fills its blocks
 // evenly).  1 for the SM-pair form, the quantised modes and H % 256 != 0.
+int splits_for_tiles(const moe_problem* p, int64_t tiles);
+
 int gemm2_splits(const moe_problem* p) {
   if (p->quant != MOE_Q_BF16 || p->H % 256 != 0 || g_bf16_form == 2) return 1;
   const int64_t R = (int64_t)p->M * p->topk;
   if (R <= 0 || (g_bf16_form == 0 && R / p->E >= 2 * 128)) return 1;
   const int64_t experts = std::min<int64_t>(p->E, R);
   const int64_t blocks = experts * ((R / experts + 127) / 128);
-  const int64_t tiles = blocks * (p->H / 256);
+  return splits_for_tiles(p, blocks * (p->H / 256));
+}
+
+// The slice count for a GEMM2 of `tiles` 128 x 256 output tiles (see above).
+int splits_for_tiles(const moe_problem* p, int64_t tiles) {
   const int64_t sms = num_sms();
   if (tiles >= sms) return 1;
   int best = 1;
@@ -468,7 +474,7 @@ moe_status grouped_gemm_w2_split(const moe_problem* p, const void* z, const void
   if (!valid_problem(p) || p->quant != MOE_Q_BF16 || p->H % 256 != 0) return MOE_ERR_INVALID_ARG;
   if (p->M == 0) return MOE_OK;
   if (!z || !w2 || !block_expert_ids || !num_post_padded || !sorted_ids || !partial ||
-      splits < 1 || splits > p->I / 64)
+      splits < 1 || splits > 8 || splits > p->I / 64)
     return MOE_ERR_INVALID_ARG;
   if (!gemm_supported(p)) return MOE_ERR_UNSUPPORTED;
   const Epilogue ep = make_epilogue(p, nullptr, p->H, nullptr, nullptr);
@@ -486,7 +492,8 @@ moe_status unpermute_reduce_split(const moe_problem* p, const float* partial, in
       p->router_weight_in_gemm2)
     return MOE_ERR_INVALID_ARG;
   if (p->M == 0) return MOE_OK;
-  if (!partial || !inv_perm || !topk_weights || !y || splits < 1) return MOE_ERR_INVALID_ARG;
+  if (!partial || !inv_perm || !topk_weights || !y || splits < 1 || splits > 8)
+    return MOE_ERR_INVALID_ARG;
   return cuda_status(launch_unpermute_reduce_split(partial, splits, p->H, p->M, p->topk, inv_perm,
                                                    topk_weights, y,
                                                    static_cast<cudaStream_t>(stream)));
@@ -667,9 +674,9 @@ moe_status fused_experts_batched(const moe_problem* p, const void* x,
     // the layout's rows are GEMM1's rows as they are: no permute
     e = launch_bf16_gemm(expected_m, x, rows, H, w13, E * 2 * I, 2 * I, 2 * I, blocks, npp,
                          ws + L.z, true, ep, s);
-    if (e == cudaSuccess)
-      e = launch_bf16_gemm(expected_m, ws + L.z, rows, I, w2, E * H, H, H, blocks, npp, y,
-                           false, ep, s);
+    if (e != cudaSuccess) return cuda_status(e);
+    e = launch_bf16_gemm(expected_m, ws + L.z, rows, I, w2, E * H, H, H, blocks, npp, y, false,
+                         ep, s);
     return cuda_status(e);
   }
   // quantised: per-row dynamic quantisation of the layout, then the same stages

@@ -112,8 +112,8 @@ def test_gemm2_split_k_stages(counts, H, I, topk):
     """GEMM2 in K slices: each live routed item's slice sums add up to its
     fp32 GEMM2 row (isolated on the GPU's own z), the sliced reduce matches
     the oracle's reduce of the bf16-rounded sums, and both match the unsliced
-    stages; every slice count from 1 to the K steps that leaves no slice
-    empty is accepted, others are rejected."""
+    stages; every slice count that leaves no slice empty (at most 8) is
+    accepted, others are rejected."""
     if counts is None:           # top-3, random experts, a quarter of the slots skipped
         g = torch.Generator().manual_seed(2)
         M, E = 40, 6
@@ -146,7 +146,7 @@ def test_gemm2_split_k_stages(counts, H, I, topk):
     zg[:n] = np32(b["z"])[:n]
     y2_iso = experts.grouped_gemm(zg, None, np32(d["w2"]), None, route, 128, "bf16")
     num_kb = I // 64
-    valid = sorted({-(-num_kb // (-(-num_kb // s))) for s in range(1, num_kb + 1)})
+    valid = sorted({-(-num_kb // (-(-num_kb // s))) for s in range(1, num_kb + 1)} & set(range(1, 9)))
     assert moe.moe_gemm2_splits(p) in valid or moe.moe_gemm2_splits(p) == 1
     for splits in sorted({1, 2, valid[len(valid) // 2], valid[-1]}):
         part = torch.full((moe.moe_gemm2_partial_bytes(p, splits) // 4,), float("nan"),
@@ -170,7 +170,7 @@ def test_gemm2_split_k_stages(counts, H, I, topk):
         check_close(np32(y), np32(b["y"]).astype(np.float64), BF16_TOL,
                     f"split vs unsplit s={splits}",
                     allow=flip_allowance(np32(b["y"]), items, np32(d["w"])))
-    bad = [s for s in range(2, num_kb + 2) if s not in valid][:1]
+    bad = [s for s in range(2, num_kb + 2) if s not in valid][:1] + [9]   # at most 8 slices
     for splits in bad:
         part = torch.empty(moe.moe_gemm2_partial_bytes(p, splits) // 4, device="cuda")
         with pytest.raises(moe.MoEError):
