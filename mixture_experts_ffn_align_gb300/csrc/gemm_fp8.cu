@@ -373,20 +373,23 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
         if (half == 0) args.zs[row * (size_t)(args.I / 128) + n_tile] = sc;
       } else if (active) {
-        uint4* dst = reinterpret_cast<uint4*>(args.out + row * args.ldo + (size_t)nblk * 128);
+        __nv_bfloat16* dst = args.out + row * args.ldo + (size_t)nblk * 128;
         const float w = epi_row_weight(args.ep, row);
         const bool bias = args.ep.bias != nullptr;
 #pragma unroll
-        for (int v = 0; v < 16; ++v) {
-          uint4 pk;
-          __nv_bfloat16* pb = reinterpret_cast<__nv_bfloat16*>(&pk);
+        for (int v = 0; v < 4; ++v) {                // 32 columns per 64-byte store
+          uint32_t pk[16];
 #pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            float x = acc[v * 8 + j];
-            if (bias) x += epi_bias(args.ep, e, nblk * 128 + v * 8 + j);
-            pb[j] = __float2bfloat16_rn(x * w);
+          for (int j = 0; j < 16; ++j) {
+            const int c = v * 32 + 2 * j;
+            float x0 = acc[c], x1 = acc[c + 1];
+            if (bias) {
+              x0 += epi_bias(args.ep, e, nblk * 128 + c);
+              x1 += epi_bias(args.ep, e, nblk * 128 + c + 1);
+            }
+            pk[j] = bf16x2_bits(__float2bfloat16_rn(x0 * w), __float2bfloat16_rn(x1 * w));
           }
-          dst[v] = pk;
+          st_row64(dst + v * 32, pk);
         }
       }
     }

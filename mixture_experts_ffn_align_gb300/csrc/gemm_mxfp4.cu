@@ -728,20 +728,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           if (lane == 0) mbar_arrive(tempty_bar);
         }
         if (store) {
-          uint4* dst = reinterpret_cast<uint4*>(out_row);
           const int col0 = n_tile * BN + half * 128;
 #pragma unroll
-          for (int v = 0; v < 16; ++v) {
-            uint4 pk;
-            __nv_bfloat16* pb = reinterpret_cast<__nv_bfloat16*>(&pk);
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-              float x = __uint_as_float(r[v >> 2][8 * (v & 3) + j]);
-              if (bias) x += epi_bias(args.ep, e, col0 + 8 * v + j);
-              pb[j] = __float2bfloat16_rn(x * w);
-            }
-            dst[v] = pk;
-          }
+          for (int c = 0; c < 4; ++c) epi_store32(args.ep, e, col0 + 32 * c, w, r[c], out_row + 32 * c);
         }
       }
       }

@@ -471,43 +471,74 @@ __device__ __forceinline__ float act_glu(const Epilogue& ep, float g, float u) {
   return __fdividef(g, 1.0f + __expf(-ep.alpha * g)) * (u + ep.beta);
 }
 
+// Two bf16 values as one 32-bit word, the first in the low half (memory order).
+__device__ __forceinline__ uint32_t bf16x2_bits(__nv_bfloat16 lo, __nv_bfloat16 hi) {
+  return static_cast<uint32_t>(__bfloat16_as_ushort(lo)) |
+         (static_cast<uint32_t>(__bfloat16_as_ushort(hi)) << 16);
+}
+
+// 64 bytes of one output row.  Where dst is 32-byte aligned (every row of a
+// tile is, when the row pitch is a multiple of 32 bytes) it goes out as two
+// 256-bit stores, each filling a whole L2 sector; 16-byte stores fill half a
+// sector each and take twice the load/store-queue entries, which throttled
+// the epilogue warps at the end of every tile.  Otherwise four 16-byte stores.
+__device__ __forceinline__ void st_row64(void* dst, const uint32_t (&w)[16]) {
+  if ((reinterpret_cast<uintptr_t>(dst) & 31u) == 0) {
+    uint32_t* d = static_cast<uint32_t*>(dst);
+    asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(d),
+                 "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]),
+                 "r"(w[7])
+                 : "memory");
+    asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(d + 8),
+                 "r"(w[8]), "r"(w[9]), "r"(w[10]), "r"(w[11]), "r"(w[12]), "r"(w[13]),
+                 "r"(w[14]), "r"(w[15])
+                 : "memory");
+  } else {
+    uint4* d = static_cast<uint4*>(dst);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) d[j] = make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
+  }
+}
+
 // Fused GEMM1 epilogue for 32 columns of one row: the gate and up sums
 // (plus bias), each rounded to bf16 as a stored H1 would be, through the gated
 // activation, as 32 bf16 values at dst (16-byte aligned).
 __device__ __forceinline__ void epi_glu_store32(const Epilogue& ep, int e, int gcol0, int ucol0,
                                                 const uint32_t (&g)[32], const uint32_t (&u)[32],
                                                 __nv_bfloat16* dst) {
-  uint4 pk[4];
-  __nv_bfloat16* pb = reinterpret_cast<__nv_bfloat16*>(pk);
+  uint32_t w[16];
   const bool bias = ep.bias != nullptr;
 #pragma unroll
-  for (int j = 0; j < 32; ++j) {
-    float gs = __uint_as_float(g[j]), us = __uint_as_float(u[j]);
-    if (bias) {
-      gs += epi_bias(ep, e, gcol0 + j);
-      us += epi_bias(ep, e, ucol0 + j);
-    }
-    pb[j] = __float2bfloat16_rn(act_glu(ep, bf16_round(gs), bf16_round(us)));
-  }
-  uint4* d = reinterpret_cast<uint4*>(dst);
+  for (int j = 0; j < 16; ++j) {
+    __nv_bfloat16 z[2];
 #pragma unroll
-  for (int j = 0; j < 4; ++j) d[j] = pk[j];
+    for (int h = 0; h < 2; ++h) {
+      float gs = __uint_as_float(g[2 * j + h]), us = __uint_as_float(u[2 * j + h]);
+      if (bias) {
+        gs += epi_bias(ep, e, gcol0 + 2 * j + h);
+        us += epi_bias(ep, e, ucol0 + 2 * j + h);
+      }
+      z[h] = __float2bfloat16_rn(act_glu(ep, bf16_round(gs), bf16_round(us)));
+    }
+    w[j] = bf16x2_bits(z[0], z[1]);
+  }
+  st_row64(dst, w);
 }
 // Plain epilogue for 32 columns of one row: bf16((acc + bias) * w) at dst.
 __device__ __forceinline__ void epi_store32(const Epilogue& ep, int e, int col0, float w,
                                             const uint32_t (&r)[32], __nv_bfloat16* dst) {
-  uint4 pk[4];
-  __nv_bfloat16* pb = reinterpret_cast<__nv_bfloat16*>(pk);
+  uint32_t pk[16];
   const bool bias = ep.bias != nullptr;
 #pragma unroll
-  for (int j = 0; j < 32; ++j) {
-    float v = __uint_as_float(r[j]);
-    if (bias) v += epi_bias(ep, e, col0 + j);
-    pb[j] = __float2bfloat16_rn(v * w);
+  for (int j = 0; j < 16; ++j) {
+    float v0 = __uint_as_float(r[2 * j]), v1 = __uint_as_float(r[2 * j + 1]);
+    if (bias) {
+      v0 += epi_bias(ep, e, col0 + 2 * j);
+      v1 += epi_bias(ep, e, col0 + 2 * j + 1);
+    }
+    pk[j] = bf16x2_bits(__float2bfloat16_rn(v0 * w), __float2bfloat16_rn(v1 * w));
   }
-  uint4* d = reinterpret_cast<uint4*>(dst);
-#pragma unroll
-  for (int j = 0; j < 4; ++j) d[j] = pk[j];
+  st_row64(dst, pk);
 }
 
 // fp32 -> e4m3fn, round to nearest even, saturating to +-448.
