@@ -177,9 +177,9 @@ def _time_oracle(arrs, tokens, cfg):
 _KERNEL_SOURCES = {
     "bf16": ["gemm_bf16.cu", "moe_common.cuh", "tile_sched.cuh"],
     "bf16_2sm": ["gemm_bf16_2sm.cu", "moe_common.cuh", "tile_sched.cuh"],
-    "fp8": ["gemm_fp8.cu", "moe_common.cuh", "tile_sched.cuh"],
-    "mxfp4": ["gemm_mxfp4.cu", "moe_common.cuh", "tile_sched.cuh"],
-    "mxfp8": ["gemm_mxfp4.cu", "moe_common.cuh", "tile_sched.cuh"],
+    "fp8": ["gemm_fp8.cu", "moe_common.cuh", "tile_sched.cuh", "e4m3_pack.cuh"],
+    "mxfp4": ["gemm_mxfp4.cu", "moe_common.cuh", "tile_sched.cuh", "e4m3_pack.cuh"],
+    "mxfp8": ["gemm_mxfp4.cu", "moe_common.cuh", "tile_sched.cuh", "e4m3_pack.cuh"],
 }
 
 
