@@ -354,8 +354,9 @@ def run_ours(args):
     x, ids, wts, w13, w2 = d["x"], d["topk_ids"], d["topk_weights"], d["w13"], d["w2"]
     w13s, w2s = d["w13_scale"], d["w2_scale"]
     plan = _stage_plan(moe, p, cfg, d, b, stream)
-    # route hist/scan/scatter + permute, then one launch per remaining stage
-    launches_per_step = 4 + (len(plan) - 1)
+    # routing (one CTA, or hist/scan/scatter) + permute, then one launch per
+    # remaining stage
+    launches_per_step = moe.moe_align_permute_launches(p) + (len(plan) - 1)
 
     def barrier():
         torch.cuda.synchronize(dev)

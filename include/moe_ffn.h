@@ -134,6 +134,13 @@ size_t moe_m_sum_bound(const moe_problem* p);
  * expert histograms).  0 for an invalid problem. */
 size_t moe_align_workspace_bytes(const moe_problem* p);
 
+/* Number of kernels moe_align_permute launches for p when it is given x and
+ * x_perm (for launch accounting): the routing kernels -- 1 when the problem
+ * routes in one CTA (M*topk <= 2048, or <= 8192 with E <= 64), else 3
+ * (histograms, scan, scatter) -- plus the permute.  0 when M == 0 and for an
+ * invalid problem.  Host-only; launches nothing. */
+int moe_align_permute_launches(const moe_problem* p);
+
 /* Bytes of workspace fused_experts needs (routing scratch, indices and every
  * intermediate, sized for moe_m_sum_bound rows, with the permuted input and
  * the GEMM2 output sharing storage as the page's workspace13 does, §2.8(a)).

@@ -25,7 +25,8 @@ STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED", 3: "M
           4: "MOE_ERR_DEVICE_TIMEOUT", 5: "MOE_ERR_WORKSPACE_TOO_SMALL",
           6: "MOE_ERR_DEVICE_BAD_INDEX"}
 
-EXPORTS = ["moe_m_sum_bound", "moe_align_workspace_bytes", "moe_workspace_bytes",
+EXPORTS = ["moe_m_sum_bound", "moe_align_workspace_bytes", "moe_align_permute_launches",
+           "moe_workspace_bytes",
            "moe_host_workspace_bytes", "moe_align_permute", "grouped_gemm_w13", "act_mul_quant",
            "grouped_gemm_w2", "unpermute_reduce", "fused_experts", "fused_experts_from_host",
            "moe_sync_status", "moe_status_string", "moe_debug_set_watchdog",
@@ -118,6 +119,8 @@ def lib() -> ctypes.CDLL:
         L.grouped_gemm_w2_ex.argtypes = [P, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
         L.fused_experts_ex.argtypes = [P] + [vp] * 11 + [sz, vp]
         L.moe_gemm2_splits.argtypes, L.moe_gemm2_splits.restype = [P], i32
+        L.moe_align_permute_launches.argtypes = [P]
+        L.moe_align_permute_launches.restype = i32
         L.moe_gemm2_partial_bytes.argtypes, L.moe_gemm2_partial_bytes.restype = [P, i32], sz
         L.grouped_gemm_w2_split.argtypes = [P, vp, vp, vp, vp, vp, i32, vp, vp]
         L.unpermute_reduce_split.argtypes = [P, vp, i32, vp, vp, vp, vp]
@@ -166,6 +169,11 @@ def moe_m_sum_bound(p: Problem) -> int:
 
 def moe_align_workspace_bytes(p: Problem) -> int:
     return int(lib().moe_align_workspace_bytes(_cp(p)))
+
+
+def moe_align_permute_launches(p: Problem) -> int:
+    """Kernels moe_align_permute launches for p (routing + permute)."""
+    return int(lib().moe_align_permute_launches(_cp(p)))
 
 
 def moe_workspace_bytes(p: Problem) -> int:

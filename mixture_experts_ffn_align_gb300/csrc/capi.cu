@@ -462,6 +462,11 @@ moe_status unpermute_reduce(const moe_problem* p, const void* y2, const int32_t*
 
 int moe_gemm2_splits(const moe_problem* p) { return valid_problem(p) ? gemm2_splits(p) : 0; }
 
+int moe_align_permute_launches(const moe_problem* p) {
+  if (!valid_problem(p) || p->M == 0) return 0;
+  return (route_in_one_cta(p->M * p->topk, p->E) ? 1 : 3) + 1;
+}
+
 size_t moe_gemm2_partial_bytes(const moe_problem* p, int splits) {
   if (!valid_problem(p) || splits < 1) return 0;
   return (size_t)splits * p->M * p->topk * p->H * 4;

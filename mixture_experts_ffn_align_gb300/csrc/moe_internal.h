@@ -21,6 +21,9 @@ int* dev_error_word();                        // device address of the error wor
 void watchdog_params(uint64_t* limit_ns, int* never_arrive);
 
 // Routing half of moe_align_permute (three launches).
+// Stage 1 routes R items over E experts in one CTA (k_route_small) rather than
+// three kernels (histograms, scan, scatter).
+bool route_in_one_cta(int R, int E);
 cudaError_t launch_route(const int32_t* topk_ids, int R, int E, int block_size, int cap,
                          int32_t* hist, int32_t* sorted_ids, int32_t* block_expert_ids,
                          int32_t* expert_offsets, int32_t* num_post_padded, int32_t* inv_perm,

@@ -201,7 +201,7 @@ constexpr int kSmallThreads = 1024;
 // (measured on GB300, routing alone: Mixtral-shaped 8192 items over 8
 // experts 10.9 vs 20.9 us for the three kernels; 16384 items over 256 experts
 // 34.6 vs 31.0 us and 65536 over 256 experts 91.5 vs 37.2 us favour them).
-inline bool route_in_one_cta(int R, int E) { return R <= 2048 || (R <= 8192 && E <= 64); }
+bool route_in_one_cta(int R, int E) { return R <= 2048 || (R <= 8192 && E <= 64); }
 
 __global__ void __launch_bounds__(kSmallThreads)
     k_route_small(const int32_t* __restrict__ ids, int R, int E, int A, int cap, int S, int G,

@@ -144,3 +144,18 @@ def test_gemm2_split_sizes_and_argument_checks():
                                  apply_router_weight_on_input=True).c())
     assert L.unpermute_reduce_split(w, fake, 2, fake, fake, fake, None) == 1
     assert L.unpermute_reduce_split(c, None, 2, None, None, None, None) == 1
+
+
+def test_align_permute_launch_count():
+    """Kernels stage 1 launches (the bench's launch accounting): one-CTA routing
+    for small batches (up to 2048 routed items, or 8192 over at most 64 experts),
+    else histograms + scan + scatter; plus the permute."""
+    want = {"tiny": 2, "mixtral": 2, "decode": 2, "dsfp8": 4, "mxfp4": 4, "mxfp8": 4}
+    for name, n in want.items():
+        assert moe.moe_align_permute_launches(moe.Problem.from_config(CONFIGS[name])) == n, name
+    edge = [(2048, 1, 256, 2), (2049, 1, 256, 4), (4096, 2, 64, 2), (4096, 2, 65, 4),
+            (8193, 1, 8, 4)]
+    for M, k, E, n in edge:
+        assert moe.moe_align_permute_launches(moe.Problem(M=M, H=256, I=128, E=E, topk=k)) == n
+    assert moe.moe_align_permute_launches(moe.Problem(M=0, H=256, I=128, E=8, topk=2)) == 0
+    assert moe.moe_align_permute_launches(moe.Problem(M=16, H=100, I=128, E=8, topk=2)) == 0
