@@ -22,7 +22,6 @@ namespace moe {
 __device__ int g_dev_error_word = 0;
 
 namespace {
-constexpr int kMaxDevices = 64;
 int g_sms[kMaxDevices];
 int* g_err_ptr[kMaxDevices];
 std::mutex g_dev_mu;
@@ -36,6 +35,8 @@ int current_device() {
   return d;
 }
 }  // namespace
+
+int device_index() { return current_device(); }
 
 int num_sms() {
   const int d = current_device();

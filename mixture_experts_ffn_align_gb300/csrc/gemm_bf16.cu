@@ -426,20 +426,20 @@ cudaError_t launch_ggemm_bf16(const void* A, int cap, int K, const void* B, int 
   a.part_R = part_R;
   const int grid = num_sms();
   if (fuse_act) {
-    static bool attr_done = false;
-    if (!attr_done) {
-      cudaFuncSetAttribute(k_ggemm_bf16<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           SMEM_BYTES);
-      attr_done = true;
-    }
+    static DeviceOnce attr;
+    const cudaError_t ea = attr.call([] {
+      return cudaFuncSetAttribute(k_ggemm_bf16<true>,
+                                  cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    });
+    if (ea != cudaSuccess) return ea;
     k_ggemm_bf16<true><<<grid, NUM_THREADS, SMEM_BYTES, stream>>>(tmA, tmB, a);
   } else {
-    static bool attr_done = false;
-    if (!attr_done) {
-      cudaFuncSetAttribute(k_ggemm_bf16<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           SMEM_BYTES);
-      attr_done = true;
-    }
+    static DeviceOnce attr;
+    const cudaError_t ea = attr.call([] {
+      return cudaFuncSetAttribute(k_ggemm_bf16<false>,
+                                  cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    });
+    if (ea != cudaSuccess) return ea;
     k_ggemm_bf16<false><<<grid, NUM_THREADS, SMEM_BYTES, stream>>>(tmA, tmB, a);
   }
   return cudaGetLastError();

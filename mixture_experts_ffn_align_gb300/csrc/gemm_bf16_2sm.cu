@@ -407,8 +407,10 @@ cudaError_t launch_pairs(const CUtensorMap& tmA, const CUtensorMap& tmB, const P
   cfg.dynamicSmemBytes = SMEM_BYTES;
   cfg.attrs = &attr;
   cfg.numAttrs = 1;
-  static int max_pairs = -1;
-  if (max_pairs < 0) {
+  static DeviceOnce setup;
+  static int max_pairs[kMaxDevices];
+  const int dev = device_index();
+  const cudaError_t es = setup.call([&] {
     cudaError_t e = cudaFuncSetAttribute(k_ggemm_bf16_2sm<FUSE>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
     if (e != cudaSuccess) return e;
@@ -416,11 +418,13 @@ cudaError_t launch_pairs(const CUtensorMap& tmA, const CUtensorMap& tmB, const P
     int n = 0;
     e = cudaOccupancyMaxActiveClusters(&n, k_ggemm_bf16_2sm<FUSE>, &cfg);
     if (e != cudaSuccess) return e;
-    max_pairs = n;
-  }
-  if (max_pairs <= 0) return cudaErrorInvalidConfiguration;
+    max_pairs[dev] = n;
+    return cudaSuccess;
+  });
+  if (es != cudaSuccess) return es;
+  if (max_pairs[dev] <= 0) return cudaErrorInvalidConfiguration;
   // one wave of persistent pairs (as many as fit on the GPU at once)
-  cfg.gridDim = dim3(2 * max_pairs, 1, 1);
+  cfg.gridDim = dim3(2 * max_pairs[dev], 1, 1);
   cfg.stream = stream;
   return cudaLaunchKernelEx(&cfg, k_ggemm_bf16_2sm<FUSE>, tmA, tmB, a);
 }

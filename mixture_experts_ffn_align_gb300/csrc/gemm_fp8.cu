@@ -410,18 +410,18 @@ namespace {
 template <bool FUSE>
 cudaError_t launch_fp8_form(const CUtensorMap& tmA, const CUtensorMap& tmB, const Fp8Args& a,
                             cudaStream_t stream) {
-  static bool attr_done = false;
-  static bool regs_ok = false;
-  if (!attr_done) {
-    cudaFuncSetAttribute(k_ggemm_fp8<FUSE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                         SMEM_BYTES);
+  static DeviceOnce setup;
+  const cudaError_t es = setup.call([] {
+    cudaError_t e = cudaFuncSetAttribute(k_ggemm_fp8<FUSE>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    if (e != cudaSuccess) return e;
     // the register split above is only safe at exactly LAUNCH_REGS a thread
     cudaFuncAttributes fa;
-    regs_ok = cudaFuncGetAttributes(&fa, k_ggemm_fp8<FUSE>) == cudaSuccess &&
-              fa.numRegs == LAUNCH_REGS;
-    attr_done = true;
-  }
-  if (!regs_ok) return cudaErrorInvalidConfiguration;
+    e = cudaFuncGetAttributes(&fa, k_ggemm_fp8<FUSE>);
+    if (e != cudaSuccess) return e;
+    return fa.numRegs == LAUNCH_REGS ? cudaSuccess : cudaErrorInvalidConfiguration;
+  });
+  if (es != cudaSuccess) return es;
   k_ggemm_fp8<FUSE><<<num_sms(), NUM_THREADS, SMEM_BYTES, stream>>>(tmA, tmB, a);
   return cudaGetLastError();
 }

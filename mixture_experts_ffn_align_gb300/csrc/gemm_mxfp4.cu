@@ -753,12 +753,12 @@ namespace {
 template <bool STAGED, bool MX8, bool FUSE>
 void launch_form(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmS,
                  const Mx4Args& a, cudaStream_t stream) {
-  static bool attr_done = false;
-  if (!attr_done) {
-    cudaFuncSetAttribute(k_ggemm_mxfp4<STAGED, MX8, FUSE>,
-                         cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
-    attr_done = true;
-  }
+  // a failed opt-in shows as the launch's error (cudaGetLastError in the caller)
+  static DeviceOnce attr;
+  (void)attr.call([] {
+    return cudaFuncSetAttribute(k_ggemm_mxfp4<STAGED, MX8, FUSE>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+  });
   k_ggemm_mxfp4<STAGED, MX8, FUSE><<<num_sms(), NUM_THREADS, SMEM_BYTES, stream>>>(tmA, tmB, tmS,
                                                                                   a);
 }

@@ -7,6 +7,8 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include <mutex>
+
 namespace moe {
 
 struct Epilogue;   // optional GEMM epilogue work (moe_common.cuh)
@@ -16,14 +18,37 @@ constexpr int kRouteWarps = 8;        // warps per routing CTA
 
 inline int route_segments(int R) { return (R + kRouteSeg - 1) / kRouteSeg; }
 
+constexpr int kMaxDevices = 64;               // devices the per-device caches cover
+int device_index();                           // current device, in [0, kMaxDevices)
 int num_sms();                                // SMs of the current device
 int* dev_error_word();                        // device address of the error word
 void watchdog_params(uint64_t* limit_ns, int* never_arrive);
 
-// Routing half of moe_align_permute (three launches).
+// One-time setup per device: kernel attributes (the dynamic shared-memory
+// opt-in) belong to the device they were set on.  call(f) runs f() on the
+// current device until it has succeeded there once; later calls return
+// cudaSuccess without running it.  Thread-safe.
+class DeviceOnce {
+ public:
+  template <class F>
+  cudaError_t call(F&& f) {
+    const int d = device_index();
+    std::lock_guard<std::mutex> lk(mu_);
+    if ((done_ >> d) & 1u) return cudaSuccess;
+    const cudaError_t e = f();
+    if (e == cudaSuccess) done_ |= 1ull << d;
+    return e;
+  }
+
+ private:
+  std::mutex mu_;
+  uint64_t done_ = 0;
+};
+
 // Stage 1 routes R items over E experts in one CTA (k_route_small) rather than
 // three kernels (histograms, scan, scatter).
 bool route_in_one_cta(int R, int E);
+// Routing half of moe_align_permute (one or three launches).
 cudaError_t launch_route(const int32_t* topk_ids, int R, int E, int block_size, int cap,
                          int32_t* hist, int32_t* sorted_ids, int32_t* block_expert_ids,
                          int32_t* expert_offsets, int32_t* num_post_padded, int32_t* inv_perm,

@@ -305,12 +305,12 @@ cudaError_t launch_route(const int32_t* topk_ids, int R, int E, int block_size, 
   const int Gs = R > 0 ? (R + S - 1) / S : 0;
   if (route_in_one_cta(R, E)) {
     const size_t sh_small = (size_t)Gs * E * sizeof(int32_t);   // <= 32 x 1024 x 4 B
-    static bool attr_done = false;
-    if (!attr_done) {
-      cudaFuncSetAttribute(k_route_small, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           32 * MOE_MAX_EXPERTS * (int)sizeof(int32_t));
-      attr_done = true;
-    }
+    static DeviceOnce attr;
+    const cudaError_t ea = attr.call([] {
+      return cudaFuncSetAttribute(k_route_small, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  32 * MOE_MAX_EXPERTS * (int)sizeof(int32_t));
+    });
+    if (ea != cudaSuccess) return ea;
     k_route_small<<<1, kSmallThreads, sh_small, stream>>>(
         topk_ids, R, E, block_size, cap, S, Gs, expert_offsets, num_post_padded,
         block_expert_ids, sorted_ids, inv_perm, dev_error_word());
