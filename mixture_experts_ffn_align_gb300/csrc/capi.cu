@@ -11,6 +11,7 @@
 #include <cmath>
 #include <cstdio>
 #include <cstring>
+#include <atomic>
 #include <mutex>
 
 #include "../../include/moe_ffn.h"
@@ -22,7 +23,7 @@ namespace moe {
 __device__ int g_dev_error_word = 0;
 
 namespace {
-int g_sms[kMaxDevices];
+std::atomic<int> g_sms[kMaxDevices];   // SM count per device, 0 until queried
 int* g_err_ptr[kMaxDevices];
 std::mutex g_dev_mu;
 int64_t g_watchdog_ns = 0;
@@ -40,12 +41,13 @@ int device_index() { return current_device(); }
 
 int num_sms() {
   const int d = current_device();
-  if (g_sms[d] == 0) {
-    int n = 0;
+  int n = g_sms[d].load(std::memory_order_relaxed);
+  if (n == 0) {
     cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, d);
-    g_sms[d] = n > 0 ? n : 1;
+    if (n <= 0) n = 1;
+    g_sms[d].store(n, std::memory_order_relaxed);
   }
-  return g_sms[d];
+  return n;
 }
 
 int* dev_error_word() {
