@@ -298,7 +298,16 @@ moe_status act_mul_quant(const moe_problem* p, const void* h1, const int32_t* nu
                          void* z, float* z_scale, void* stream);
 
 /* Stage 4: grouped GEMM2, Y2[row, h] = sum_j z[row, j] * w2[e, h, j] (same
- * passages as stage 2).  out: y2 [S,H] bf16. */
+ * passages as stage 2).  out: y2 [S,H] bf16.
+ *
+ * Concurrency of stages 2 and 4 in MOE_Q_BF16: at prefill sizes the GEMM runs
+ * on SM pairs whose tiles are handed out by a device counter.  These entry
+ * points take the counter from a library-owned ring of 64 per device, so
+ * launches of them that overlap on the GPU (other streams, or graph replays
+ * running beside them) must number fewer than 64, and a launch captured in a
+ * CUDA graph keeps its counter at every replay: order such replays with the
+ * other stage-2/4 launches on one stream.  fused_experts and its variants
+ * keep their counters in the caller's workspace and have no such limit. */
 moe_status grouped_gemm_w2(const moe_problem* p, const void* z, const float* z_scale,
                            const void* w2, const void* w2_scale,
                            const int32_t* block_expert_ids, const int32_t* num_post_padded,

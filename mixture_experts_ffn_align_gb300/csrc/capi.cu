@@ -30,9 +30,12 @@ int64_t g_watchdog_ns = 0;
 int g_never_arrive = 0;
 int g_bf16_form = 0;   // 0: by size, 1: single SM, 2: SM pairs
 
+// The current device, or -1 when it cannot be read or lies beyond the
+// per-device caches (kMaxDevices); callers then fail instead of borrowing
+// another device's cached values.
 int current_device() {
-  int d = 0;
-  if (cudaGetDevice(&d) != cudaSuccess || d < 0 || d >= kMaxDevices) return 0;
+  int d = -1;
+  if (cudaGetDevice(&d) != cudaSuccess || d < 0 || d >= kMaxDevices) return -1;
   return d;
 }
 }  // namespace
@@ -41,6 +44,7 @@ int device_index() { return current_device(); }
 
 int num_sms() {
   const int d = current_device();
+  if (d < 0) return 0;            // a zero grid: the launch fails with a CUDA error
   int n = g_sms[d].load(std::memory_order_relaxed);
   if (n == 0) {
     cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, d);
@@ -52,6 +56,7 @@ int num_sms() {
 
 int* dev_error_word() {
   const int d = current_device();
+  if (d < 0) return nullptr;
   std::lock_guard<std::mutex> lk(g_dev_mu);
   if (g_err_ptr[d] == nullptr) {
     void* p = nullptr;
@@ -166,8 +171,13 @@ int splits_for_tiles(const moe_problem* p, int64_t tiles) {
 }
 
 struct Layout {
-  size_t hist, sorted, blocks, offsets, npp, inv, xperm, xscale, h1, z, zscale, y2, part, total;
+  size_t hist, sorted, blocks, offsets, npp, inv, ctr, xperm, xscale, h1, z, zscale, y2, part,
+      total;
 };
+
+// Tile counters of the SM-pair bf16 GEMMs of one call (GEMM1's, then GEMM2's:
+// two ints each), zeroed on the call's stream before them.
+constexpr size_t kTileCtrBytes = 4 * sizeof(int32_t);
 
 Layout layout(const moe_problem* p) {
   Layout L{};
@@ -187,6 +197,7 @@ Layout layout(const moe_problem* p) {
   L.offsets = take(((size_t)p->E + 1) * 4);
   L.npp = take(4);
   L.inv = take(R * 4);
+  L.ctr = take(kTileCtrBytes);
   // x_perm is dead once GEMM1 has run, so GEMM2's output reuses its storage
   L.xperm = take(std::max(cap * H * xb, cap * H * 2));
   L.y2 = L.xperm;
@@ -216,7 +227,7 @@ bool valid_batched(const moe_problem* p, int max_tokens) {
 }
 
 struct BatchedLayout {
-  size_t blocks, npp, sorted, xq, xscale, h1, z, zscale, total;
+  size_t blocks, npp, ctr, sorted, xq, xscale, h1, z, zscale, total;
 };
 
 BatchedLayout batched_layout(const moe_problem* p, int max_tokens) {
@@ -231,6 +242,7 @@ BatchedLayout batched_layout(const moe_problem* p, int max_tokens) {
   };
   L.blocks = take(rows / 128 * 4);
   L.npp = take(4);
+  L.ctr = take(kTileCtrBytes);
   L.sorted = q ? take(rows * 4) : 0;
   L.xq = q ? take(rows * H) : 0;
   L.xscale = q ? take(rows * (H / act_group(p)) * 4) : 0;
@@ -346,11 +358,13 @@ namespace {
 cudaError_t launch_bf16_gemm(int64_t rows_per_expert, const void* A, int cap, int K,
                              const void* B, int b_rows_total, int b_rows_per_expert, int n_out,
                              const int32_t* block_expert_ids, const int32_t* num_post_padded,
-                             void* out, bool fuse_act, const Epilogue& ep, cudaStream_t s) {
+                             void* out, bool fuse_act, const Epilogue& ep, cudaStream_t s,
+                             int* tile_ctr = nullptr) {
   const bool pairs = g_bf16_form == 2 || (g_bf16_form == 0 && rows_per_expert >= 2 * 128);
   if (pairs)
     return launch_ggemm_bf16_2sm(A, cap, K, B, b_rows_total, b_rows_per_expert, n_out,
-                                 block_expert_ids, num_post_padded, out, fuse_act, ep, s);
+                                 block_expert_ids, num_post_padded, out, fuse_act, ep, s,
+                                 tile_ctr);
   return launch_ggemm_bf16(A, cap, K, B, b_rows_total, b_rows_per_expert, n_out,
                            block_expert_ids, num_post_padded, out, fuse_act, ep, s);
 }
@@ -358,11 +372,15 @@ cudaError_t launch_bf16_gemm(int64_t rows_per_expert, const void* A, int cap, in
 
 extern "C" {
 
-moe_status grouped_gemm_w13_ex(const moe_problem* p, const void* x_perm, const float* x_scale,
-                               const void* w13, const void* w13_scale, const void* w13_bias,
-                               const int32_t* block_expert_ids,
-                               const int32_t* num_post_padded, void* out, float* out_scale,
-                               int fuse_act, void* stream) {
+}  // extern "C"
+
+namespace {
+// Stage 2 with the tile counter of the SM-pair bf16 form given (nullptr: the
+// library ring), shared by the entry point and fused_experts.
+moe_status gemm_w13(const moe_problem* p, const void* x_perm, const float* x_scale,
+                    const void* w13, const void* w13_scale, const void* w13_bias,
+                    const int32_t* block_expert_ids, const int32_t* num_post_padded, void* out,
+                    float* out_scale, int fuse_act, void* stream, int* tile_ctr) {
   if (!valid_problem(p)) return MOE_ERR_INVALID_ARG;
   if (p->M == 0) return MOE_OK;
   if (!x_perm || !w13 || !block_expert_ids || !num_post_padded || !out) return MOE_ERR_INVALID_ARG;
@@ -373,7 +391,7 @@ moe_status grouped_gemm_w13_ex(const moe_problem* p, const void* x_perm, const f
   if (p->quant == MOE_Q_BF16) {
     return cuda_status(launch_bf16_gemm((int64_t)p->M * p->topk / p->E, x_perm, cap, p->H, w13,
                                         p->E * 2 * p->I, 2 * p->I, 2 * p->I, block_expert_ids,
-                                        num_post_padded, out, fuse_act != 0, ep, s));
+                                        num_post_padded, out, fuse_act != 0, ep, s, tile_ctr));
   }
   if (!x_scale || !w13_scale) return MOE_ERR_INVALID_ARG;
   if (fuse_act && !out_scale) return MOE_ERR_INVALID_ARG;
@@ -388,6 +406,18 @@ moe_status grouped_gemm_w13_ex(const moe_problem* p, const void* x_perm, const f
                                       2 * p->I, 2 * p->I, block_expert_ids, num_post_padded, out,
                                       ep, s, out_scale, fuse_act != 0,
                                       p->act_scale_fmt == MOE_SCALE_UE8M0));
+}
+}  // namespace
+
+extern "C" {
+
+moe_status grouped_gemm_w13_ex(const moe_problem* p, const void* x_perm, const float* x_scale,
+                               const void* w13, const void* w13_scale, const void* w13_bias,
+                               const int32_t* block_expert_ids,
+                               const int32_t* num_post_padded, void* out, float* out_scale,
+                               int fuse_act, void* stream) {
+  return gemm_w13(p, x_perm, x_scale, w13, w13_scale, w13_bias, block_expert_ids,
+                  num_post_padded, out, out_scale, fuse_act, stream, nullptr);
 }
 
 moe_status grouped_gemm_w13(const moe_problem* p, const void* x_perm, const float* x_scale,
@@ -412,11 +442,14 @@ moe_status act_mul_quant(const moe_problem* p, const void* h1, const int32_t* nu
                                     static_cast<cudaStream_t>(stream)));
 }
 
-moe_status grouped_gemm_w2_ex(const moe_problem* p, const void* z, const float* z_scale,
-                              const void* w2, const void* w2_scale, const void* w2_bias,
-                              const int32_t* block_expert_ids, const int32_t* num_post_padded,
-                              const int32_t* sorted_ids, const float* topk_weights, void* y2,
-                              void* stream) {
+}  // extern "C"
+
+namespace {
+// Stage 4 with the SM-pair tile counter given (see gemm_w13).
+moe_status gemm_w2(const moe_problem* p, const void* z, const float* z_scale, const void* w2,
+                   const void* w2_scale, const void* w2_bias, const int32_t* block_expert_ids,
+                   const int32_t* num_post_padded, const int32_t* sorted_ids,
+                   const float* topk_weights, void* y2, void* stream, int* tile_ctr) {
   if (!valid_problem(p)) return MOE_ERR_INVALID_ARG;
   if (p->M == 0) return MOE_OK;
   if (!z || !w2 || !block_expert_ids || !num_post_padded || !y2) return MOE_ERR_INVALID_ARG;
@@ -430,7 +463,7 @@ moe_status grouped_gemm_w2_ex(const moe_problem* p, const void* z, const float* 
   if (p->quant == MOE_Q_BF16) {
     return cuda_status(launch_bf16_gemm((int64_t)p->M * p->topk / p->E, z, cap, p->I, w2,
                                         p->E * p->H, p->H, p->H, block_expert_ids,
-                                        num_post_padded, y2, false, ep, s));
+                                        num_post_padded, y2, false, ep, s, tile_ctr));
   }
   if (!z_scale || !w2_scale) return MOE_ERR_INVALID_ARG;
   if (block_scaled(p))
@@ -441,6 +474,18 @@ moe_status grouped_gemm_w2_ex(const moe_problem* p, const void* z, const float* 
   return cuda_status(launch_ggemm_fp8(z, z_scale, cap, p->I, w2,
                                       static_cast<const float*>(w2_scale), p->E * p->H, p->H,
                                       p->H, block_expert_ids, num_post_padded, y2, ep, s));
+}
+}  // namespace
+
+extern "C" {
+
+moe_status grouped_gemm_w2_ex(const moe_problem* p, const void* z, const float* z_scale,
+                              const void* w2, const void* w2_scale, const void* w2_bias,
+                              const int32_t* block_expert_ids, const int32_t* num_post_padded,
+                              const int32_t* sorted_ids, const float* topk_weights, void* y2,
+                              void* stream) {
+  return gemm_w2(p, z, z_scale, w2, w2_scale, w2_bias, block_expert_ids, num_post_padded,
+                 sorted_ids, topk_weights, y2, stream, nullptr);
 }
 
 moe_status grouped_gemm_w2(const moe_problem* p, const void* z, const float* z_scale,
@@ -524,7 +569,10 @@ moe_status fused_experts_ex(const moe_problem* p, const void* x, const void* w13
   auto i32 = [&](size_t off) { return reinterpret_cast<int32_t*>(ws + off); };
   auto f32 = [&](size_t off) { return reinterpret_cast<float*>(ws + off); };
   int32_t *sorted = i32(L.sorted), *blocks = i32(L.blocks), *offs = i32(L.offsets),
-          *npp = i32(L.npp), *inv = i32(L.inv);
+          *npp = i32(L.npp), *inv = i32(L.inv), *ctr = i32(L.ctr);
+  if (!quantised(p) &&
+      cudaMemsetAsync(ctr, 0, kTileCtrBytes, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return cuda_status(cudaGetLastError());
   moe_status st = moe_align_permute(p, x, topk_ids, topk_weights, sorted, blocks, offs, npp, inv,
                                     ws + L.xperm, quantised(p) ? f32(L.xscale) : nullptr,
                                     ws + L.hist, L.sorted - L.hist, stream);
@@ -533,8 +581,8 @@ moe_status fused_experts_ex(const moe_problem* p, const void* x, const void* w13
   if (!quantised(p) && splits > 1 && !w2_bias && !p->router_weight_in_gemm2 &&
       !p->apply_router_weight_on_input) {
     // decode-sized: GEMM2 in K slices over all SMs, the reduce sums them
-    st = grouped_gemm_w13_ex(p, ws + L.xperm, nullptr, w13, nullptr, w13_bias, blocks, npp,
-                             ws + L.z, nullptr, 1, stream);
+    st = gemm_w13(p, ws + L.xperm, nullptr, w13, nullptr, w13_bias, blocks, npp, ws + L.z,
+                  nullptr, 1, stream, ctr);
     if (st != MOE_OK) return st;
     st = grouped_gemm_w2_split(p, ws + L.z, w2, blocks, npp, sorted, splits, f32(L.part),
                                stream);
@@ -542,11 +590,11 @@ moe_status fused_experts_ex(const moe_problem* p, const void* x, const void* w13
     return unpermute_reduce_split(p, f32(L.part), splits, inv, topk_weights, y, stream);
   }
   if (!quantised(p)) {
-    st = grouped_gemm_w13_ex(p, ws + L.xperm, nullptr, w13, nullptr, w13_bias, blocks, npp,
-                             ws + L.z, nullptr, 1, stream);
+    st = gemm_w13(p, ws + L.xperm, nullptr, w13, nullptr, w13_bias, blocks, npp, ws + L.z,
+                  nullptr, 1, stream, ctr);
     if (st != MOE_OK) return st;
-    st = grouped_gemm_w2_ex(p, ws + L.z, nullptr, w2, nullptr, w2_bias, blocks, npp, sorted,
-                            topk_weights, ws + L.y2, stream);
+    st = gemm_w2(p, ws + L.z, nullptr, w2, nullptr, w2_bias, blocks, npp, sorted, topk_weights,
+                 ws + L.y2, stream, ctr + 2);
   } else if (block_scaled(p)) {
     // GEMM1 writes the quantised activation directly (act_mul_quant fused)
     st = grouped_gemm_w13_ex(p, ws + L.xperm, f32(L.xscale), w13, w13_scale, w13_bias, blocks,
@@ -669,6 +717,7 @@ moe_status fused_experts_batched(const moe_problem* p, const void* x,
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   int32_t* blocks = reinterpret_cast<int32_t*>(ws + L.blocks);
   int32_t* npp = reinterpret_cast<int32_t*>(ws + L.npp);
+  int32_t* ctr = reinterpret_cast<int32_t*>(ws + L.ctr);
   int32_t* sorted = quantised(p) ? reinterpret_cast<int32_t*>(ws + L.sorted) : nullptr;
   float* xscale = reinterpret_cast<float*>(ws + L.xscale);
   float* zscale = reinterpret_cast<float*>(ws + L.zscale);
@@ -680,11 +729,13 @@ moe_status fused_experts_batched(const moe_problem* p, const void* x,
   if (e != cudaSuccess) return cuda_status(e);
   if (!quantised(p)) {
     // the layout's rows are GEMM1's rows as they are: no permute
-    e = launch_bf16_gemm(expected_m, x, rows, H, w13, E * 2 * I, 2 * I, 2 * I, blocks, npp,
-                         ws + L.z, true, ep, s);
+    e = cudaMemsetAsync(ctr, 0, kTileCtrBytes, s);
+    if (e == cudaSuccess)
+      e = launch_bf16_gemm(expected_m, x, rows, H, w13, E * 2 * I, 2 * I, 2 * I, blocks, npp,
+                           ws + L.z, true, ep, s, ctr);
     if (e != cudaSuccess) return cuda_status(e);
     e = launch_bf16_gemm(expected_m, ws + L.z, rows, I, w2, E * H, H, H, blocks, npp, y, false,
-                         ep, s);
+                         ep, s, ctr + 2);
     return cuda_status(e);
   }
   // quantised: per-row dynamic quantisation of the layout, then the same stages

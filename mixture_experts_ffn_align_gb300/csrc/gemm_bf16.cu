@@ -414,6 +414,7 @@ cudaError_t launch_ggemm_bf16(const void* A, int cap, int K, const void* B, int 
   }
   watchdog_params(&a.limit_ns, &a.never_arrive);
   a.err = dev_error_word();
+  if (a.err == nullptr) return cudaErrorInvalidDevice;   // no usable current device
   a.ep = ep;
   // K slices of kb_per_split steps each; the caller sizes and reads the
   // partials by `splits`, so a count that would leave a slice empty is an

@@ -28,7 +28,9 @@
 //    only after all ten readers have released it.  A statically strided
 //    order let the pairs drift apart by several tiles, so that pairs meant to
 //    share a weight tile read it from DRAM at different times.  The counter
-//    is one of a ring of slots, one per launch in flight; the last CTA to
+//    is the caller's (two ints in the fused_experts workspace, zeroed on its
+//    stream before the launch) or, for the stage entry points, one of a
+//    library-owned ring of slots, one per launch in flight; the last CTA to
 //    finish resets it.
 //  * every wait is bounded; the final cluster barrier is reached by both CTAs
 //    after their bounded loops.
@@ -429,18 +431,23 @@ cudaError_t launch_pairs(const CUtensorMap& tmA, const CUtensorMap& tmB, const P
   return cudaLaunchKernelEx(&cfg, k_ggemm_bf16_2sm<FUSE>, tmA, tmB, a);
 }
 
-// A tile counter for the next launch: slots rotate so that launches in
-// flight at the same time (other streams) use different counters.
+// A tile counter for the next launch that brings none of its own (the stage
+// entry points): slots of a library-owned ring rotate, so launches in flight
+// at the same time (other streams) use different counters as long as fewer
+// than CTR_SLOTS of them overlap.  The device address of the ring is looked
+// up once per device under a lock.
 int* next_tile_counter() {
-  static int* base[64] = {};
+  static DeviceOnce once;
+  static int* base[kMaxDevices] = {};
   static std::atomic<unsigned> seq{0};
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
-  if (base[dev] == nullptr) {
+  const int dev = device_index();
+  const cudaError_t e = once.call([&] {
     void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_pair_tile_ctr) != cudaSuccess) return nullptr;
-    base[dev] = static_cast<int*>(p);
-  }
+    const cudaError_t r = cudaGetSymbolAddress(&p, g_pair_tile_ctr);
+    if (r == cudaSuccess) base[dev] = static_cast<int*>(p);
+    return r;
+  });
+  if (e != cudaSuccess || dev < 0) return nullptr;
   return base[dev] + 2 * (seq.fetch_add(1) % CTR_SLOTS);
 }
 
@@ -450,7 +457,7 @@ cudaError_t launch_ggemm_bf16_2sm(const void* A, int cap, int K, const void* B, 
                                   int b_rows_per_expert, int n_out,
                                   const int32_t* block_expert_ids,
                                   const int32_t* num_post_padded, void* out, bool fuse_act,
-                                  const Epilogue& ep, cudaStream_t stream) {
+                                  const Epilogue& ep, cudaStream_t stream, int* tile_ctr) {
   if (cap <= 0) return cudaSuccess;
   CUtensorMap tmA, tmB;
   if (!make_tmap_k_sw128(&tmA, A, (uint64_t)cap, (uint64_t)K, 2, 128) ||
@@ -480,8 +487,9 @@ cudaError_t launch_ggemm_bf16_2sm(const void* A, int cap, int K, const void* B, 
   }
   watchdog_params(&a.limit_ns, &a.never_arrive);
   a.err = dev_error_word();
+  if (a.err == nullptr) return cudaErrorInvalidDevice;   // no usable current device
   a.ep = ep;
-  a.tile_ctr = next_tile_counter();
+  a.tile_ctr = tile_ctr != nullptr ? tile_ctr : next_tile_counter();
   if (a.tile_ctr == nullptr) return cudaErrorInvalidDevice;
   return fuse_act ? launch_pairs<true>(tmA, tmB, a, stream)
                   : launch_pairs<false>(tmA, tmB, a, stream);

@@ -463,6 +463,7 @@ cudaError_t launch_ggemm_fp8(const void* A, const float* a_scale, int cap, int K
   a.group_max = sched_group_max(K, 1);
   watchdog_params(&a.limit_ns, &a.never_arrive);
   a.err = dev_error_word();
+  if (a.err == nullptr) return cudaErrorInvalidDevice;   // no usable current device
   return fuse_act ? launch_fp8_form<true>(tmA, tmB, a, stream)
                   : launch_fp8_form<false>(tmA, tmB, a, stream);
 }

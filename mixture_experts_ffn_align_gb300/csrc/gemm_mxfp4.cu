@@ -815,6 +815,7 @@ cudaError_t launch_ggemm_mxfp4(const void* A, const float* a_scale, int cap, int
   a.group_max = sched_group_max(K, 1);
   watchdog_params(&a.limit_ns, &a.never_arrive);
   a.err = dev_error_word();
+  if (a.err == nullptr) return cudaErrorInvalidDevice;   // no usable current device
   // weight scales staged by TMA when their rows are 16-byte multiples
   const bool staged = K % 512 == 0 && (reinterpret_cast<uintptr_t>(b_scale) & 15u) == 0;
   CUtensorMap tmS = tmB;        // unused by the register form

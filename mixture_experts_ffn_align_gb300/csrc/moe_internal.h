@@ -19,9 +19,11 @@ constexpr int kRouteWarps = 8;        // warps per routing CTA
 inline int route_segments(int R) { return (R + kRouteSeg - 1) / kRouteSeg; }
 
 constexpr int kMaxDevices = 64;               // devices the per-device caches cover
-int device_index();                           // current device, in [0, kMaxDevices)
-int num_sms();                                // SMs of the current device
-int* dev_error_word();                        // device address of the error word
+// Current device in [0, kMaxDevices), or -1 when cudaGetDevice fails or the
+// index is beyond the caches (the library then reports an error).
+int device_index();
+int num_sms();                                // SMs of the current device (0 if -1)
+int* dev_error_word();                        // device address of the error word (or null)
 void watchdog_params(uint64_t* limit_ns, int* never_arrive);
 
 // One-time setup per device: kernel attributes (the dynamic shared-memory
@@ -33,6 +35,7 @@ class DeviceOnce {
   template <class F>
   cudaError_t call(F&& f) {
     const int d = device_index();
+    if (d < 0) return cudaErrorInvalidDevice;
     std::lock_guard<std::mutex> lk(mu_);
     if ((done_ >> d) & 1u) return cudaSuccess;
     const cudaError_t e = f();
@@ -119,12 +122,17 @@ cudaError_t launch_ggemm_bf16(const void* A, int cap, int K, const void* B, int 
 cudaError_t launch_unpermute_reduce_split(const float* part, int splits, int H, int M, int topk,
                                           const int32_t* inv_perm, const float* topk_weights,
                                           void* y, cudaStream_t stream);
-// The same GEMM issued on SM pairs (cta_group::2, 256 x 256 tiles).
+// The same GEMM issued on SM pairs (cta_group::2, 256 x 256 tiles).  Tiles
+// are handed out by a device counter of two ints: tile_ctr (zero when the
+// launch starts; the launch leaves it zero), or with nullptr one slot of a
+// library-owned ring (launches that overlap on the GPU must be fewer than its
+// 64 slots, and a launch captured in a graph keeps its slot).
 cudaError_t launch_ggemm_bf16_2sm(const void* A, int cap, int K, const void* B,
                                   int b_rows_total, int b_rows_per_expert, int n_out,
                                   const int32_t* block_expert_ids,
                                   const int32_t* num_post_padded, void* out, bool fuse_act,
-                                  const Epilogue& ep, cudaStream_t stream);
+                                  const Epilogue& ep, cudaStream_t stream,
+                                  int* tile_ctr = nullptr);
 
 // FP8 (e4m3) grouped GEMM with fp32 1x128 activation scales and 128x128
 // weight block scales: out = sum_kb sa*sb*partial_kb (bf16 output).

@@ -300,6 +300,8 @@ cudaError_t launch_route(const int32_t* topk_ids, int R, int E, int block_size, 
                          int32_t* hist, int32_t* sorted_ids, int32_t* block_expert_ids,
                          int32_t* expert_offsets, int32_t* num_post_padded, int32_t* inv_perm,
                          cudaStream_t stream) {
+  int* err = dev_error_word();
+  if (err == nullptr) return cudaErrorInvalidDevice;   // no usable current device
   // small batches: one CTA, histograms in shared memory
   const int S = 32 * ((R + 32 * 32 - 1) / (32 * 32));   // items per warp, a multiple of 32
   const int Gs = R > 0 ? (R + S - 1) / S : 0;
@@ -313,15 +315,14 @@ cudaError_t launch_route(const int32_t* topk_ids, int R, int E, int block_size, 
     if (ea != cudaSuccess) return ea;
     k_route_small<<<1, kSmallThreads, sh_small, stream>>>(
         topk_ids, R, E, block_size, cap, S, Gs, expert_offsets, num_post_padded,
-        block_expert_ids, sorted_ids, inv_perm, dev_error_word());
+        block_expert_ids, sorted_ids, inv_perm, err);
     return cudaGetLastError();
   }
   const int G = route_segments(R);
   const int ctas = (G + kRouteWarps - 1) / kRouteWarps;
   const size_t sh = (size_t)kRouteWarps * E * sizeof(int32_t);
   if (G > 0) {
-    k_route_hist<<<ctas, kRouteWarps * 32, sh, stream>>>(topk_ids, R, E, G, hist,
-                                                         dev_error_word());
+    k_route_hist<<<ctas, kRouteWarps * 32, sh, stream>>>(topk_ids, R, E, G, hist, err);
   }
   k_route_scan<<<1, 1024, 0, stream>>>(hist, G, E, block_size, R, cap, expert_offsets,
                                        num_post_padded, block_expert_ids, sorted_ids);

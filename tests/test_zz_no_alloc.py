@@ -6,9 +6,12 @@ fixed array inside the library instead of a caller workspace.
 The check: two calls in a row through the C ABI, on two different problems,
 each compared with the workspace-taking moe_align_permute on the same inputs.
 Indices and permuted rows are compared bit for bit (the tolerance the other
-stage-1 tests use).  The second call runs on a smaller problem right after a
-larger one, so stale histogram contents left in the shared array would show.
-This file is named to be collected last."""
+stage-1 tests use).  Both problems are large enough to route in several CTAs,
+the path that keeps its per-segment histograms in the shared array (a small
+problem routes in one CTA with its histograms in shared memory).  The second
+has fewer segments and experts than the first, so stale histogram contents
+left in the array by the first call would show.  This file is named to be
+collected last."""
 import numpy as np
 import pytest
 import torch
@@ -49,8 +52,14 @@ def _compare(p, d):
 
 def test_noalloc_matches_workspace_entry_on_two_calls_in_a_row():
     big = CONFIGS["dsfp8"]                       # 128 segments x 256 experts, FP8 permute
-    small = MoEConfig("small", M=300, H=512, I=256, E=8, topk=2, quant="bf16",
+    # 32 segments x 128 experts: 16384 routed items take the multi-CTA routing
+    # too, and read a smaller corner of the array the first call filled
+    small = MoEConfig("small", M=2048, H=512, I=256, E=128, topk=8, quant="bf16",
                       routing="softmax", seed=71, invalid_frac=0.1)
+    # three routing kernels (histograms, scan, scatter) + the permute
+    assert moe.moe_align_permute_launches(moe.Problem.from_config(small)) == 4
+    assert moe.moe_align_workspace_bytes(moe.Problem.from_config(small)) < \
+        moe.moe_align_workspace_bytes(moe.Problem.from_config(big))
     for cfg in (big, small):
         d = make_inputs(cfg, "cuda", weights=False)
         _compare(moe.Problem.from_config(cfg), d)
