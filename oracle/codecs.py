@@ -64,11 +64,23 @@ def minifloat_decode(codes, exp_bits: int, man_bits: int, bias: int):
     return sign * np.where(ef == 0, sub, nrm)
 
 
-def e4m3_decode(codes):
-    """uint8 e4m3fn codes -> fp64 values; 0x7F/0xFF decode to NaN."""
+def _e4m3_decode_fields(codes):
     c = np.asarray(codes, dtype=np.int64)
     v = minifloat_decode(c, 4, 3, 7)
     return np.where((c & 0x7F) == 0x7F, np.nan, v)
+
+
+_E4M3_TABLE = _e4m3_decode_fields(np.arange(256))
+
+
+def e4m3_decode(codes):
+    """uint8 e4m3fn codes -> fp64 values; 0x7F/0xFF decode to NaN.  Each code
+    is decoded from its bit fields (``minifloat_decode``); uint8 arrays look
+    the same values up in the table of all 256 codes."""
+    c = np.asarray(codes)
+    if c.dtype == np.uint8:
+        return _E4M3_TABLE[c]
+    return _e4m3_decode_fields(c)
 
 
 def e4m3_encode(values):
@@ -88,15 +100,32 @@ def e4m3_encode(values):
     return code.astype(np.uint8)
 
 
-def e2m1_decode(codes):
-    """4-bit E2M1 codes -> fp64 values: +-{0, .5, 1, 1.5, 2, 3, 4, 6}."""
+def _e2m1_decode_fields(codes):
     return minifloat_decode(np.asarray(codes, dtype=np.int64) & 0xF, 2, 1, 1)
+
+
+_E2M1_TABLE = _e2m1_decode_fields(np.arange(256))
+
+
+def e2m1_decode(codes):
+    """4-bit E2M1 codes -> fp64 values: +-{0, .5, 1, 1.5, 2, 3, 4, 6} (the
+    high nibble of a byte is ignored; uint8 arrays use the table of the
+    field decode)."""
+    c = np.asarray(codes)
+    if c.dtype == np.uint8:
+        return _E2M1_TABLE[c]
+    return _e2m1_decode_fields(c)
+
+
+_E8M0_TABLE = np.ldexp(1.0, np.arange(256) - 127)
 
 
 def e8m0_decode(codes):
     """E8M0 scale codes -> 2**(code - 127)."""
-    c = np.asarray(codes, dtype=np.int64)
-    return np.ldexp(1.0, c - 127)
+    c = np.asarray(codes)
+    if c.dtype == np.uint8:
+        return _E8M0_TABLE[c]
+    return np.ldexp(1.0, c.astype(np.int64) - 127)
 
 
 def unpack_fp4(packed, k: int):

@@ -310,10 +310,15 @@ def fused_experts_per_token(x, topk_ids, topk_weights, w13, w2, w13_scale=None,
     # weights are decoded once per expert; items are still evaluated one by one
     experts = sorted({int(ids[t, i]) for t in tokens for i in range(k) if ids[t, i] >= 0})
     for e in experts:
-        W13 = dequant_weights(w13[e][None], None if w13_scale is None else
-                              np.asarray(w13_scale)[e][None], quant)[0]
-        W2 = dequant_weights(w2[e][None], None if w2_scale is None else
-                             np.asarray(w2_scale)[e][None], quant)[0]
+        if quant == "fp8":
+            # codes decoded once per expert; the scales enter per K block
+            W13 = codecs.e4m3_decode(w13[e])
+            W2 = codecs.e4m3_decode(w2[e])
+        else:
+            W13 = dequant_weights(w13[e][None], None if w13_scale is None else
+                                  np.asarray(w13_scale)[e][None], quant)[0]
+            W2 = dequant_weights(w2[e][None], None if w2_scale is None else
+                                 np.asarray(w2_scale)[e][None], quant)[0]
         I = W2.shape[1]
         for t in tokens:
             for i in range(k):
@@ -327,7 +332,7 @@ def fused_experts_per_token(x, topk_ids, topk_weights, w13, w2, w13_scale=None,
                 else:
                     q, s = quant_act_1x128(xt[None], fmt, act_group(quant))
                     if quant == "fp8":
-                        h = _fp8_matvec(q[0], s[0], w13[e], np.asarray(w13_scale)[e])
+                        h = _fp8_matvec(q[0], s[0], W13, np.asarray(w13_scale)[e])
                     else:
                         h = W13 @ (q[0] * np.repeat(s[0], act_group(quant)))
                 if w13_bias is not None:
@@ -342,7 +347,7 @@ def fused_experts_per_token(x, topk_ids, topk_weights, w13, w2, w13_scale=None,
                 else:
                     q, s = quant_act_1x128(z[None], fmt, act_group(quant))
                     if quant == "fp8":
-                        o = _fp8_matvec(q[0], s[0], w2[e], np.asarray(w2_scale)[e])
+                        o = _fp8_matvec(q[0], s[0], W2, np.asarray(w2_scale)[e])
                     else:
                         o = W2 @ (q[0] * np.repeat(s[0], act_group(quant)))
                 if w2_bias is not None:
@@ -367,9 +372,9 @@ def fused_experts_per_token(x, topk_ids, topk_weights, w13, w2, w13_scale=None,
     return (y, items, used_w) if return_items else y
 
 
-def _fp8_matvec(qa, sa, w_codes, w_scale):
-    """h[n] = sum_kb sa[kb] * sb[n/128, kb] * sum_{k in kb} qa[k] * qb[n, k]."""
-    qb = codecs.e4m3_decode(w_codes)             # [N, K]
+def _fp8_matvec(qa, sa, qb, w_scale):
+    """h[n] = sum_kb sa[kb] * sb[n/128, kb] * sum_{k in kb} qa[k] * qb[n, k]
+    (qb: the decoded e4m3 weight values [N, K])."""
     N, K = qb.shape
     part = np.einsum("nbj,bj->nb", qb.reshape(N, K // 128, 128), qa.reshape(K // 128, 128))
     sb = np.repeat(np.asarray(w_scale, dtype=np.float64), 128, axis=0)[:N]   # [N, K/128]
