@@ -10,6 +10,14 @@ events can bracket each stage on the launching stream.  The fused_experts
 call itself is timed as well (fused_call_ms).  The weights (2.82 GB) are far
 larger than L2, so no flush is needed between steps.
 
+The same run then measures the other workloads the same way, each with its
+own inputs, and reports them under "workloads": Mixtral-shaped decode (M=64),
+the DeepSeek-class FP8 layer (M=8192, H=7168, I=2048, E=256, top-8, 128x128
+fp32 block scales, skewed routing), the same shape with MXFP4 W4A8 weights
+(M=2048, uniform routing) and with MXFP8 1x32 weights; plus a dense e4m3
+GEMM probe (torch._scaled_mm) as a measured FP8 denominator beside the
+nominal one.  --no-extra times the --workload alone.
+
 Metric: routed tokens/s (M * top-k per second), whole job over all ranks.
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
@@ -237,7 +245,7 @@ def _gemm1_roofline(cfg, peaks, peak, ratio, flops, w13_bytes, ms):
     if t_flop >= t_mem:
         return {"bound": "tensor", "achieved": tflops, "peak": peak, "unit": "TFLOP/s",
                 "frac": tflops / peak,
-                "peak_source": f"bf16_tflops_sustained x {ratio:g} ({peaks['source']})",
+                "peak_source": f"bf16 x {ratio:g} ({peaks['source']})",
                 "algorithmic_per_launch": f"2*R*H*2I = {flops:.4e} FLOP", **common}
     return {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
             "frac": gbs / peaks["hbm_gbs"], "peak_source": f"hbm_gbs ({peaks['source']})",
@@ -328,22 +336,57 @@ def _stage_plan(moe, p, cfg, d, b, stream):
     return plan
 
 
-def run_ours(args):
+def _peak_for(peaks, q, timed_s):
+    """Tensor peak of a GEMM timed over a region of timed_s seconds: the
+    measured burst bf16 rate when the region is short (< 1 s: the clocks do
+    not reach the power cap's steady state), else the sustained one; FP8
+    contractions take 2 x that (the recipe's nominal FP8 / bf16 ratio)."""
+    burst = timed_s < 1.0
+    ratio = 2.0 if q else 1.0
+    base = peaks["bf16_tflops"] if burst else peaks["bf16_tflops_sustained"]
+    name = "bf16_tflops (burst)" if burst else "bf16_tflops_sustained"
+    return base * ratio, ratio, f"{name} x {ratio:g} ({peaks['source']}; timed region " \
+                                f"{timed_s:.3f} s)"
+
+
+def fp8_probe(dev):
+    """Dense e4m3 GEMM throughput of torch._scaled_mm (cuBLASLt), 8192^3, best
+    of 10 launches timed with CUDA events: a measured FP8 denominator shown
+    beside the nominal 2 x bf16 one.  None where the call is unavailable."""
+    import torch
+    try:
+        n = 8192
+        g = torch.Generator(device=dev).manual_seed(0)
+        a = torch.randn(n, n, device=dev, generator=g).to(torch.float8_e4m3fn)
+        b = torch.randn(n, n, device=dev, generator=g).to(torch.float8_e4m3fn).t()
+        one = torch.ones((), device=dev)
+        f = lambda: torch._scaled_mm(a, b, scale_a=one, scale_b=one, out_dtype=torch.bfloat16)
+        for _ in range(3):
+            f()
+        best = None
+        for _ in range(10):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            f()
+            e1.record()
+            e1.synchronize()
+            ms = e0.elapsed_time(e1)
+            best = ms if best is None else min(best, ms)
+        return {"tflops": 2.0 * n ** 3 / (best * 1e-3) / 1e12, "ms": best,
+                "how": "torch._scaled_mm e4m3 x e4m3 -> bf16, 8192^3, best of 10 (CUDA events)"}
+    except Exception as ex:       # noqa: BLE001 -- reported, not fatal
+        return {"tflops": None, "error": str(ex)[:200]}
+
+
+def _measure(moe, cfg, args, dev, world, rank, full, fp8_tflops=None):
+    """One workload: inputs generated on the device, W warm-up steps, K timed
+    steps of the stage plan (CUDA events per stage on the launching stream),
+    then the fused_experts call and the end-to-end host-buffer entry.  With
+    ``full`` also the router timing.  Returns (rank 0's record, ms_per_step)."""
     import torch
     import torch.distributed as dist
+    from moe_synth import make_inputs
 
-    import mixture_experts_ffn_align_gb300 as moe
-    from moe_synth import get_config, make_inputs
-
-    world, rank, local = _dist()
-    if world > 1:
-        torch.cuda.set_device(local)
-        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
-    dev = torch.device("cuda", local)
-    torch.cuda.set_device(dev)
-    moe.lib()
-
-    cfg = _workload(args)
     if rank > 0:
         cfg = cfg.with_(seed=cfg.seed + 100 * rank)
     d = make_inputs(cfg, dev)
@@ -424,39 +467,44 @@ def run_ours(args):
     if moe.moe_sync_status(stream) != 0:
         raise RuntimeError("device error in the e2e region")
 
-    # the step before the path (not in the step): the router on logits of
-    # this workload's shape, softmax + renormalise
-    gen = torch.Generator(device=dev).manual_seed(cfg.seed)
-    logits = torch.randn(cfg.M, cfg.E, device=dev, generator=gen)
-    r_w = torch.empty(cfg.M, cfg.topk, dtype=torch.float32, device=dev)
-    r_ids = torch.empty(cfg.M, cfg.topk, dtype=torch.int32, device=dev)
-    for _ in range(3):
-        moe.moe_topk_router(logits, cfg.topk, r_w, r_ids, stream=stream)
-    barrier()
-    # a launch is a few microseconds of GPU work, less than its host-side
-    # call: time 20 launches captured in a CUDA graph
-    graph = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(graph):          # captured on torch's side stream
-        for _ in range(20):
-            moe.moe_topk_router(logits, cfg.topk, r_w, r_ids)
-    graph.replay()
-    barrier()
-    rs, re_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    r_reps = 10
-    rs.record(stream)
-    for _ in range(r_reps):
+    router = None
+    if full:
+        # the step before the path (not in the step): the router on logits of
+        # this workload's shape, softmax + renormalise
+        gen = torch.Generator(device=dev).manual_seed(cfg.seed)
+        logits = torch.randn(cfg.M, cfg.E, device=dev, generator=gen)
+        r_w = torch.empty(cfg.M, cfg.topk, dtype=torch.float32, device=dev)
+        r_ids = torch.empty(cfg.M, cfg.topk, dtype=torch.int32, device=dev)
+        for _ in range(3):
+            moe.moe_topk_router(logits, cfg.topk, r_w, r_ids, stream=stream)
+        barrier()
+        # a launch is a few microseconds of GPU work, less than its host-side
+        # call: time 20 launches captured in a CUDA graph
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):          # captured on torch's side stream
+            for _ in range(20):
+                moe.moe_topk_router(logits, cfg.topk, r_w, r_ids)
         graph.replay()
-    re_.record(stream)
-    barrier()
-    router_ms = rs.elapsed_time(re_) / (20 * r_reps)
-    router_bytes = cfg.M * cfg.E * 4 + cfg.M * cfg.topk * 8
+        barrier()
+        rs, re_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        r_reps = 10
+        rs.record(stream)
+        for _ in range(r_reps):
+            graph.replay()
+        re_.record(stream)
+        barrier()
+        router_ms = rs.elapsed_time(re_) / (20 * r_reps)
+        router_bytes = cfg.M * cfg.E * 4 + cfg.M * cfg.topk * 8
+        router = {"ms": router_ms, "bytes": router_bytes,
+                  "gbs": router_bytes / (router_ms * 1e-3) / 1e9,
+                  "note": "moe_topk_router on [M, E] fp32 logits (softmax, renormalise); "
+                          "the step before the path, not part of a step"}
 
     # max over ranks
     elapsed_ms, e2e_s, fused_ms = max_over_ranks([elapsed_ms, e2e_s, fused_ms], world, dev)
     ms = elapsed_ms / args.steps
     R = cfg.R
-    value = world * R / (ms * 1e-3)
-
+    out = None
     if rank == 0:
         peaks = _peaks()
         q = cfg.quant != "bf16"
@@ -464,15 +512,19 @@ def run_ours(args):
         gemm2_flops = 2.0 * R * cfg.I * cfg.H
         g1 = [n for n, _ in plan if n.startswith("gemm1")][0]
         g2 = [n for n, _ in plan if n.startswith("gemm2")][0]
-        # a contraction takes the peak of its own dtype: FP8 = bf16 x 2 (4.5 / 2.25 nominal)
-        ratio = 2.0 if q else 1.0
-        peak = peaks["bf16_tflops_sustained"] * ratio
-        ach = gemm1_flops / (stage_ms[g1] * 1e-3) / 1e12
+        peak, ratio, peak_src = _peak_for(peaks, q, elapsed_ms * 1e-3)
         wbytes = {"bf16": 2.0, "fp8": 1.0, "mxfp4": 0.5, "mxfp8": 1.0}[cfg.quant]
         w13_bytes = cfg.E * 2 * cfg.I * cfg.H * wbytes
         w2_bytes = cfg.E * cfg.H * cfg.I * wbytes
+        g2_tf = gemm2_flops / (stage_ms[g2] * 1e-3) / 1e12
+        roof = _gemm1_roofline(cfg, peaks, peak, ratio, gemm1_flops, w13_bytes, stage_ms[g1])
+        roof["peak_source"] = peak_src if roof["bound"] == "tensor" else roof["peak_source"]
+        sust = peaks["bf16_tflops_sustained"] * ratio
+        roof["tensor_frac_vs_sustained"] = roof["tensor_frac"] * peak / sust
+        if q and fp8_tflops:
+            roof["tensor_frac_vs_fp8_probe"] = roof["tensor_frac"] * peak / fp8_tflops
         out = {
-            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "metric": METRIC, "value": world * R / (ms * 1e-3), "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": {"bf16": "bf16", "fp8": "e4m3 (fp32 accumulate)",
@@ -482,10 +534,8 @@ def run_ours(args):
             "tflops": (gemm1_flops + gemm2_flops) / (ms * 1e-3) / 1e12,
             "stages_ms": stage_ms,
             "fused_call_ms": fused_ms,
-            "roofline": _gemm1_roofline(cfg, peaks, peak, ratio, gemm1_flops, w13_bytes,
-                                        stage_ms[g1]),
-            "gemm2_roofline": {"achieved": gemm2_flops / (stage_ms[g2] * 1e-3) / 1e12,
-                               "frac": gemm2_flops / (stage_ms[g2] * 1e-3) / 1e12 / peak,
+            "roofline": roof,
+            "gemm2_roofline": {"kernel": g2, "achieved": g2_tf, "frac": g2_tf / peak,
                                "weight_hbm_frac": w2_bytes / (stage_ms[g2] * 1e-3) / 1e9 /
                                peaks["hbm_gbs"]},
             "e2e": {"value": world * R / e2e_s, "unit": UNIT, "h2d_bytes_per_step": h2d,
@@ -493,14 +543,12 @@ def run_ours(args):
                     "path": "fused_experts_from_host on pinned host buffers: topk ids/weights "
                             "copied in; x read and y written in place in host memory by the "
                             "permute and reduce kernels (each row once, over the host link)"},
-            "router": {"ms": router_ms, "bytes": router_bytes,
-                       "gbs": router_bytes / (router_ms * 1e-3) / 1e9,
-                       "note": "moe_topk_router on [M, E] fp32 logits (softmax, renormalise); "
-                               "the step before the path, not part of a step"},
             "gpu_launches": launches_per_step * args.steps,
             "clocks": clk.summary(),
         }
-        if world == 1 and not args.no_cpu_baseline:
+        if router is not None:
+            out["router"] = router
+        if world == 1 and full and not args.no_cpu_baseline:
             arrs = _oracle_arrays(d, cfg)
             t2 = _time_oracle(arrs, [0, 1], cfg)   # also warms the BLAS threads
             # about 15 s of CPU work, at least 4 tokens
@@ -513,6 +561,48 @@ def run_ours(args):
                 "sample": f"{len(tokens)} tokens ({len(tokens) * cfg.topk} routed items) of the "
                           f"{cfg.name} workload through the per-token fp64 oracle, weights "
                           f"decoded once outside timing; {secs:.1f} s"}
+    del d, b, ws, hws
+    torch.cuda.empty_cache()
+    return out
+
+
+# the other workloads measured in the same default run, after the headline
+EXTRA_WORKLOADS = ("decode", "dsfp8", "mxfp4", "mxfp8")
+
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    import mixture_experts_ffn_align_gb300 as moe
+
+    world, rank, local = _dist()
+    if world > 1:
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    moe.lib()
+
+    cfg = _workload(args)
+    probe = fp8_probe(dev) if rank == 0 and world == 1 and not args.no_extra else None
+    fp8_tf = probe["tflops"] if probe else None
+    out = _measure(moe, cfg, args, dev, world, rank, True, fp8_tf)
+    extra = {}
+    if world == 1 and not args.no_extra and args.workload == WORKLOAD and not args.tokens \
+            and not args.experts:
+        from moe_synth import get_config
+        for name in EXTRA_WORKLOADS:
+            rec = _measure(moe, get_config(name), args, dev, world, rank, False, fp8_tf)
+            keep = ("value", "unit", "ms_per_step", "dtype", "config", "tflops", "stages_ms",
+                    "fused_call_ms", "roofline", "gemm2_roofline", "e2e", "gpu_launches",
+                    "clocks")
+            extra[name] = {k: rec[k] for k in keep}
+    if rank == 0:
+        if extra:
+            out["workloads"] = extra
+        if probe is not None:
+            out["fp8_probe"] = probe
         print(json.dumps(out), flush=True)
     if world > 1:
         dist.destroy_process_group()
@@ -661,6 +751,8 @@ def main():
     ap.add_argument("--experts", type=int, default=0,
                     help="override E (smaller cases for profiling captures)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extra", action="store_true",
+                    help="time only --workload (no FP8 probe, no other workloads)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

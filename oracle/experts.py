@@ -292,7 +292,8 @@ def fused_experts_per_token(x, topk_ids, topk_weights, w13, w2, w13_scale=None,
 
     For each (t, i) with e = id[t, i] >= 0: quantise x_t (quantised modes),
     h = W13_e x_t, z = SiLU(h_gate) * h_up, o = W2_e z, y_t += w * o.  The
-    same roundings as form 2 are applied item by item.  ``tokens`` restricts
+    same roundings as form 2 are applied item by item (an expert's items are
+    stacked as the rows of one matrix product; every step is row-wise).  ``tokens`` restricts
     the tokens evaluated (outputs of different tokens are independent).
     Returns y [len(tokens), H]; with ``return_items`` also the per-item W2
     outputs o [len(tokens), k, H] (zero for skipped slots) and the weights
@@ -307,7 +308,9 @@ def fused_experts_per_token(x, topk_ids, topk_weights, w13, w2, w13_scale=None,
     w2 = np.asarray(w2)
     H = x.shape[1]
     outs = {}
-    # weights are decoded once per expert; items are still evaluated one by one
+    # weights are decoded once per expert; the expert's routed items are rows
+    # of one matrix, each row put through the steps on its own (quantisation
+    # per row, the products row by row in one matrix product)
     experts = sorted({int(ids[t, i]) for t in tokens for i in range(k) if ids[t, i] >= 0})
     for e in experts:
         if quant == "fp8":
@@ -320,43 +323,42 @@ def fused_experts_per_token(x, topk_ids, topk_weights, w13, w2, w13_scale=None,
             W2 = dequant_weights(w2[e][None], None if w2_scale is None else
                                  np.asarray(w2_scale)[e][None], quant)[0]
         I = W2.shape[1]
-        for t in tokens:
-            for i in range(k):
-                if ids[t, i] != e:
-                    continue
-                xt = x[t]
-                if apply_router_weight_on_input:
-                    xt = codecs.round_bf16(codecs.round_fp32(xt * wts[t, i]))
-                if fmt is None:
-                    h = W13 @ xt
-                else:
-                    q, s = quant_act_1x128(xt[None], fmt, act_group(quant))
-                    if quant == "fp8":
-                        h = _fp8_matvec(q[0], s[0], W13, np.asarray(w13_scale)[e])
-                    else:
-                        h = W13 @ (q[0] * np.repeat(s[0], act_group(quant)))
-                if w13_bias is not None:
-                    h = h + np.asarray(w13_bias, dtype=np.float64)[e]
-                if not exact:
-                    h = codecs.round_bf16(h)
-                z = gated(h[:I], h[I:], act_recipe)
-                if fmt is None:
-                    if not exact:
-                        z = codecs.round_bf16(z)
-                    o = W2 @ z
-                else:
-                    q, s = quant_act_1x128(z[None], fmt, act_group(quant))
-                    if quant == "fp8":
-                        o = _fp8_matvec(q[0], s[0], W2, np.asarray(w2_scale)[e])
-                    else:
-                        o = W2 @ (q[0] * np.repeat(s[0], act_group(quant)))
-                if w2_bias is not None:
-                    o = o + np.asarray(w2_bias, dtype=np.float64)[e]
-                if router_weight_in_gemm2:
-                    o = wts[t, i] * o
-                if not exact:
-                    o = codecs.round_bf16(o)
-                outs[(t, i)] = o
+        its = [(t, i) for t in tokens for i in range(k) if ids[t, i] == e]
+        xt = np.stack([x[t] for t, _ in its])
+        if apply_router_weight_on_input:
+            w_in = np.array([wts[t, i] for t, i in its])
+            xt = codecs.round_bf16(codecs.round_fp32(xt * w_in[:, None]))
+        if fmt is None:
+            h = xt @ W13.T
+        else:
+            q, s = quant_act_1x128(xt, fmt, act_group(quant))
+            if quant == "fp8":
+                h = _fp8_rows(q, s, W13, np.asarray(w13_scale)[e])
+            else:
+                h = (q * np.repeat(s, act_group(quant), axis=1)) @ W13.T
+        if w13_bias is not None:
+            h = h + np.asarray(w13_bias, dtype=np.float64)[e]
+        if not exact:
+            h = codecs.round_bf16(h)
+        z = gated(h[:, :I], h[:, I:], act_recipe)
+        if fmt is None:
+            if not exact:
+                z = codecs.round_bf16(z)
+            o = z @ W2.T
+        else:
+            q, s = quant_act_1x128(z, fmt, act_group(quant))
+            if quant == "fp8":
+                o = _fp8_rows(q, s, W2, np.asarray(w2_scale)[e])
+            else:
+                o = (q * np.repeat(s, act_group(quant), axis=1)) @ W2.T
+        if w2_bias is not None:
+            o = o + np.asarray(w2_bias, dtype=np.float64)[e]
+        if router_weight_in_gemm2:
+            o = np.array([wts[t, i] for t, i in its])[:, None] * o
+        if not exact:
+            o = codecs.round_bf16(o)
+        for j, ti in enumerate(its):
+            outs[ti] = o[j]
     y = np.zeros((len(tokens), H))
     items = np.zeros((len(tokens), k, H))
     used_w = np.zeros((len(tokens), k))
@@ -372,13 +374,18 @@ def fused_experts_per_token(x, topk_ids, topk_weights, w13, w2, w13_scale=None,
     return (y, items, used_w) if return_items else y
 
 
-def _fp8_matvec(qa, sa, qb, w_scale):
-    """h[n] = sum_kb sa[kb] * sb[n/128, kb] * sum_{k in kb} qa[k] * qb[n, k]
-    (qb: the decoded e4m3 weight values [N, K])."""
+def _fp8_rows(qa, sa, qb, w_scale):
+    """h[r, n] = sum_kb sa[r, kb] * sb[n/128, kb] * sum_{k in kb} qa[r, k] * qb[n, k]
+    for each row r (qa [R, K] e4m3 values, sa [R, K/128]; qb the decoded e4m3
+    weight values [N, K], w_scale [N/128, K/128])."""
     N, K = qb.shape
-    part = np.einsum("nbj,bj->nb", qb.reshape(N, K // 128, 128), qa.reshape(K // 128, 128))
     sb = np.repeat(np.asarray(w_scale, dtype=np.float64), 128, axis=0)[:N]   # [N, K/128]
-    return (sa[None, :] * sb * part).sum(axis=1)
+    h = np.zeros((qa.shape[0], N))
+    for kb in range(K // 128):
+        ks = slice(kb * 128, (kb + 1) * 128)
+        part = qa[:, ks] @ qb[:, ks].T            # exact: products of e4m3 values
+        h += sa[:, kb][:, None] * sb[None, :, kb] * part
+    return h
 
 
 def batched_experts(x_b, counts, w13, w2, w13_scale=None, w2_scale=None, *, quant="bf16",

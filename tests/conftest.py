@@ -17,3 +17,21 @@ def pytest_configure(config):
 @pytest.fixture(scope="session")
 def golden_dir():
     return GOLDEN
+
+
+def pytest_terminal_summary(terminalreporter):
+    """One line per floating-point parity comparison of the run: the plain
+    max|err| / RMS(y_ref) next to the tolerance and the asserted excess over
+    the bf16 flip allowance (tests/gpu_util.py)."""
+    try:
+        from tests.gpu_util import PARITY_LOG
+    except Exception:
+        return
+    if not PARITY_LOG:
+        return
+    terminalreporter.section("parity: max|err|/RMS per comparison")
+    for what, st in PARITY_LOG:
+        terminalreporter.write_line(
+            f"{what:<40s} max|err|/RMS {st['max_err_over_rms']:.3e}  "
+            f"excess/RMS {st['max_excess_over_rms']:.3e}  rms_err/RMS "
+            f"{st['rms_err_over_rms']:.3e}  tol {st['tol']:g}  n {st['n']}")

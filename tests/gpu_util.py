@@ -21,10 +21,17 @@ import torch
 BF16_TOL = 1e-2
 QUANT_TOL = 3e-2
 
+# (what, stats) of every check_close call, printed at the end of the run by
+# the terminal-summary hook in conftest.py, so the log records the plain
+# max|err| / RMS of each comparison next to the asserted quantities.
+PARITY_LOG = []
+
 
 def np32(t):
     if t is None:
         return None
+    if isinstance(t, np.ndarray):
+        return t
     t = t.detach()
     if t.dtype == torch.bfloat16:
         return t.float().cpu().numpy()
@@ -71,7 +78,8 @@ def check_close(gpu, ref, tol, what="", allow=None):
     excess = float(np.max(err - allow))
     rms_err = float(np.sqrt(np.mean(err ** 2)))
     stats = {"max_err_over_rms": float(err.max() / rms), "rms_err_over_rms": rms_err / rms,
-             "max_excess_over_rms": excess / rms}
+             "max_excess_over_rms": excess / rms, "tol": tol, "n": int(ref.size)}
+    PARITY_LOG.append((what, stats))
     assert excess <= tol * rms, f"{what}: {stats}"
     assert rms_err <= tol / 3 * rms, f"{what}: {stats}"
     return stats
@@ -98,3 +106,33 @@ def bf16_gemm_form(form):
         yield
     finally:
         moe.moe_debug_set_bf16_gemm_form("auto")
+
+
+def cover_tokens(topk_ids, E, n, seed, experts=None, block=128,
+                 which=("first", "last_block", "last")):
+    """Tokens for a sampled check of a full-size output: for each expert in
+    ``experts`` (default: every expert with routed items) the tokens of its
+    first routed row ("first"), of the first row of its last padded block
+    ("last_block") and of its last live row ("last", the partial block's
+    edge), then random other tokens up to ``n`` in all.  Rows and blocks
+    follow the oracle's routing (ascending routed item within an expert)."""
+    from oracle import routing
+    ids = np.asarray(np32(topk_ids))
+    M, k = ids.shape
+    route = routing.align_permute(ids, E, block)
+    sid, offs, cnt = route["sorted_token_ids"], route["expert_offsets"], route["expert_counts"]
+    chosen = set()
+    for e in (range(E) if experts is None else experts):
+        c = int(cnt[e])
+        if c == 0:
+            continue
+        lo = int(offs[e])
+        rows = {"first": lo, "last_block": lo + (c - 1) // block * block, "last": lo + c - 1}
+        for w in which:
+            chosen.add(int(sid[rows[w]]) // k)
+    rng = np.random.default_rng(seed)
+    rest = np.setdiff1d(np.arange(M), np.fromiter(chosen, dtype=np.int64))
+    extra = max(0, n - len(chosen))
+    if extra:
+        chosen.update(int(t) for t in rng.choice(rest, min(extra, rest.size), replace=False))
+    return np.array(sorted(chosen), dtype=np.int64)

@@ -66,3 +66,23 @@ def test_reference_arm_other_ranks_exit_quietly():
 def test_warmup_below_three_is_refused():
     r = _bench({}, "--impl", "reference", "--workload", "tiny", "--warmup", "2")
     assert r.returncode != 0
+
+
+def test_cover_tokens_reaches_each_experts_block_edges():
+    """The sampled full-size checks pick, per expert, the tokens of its first
+    routed row, of its last block's first row and of its last live row."""
+    import numpy as np
+
+    from oracle import routing
+    from tests.gpu_util import cover_tokens
+    rng = np.random.default_rng(0)
+    M, k, E = 700, 2, 4
+    ids = rng.integers(0, E, size=(M, k)).astype(np.int32)
+    toks = cover_tokens(ids, E, 40, 1)
+    route = routing.align_permute(ids, E, 128)
+    sid, offs, cnt = route["sorted_token_ids"], route["expert_offsets"], route["expert_counts"]
+    for e in range(E):
+        lo, c = int(offs[e]), int(cnt[e])
+        for row in (lo, lo + (c - 1) // 128 * 128, lo + c - 1):
+            assert sid[row] // k in toks
+    assert len(toks) == 40 and np.all(np.diff(toks) > 0)

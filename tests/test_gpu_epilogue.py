@@ -125,3 +125,75 @@ def test_variant_arguments_rejected():
         moe.fused_experts(q, d["x"], d["w13"], None, d["w2"], None, d["topk_weights"][:, :1],
                           d["topk_ids"][:, :1].contiguous(), torch.empty_like(d["x"]), ws)
     assert ei.value.status == 1
+
+
+@pytest.mark.parametrize("bias,in_gemm2,recipe", VARIANTS)
+def test_fp8_fp32_scales_epilogue_stage_by_stage(bias, in_gemm2, recipe):
+    """FP8 block scales with fp32 (not power-of-two) activation scales and
+    every epilogue variant, stage by stage through the _ex entry points: each
+    GPU stage against the oracle's same stage fed the GPU's own input (so a
+    one-ulp difference upstream cannot move a group scale downstream), then
+    the whole path against the oracle."""
+    cfg = CASES["fp8"][0].with_(act_scale_fmt="fp32", seed=84)
+    d = make_inputs(cfg, "cuda")
+    b13, b2 = _biases(cfg, 5) if bias else (None, None)
+    p = moe.Problem.from_config(cfg, router_weight_in_gemm2=in_gemm2, act_recipe=recipe)
+    b = moe.stage_buffers(p)
+    moe.moe_align_permute(p, d["x"], d["topk_ids"], None, b["sorted_ids"], b["block_expert_ids"],
+                          b["expert_offsets"], b["num_post_padded"], b["inv_perm"], b["x_perm"],
+                          b["x_perm_scale"], b["align_ws"])
+    moe.grouped_gemm_w13_ex(p, b["x_perm"], b["x_perm_scale"], d["w13"], d["w13_scale"], b13,
+                            b["block_expert_ids"], b["num_post_padded"], b["h1"], None,
+                            fuse_act=False)
+    moe.act_mul_quant(p, b["h1"], b["num_post_padded"], b["z"], b["z_scale"])
+    moe.grouped_gemm_w2_ex(p, b["z"], b["z_scale"], d["w2"], d["w2_scale"], b2,
+                           b["block_expert_ids"], b["num_post_padded"], b["sorted_ids"],
+                           d["topk_weights"], b["y2"])
+    moe.unpermute_reduce(p, b["y2"], b["inv_perm"], d["topk_weights"], b["y"])
+    assert moe.moe_sync_status() == 0
+    a = oracle_inputs(d)
+    route = experts.align_permute(a["topk_ids"], cfg.E, 128)
+    n = route["num_tokens_post_padded"]
+    R = cfg.M * cfg.topk
+    sid = route["sorted_token_ids"]
+    live = sid[:n] < R
+    xq, xs = experts.permute_rows(a["x"], route, cfg.topk, scale_fmt="fp32")
+    # the quantising permute: codes and fp32 scales bit for bit
+    assert np.array_equal(codecs.e4m3_decode(np32(b["x_perm"]))[:n][live], xq[:n][live])
+    assert np.array_equal(np32(b["x_perm_scale"])[:n][live], xs[:n][live])
+    h1 = experts.grouped_gemm(xq, xs, a["w13"], a["w13_scale"], route, 128, "fp8")
+    h1 = experts.add_expert_bias(h1, None if b13 is None else np32(b13), route, 128)
+    check_close(np32(b["h1"])[:n][live], codecs.round_bf16(h1[:n][live]), QUANT_TOL,
+                "fp8 fp32-scale h1 (+bias)")
+    # activation recipe + fp32 1x128 quantisation of the GPU's own h1
+    h1g = np32(b["h1"]).astype(np.float64)
+    zo, zso = experts.quant_act_1x128(experts.act_mul(h1g[:n], cfg.I, recipe=recipe), "fp32")
+    zq = codecs.e4m3_decode(np32(b["z"])).astype(np.float64)
+    zs = np32(b["z_scale"]).astype(np.float64)
+    # scales: fp32 amax/448 on both sides, amax may differ in its last fp32 bit
+    np.testing.assert_allclose(zs[:n][live], zso[live], rtol=2 ** -20)
+    zg = zq[:n] * np.repeat(zs[:n], 128, axis=1)
+    check_close(zg[live], (zo * np.repeat(zso, 128, axis=1))[live], QUANT_TOL,
+                "fp8 fp32-scale z (recipe)" if recipe else "fp8 fp32-scale z")
+    codes_equal = np.mean(np32(b["z"])[:n][live] == codecs.e4m3_encode(zo[live]))
+    assert codes_equal > 0.999, codes_equal
+    # GEMM2 (+bias, router weight) on the GPU's own z
+    zq[n:] = 0
+    zs[n:] = 0
+    zq[:n][~live] = 0
+    zs[:n][~live] = 0
+    y2 = experts.grouped_gemm(zq, zs, a["w2"], a["w2_scale"], route, 128, "fp8")
+    y2 = experts.add_expert_bias(y2, None if b2 is None else np32(b2), route, 128)
+    if in_gemm2:
+        wflat = a["topk_weights"].reshape(-1).astype(np.float64)
+        y2 = y2 * np.where(sid < R, wflat[np.minimum(sid, R - 1)], 0.0)[:, None]
+    check_close(np32(b["y2"])[:n][live], codecs.round_bf16(y2[:n][live]), QUANT_TOL,
+                "fp8 fp32-scale y2")
+    # the reduce of the GPU's y2
+    y2g = np32(b["y2"]).astype(np.float64)
+    want = experts.unpermute_reduce(y2g, route["inv_perm"], a["topk_weights"],
+                                    apply_router_weight_on_input=in_gemm2)
+    check_close(np32(b["y"]), want, QUANT_TOL, "fp8 fp32-scale reduce")
+    # and the whole path against the oracle
+    ref, allow = _oracle(cfg, d, b13, b2, in_gemm2, recipe)
+    check_close(np32(b["y"]), ref, QUANT_TOL, "fp8 fp32-scale whole path", allow)

@@ -10,7 +10,7 @@ import mixture_experts_ffn_align_gb300 as moe
 from moe_synth import CONFIGS, MoEConfig, make_inputs
 from oracle import codecs, experts, routing
 
-from .gpu_util import QUANT_TOL, check_close, flip_allowance, np32, oracle_inputs
+from .gpu_util import QUANT_TOL, check_close, cover_tokens, flip_allowance, np32, oracle_inputs
 
 pytestmark = pytest.mark.gpu
 
@@ -101,8 +101,10 @@ def test_fp8_deepseek_full_size_sampled():
     y = _run_fused(cfg, d)
     yn = np32(y)
     assert np.all(np.isfinite(yn)) and np.all(np.abs(yn).max(axis=1) > 0)
-    tokens = np.unique(np.concatenate([[0, cfg.M - 1],
-                                       np.random.default_rng(7).choice(cfg.M, 6, replace=False)]))
+    # every hot expert's first block, last block and last live row, and
+    # random other tokens: 256 in all
+    tokens = cover_tokens(d["topk_ids"], cfg.E, 256, 7, experts=range(info["hot_experts"]))
+    assert len(tokens) >= 256
     ref, allow = _oracle(cfg, d, tokens)
-    check_close(yn[tokens], ref, QUANT_TOL, "dsfp8", allow)
+    check_close(yn[tokens], ref, QUANT_TOL, f"dsfp8 full size, {len(tokens)} tokens", allow)
     assert torch.equal(_run_fused(cfg, d), y)

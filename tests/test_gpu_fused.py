@@ -13,7 +13,8 @@ import mixture_experts_ffn_align_gb300 as moe
 from moe_synth import CONFIGS, MoEConfig, make_inputs
 from oracle import experts
 
-from .gpu_util import BF16_TOL, bf16_gemm_form, check_close, flip_allowance, np32, oracle_inputs
+from .gpu_util import (BF16_TOL, bf16_gemm_form, check_close, cover_tokens, flip_allowance,
+                       np32, oracle_inputs)
 
 pytestmark = pytest.mark.gpu
 
@@ -114,10 +115,51 @@ def test_fused_experts_full_size_sampled(name, form):
     assert np.all(np.isfinite(yn))
     assert np.all(np.abs(yn).max(axis=1) > 0)
     # sampled tokens against the per-token oracle
-    rng = np.random.default_rng(123)
-    tokens = np.sort(rng.choice(cfg.M, 24, replace=False))
-    tokens = np.unique(np.concatenate([[0, cfg.M - 1], tokens]))
+    # every expert's first block, last block and last live row, then random
+    # other tokens: 128 in all
+    tokens = cover_tokens(d["topk_ids"], cfg.E, 128, 123)
+    assert len(tokens) >= 128
     ref, allow = _oracle_tokens(cfg, d, tokens)
-    check_close(yn[tokens], ref, BF16_TOL, name, allow)
+    check_close(yn[tokens], ref, BF16_TOL, f"{name} {form} full size, {len(tokens)} tokens", allow)
     # a second run gives bit-identical output (no atomics on the data path)
     assert torch.equal(y_again, y)
+
+
+def test_fused_experts_on_two_streams_at_once():
+    """Two fused_experts calls, each with its own workspace, on two streams
+    with no ordering between them: the SM-pair GEMMs take their tile counters
+    from each call's workspace, so the calls cannot hand each other's tiles
+    out.  The staged entry points on two streams draw different slots of the
+    library's counter ring.  Every result equals the single-stream one."""
+    cfg = MoEConfig("two", M=1024, H=512, I=512, E=2, topk=2, quant="bf16",
+                    routing="softmax", seed=46)
+    assert cfg.M * cfg.topk >= 256 * cfg.E            # the SM-pair form
+    d = make_inputs(cfg, "cuda")
+    y_ref = _run(cfg, d)
+    p = moe.Problem.from_config(cfg)
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+    ws = [torch.empty(moe.moe_workspace_bytes(p), dtype=torch.uint8, device="cuda")
+          for _ in range(2)]
+    ys = [torch.zeros_like(d["x"]) for _ in range(2)]
+    bs = [moe.stage_buffers(p) for _ in range(2)]
+    torch.cuda.synchronize()
+    for _ in range(6):
+        for j, s in enumerate((s1, s2)):
+            moe.fused_experts(p, d["x"], d["w13"], None, d["w2"], None, d["topk_weights"],
+                              d["topk_ids"], ys[j], ws[j], stream=s)
+        for j, s in enumerate((s1, s2)):
+            b = bs[j]
+            moe.moe_align_permute(p, d["x"], d["topk_ids"], None, b["sorted_ids"],
+                                  b["block_expert_ids"], b["expert_offsets"],
+                                  b["num_post_padded"], b["inv_perm"], b["x_perm"], None,
+                                  b["align_ws"], stream=s)
+            moe.grouped_gemm_w13(p, b["x_perm"], None, d["w13"], None, b["block_expert_ids"],
+                                 b["num_post_padded"], b["z"], None, fuse_act=True, stream=s)
+            moe.grouped_gemm_w2(p, b["z"], None, d["w2"], None, b["block_expert_ids"],
+                                b["num_post_padded"], b["y2"], stream=s)
+            moe.unpermute_reduce(p, b["y2"], b["inv_perm"], d["topk_weights"], b["y"], stream=s)
+    torch.cuda.synchronize()
+    assert moe.moe_sync_status() == 0
+    for j in range(2):
+        assert torch.equal(ys[j], y_ref)
+        assert torch.equal(bs[j]["y"], y_ref)
