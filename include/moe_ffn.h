@@ -428,13 +428,14 @@ const char* moe_last_error_string(void);
  * (0, 0) to restore the defaults.  Not thread-safe; affects later launches. */
 void moe_debug_set_watchdog(int64_t limit_ns, int never_arrive);
 
-/* Test hook for the bf16 grouped GEMMs (stages 2 and 4), which come in two
- * forms with identical results up to fp32 summation order: 128 x 256 tiles
- * on one SM, and 256 x 256 tiles on SM pairs (cta_group::2), used when the
- * experts average at least two 128-row blocks (M * topk >= 256 * E).
- * mode 0 restores that choice, 1 forces the single-SM form, 2 the pair form.
- * Not thread-safe; affects later launches.  No counterpart on the pages: it
- * only lets tests reach both forms at any size. */
+/* Test hook for the bf16 and FP8-block grouped GEMMs (stages 2 and 4), which
+ * come in two forms with identical results up to fp32 summation order:
+ * 128 x 256 tiles on one SM, and 256 x 256 tiles on SM pairs (cta_group::2),
+ * used when the experts average at least two 128-row blocks
+ * (M * topk >= 256 * E; the FP8 GEMM1 with the activation fused has the
+ * single-SM form only).  mode 0 restores that choice, 1 forces the single-SM
+ * form, 2 the pair form.  Not thread-safe; affects later launches.  No
+ * counterpart on the pages: it only lets tests reach both forms at any size. */
 void moe_debug_set_bf16_gemm_form(int mode);
 
 #ifdef __cplusplus

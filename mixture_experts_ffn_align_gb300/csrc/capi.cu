@@ -355,13 +355,18 @@ namespace {
 // blocks; below that most pairs would carry a lone block whose second half
 // repeats the first.
 // rows_per_expert: the expected routed rows per expert.
+// SM-pair tiles for the bf16 and FP8-block GEMMs (the debug hook can force
+// either form).
+bool use_pairs(int64_t rows_per_expert) {
+  return g_bf16_form == 2 || (g_bf16_form == 0 && rows_per_expert >= 2 * 128);
+}
+
 cudaError_t launch_bf16_gemm(int64_t rows_per_expert, const void* A, int cap, int K,
                              const void* B, int b_rows_total, int b_rows_per_expert, int n_out,
                              const int32_t* block_expert_ids, const int32_t* num_post_padded,
                              void* out, bool fuse_act, const Epilogue& ep, cudaStream_t s,
                              int* tile_ctr = nullptr) {
-  const bool pairs = g_bf16_form == 2 || (g_bf16_form == 0 && rows_per_expert >= 2 * 128);
-  if (pairs)
+  if (use_pairs(rows_per_expert))
     return launch_ggemm_bf16_2sm(A, cap, K, B, b_rows_total, b_rows_per_expert, n_out,
                                  block_expert_ids, num_post_padded, out, fuse_act, ep, s,
                                  tile_ctr);
@@ -401,6 +406,12 @@ moe_status gemm_w13(const moe_problem* p, const void* x_perm, const float* x_sca
         2 * p->I, 2 * p->I, block_expert_ids, num_post_padded, out,
         p->quant == MOE_Q_MXFP8_1X32, ep, s, out_scale, fuse_act != 0,
         p->act_scale_fmt == MOE_SCALE_UE8M0));
+  if (!fuse_act && use_pairs((int64_t)p->M * p->topk / p->E))
+    return cuda_status(launch_ggemm_fp8_2sm(x_perm, x_scale, cap, p->H, w13,
+                                            static_cast<const float*>(w13_scale),
+                                            p->E * 2 * p->I, 2 * p->I, 2 * p->I,
+                                            block_expert_ids, num_post_padded, out, ep, s,
+                                            tile_ctr));
   return cuda_status(launch_ggemm_fp8(x_perm, x_scale, cap, p->H, w13,
                                       static_cast<const float*>(w13_scale), p->E * 2 * p->I,
                                       2 * p->I, 2 * p->I, block_expert_ids, num_post_padded, out,
@@ -471,6 +482,11 @@ moe_status gemm_w2(const moe_problem* p, const void* z, const float* z_scale, co
                                           static_cast<const uint8_t*>(w2_scale), p->E * p->H,
                                           p->H, p->H, block_expert_ids, num_post_padded, y2,
                                           p->quant == MOE_Q_MXFP8_1X32, ep, s));
+  if (use_pairs((int64_t)p->M * p->topk / p->E))
+    return cuda_status(launch_ggemm_fp8_2sm(z, z_scale, cap, p->I, w2,
+                                            static_cast<const float*>(w2_scale), p->E * p->H,
+                                            p->H, p->H, block_expert_ids, num_post_padded, y2,
+                                            ep, s, tile_ctr));
   return cuda_status(launch_ggemm_fp8(z, z_scale, cap, p->I, w2,
                                       static_cast<const float*>(w2_scale), p->E * p->H, p->H,
                                       p->H, block_expert_ids, num_post_padded, y2, ep, s));
@@ -570,8 +586,7 @@ moe_status fused_experts_ex(const moe_problem* p, const void* x, const void* w13
   auto f32 = [&](size_t off) { return reinterpret_cast<float*>(ws + off); };
   int32_t *sorted = i32(L.sorted), *blocks = i32(L.blocks), *offs = i32(L.offsets),
           *npp = i32(L.npp), *inv = i32(L.inv), *ctr = i32(L.ctr);
-  if (!quantised(p) &&
-      cudaMemsetAsync(ctr, 0, kTileCtrBytes, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+  if (cudaMemsetAsync(ctr, 0, kTileCtrBytes, static_cast<cudaStream_t>(stream)) != cudaSuccess)
     return cuda_status(cudaGetLastError());
   moe_status st = moe_align_permute(p, x, topk_ids, topk_weights, sorted, blocks, offs, npp, inv,
                                     ws + L.xperm, quantised(p) ? f32(L.xscale) : nullptr,
@@ -597,22 +612,22 @@ moe_status fused_experts_ex(const moe_problem* p, const void* x, const void* w13
                  ws + L.y2, stream, ctr + 2);
   } else if (block_scaled(p)) {
     // GEMM1 writes the quantised activation directly (act_mul_quant fused)
-    st = grouped_gemm_w13_ex(p, ws + L.xperm, f32(L.xscale), w13, w13_scale, w13_bias, blocks,
-                             npp, ws + L.z, f32(L.zscale), 1, stream);
+    st = gemm_w13(p, ws + L.xperm, f32(L.xscale), w13, w13_scale, w13_bias, blocks, npp,
+                  ws + L.z, f32(L.zscale), 1, stream, ctr);
     if (st != MOE_OK) return st;
-    st = grouped_gemm_w2_ex(p, ws + L.z, f32(L.zscale), w2, w2_scale, w2_bias, blocks, npp,
-                            sorted, topk_weights, ws + L.y2, stream);
+    st = gemm_w2(p, ws + L.z, f32(L.zscale), w2, w2_scale, w2_bias, blocks, npp, sorted,
+                 topk_weights, ws + L.y2, stream, ctr + 2);
   } else {
     // FP8 block scales: the promotion epilogue bounds this GEMM, and the
     // activation at the end of each tile lengthened it by more than the
     // separate pass costs, so H1 goes through HBM
-    st = grouped_gemm_w13_ex(p, ws + L.xperm, f32(L.xscale), w13, w13_scale, w13_bias, blocks,
-                             npp, ws + L.h1, nullptr, 0, stream);
+    st = gemm_w13(p, ws + L.xperm, f32(L.xscale), w13, w13_scale, w13_bias, blocks, npp,
+                  ws + L.h1, nullptr, 0, stream, ctr);
     if (st != MOE_OK) return st;
     st = act_mul_quant(p, ws + L.h1, npp, ws + L.z, f32(L.zscale), stream);
     if (st != MOE_OK) return st;
-    st = grouped_gemm_w2_ex(p, ws + L.z, f32(L.zscale), w2, w2_scale, w2_bias, blocks, npp,
-                            sorted, topk_weights, ws + L.y2, stream);
+    st = gemm_w2(p, ws + L.z, f32(L.zscale), w2, w2_scale, w2_bias, blocks, npp, sorted,
+                 topk_weights, ws + L.y2, stream, ctr + 2);
   }
   if (st != MOE_OK) return st;
   return unpermute_reduce(p, ws + L.y2, inv, topk_weights, y, stream);

@@ -431,6 +431,8 @@ cudaError_t launch_pairs(const CUtensorMap& tmA, const CUtensorMap& tmB, const P
   return cudaLaunchKernelEx(&cfg, k_ggemm_bf16_2sm<FUSE>, tmA, tmB, a);
 }
 
+}  // namespace
+
 // A tile counter for the next launch that brings none of its own (the stage
 // entry points): slots of a library-owned ring rotate, so launches in flight
 // at the same time (other streams) use different counters as long as fewer
@@ -450,8 +452,6 @@ int* next_tile_counter() {
   if (e != cudaSuccess || dev < 0) return nullptr;
   return base[dev] + 2 * (seq.fetch_add(1) % CTR_SLOTS);
 }
-
-}  // namespace
 
 cudaError_t launch_ggemm_bf16_2sm(const void* A, int cap, int K, const void* B, int b_rows_total,
                                   int b_rows_per_expert, int n_out,

@@ -412,6 +412,17 @@ __device__ __forceinline__ void umma_f16_pair(uint32_t d_tmem, uint64_t a_desc, 
       : "memory");
 }
 
+// Same for 8-bit float operands (kind::f8f6f4, e4m3 x e4m3 here) on the pair.
+__device__ __forceinline__ void umma_f8_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                             uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 // Warpgroup register reallocation: every thread of a 128-thread warpgroup
 // executes the same one; increases wait until decreases elsewhere in the CTA
 // have released enough of the registers the CTA was launched with.

@@ -134,6 +134,11 @@ cudaError_t launch_ggemm_bf16_2sm(const void* A, int cap, int K, const void* B,
                                   const Epilogue& ep, cudaStream_t stream,
                                   int* tile_ctr = nullptr);
 
+// A tile counter (two ints, zero between launches) from the library-owned
+// ring of the SM-pair GEMMs, for launches that bring none of their own;
+// nullptr when the current device is unusable.
+int* next_tile_counter();
+
 // FP8 (e4m3) grouped GEMM with fp32 1x128 activation scales and 128x128
 // weight block scales: out = sum_kb sa*sb*partial_kb (bf16 output).
 // fuse_act (GEMM1 only, n_out = b_rows_per_expert = 2I): the gated
@@ -144,6 +149,16 @@ cudaError_t launch_ggemm_fp8(const void* A, const float* a_scale, int cap, int K
                              const int32_t* num_post_padded, void* out, const Epilogue& ep,
                              cudaStream_t stream, float* z_scale = nullptr,
                              bool fuse_act = false, bool ue8m0 = false);
+
+// The same FP8 GEMM (no fused activation) issued on SM pairs (cta_group::2,
+// 256 x 256 tiles); n_out == b_rows_per_expert, a multiple of 128.  Tile
+// counter as for launch_ggemm_bf16_2sm.
+cudaError_t launch_ggemm_fp8_2sm(const void* A, const float* a_scale, int cap, int K,
+                                 const void* B, const float* b_scale, int b_rows_total,
+                                 int b_rows_per_expert, int n_out,
+                                 const int32_t* block_expert_ids,
+                                 const int32_t* num_post_padded, void* out, const Epilogue& ep,
+                                 cudaStream_t stream, int* tile_ctr = nullptr);
 
 // MXFP4 (E2M1 + E8M0 per 32) weights x e4m3 activations with power-of-two
 // 1x128 scales (or MXFP8: e4m3 weights, b_e4m3, with 1x32 scales),

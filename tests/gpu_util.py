@@ -98,8 +98,9 @@ def oracle_inputs(d):
 
 @contextlib.contextmanager
 def bf16_gemm_form(form):
-    """Run the block with the bf16 GEMMs forced to one form ("single": 128 x 256
-    tiles on one SM, "pairs": 256 x 256 tiles on SM pairs, "auto": by size)."""
+    """Run the block with the bf16 and FP8-block GEMMs forced to one form
+    ("single": 128 x 256 tiles on one SM, "pairs": 256 x 256 tiles on SM
+    pairs, "auto": by size)."""
     import mixture_experts_ffn_align_gb300 as moe
     moe.moe_debug_set_bf16_gemm_form(form)
     try:

@@ -10,7 +10,8 @@ import mixture_experts_ffn_align_gb300 as moe
 from moe_synth import CONFIGS, MoEConfig, make_inputs
 from oracle import codecs, experts, routing
 
-from .gpu_util import QUANT_TOL, check_close, cover_tokens, flip_allowance, np32, oracle_inputs
+from .gpu_util import (QUANT_TOL, bf16_gemm_form, check_close, cover_tokens, flip_allowance,
+                       np32, oracle_inputs)
 
 pytestmark = pytest.mark.gpu
 
@@ -27,10 +28,19 @@ def _fp8_ragged(counts, H, I, seed, fmt):
     return cfg, d
 
 
+@pytest.mark.parametrize("form", ["single", "pairs"])
 @pytest.mark.parametrize("fmt", ["fp32", "ue8m0"])
 @pytest.mark.parametrize("counts,H,I", [([0, 1, 127, 128, 129, 300], 512, 256),
-                                        ([7, 0, 260], 384, 384)])
-def test_fp8_stages_ragged(counts, H, I, fmt):
+                                        ([7, 0, 260], 384, 384),
+                                        ([385, 0, 1, 640], 640, 384)])
+def test_fp8_stages_ragged(counts, H, I, fmt, form):
+    """Both GEMM forms (one SM; SM pairs, with lone and paired blocks and a
+    128-wide last column tile at H = 640) on ragged expert loads."""
+    with bf16_gemm_form(form):
+        _fp8_stages_ragged(counts, H, I, fmt)
+
+
+def _fp8_stages_ragged(counts, H, I, fmt):
     cfg, d = _fp8_ragged(counts, H, I, 5, fmt)
     p = moe.Problem.from_config(cfg)
     b = moe.stage_buffers(p)
@@ -84,13 +94,15 @@ def _oracle(cfg, d, tokens):
     return y, flip_allowance(y, items, w)
 
 
-def test_fp8_fused_small_skewed():
+@pytest.mark.parametrize("form", ["auto", "single", "pairs"])
+def test_fp8_fused_small_skewed(form):
     cfg = MoEConfig("fp8s", M=256, H=512, I=256, E=16, topk=4, quant="fp8", routing="skew",
                     seed=61)
     d = make_inputs(cfg, "cuda")
-    y = _run_fused(cfg, d)
+    with bf16_gemm_form(form):
+        y = _run_fused(cfg, d)
     ref, allow = _oracle(cfg, d, range(cfg.M))
-    check_close(np32(y), ref, QUANT_TOL, "fp8 small", allow)
+    check_close(np32(y), ref, QUANT_TOL, f"fp8 small {form}", allow)
 
 
 def test_fp8_deepseek_full_size_sampled():

@@ -93,3 +93,8 @@ def test_bf16_epilogue_stores_at_both_alignments(form, fuse):
 def test_quantised_epilogue_stores_at_both_alignments(quant):
     # H = 640: GEMM2's last column tile is 128 wide (N % 256 == 128)
     _run(quant, 640, 256, False)
+
+
+def test_fp8_pair_epilogue_stores_at_both_alignments():
+    with bf16_gemm_form("pairs"):
+        _run("fp8", 640, 256, False)

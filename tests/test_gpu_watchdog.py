@@ -37,7 +37,8 @@ def _fused(cfg, d):
     return y
 
 
-@pytest.mark.parametrize("name,form", [("bf16", "single"), ("bf16", "pairs"), ("fp8", "auto")])
+@pytest.mark.parametrize("name,form", [("bf16", "single"), ("bf16", "pairs"), ("fp8", "auto"),
+                                       ("fp8", "pairs")])
 def test_wait_that_runs_out_reports_timeout_and_context_survives(name, form):
     with bf16_gemm_form(form):
         _timeout_then_recover(name)
