@@ -583,6 +583,7 @@ def run_ours(args):
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     moe.lib()
+    moe.moe_debug_set_bf16_gemm_form(args.gemm_form)
 
     cfg = _workload(args)
     probe = fp8_probe(dev) if rank == 0 and world == 1 and not args.no_extra else None
@@ -751,6 +752,8 @@ def main():
     ap.add_argument("--experts", type=int, default=0,
                     help="override E (smaller cases for profiling captures)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--gemm-form", choices=["auto", "single", "pairs"], default="auto",
+                    help="force the bf16 / FP8-block GEMM form (profiling comparisons)")
     ap.add_argument("--no-extra", action="store_true",
                     help="time only --workload (no FP8 probe, no other workloads)")
     args = ap.parse_args()

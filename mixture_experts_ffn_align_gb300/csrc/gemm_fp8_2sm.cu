@@ -290,8 +290,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       if (e < 0 || e >= args.num_experts) continue;
       for (int kb = 0; kb < args.num_kb; ++kb, ++pc) {
         const uint32_t buf = pc % NPART, pphase = (pc / NPART) & 1;
-        if (!mbar_wait_bounded<true>(pempty_bar(buf), pphase ^ 1, abort_flag, args.limit_ns,
-                                     args.err) ||
+        if (!mbar_wait_bounded(pempty_bar(buf), pphase ^ 1, abort_flag, args.limit_ns,
+                               args.err) ||
             !mbar_wait_bounded(full_bar(stage), phase, abort_flag, args.limit_ns, args.err)) {
           ok = false;
           break;
@@ -384,7 +384,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             if (c == 1) {     // every read of this buffer by this warp is done
               tc_fence_before();
               __syncwarp();
-              if (lane == 0) mbar_arrive_cluster(mapa_shared(pempty_bar(buf), 0));
+              // no data passes through memory (the reads have completed into
+              // registers), so no release: a cluster-scope release here put a
+              // memory barrier into every K block (ncu: membar the top stall)
+              if (lane == 0) mbar_arrive_cluster_relaxed(mapa_shared(pempty_bar(buf), 0));
             }
 #pragma unroll
             for (int i2 = 0; i2 < 16; ++i2) {

@@ -367,6 +367,14 @@ __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_bar) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar)
                : "memory");
 }
+// Arrive on an mbarrier that may live in the peer CTA, with no memory
+// ordering: for signals that carry no data through memory (a tensor-memory
+// buffer read to registers, its tcgen05.ld completed).  The release form
+// above costs a cluster-scope memory barrier per arrive.
+__device__ __forceinline__ void mbar_arrive_cluster_relaxed(uint32_t cluster_bar) {
+  asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar)
+               : "memory");
+}
 // 2-D tensor load into this CTA's shared memory whose completion is counted
 // on an mbarrier of the CTA pair (here: the leader's).
 __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap* map,
