@@ -355,11 +355,18 @@ namespace {
 // blocks; below that most pairs would carry a lone block whose second half
 // repeats the first.
 // rows_per_expert: the expected routed rows per expert.
-// SM-pair tiles for the bf16 and FP8-block GEMMs (the debug hook can force
-// either form).
+// SM-pair tiles for the bf16 GEMMs once the experts average two 128-row
+// blocks (the debug hook can force either form).
 bool use_pairs(int64_t rows_per_expert) {
   return g_bf16_form == 2 || (g_bf16_form == 0 && rows_per_expert >= 2 * 128);
 }
+// The FP8-block GEMMs run on one SM unless the debug hook forces the pair
+// form: with fp32 block scales each 128-deep K block's partial is read out of
+// tensor memory and promoted on the CUDA cores, and that readout, not the
+// shared-memory staging the pair form halves, bounds both forms (the pair form
+// measured 2.64 / 1.70 ms against 2.54 / 1.54 ms for the DeepSeek-class
+// GEMM1 / GEMM2).
+bool use_fp8_pairs() { return g_bf16_form == 2; }
 
 cudaError_t launch_bf16_gemm(int64_t rows_per_expert, const void* A, int cap, int K,
                              const void* B, int b_rows_total, int b_rows_per_expert, int n_out,
@@ -406,7 +413,7 @@ moe_status gemm_w13(const moe_problem* p, const void* x_perm, const float* x_sca
         2 * p->I, 2 * p->I, block_expert_ids, num_post_padded, out,
         p->quant == MOE_Q_MXFP8_1X32, ep, s, out_scale, fuse_act != 0,
         p->act_scale_fmt == MOE_SCALE_UE8M0));
-  if (!fuse_act && use_pairs((int64_t)p->M * p->topk / p->E))
+  if (!fuse_act && use_fp8_pairs())
     return cuda_status(launch_ggemm_fp8_2sm(x_perm, x_scale, cap, p->H, w13,
                                             static_cast<const float*>(w13_scale),
                                             p->E * 2 * p->I, 2 * p->I, 2 * p->I,
@@ -482,7 +489,7 @@ moe_status gemm_w2(const moe_problem* p, const void* z, const float* z_scale, co
                                           static_cast<const uint8_t*>(w2_scale), p->E * p->H,
                                           p->H, p->H, block_expert_ids, num_post_padded, y2,
                                           p->quant == MOE_Q_MXFP8_1X32, ep, s));
-  if (use_pairs((int64_t)p->M * p->topk / p->E))
+  if (use_fp8_pairs())
     return cuda_status(launch_ggemm_fp8_2sm(z, z_scale, cap, p->I, w2,
                                             static_cast<const float*>(w2_scale), p->E * p->H,
                                             p->H, p->H, block_expert_ids, num_post_padded, y2,
