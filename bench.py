@@ -164,9 +164,10 @@ def _oracle_arrays(d, cfg):
     import numpy as np
     f = (lambda t: None if t is None else
          (t.float().cpu().numpy() if t.dtype.is_floating_point else t.cpu().numpy()))
+    # the oracle takes the weight scales as generated (not a prepacked copy)
     a = dict(x=f(d["x"]), topk_ids=f(d["topk_ids"]), topk_weights=f(d["topk_weights"]),
-             w13=f(d["w13"]), w2=f(d["w2"]), w13_scale=f(d["w13_scale"]),
-             w2_scale=f(d["w2_scale"]))
+             w13=f(d["w13"]), w2=f(d["w2"]), w13_scale=f(d.get("w13_scale_raw", d["w13_scale"])),
+             w2_scale=f(d.get("w2_scale_raw", d["w2_scale"])))
     if cfg.quant == "bf16":
         a["w13"] = a["w13"].astype(np.float64)
         a["w2"] = a["w2"].astype(np.float64)
@@ -391,6 +392,15 @@ def _measure(moe, cfg, args, dev, world, rank, full, fp8_tflops=None):
         cfg = cfg.with_(seed=cfg.seed + 100 * rank)
     d = make_inputs(cfg, dev)
     p = moe.Problem.from_config(cfg)
+    if cfg.quant in ("mxfp4", "mxfp8") and not args.raw_scales:
+        # load time, outside any timed region: the weight scales rewritten once
+        # into the block-scaled MMA's operand layout (moe_prepack_weights)
+        s13 = torch.empty(moe.moe_prepacked_scale_bytes(p, 0), dtype=torch.uint8, device=dev)
+        s2 = torch.empty(moe.moe_prepacked_scale_bytes(p, 1), dtype=torch.uint8, device=dev)
+        moe.moe_prepack_weights(p, d["w13_scale"], d["w2_scale"], s13, s2)
+        d["w13_scale_raw"], d["w2_scale_raw"] = d["w13_scale"], d["w2_scale"]
+        d["w13_scale"], d["w2_scale"] = s13, s2
+        p = moe.Problem.from_config(cfg, weight_scales_prepacked=True)
     b = moe.stage_buffers(p, dev)
     ws = torch.empty(moe.moe_workspace_bytes(p), dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
@@ -754,6 +764,9 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--gemm-form", choices=["auto", "single", "pairs"], default="auto",
                     help="force the bf16 / FP8-block GEMM form (profiling comparisons)")
+    ap.add_argument("--raw-scales", action="store_true",
+                    help="MXFP4 / MXFP8: use the weight scales as generated instead of "
+                         "prepacked ones")
     ap.add_argument("--no-extra", action="store_true",
                     help="time only --workload (no FP8 probe, no other workloads)")
     args = ap.parse_args()

@@ -99,6 +99,9 @@ typedef enum { MOE_SCALE_FP32 = 0, MOE_SCALE_UE8M0 = 1 } moe_scale_fmt;
  *              fused_moe_kernel post-processing "optional router weight";
  *              TopKWeightAndReduce when the experts already applied it).
  *              Not together with apply_router_weight_on_input.
+ *  weight_scales_prepacked: (MOE_Q_MXFP4_W4A8, MOE_Q_MXFP8_1X32) w13_scale and
+ *              w2_scale passed to the GEMM entry points are the buffers
+ *              moe_prepack_weights wrote, not the [E, N, K/32] E8M0 arrays.
  *  act_recipe: 0: z = SiLU(gate) * up.  1: the recipe of gemm1_alpha,
  *              gemm1_beta and gemm1_clamp_limit (page "Blackwell 上的 DeepGEMM
  *              FusedMoE（vLLM）", §2.6.4): with L = gemm1_clamp_limit,
@@ -115,6 +118,7 @@ typedef struct {
   int32_t router_weight_in_gemm2;
   int32_t act_recipe;
   float gemm1_alpha, gemm1_beta, gemm1_clamp_limit;
+  int32_t weight_scales_prepacked;
 } moe_problem;
 
 /* Limits checked by every entry point: 0 <= M <= MOE_MAX_TOKENS (the pages'
@@ -146,6 +150,27 @@ int moe_align_permute_launches(const moe_problem* p);
  * the GEMM2 output sharing storage as the page's workspace13 does, §2.8(a)).
  * 0 for an invalid problem. */
 size_t moe_workspace_bytes(const moe_problem* p);
+
+/* Load-time rewrite of the block-scaled weights' scales (page "Blackwell 上的
+ * DeepGEMM FusedMoE（vLLM）", §2.8: the weight scale factors are transformed
+ * once, when the weights are loaded, into the layout the GEMM kernel reads --
+ * transform_sf_into_required_layout).  For MOE_Q_MXFP4_W4A8 and
+ * MOE_Q_MXFP8_1X32 only (other modes: MOE_ERR_UNSUPPORTED).
+ *  in : w13_scale [E, 2I, H/32] and w2_scale [E, H, I/32] E8M0 bytes (device).
+ *  out: w13_scale_packed and w2_scale_packed (device, 16-byte aligned, each
+ *       moe_prepacked_scale_bytes(p, 0 / 1) bytes, the same size as the
+ *       input): for every expert e, K block kb (128 deep) and group g of 128
+ *       weight rows, in that order ([E][K/128][N/128]), one 512-byte block
+ *       whose byte 16 l + 4 c + j is the scale of row 128 g + 32 c + l, K
+ *       chunk 4 kb + j -- the 32 x 16-byte operand the block-scaled MMA copies
+ *       into tensor memory, so the GEMM loads it as it is.
+ * The weights themselves keep their layout.  Set p->weight_scales_prepacked
+ * and pass the packed buffers as w13_scale / w2_scale to the GEMM entry points
+ * and fused_experts; results are identical to the unpacked call.  Asynchronous
+ * on `stream`; the inputs must not be written until it completes. */
+size_t moe_prepacked_scale_bytes(const moe_problem* p, int which /* 0: w13, 1: w2 */);
+moe_status moe_prepack_weights(const moe_problem* p, const void* w13_scale, const void* w2_scale,
+                               void* w13_scale_packed, void* w2_scale_packed, void* stream);
 
 /* Stage 1: block-aligned routing and permute (page "fused_moe.py 分析",
  * "moe_align_block_size 的作用"; page "Blackwell 上的 DeepGEMM FusedMoE（vLLM）",

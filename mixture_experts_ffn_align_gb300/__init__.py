@@ -34,7 +34,8 @@ EXPORTS = ["moe_m_sum_bound", "moe_align_workspace_bytes", "moe_align_permute_la
            "moe_align_permute_noalloc", "moe_last_error_string", "moe_topk_router",
            "moe_batched_workspace_bytes", "fused_experts_batched", "grouped_gemm_w13_ex",
            "grouped_gemm_w2_ex", "fused_experts_ex", "moe_gemm2_splits",
-           "moe_gemm2_partial_bytes", "grouped_gemm_w2_split", "unpermute_reduce_split"]
+           "moe_gemm2_partial_bytes", "grouped_gemm_w2_split", "unpermute_reduce_split",
+           "moe_prepacked_scale_bytes", "moe_prepack_weights"]
 
 NOALLOC_SCRATCH_BYTES = 1 << 20   # MOE_NOALLOC_SCRATCH_BYTES in include/moe_ffn.h
 
@@ -49,7 +50,8 @@ class CProblem(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in
                 ("M", "H", "I", "E", "topk", "block_size", "quant", "act_scale_fmt",
                  "apply_router_weight_on_input", "router_weight_in_gemm2", "act_recipe")] + \
-               [(n, ctypes.c_float) for n in ("gemm1_alpha", "gemm1_beta", "gemm1_clamp_limit")]
+               [(n, ctypes.c_float) for n in ("gemm1_alpha", "gemm1_beta", "gemm1_clamp_limit")] + \
+               [("weight_scales_prepacked", ctypes.c_int32)]
 
 
 @dataclass(frozen=True)
@@ -67,6 +69,8 @@ class Problem:
     router_weight_in_gemm2: bool = False
     # None: SiLU(gate) * up; else (alpha, beta, clamp_limit) of the gemm1 recipe
     act_recipe: tuple | None = None
+    # MXFP4 / MXFP8: the weight scales passed are moe_prepack_weights' output
+    weight_scales_prepacked: bool = False
 
     def c(self) -> CProblem:
         a, b, lim = self.act_recipe if self.act_recipe is not None else (0.0, 0.0, 0.0)
@@ -74,7 +78,7 @@ class Problem:
                         QUANT[self.quant], SCALE_FMT[self.act_scale_fmt],
                         int(self.apply_router_weight_on_input),
                         int(self.router_weight_in_gemm2), int(self.act_recipe is not None),
-                        float(a), float(b), float(lim))
+                        float(a), float(b), float(lim), int(self.weight_scales_prepacked))
 
     @classmethod
     def from_config(cls, cfg, **kw):
@@ -111,6 +115,9 @@ def lib() -> ctypes.CDLL:
         L.fused_experts.argtypes = [P] + [vp] * 9 + [sz, vp]
         L.fused_experts_from_host.argtypes = [P] + [vp] * 9 + [sz, vp]
         L.moe_sync_status.argtypes = [vp]
+        L.moe_prepacked_scale_bytes.argtypes = [P, i32]
+        L.moe_prepacked_scale_bytes.restype = sz
+        L.moe_prepack_weights.argtypes = [P, vp, vp, vp, vp, vp]
         L.moe_topk_router.argtypes = [i32, i32, i32, vp, i32, i32, i32, vp, vp, vp, vp, vp]
         L.moe_batched_workspace_bytes.argtypes = [P, i32]
         L.moe_batched_workspace_bytes.restype = sz
@@ -134,7 +141,7 @@ def lib() -> ctypes.CDLL:
                   "unpermute_reduce", "fused_experts", "fused_experts_from_host",
                   "moe_sync_status", "moe_topk_router", "fused_experts_batched",
                   "grouped_gemm_w13_ex", "grouped_gemm_w2_ex", "fused_experts_ex",
-                  "grouped_gemm_w2_split", "unpermute_reduce_split"):
+                  "grouped_gemm_w2_split", "unpermute_reduce_split", "moe_prepack_weights"):
             getattr(L, n).restype = i32
         _lib = L
     return _lib
@@ -182,6 +189,18 @@ def moe_workspace_bytes(p: Problem) -> int:
 
 def moe_host_workspace_bytes(p: Problem) -> int:
     return int(lib().moe_host_workspace_bytes(_cp(p)))
+
+
+def moe_prepacked_scale_bytes(p: Problem, which: int) -> int:
+    """Bytes of the prepacked w13 (which=0) or w2 (which=1) weight scales."""
+    return int(lib().moe_prepacked_scale_bytes(_cp(p), int(which)))
+
+
+def moe_prepack_weights(p: Problem, w13_scale, w2_scale, w13_scale_packed, w2_scale_packed,
+                        stream=None):
+    _check(lib().moe_prepack_weights(_cp(p), _p(w13_scale), _p(w2_scale), _p(w13_scale_packed),
+                                     _p(w2_scale_packed), _stream(stream)),
+           "moe_prepack_weights")
 
 
 # ------------------------------------------------------------------ stages

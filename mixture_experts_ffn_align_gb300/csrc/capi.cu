@@ -98,6 +98,10 @@ bool valid_problem(const moe_problem* p) {
       !(std::isfinite(p->gemm1_alpha) && std::isfinite(p->gemm1_beta) &&
         std::isfinite(p->gemm1_clamp_limit)))
     return false;
+  if (p->weight_scales_prepacked != 0 && p->weight_scales_prepacked != 1) return false;
+  if (p->weight_scales_prepacked && p->quant != MOE_Q_MXFP4_W4A8 &&
+      p->quant != MOE_Q_MXFP8_1X32)
+    return false;
   return true;
 }
 
@@ -294,6 +298,32 @@ extern "C" {
 
 size_t moe_m_sum_bound(const moe_problem* p) { return valid_problem(p) ? cap_rows(p) : 0; }
 
+size_t moe_prepacked_scale_bytes(const moe_problem* p, int which) {
+  if (!valid_problem(p) || !block_scaled(p) || (which != 0 && which != 1)) return 0;
+  const size_t N = which == 0 ? 2 * (size_t)p->I : (size_t)p->H;
+  const size_t K = which == 0 ? (size_t)p->H : (size_t)p->I;
+  return (size_t)p->E * N * (K / 32);
+}
+
+moe_status moe_prepack_weights(const moe_problem* p, const void* w13_scale, const void* w2_scale,
+                               void* w13_scale_packed, void* w2_scale_packed, void* stream) {
+  if (!valid_problem(p)) return MOE_ERR_INVALID_ARG;
+  if (!block_scaled(p)) return MOE_ERR_UNSUPPORTED;
+  if (!w13_scale || !w2_scale || !w13_scale_packed || !w2_scale_packed)
+    return MOE_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(w13_scale) | reinterpret_cast<uintptr_t>(w2_scale)) & 3u ||
+      (reinterpret_cast<uintptr_t>(w13_scale_packed) |
+       reinterpret_cast<uintptr_t>(w2_scale_packed)) & 15u)
+    return MOE_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = launch_prepack_mx_scales(static_cast<const uint8_t*>(w13_scale), p->E,
+                                           2 * p->I, p->H, w13_scale_packed, s);
+  if (e == cudaSuccess)
+    e = launch_prepack_mx_scales(static_cast<const uint8_t*>(w2_scale), p->E, p->H, p->I,
+                                 w2_scale_packed, s);
+  return cuda_status(e);
+}
+
 size_t moe_align_workspace_bytes(const moe_problem* p) {
   if (!valid_problem(p)) return 0;
   const size_t G = (size_t)route_segments(p->M * p->topk);
@@ -412,7 +442,7 @@ moe_status gemm_w13(const moe_problem* p, const void* x_perm, const float* x_sca
         x_perm, x_scale, cap, p->H, w13, static_cast<const uint8_t*>(w13_scale), p->E * 2 * p->I,
         2 * p->I, 2 * p->I, block_expert_ids, num_post_padded, out,
         p->quant == MOE_Q_MXFP8_1X32, ep, s, out_scale, fuse_act != 0,
-        p->act_scale_fmt == MOE_SCALE_UE8M0));
+        p->act_scale_fmt == MOE_SCALE_UE8M0, p->weight_scales_prepacked != 0));
   if (!fuse_act && use_fp8_pairs())
     return cuda_status(launch_ggemm_fp8_2sm(x_perm, x_scale, cap, p->H, w13,
                                             static_cast<const float*>(w13_scale),
@@ -488,7 +518,8 @@ moe_status gemm_w2(const moe_problem* p, const void* z, const float* z_scale, co
     return cuda_status(launch_ggemm_mxfp4(z, z_scale, cap, p->I, w2,
                                           static_cast<const uint8_t*>(w2_scale), p->E * p->H,
                                           p->H, p->H, block_expert_ids, num_post_padded, y2,
-                                          p->quant == MOE_Q_MXFP8_1X32, ep, s));
+                                          p->quant == MOE_Q_MXFP8_1X32, ep, s, nullptr, false,
+                                          true, p->weight_scales_prepacked != 0));
   if (use_fp8_pairs())
     return cuda_status(launch_ggemm_fp8_2sm(z, z_scale, cap, p->I, w2,
                                             static_cast<const float*>(w2_scale), p->E * p->H,
@@ -768,7 +799,8 @@ moe_status fused_experts_batched(const moe_problem* p, const void* x,
     // GEMM1 with the activation and its quantisation in the epilogue
     e = launch_ggemm_mxfp4(ws + L.xq, xscale, rows, H, w13, static_cast<const uint8_t*>(w13_scale),
                            E * 2 * I, 2 * I, 2 * I, blocks, npp, ws + L.z,
-                           p->quant == MOE_Q_MXFP8_1X32, ep, s, zscale, true, ue8m0);
+                           p->quant == MOE_Q_MXFP8_1X32, ep, s, zscale, true, ue8m0,
+                           p->weight_scales_prepacked != 0);
   } else {   // FP8 block scales: two steps (see fused_experts_ex)
     e = launch_ggemm_fp8(ws + L.xq, xscale, rows, H, w13, static_cast<const float*>(w13_scale),
                          E * 2 * I, 2 * I, 2 * I, blocks, npp, ws + L.h1, ep, s);
@@ -778,7 +810,8 @@ moe_status fused_experts_batched(const moe_problem* p, const void* x,
   if (e != cudaSuccess) return cuda_status(e);
   if (block_scaled(p))
     e = launch_ggemm_mxfp4(ws + L.z, zscale, rows, I, w2, static_cast<const uint8_t*>(w2_scale),
-                           E * H, H, H, blocks, npp, y, p->quant == MOE_Q_MXFP8_1X32, ep, s);
+                           E * H, H, H, blocks, npp, y, p->quant == MOE_Q_MXFP8_1X32, ep, s,
+                           nullptr, false, true, p->weight_scales_prepacked != 0);
   else
     e = launch_ggemm_fp8(ws + L.z, zscale, rows, I, w2, static_cast<const float*>(w2_scale),
                          E * H, H, H, blocks, npp, y, ep, s);

@@ -62,6 +62,7 @@
 //  * a last column tile narrower than 256 (N % 256 == 128) is computed on
 //    whatever the weight box held above N and its upper half is not stored.
 //  * tiles walked expert by expert (tile_sched.cuh); every wait is bounded.
+#include <algorithm>
 #include <mutex>
 
 #include "../../include/moe_ffn.h"
@@ -80,6 +81,12 @@ bool make_tmap_u8_rows(CUtensorMap* map, const void* base, uint64_t rows, uint64
                        uint32_t box_bytes, uint32_t box_rows);
 
 namespace {
+
+// Where the weight-scale operand of each K block comes from: built by warp 3
+// from E8M0 bytes it loads to registers (any K), transposed from TMA boxes of
+// 4 K blocks (K % 512 == 0), or copied in ready-made from scales that
+// moe_prepack_weights rewrote into the operand layout.
+enum : int { SRC_REGS = 0, SRC_STAGED = 1, SRC_PACKED = 2 };
 
 constexpr int BM = 128, BN = 256, BK = 128, STAGES = 4, SSLOTS = 4;
 // Staged weight scales (K % 512 == 0): 16 bytes = 4 K blocks of each of the
@@ -176,7 +183,7 @@ __device__ __forceinline__ uint32_t a_word(const AGroup<MX8>& A, int c, int j) {
   }
 }
 
-template <bool STAGED, bool MX8, bool FUSE>
+template <int SRC, bool MX8, bool FUSE>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     k_ggemm_mxfp4(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                   const __grid_constant__ CUtensorMap tmS, const Mx4Args args) {
@@ -184,7 +191,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
   uint8_t* sf_ring = smem + STAGES * STAGE_BYTES;    // SSLOTS x SF_BYTES, 16-byte aligned
-  uint8_t* stg_ring = sf_ring + SSLOTS * SF_BYTES;     // NSTG x STG_BYTES (STAGED)
+  uint8_t* stg_ring = sf_ring + SSLOTS * SF_BYTES;     // NSTG x STG_BYTES (SRC_STAGED)
   uint64_t* bars = reinterpret_cast<uint64_t*>(stg_ring + NSTG * STG_BYTES);
   // full[S], empty[S], sfull[SS], sempty[SS], tfull, tempty, drain, stg_full[NSTG]
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 2 * SSLOTS + 3 + NSTG);
@@ -225,7 +232,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
-    if (STAGED) tma_prefetch_desc(&tmS);
+    if (SRC == SRC_STAGED) tma_prefetch_desc(&tmS);
   }
   if (warp == 1) {
     __syncwarp();
@@ -323,7 +330,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       }
       return true;
     };
-    if constexpr (STAGED) {
+    if constexpr (SRC == SRC_STAGED) {
       // Warp 3: the weight scales of 4 K blocks x the tile's 256 rows arrive
       // as one TMA box (row n at byte 16 n) NSTG groups ahead.  Warp 2: the
       // activation scales (in L2: the permute/act kernel just wrote them)
@@ -468,6 +475,85 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           for (int k = nuse; k < nfill; ++k)
             mbar_wait_bounded(stg_full(k % NSTG), (k / NSTG) & 1, nullptr, args.limit_ns,
                               args.err);
+      }
+    } else if constexpr (SRC == SRC_PACKED) {
+      // Prepacked weight scales ([E][K/128][N/128] blocks of 512 bytes, each
+      // the 32 x 16-byte operand of one 128-row group and K block): lane 0 of
+      // warp 3 copies a K block's weight operand (two groups: 256 rows, or
+      // the gate group and its up group) straight into the slot with bulk
+      // copies that complete on the slot's full barrier.  The activation
+      // words are built as in the other forms (warp 2 for MXFP8, warp 3 for
+      // W4A8), one group of 4 K blocks ahead.
+      const int G = N / 128;                     // 128-row scale groups per expert
+      const bool writes_a = wa || !MX8;
+      const bool writes_b = !wa;
+      bool ok = true;
+      for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+        int m_blk, n_tile;
+        sched_tile(sched, t, m_blk, n_tile);
+        const int e = s_ids[m_blk];
+        if (e < 0 || e >= args.num_experts) continue;
+        const size_t arow = (size_t)m_blk * BM + lane;
+        AGroup<MX8> a_cur, a_nxt;
+        if (writes_a) {
+          load_ascales<MX8>(a_cur, args.a_scale, arow, args.num_kb, 0);
+          if (args.num_kb > 4) load_ascales<MX8>(a_nxt, args.a_scale, arow, args.num_kb, 4);
+        }
+        // group offsets (in 512-byte blocks) of the operand's two halves
+        const int g0 = FUSE ? n_tile : 2 * n_tile;
+        const int g1 = FUSE ? args.I / 128 + n_tile : 2 * n_tile + 1;
+        const bool two = g1 < G;                   // false: a 128-row last tile
+        for (int kb0 = 0; kb0 < args.num_kb && ok; kb0 += 4) {
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const int kb = kb0 + j;
+            if (kb >= args.num_kb) break;
+            int got = 1;
+            if (lane == 0)
+              got = mbar_wait_bounded(sempty_bar(sslot), sphase ^ 1, abort_flag, args.limit_ns,
+                                      args.err);
+            got = __shfl_sync(0xffffffffu, got, 0);
+            if (!got) {
+              ok = false;
+              break;
+            }
+            uint8_t* slot = sf_ring + sslot * SF_BYTES;
+            if (writes_b && lane == 0) {
+              const uint8_t* src = args.b_scale + ((size_t)e * args.num_kb + kb) * G * 512;
+              const uint32_t dst = smem_u32(slot + SF_A_BYTES);
+              const uint32_t bytes = two ? 1024u : 512u;
+              // MXFP8: this arrival is warp 3's; W4A8: warp 3 arrives below
+              if (MX8)
+                mbar_arrive_expect_tx(sfull_bar(sslot), bytes);
+              else
+                mbar_expect_tx(sfull_bar(sslot), bytes);
+              if (FUSE || !two) {
+                bulk_load(dst, src + (size_t)g0 * 512, 512, sfull_bar(sslot));
+                if (two) bulk_load(dst + 512, src + (size_t)g1 * 512, 512, sfull_bar(sslot));
+              } else {
+                bulk_load(dst, src + (size_t)g0 * 512, 1024, sfull_bar(sslot));
+              }
+            }
+            if (writes_a) {
+              uint32_t aw[4];
+#pragma unroll
+              for (int c = 0; c < 4; ++c) aw[c] = a_word<MX8>(a_cur, c, j);
+              reinterpret_cast<uint4*>(slot)[lane] = make_uint4(aw[0], aw[1], aw[2], aw[3]);
+              fence_proxy_async_smem();
+              __syncwarp();
+              if (lane == 0) mbar_arrive(sfull_bar(sslot));
+            }
+            if (++sslot == SSLOTS) {
+              sslot = 0;
+              sphase ^= 1;
+            }
+          }
+          if (writes_a) {
+            a_cur = a_nxt;
+            if (kb0 + 8 < args.num_kb)
+              load_ascales<MX8>(a_nxt, args.a_scale, arow, args.num_kb, kb0 + 8);
+          }
+        }
       }
     } else {
       const int kq = args.num_kb * 4;            // E8M0 bytes per weight row
@@ -750,27 +836,29 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 }  // namespace
 
 namespace {
-template <bool STAGED, bool MX8, bool FUSE>
+template <int SRC, bool MX8, bool FUSE>
 void launch_form(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmS,
                  const Mx4Args& a, cudaStream_t stream) {
   // a failed opt-in shows as the launch's error (cudaGetLastError in the caller)
   static DeviceOnce attr;
   (void)attr.call([] {
-    return cudaFuncSetAttribute(k_ggemm_mxfp4<STAGED, MX8, FUSE>,
+    return cudaFuncSetAttribute(k_ggemm_mxfp4<SRC, MX8, FUSE>,
                                 cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
   });
-  k_ggemm_mxfp4<STAGED, MX8, FUSE><<<num_sms(), NUM_THREADS, SMEM_BYTES, stream>>>(tmA, tmB, tmS,
-                                                                                  a);
+  k_ggemm_mxfp4<SRC, MX8, FUSE><<<num_sms(), NUM_THREADS, SMEM_BYTES, stream>>>(tmA, tmB, tmS, a);
 }
 template <bool FUSE>
-void launch_forms(bool staged, bool mx8, const CUtensorMap& tmA, const CUtensorMap& tmB,
+void launch_forms(int src, bool mx8, const CUtensorMap& tmA, const CUtensorMap& tmB,
                   const CUtensorMap& tmS, const Mx4Args& a, cudaStream_t stream) {
-  if (staged)
-    mx8 ? launch_form<true, true, FUSE>(tmA, tmB, tmS, a, stream)
-        : launch_form<true, false, FUSE>(tmA, tmB, tmS, a, stream);
+  if (src == SRC_PACKED)
+    mx8 ? launch_form<SRC_PACKED, true, FUSE>(tmA, tmB, tmS, a, stream)
+        : launch_form<SRC_PACKED, false, FUSE>(tmA, tmB, tmS, a, stream);
+  else if (src == SRC_STAGED)
+    mx8 ? launch_form<SRC_STAGED, true, FUSE>(tmA, tmB, tmS, a, stream)
+        : launch_form<SRC_STAGED, false, FUSE>(tmA, tmB, tmS, a, stream);
   else
-    mx8 ? launch_form<false, true, FUSE>(tmA, tmB, tmS, a, stream)
-        : launch_form<false, false, FUSE>(tmA, tmB, tmS, a, stream);
+    mx8 ? launch_form<SRC_REGS, true, FUSE>(tmA, tmB, tmS, a, stream)
+        : launch_form<SRC_REGS, false, FUSE>(tmA, tmB, tmS, a, stream);
 }
 }  // namespace
 
@@ -779,11 +867,14 @@ cudaError_t launch_ggemm_mxfp4(const void* A, const float* a_scale, int cap, int
                                int n_out, const int32_t* block_expert_ids,
                                const int32_t* num_post_padded, void* out, bool b_e4m3,
                                const Epilogue& ep, cudaStream_t stream, float* z_scale,
-                               bool fuse_act, bool ue8m0) {
+                               bool fuse_act, bool ue8m0, bool scales_prepacked) {
   if (cap <= 0) return cudaSuccess;
-  // packed E2M1 tensor maps want 32-byte aligned bases, byte maps 16
+  // packed E2M1 tensor maps want 32-byte aligned bases, byte maps 16; bulk
+  // copies of prepacked scales 16
   if ((reinterpret_cast<uintptr_t>(B) & (b_e4m3 ? 15u : 31u)) != 0 ||
-      (reinterpret_cast<uintptr_t>(b_scale) & 3u))
+      (reinterpret_cast<uintptr_t>(b_scale) & (scales_prepacked ? 15u : 3u)))
+    return cudaErrorInvalidValue;
+  if (scales_prepacked && (b_rows_per_expert % 128 != 0 || K % 128 != 0))
     return cudaErrorInvalidValue;
   // fused GEMM1: B rows per expert = 2I (gate then up), I a multiple of 128
   if (fuse_act && (z_scale == nullptr || b_rows_per_expert % 256 != 0 ||
@@ -816,16 +907,58 @@ cudaError_t launch_ggemm_mxfp4(const void* A, const float* a_scale, int cap, int
   watchdog_params(&a.limit_ns, &a.never_arrive);
   a.err = dev_error_word();
   if (a.err == nullptr) return cudaErrorInvalidDevice;   // no usable current device
-  // weight scales staged by TMA when their rows are 16-byte multiples
-  const bool staged = K % 512 == 0 && (reinterpret_cast<uintptr_t>(b_scale) & 15u) == 0;
-  CUtensorMap tmS = tmB;        // unused by the register form
+  // weight scales: prepacked operands by bulk copy; else staged by TMA when
+  // their rows are 16-byte multiples; else loaded to registers
+  const bool staged = !scales_prepacked && K % 512 == 0 &&
+                      (reinterpret_cast<uintptr_t>(b_scale) & 15u) == 0;
+  const int src = scales_prepacked ? SRC_PACKED : (staged ? SRC_STAGED : SRC_REGS);
+  CUtensorMap tmS = tmB;        // used by the staged form only
   if (staged && !make_tmap_u8_rows(&tmS, b_scale, (uint64_t)b_rows_total, (uint64_t)(K / 32), 16,
                                    fuse_act ? 128 : BN))
     return cudaErrorInvalidValue;
   if (fuse_act)
-    launch_forms<true>(staged, b_e4m3, tmA, tmB, tmS, a, stream);
+    launch_forms<true>(src, b_e4m3, tmA, tmB, tmS, a, stream);
   else
-    launch_forms<false>(staged, b_e4m3, tmA, tmB, tmS, a, stream);
+    launch_forms<false>(src, b_e4m3, tmA, tmB, tmS, a, stream);
+  return cudaGetLastError();
+}
+
+namespace {
+// One thread per (expert, K block, 128-row group, lane l): the 16 bytes of
+// operand row l -- the E8M0 bytes of rows l, l + 32, l + 64, l + 96 of the
+// group for the K block's 4 chunks of 32, row r's 4 bytes at 4 (r / 32).
+__global__ void k_prepack_mx_scales(const uint8_t* __restrict__ scale, int E, int N, int K,
+                                    uint4* __restrict__ packed) {
+  const int KB = K / 128, G = N / 128, KQ = K / 32;
+  const size_t total = (size_t)E * KB * G * 32;
+  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < total;
+       i += (size_t)gridDim.x * blockDim.x) {
+    const int l = (int)(i % 32);
+    size_t r = i / 32;
+    const int g = (int)(r % G);
+    r /= G;
+    const int kb = (int)(r % KB);
+    const int e = (int)(r / KB);
+    uint32_t w[4];
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      const size_t row = (size_t)e * N + (size_t)g * 128 + l + 32 * c;
+      w[c] = *reinterpret_cast<const uint32_t*>(scale + row * KQ + 4 * kb);
+    }
+    packed[i] = make_uint4(w[0], w[1], w[2], w[3]);
+  }
+}
+}  // namespace
+
+cudaError_t launch_prepack_mx_scales(const uint8_t* scale, int E, int N, int K, void* packed,
+                                     cudaStream_t stream) {
+  if (E <= 0) return cudaSuccess;
+  const size_t total = (size_t)E * (K / 128) * (N / 128) * 32;
+  const int threads = 256;
+  const size_t want = (total + threads - 1) / threads;
+  const int grid = (int)std::min<size_t>(want, (size_t)num_sms() * 8);
+  k_prepack_mx_scales<<<grid, threads, 0, stream>>>(scale, E, N, K,
+                                                      static_cast<uint4*>(packed));
   return cudaGetLastError();
 }
 

@@ -171,6 +171,13 @@ cudaError_t launch_ggemm_mxfp4(const void* A, const float* a_scale, int cap, int
                                const int32_t* num_post_padded, void* out, bool b_e4m3,
                                const Epilogue& ep, cudaStream_t stream,
                                float* z_scale = nullptr, bool fuse_act = false,
-                               bool ue8m0 = true);
+                               bool ue8m0 = true, bool scales_prepacked = false);
+
+// E8M0 weight scales [E, N, K/32] -> the operand layout the block-scaled MMA
+// copies into tensor memory: [E][K/128][N/128] blocks of 512 bytes, block
+// byte 16 l + 4 c + j = scale of row 32 c + l of the group, K chunk 4 kb + j.
+// N and K multiples of 128, scale 4-byte and packed 16-byte aligned.
+cudaError_t launch_prepack_mx_scales(const uint8_t* scale, int E, int N, int K, void* packed,
+                                     cudaStream_t stream);
 
 }  // namespace moe
