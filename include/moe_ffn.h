@@ -90,7 +90,12 @@ typedef enum { MOE_SCALE_FP32 = 0, MOE_SCALE_UE8M0 = 1 } moe_scale_fmt;
 /* The problem statement (page 1, "FusedMoEExpertsModular.apply" and
  * "moe_problem_size": E, M, N = 2I, K = H, topk).
  *  block_size: padding granularity of each expert's rows (BLOCK_SIZE_M);
- *              one of 16, 32, 64, 128.  The grouped GEMMs need 128.
+ *              one of 16, 32, 64, 128.  The grouped GEMMs compute 128-row
+ *              tiles inside each expert's padded segment (a smaller block
+ *              size pads less and leaves a partial last tile per expert,
+ *              whose rows past the segment are not written); the SM-pair
+ *              GEMM forms and fused_experts_batched take 128 only (the
+ *              others are then used).
  *  apply_router_weight_on_input: multiply x_t by its router weight before
  *              GEMM1 and reduce with weight 1 (top-k must be 1).
  *  router_weight_in_gemm2: GEMM2's epilogue multiplies each output row by its

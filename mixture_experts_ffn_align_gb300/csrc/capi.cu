@@ -6,7 +6,8 @@
 // SiLU), the chunk bound CHUNK_SIZE = 16 * 1024 ("分 chunk 执行"), the page
 // "Blackwell 上的 DeepGEMM FusedMoE（vLLM）" §2.6.3 warning that a GEMM block
 // taller than the padding granularity reads another expert's id (so the
-// GEMMs demand block_size == 128 here), and M == 0 returning early (page 1,
+// GEMMs cut 128-row tiles inside each expert's segment and never store rows
+// past it when block_size < 128), and M == 0 returning early (page 1,
 // FusedMoEKernelModularImpl._fused_experts, "M_full == 0").
 #include <cmath>
 #include <cstdio>
@@ -146,10 +147,12 @@ size_t cap_rows(const moe_problem* p) {
 // evenly).  1 for the SM-pair form, the quantised modes and H % 256 != 0.
 int splits_for_tiles(const moe_problem* p, int64_t tiles);
 
+bool use_pairs_for(const moe_problem* p, int64_t rows_per_expert);
+
 int gemm2_splits(const moe_problem* p) {
   if (p->quant != MOE_Q_BF16 || p->H % 256 != 0 || g_bf16_form == 2) return 1;
   const int64_t R = (int64_t)p->M * p->topk;
-  if (R <= 0 || (g_bf16_form == 0 && R / p->E >= 2 * 128)) return 1;
+  if (R <= 0 || use_pairs_for(p, R / p->E)) return 1;
   const int64_t experts = std::min<int64_t>(p->E, R);
   const int64_t blocks = experts * ((R / experts + 127) / 128);
   return splits_for_tiles(p, blocks * (p->H / 256));
@@ -282,11 +285,12 @@ moe_status cuda_status(cudaError_t e) {
   return MOE_ERR_CUDA;
 }
 
-// The GEMM tiles are 128 rows high, so the padding granularity must be 128;
-// bf16 GEMM2 tiles are 256 columns wide.  The MXFP4 kernel applies scales in
-// the tensor core, which takes powers of two only: activations need UE8M0.
+// The GEMMs cut each expert's segment into 128-row m-tiles whatever the block
+// size (16, 32, 64 or 128; a partial last m-tile's rows past the segment are
+// not stored), so every valid block size is served; bf16 GEMM2 tiles are 256
+// columns wide.  The MXFP4 kernel applies scales in the tensor core, which
+// takes powers of two only: activations need UE8M0.
 bool gemm_supported(const moe_problem* p) {
-  if (p->block_size != 128) return false;
   if (p->quant == MOE_Q_BF16) return p->H % 256 == 0;
   if (block_scaled(p)) return p->act_scale_fmt == MOE_SCALE_UE8M0;
   return p->quant == MOE_Q_FP8_BLOCK128;
@@ -386,8 +390,10 @@ namespace {
 // repeats the first.
 // rows_per_expert: the expected routed rows per expert.
 // SM-pair tiles for the bf16 GEMMs once the experts average two 128-row
-// blocks (the debug hook can force either form).
-bool use_pairs(int64_t rows_per_expert) {
+// blocks (the debug hook can force either form); the pair forms pair whole
+// 128-row blocks, so they take block size 128 only.
+bool use_pairs(int64_t rows_per_expert, int block_size) {
+  if (block_size != 128) return false;
   return g_bf16_form == 2 || (g_bf16_form == 0 && rows_per_expert >= 2 * 128);
 }
 // The FP8-block GEMMs run on one SM unless the debug hook forces the pair
@@ -396,19 +402,23 @@ bool use_pairs(int64_t rows_per_expert) {
 // shared-memory staging the pair form halves, bounds both forms (the pair form
 // measured 2.64 / 1.70 ms against 2.54 / 1.54 ms for the DeepSeek-class
 // GEMM1 / GEMM2).
-bool use_fp8_pairs() { return g_bf16_form == 2; }
+bool use_fp8_pairs(int block_size) { return block_size == 128 && g_bf16_form == 2; }
+bool use_pairs_for(const moe_problem* p, int64_t rows_per_expert) {
+  return use_pairs(rows_per_expert, p->block_size);
+}
 
 cudaError_t launch_bf16_gemm(int64_t rows_per_expert, const void* A, int cap, int K,
                              const void* B, int b_rows_total, int b_rows_per_expert, int n_out,
                              const int32_t* block_expert_ids, const int32_t* num_post_padded,
                              void* out, bool fuse_act, const Epilogue& ep, cudaStream_t s,
-                             int* tile_ctr = nullptr) {
-  if (use_pairs(rows_per_expert))
+                             int* tile_ctr = nullptr, int block_size = 128) {
+  if (use_pairs(rows_per_expert, block_size))
     return launch_ggemm_bf16_2sm(A, cap, K, B, b_rows_total, b_rows_per_expert, n_out,
                                  block_expert_ids, num_post_padded, out, fuse_act, ep, s,
                                  tile_ctr);
   return launch_ggemm_bf16(A, cap, K, B, b_rows_total, b_rows_per_expert, n_out,
-                           block_expert_ids, num_post_padded, out, fuse_act, ep, s);
+                           block_expert_ids, num_post_padded, out, fuse_act, ep, s, 1, nullptr,
+                           nullptr, 0, block_size);
 }
 }  // namespace
 
@@ -433,7 +443,8 @@ moe_status gemm_w13(const moe_problem* p, const void* x_perm, const float* x_sca
   if (p->quant == MOE_Q_BF16) {
     return cuda_status(launch_bf16_gemm((int64_t)p->M * p->topk / p->E, x_perm, cap, p->H, w13,
                                         p->E * 2 * p->I, 2 * p->I, 2 * p->I, block_expert_ids,
-                                        num_post_padded, out, fuse_act != 0, ep, s, tile_ctr));
+                                        num_post_padded, out, fuse_act != 0, ep, s, tile_ctr,
+                                        p->block_size));
   }
   if (!x_scale || !w13_scale) return MOE_ERR_INVALID_ARG;
   if (fuse_act && !out_scale) return MOE_ERR_INVALID_ARG;
@@ -442,8 +453,8 @@ moe_status gemm_w13(const moe_problem* p, const void* x_perm, const float* x_sca
         x_perm, x_scale, cap, p->H, w13, static_cast<const uint8_t*>(w13_scale), p->E * 2 * p->I,
         2 * p->I, 2 * p->I, block_expert_ids, num_post_padded, out,
         p->quant == MOE_Q_MXFP8_1X32, ep, s, out_scale, fuse_act != 0,
-        p->act_scale_fmt == MOE_SCALE_UE8M0, p->weight_scales_prepacked != 0));
-  if (!fuse_act && use_fp8_pairs())
+        p->act_scale_fmt == MOE_SCALE_UE8M0, p->weight_scales_prepacked != 0, p->block_size));
+  if (!fuse_act && use_fp8_pairs(p->block_size))
     return cuda_status(launch_ggemm_fp8_2sm(x_perm, x_scale, cap, p->H, w13,
                                             static_cast<const float*>(w13_scale),
                                             p->E * 2 * p->I, 2 * p->I, 2 * p->I,
@@ -453,7 +464,7 @@ moe_status gemm_w13(const moe_problem* p, const void* x_perm, const float* x_sca
                                       static_cast<const float*>(w13_scale), p->E * 2 * p->I,
                                       2 * p->I, 2 * p->I, block_expert_ids, num_post_padded, out,
                                       ep, s, out_scale, fuse_act != 0,
-                                      p->act_scale_fmt == MOE_SCALE_UE8M0));
+                                      p->act_scale_fmt == MOE_SCALE_UE8M0, p->block_size));
 }
 }  // namespace
 
@@ -511,7 +522,8 @@ moe_status gemm_w2(const moe_problem* p, const void* z, const float* z_scale, co
   if (p->quant == MOE_Q_BF16) {
     return cuda_status(launch_bf16_gemm((int64_t)p->M * p->topk / p->E, z, cap, p->I, w2,
                                         p->E * p->H, p->H, p->H, block_expert_ids,
-                                        num_post_padded, y2, false, ep, s, tile_ctr));
+                                        num_post_padded, y2, false, ep, s, tile_ctr,
+                                        p->block_size));
   }
   if (!z_scale || !w2_scale) return MOE_ERR_INVALID_ARG;
   if (block_scaled(p))
@@ -519,15 +531,17 @@ moe_status gemm_w2(const moe_problem* p, const void* z, const float* z_scale, co
                                           static_cast<const uint8_t*>(w2_scale), p->E * p->H,
                                           p->H, p->H, block_expert_ids, num_post_padded, y2,
                                           p->quant == MOE_Q_MXFP8_1X32, ep, s, nullptr, false,
-                                          true, p->weight_scales_prepacked != 0));
-  if (use_fp8_pairs())
+                                          true, p->weight_scales_prepacked != 0,
+                                          p->block_size));
+  if (use_fp8_pairs(p->block_size))
     return cuda_status(launch_ggemm_fp8_2sm(z, z_scale, cap, p->I, w2,
                                             static_cast<const float*>(w2_scale), p->E * p->H,
                                             p->H, p->H, block_expert_ids, num_post_padded, y2,
                                             ep, s, tile_ctr));
   return cuda_status(launch_ggemm_fp8(z, z_scale, cap, p->I, w2,
                                       static_cast<const float*>(w2_scale), p->E * p->H, p->H,
-                                      p->H, block_expert_ids, num_post_padded, y2, ep, s));
+                                      p->H, block_expert_ids, num_post_padded, y2, ep, s,
+                                      nullptr, false, false, p->block_size));
 }
 }  // namespace
 
@@ -588,7 +602,7 @@ moe_status grouped_gemm_w2_split(const moe_problem* p, const void* z, const void
   const cudaError_t e = launch_ggemm_bf16(z, (int)cap_rows(p), p->I, w2, p->E * p->H, p->H, p->H,
                                           block_expert_ids, num_post_padded, nullptr, false, ep,
                                           static_cast<cudaStream_t>(stream), splits, partial,
-                                          sorted_ids, p->M * p->topk);
+                                          sorted_ids, p->M * p->topk, p->block_size);
   return e == cudaErrorInvalidValue ? MOE_ERR_INVALID_ARG : cuda_status(e);
 }
 

@@ -39,8 +39,7 @@ constexpr int B_BYTES = BN * BK * 2;
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int TMEM_COLS = 2 * BN;
 constexpr int NUM_THREADS = 192;
-constexpr int SCHED_BYTES = 16 + 4 * kSchedMaxRuns + 4 * kSchedMaxBlocks;
-constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /*align*/ + 256 /*barriers*/ + SCHED_BYTES;
+constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /*align*/ + 256 /*barriers*/ + kSchedBytes;
 
 struct GemmArgs {
   const int32_t* block_expert_ids;
@@ -53,9 +52,10 @@ struct GemmArgs {
   int second_box_off;     // row offset of the second 128-row B box
   int n_tile_rows;        // B rows advanced per column tile
   int out_cols_per_tile;  // output columns per tile (256, or 128 when fused)
-  int m_blocks_cap;       // blocks the A / output buffers hold
+  int blocks_cap;         // blocks of blk_rows rows the A / output buffers hold
+  int blk_rows;           // rows per block of the padded layout (16, 32, 64, 128)
   int num_experts;
-  int group_max;          // m-blocks per scheduling group (L2 budget)
+  int group_max;          // m-tiles per scheduling group (L2 budget)
   uint64_t limit_ns;
   int never_arrive;
   int* err;
@@ -81,9 +81,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   // bars[0..S) full, [S..2S) empty, 2S..2S+1 tmem_full, 2S+2..2S+3 tmem_empty, 2S+4 drain
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 5);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
-  int* s_nruns = reinterpret_cast<int*>(smem + STAGES * STAGE_BYTES + 256);
-  int* s_runs = s_nruns + 4;
-  int* s_ids = s_runs + kSchedMaxRuns;
+  int* s_sched = reinterpret_cast<int*>(smem + STAGES * STAGE_BYTES + 256);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t smem_base = smem_u32(smem);
@@ -122,14 +120,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   const uint32_t tmem_base = *tmem_holder;
 
   // never walk past the buffers, whatever the routing wrote
-  const int nb_valid =
-      min(min(*args.num_post_padded / BM, args.m_blocks_cap), kSchedMaxBlocks);
-  const int total = nb_valid * args.n_tiles * args.splits;   // work units
-  TileSched sched;
-  sched.nruns = sched_build(args.block_expert_ids, nb_valid, s_ids, s_runs, s_nruns);
-  sched.runs = s_runs;
-  sched.n_tiles = args.n_tiles;
-  sched.group_max = args.group_max;
+  const int nb_valid = min(*args.num_post_padded / args.blk_rows, args.blocks_cap);
+  const TileSched sched =
+      sched_build(args.block_expert_ids, nb_valid, args.blk_rows, args.num_experts, s_sched,
+                  reinterpret_cast<int*>(smem), args.n_tiles, args.group_max);
+  const int total = sched_mtiles(sched) * args.n_tiles * args.splits;   // work units
 
   if (warp == 0 && lane == 0) {
     // ------------------------------------------------------------ producer
@@ -140,11 +135,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     bool skip_first = args.never_arrive != 0;
     for (int u = blockIdx.x; u < total; u += gridDim.x) {
       const int t = u / args.splits, ks = u - t * args.splits;
-      int m_blk, n_tile;
-      sched_tile(sched, t, m_blk, n_tile);
-      const int e = s_ids[m_blk];
-      if (e < 0 || e >= args.num_experts) continue;
-      const int brow = e * args.b_rows_per_expert + n_tile * args.n_tile_rows;
+      const Tile T = sched_tile(sched, t);
+      const int e = T.e;
+      const int brow = e * args.b_rows_per_expert + T.n_tile * args.n_tile_rows;
       const int kb0 = ks * args.kb_per_split;
       const int kb1 = min(args.num_kb, kb0 + args.kb_per_split);
       bool ok = true;
@@ -159,7 +152,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           const uint32_t sa = smem_base + stage * STAGE_BYTES;
           const uint32_t sb = sa + A_BYTES;
           mbar_arrive_expect_tx(full_bar(stage), STAGE_BYTES);
-          tma_load_2d(sa, &tmA, full_bar(stage), kb * BK, m_blk * BM, pol_a);
+          tma_load_2d(sa, &tmA, full_bar(stage), kb * BK, T.row0, pol_a);
           tma_load_2d(sb, &tmB, full_bar(stage), kb * BK, brow, pol_b);
           tma_load_2d(sb + 128 * 128, &tmB, full_bar(stage), kb * BK, brow + args.second_box_off,
                       pol_b);
@@ -183,13 +176,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     uint32_t stage = 0, phase = 0;
     int local = 0;
     for (int u = blockIdx.x; u < total; u += gridDim.x) {
-      const int t = u / args.splits, ks = u - t * args.splits;
-      int m_blk, n_tile;
-      sched_tile(sched, t, m_blk, n_tile);
-      const int e = s_ids[m_blk];
-      if (e < 0 || e >= args.num_experts) continue;
       const int acc = local & 1;
       const uint32_t acc_phase = (local >> 1) & 1;
+      const int ks = u % args.splits;
       if (!mbar_wait_bounded(tempty_bar(acc), acc_phase ^ 1, abort_flag, args.limit_ns, args.err)) break;
       tc_fence_after();
       const uint32_t d_tmem = tmem_base + acc * BN;
@@ -231,10 +220,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     int local = 0;
     for (int u = blockIdx.x; u < total; u += gridDim.x) {
       const int t = u / args.splits, ks = u - t * args.splits;
-      int m_blk, n_tile;
-      sched_tile(sched, t, m_blk, n_tile);
-      const int e = s_ids[m_blk];
-      if (e < 0 || e >= args.num_experts) continue;
+      const Tile T = sched_tile(sched, t);
+      const int e = T.e, n_tile = T.n_tile;
       const int acc = local & 1;
       const uint32_t acc_phase = (local >> 1) & 1;
       int ok = 0;
@@ -243,7 +230,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       if (!ok) break;
       tc_fence_after();
       const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + acc * BN;
-      const size_t row = (size_t)m_blk * BM + row_in_tile;
+      // rows past the expert's segment (a partial last m-tile) are not stored
+      const bool live = row_in_tile < T.rows;
+      const size_t row = (size_t)T.row0 + row_in_tile;
       __nv_bfloat16* out_row = args.out + row * args.ldo + (size_t)n_tile * args.out_cols_per_tile;
       if (FUSE) {
         const int gcol = n_tile * 128;          // gate columns of the tile; up at + I
@@ -253,12 +242,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           tmem_ld_32x32b_x32(taddr + c * 32, g);
           tmem_ld_32x32b_x32(taddr + 128 + c * 32, u);
           tmem_ld_wait();
-          epi_glu_store32(args.ep, e, gcol + c * 32, args.ldo + gcol + c * 32, g, u,
-                          out_row + c * 32);
+          if (live)
+            epi_glu_store32(args.ep, e, gcol + c * 32, args.ldo + gcol + c * 32, g, u,
+                            out_row + c * 32);
         }
       } else if (args.part != nullptr) {
         // split-K slice: raw fp32 sums of live rows, by routed item
-        const int item = args.part_ids[row];
+        const int item = live ? args.part_ids[row] : args.part_R;
         float* prow = args.part + ((size_t)ks * args.part_R + (item < args.part_R ? item : 0)) *
                                       args.ldo + (size_t)n_tile * BN;
 #pragma unroll 1
@@ -275,13 +265,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           }
         }
       } else {
-        const float w = epi_row_weight(args.ep, row);
+        const float w = live ? epi_row_weight(args.ep, row) : 0.0f;
 #pragma unroll 1
         for (int c = 0; c < BN / 32; ++c) {
           uint32_t r[32];
           tmem_ld_32x32b_x32(taddr + c * 32, r);
           tmem_ld_wait();
-          epi_store32(args.ep, e, n_tile * BN + c * 32, w, r, out_row + c * 32);
+          if (live) epi_store32(args.ep, e, n_tile * BN + c * 32, w, r, out_row + c * 32);
         }
       }
       tc_fence_before();
@@ -379,8 +369,9 @@ cudaError_t launch_ggemm_bf16(const void* A, int cap, int K, const void* B, int 
                               int b_rows_per_expert, int n_out, const int32_t* block_expert_ids,
                               const int32_t* num_post_padded, void* out, bool fuse_act,
                               const Epilogue& ep, cudaStream_t stream, int splits, float* part,
-                              const int32_t* part_ids, int part_R) {
+                              const int32_t* part_ids, int part_R, int blk_rows) {
   if (cap <= 0) return cudaSuccess;
+  if (blk_rows <= 0 || blk_rows > BM || cap % blk_rows != 0) return cudaErrorInvalidValue;
   // partial mode (part != nullptr): fp32 slice sums instead of bf16 out
   if ((part != nullptr && (fuse_act || part_ids == nullptr || part_R <= 0)) ||
       (part == nullptr && (splits > 1 || out == nullptr)))
@@ -395,7 +386,8 @@ cudaError_t launch_ggemm_bf16(const void* A, int cap, int K, const void* B, int 
   a.out = static_cast<__nv_bfloat16*>(out);
   a.num_kb = K / BK;
   a.b_rows_per_expert = b_rows_per_expert;
-  a.m_blocks_cap = cap / BM;
+  a.blocks_cap = cap / blk_rows;
+  a.blk_rows = blk_rows;
   a.num_experts = b_rows_total / b_rows_per_expert;
   a.group_max = sched_group_max(K, 2);
   if (fuse_act) {

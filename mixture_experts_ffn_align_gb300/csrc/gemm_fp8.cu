@@ -60,9 +60,8 @@ constexpr int LAUNCH_REGS = 168, CTRL_REGS = 56, EPI_REGS = 216;
 static_assert(128 * CTRL_REGS + 256 * EPI_REGS <= NUM_THREADS * LAUNCH_REGS,
               "register split exceeds the launch allocation");
 static_assert(32 * (CTRL_REGS + 2 * EPI_REGS) <= 16384, "register-file partition");
-constexpr int SCHED_BYTES = 16 + 4 * kSchedMaxRuns + 4 * kSchedMaxBlocks;
 constexpr int AMAX_BYTES = 2 * 2 * BM * 4;      // fused epilogue: [tile parity][half][row]
-constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + 256 + SCHED_BYTES + AMAX_BYTES;
+constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + 256 + kSchedBytes + AMAX_BYTES;
 static_assert(SMEM_BYTES <= 232448, "shared memory");
 
 struct Fp8Args {
@@ -76,9 +75,10 @@ struct Fp8Args {
   int n_tiles;            // ceil(N / 256)
   int n_blocks;           // N / 128 (weight-scale blocks per expert)
   int b_rows_per_expert;  // N
-  int m_blocks_cap;
+  int blocks_cap;         // blocks of blk_rows rows the buffers hold
+  int blk_rows;           // rows per block of the padded layout
   int num_experts;
-  int group_max;          // m-blocks per scheduling group (L2 budget)
+  int group_max;          // m-tiles per scheduling group (L2 budget)
   uint64_t limit_ns;
   int never_arrive;
   int* err;
@@ -101,9 +101,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   // full[S], empty[S], pfull[P], pempty[P], drain, amax exchange[4]
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 2 * NPART + 1 + 4);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
-  int* s_nruns = reinterpret_cast<int*>(smem + STAGES * STAGE_BYTES + 256);
-  int* s_runs = s_nruns + 4;
-  int* s_ids = s_runs + kSchedMaxRuns;
+  int* s_sched = reinterpret_cast<int*>(smem + STAGES * STAGE_BYTES + 256);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t smem_base = smem_u32(smem);
@@ -114,7 +112,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   auto pempty_bar = [&](int b) { return bar_base + 8u * (2 * STAGES + NPART + b); };
   const uint32_t drain_bar = bar_base + 8u * (2 * STAGES + 2 * NPART);
   auto amax_bar = [&](int q) { return bar_base + 8u * (2 * STAGES + 2 * NPART + 1 + q); };
-  float* s_amax = reinterpret_cast<float*>(smem + STAGES * STAGE_BYTES + 1024 + 256 + SCHED_BYTES);
+  float* s_amax = reinterpret_cast<float*>(smem + STAGES * STAGE_BYTES + 256 + kSchedBytes);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -144,14 +142,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   tc_fence_after();
   const uint32_t tmem_base = *tmem_holder;
 
-  const int nb_valid =
-      min(min(*args.num_post_padded / BM, args.m_blocks_cap), kSchedMaxBlocks);
-  const int total = nb_valid * args.n_tiles;
-  TileSched sched;
-  sched.nruns = sched_build(args.block_expert_ids, nb_valid, s_ids, s_runs, s_nruns);
-  sched.runs = s_runs;
-  sched.n_tiles = args.n_tiles;
-  sched.group_max = args.group_max;
+  const int nb_valid = min(*args.num_post_padded / args.blk_rows, args.blocks_cap);
+  const TileSched sched =
+      sched_build(args.block_expert_ids, nb_valid, args.blk_rows, args.num_experts, s_sched,
+                  reinterpret_cast<int*>(smem), args.n_tiles, args.group_max);
+  const int total = sched_mtiles(sched) * args.n_tiles;
 
   if (warp < EPI_WARP0) {
    setmaxnreg_dec<CTRL_REGS>();     // all of warpgroup 0, before its role split
@@ -162,10 +157,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     uint32_t stage = 0, phase = 0, issued_mask = 0, issued_parity = 0;
     bool skip_first = args.never_arrive != 0;
     for (int t = blockIdx.x; t < total; t += gridDim.x) {
-      int m_blk, n_tile;
-      sched_tile(sched, t, m_blk, n_tile);
-      const int e = s_ids[m_blk];
-      if (e < 0 || e >= args.num_experts) continue;
+      const Tile T = sched_tile(sched, t);
+      const int e = T.e, n_tile = T.n_tile;
       // B tile: 256 consecutive weight rows, or (FUSE) gate rows
       // [128 j, 128 j + 128) and the matching up rows I + 128 j ...
       const int brow = FUSE ? e * args.b_rows_per_expert + n_tile * 128
@@ -182,7 +175,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         } else {
           const uint32_t sa = smem_base + stage * STAGE_BYTES;
           mbar_arrive_expect_tx(full_bar(stage), STAGE_BYTES);
-          tma_load_2d(sa, &tmA, full_bar(stage), kb * BK, m_blk * BM, pol_a);
+          tma_load_2d(sa, &tmA, full_bar(stage), kb * BK, T.row0, pol_a);
           tma_load_2d(sa + A_BYTES, &tmB, full_bar(stage), kb * BK, brow, pol_b);
           tma_load_2d(sa + A_BYTES + 128 * BK, &tmB, full_bar(stage), kb * BK, brow2, pol_b);
           issued_mask |= 1u << stage;
@@ -204,10 +197,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     uint32_t stage = 0, phase = 0, pc = 0;
     bool ok = true;
     for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-      int m_blk, n_tile;
-      sched_tile(sched, t, m_blk, n_tile);
-      const int e = s_ids[m_blk];
-      if (e < 0 || e >= args.num_experts) continue;
       for (int kb = 0; kb < args.num_kb; ++kb, ++pc) {
         const uint32_t buf = pc % NPART, pphase = (pc / NPART) & 1;
         if (!mbar_wait_bounded(pempty_bar(buf), pphase ^ 1, abort_flag, args.limit_ns, args.err) ||
@@ -242,16 +231,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     uint32_t pc = 0, xpar = 0;
     bool ok = true;
     for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-      int m_blk, n_tile;
-      sched_tile(sched, t, m_blk, n_tile);
-      const int e = s_ids[m_blk];
-      if (e < 0 || e >= args.num_experts) continue;
+      const Tile T = sched_tile(sched, t);
+      const int e = T.e, n_tile = T.n_tile;
       // weight-scale block of this warp's columns (FUSE: its 64 gate columns
       // lie in block n_tile, the matching up columns in block I/128 + n_tile)
       const int nblk = FUSE ? n_tile : 2 * n_tile + half;
       const bool active = FUSE || nblk < args.n_blocks;   // false: past N on a ragged last tile
-      const size_t row = (size_t)m_blk * BM + row_in_tile;
-      const float* sa_row = args.a_scale + row * args.num_kb;
+      // rows past the expert's segment (a partial last m-tile) are computed
+      // on other rows' data and not stored; their scales are read from the
+      // tile's first row, inside the buffers
+      const bool live = row_in_tile < T.rows;
+      const size_t row = (size_t)T.row0 + row_in_tile;
+      const float* sa_row = args.a_scale + (live ? row : (size_t)T.row0) * args.num_kb;
       const float* sb_blk =
           args.b_scale + ((size_t)e * args.n_blocks + (active ? nblk : 0)) * (size_t)args.num_kb;
       const float* sb_up =
@@ -369,10 +360,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                       << (8 * bb);
             wd[qd] = word;
           }
-          zdst[v] = make_uint4(wd[0], wd[1], wd[2], wd[3]);
+          if (live) zdst[v] = make_uint4(wd[0], wd[1], wd[2], wd[3]);
         }
-        if (half == 0) args.zs[row * (size_t)(args.I / 128) + n_tile] = sc;
-      } else if (active) {
+        if (half == 0 && live) args.zs[row * (size_t)(args.I / 128) + n_tile] = sc;
+      } else if (active && live) {
         __nv_bfloat16* dst = args.out + row * args.ldo + (size_t)nblk * 128;
         const float w = epi_row_weight(args.ep, row);
         const bool bias = args.ep.bias != nullptr;
@@ -431,8 +422,10 @@ cudaError_t launch_ggemm_fp8(const void* A, const float* a_scale, int cap, int K
                              const float* b_scale, int b_rows_total, int b_rows_per_expert,
                              int n_out, const int32_t* block_expert_ids,
                              const int32_t* num_post_padded, void* out, const Epilogue& ep,
-                             cudaStream_t stream, float* z_scale, bool fuse_act, bool ue8m0) {
+                             cudaStream_t stream, float* z_scale, bool fuse_act, bool ue8m0,
+                             int blk_rows) {
   if (cap <= 0) return cudaSuccess;
+  if (blk_rows <= 0 || blk_rows > BM || cap % blk_rows != 0) return cudaErrorInvalidValue;
   // fused GEMM1: B rows per expert = 2I (gate then up), I a multiple of 128
   if (fuse_act && (z_scale == nullptr || b_rows_per_expert % 256 != 0 ||
                    n_out != b_rows_per_expert))
@@ -458,7 +451,8 @@ cudaError_t launch_ggemm_fp8(const void* A, const float* a_scale, int cap, int K
   a.zs = z_scale;
   a.ue8m0 = ue8m0 ? 1 : 0;
   a.b_rows_per_expert = b_rows_per_expert;
-  a.m_blocks_cap = cap / BM;
+  a.blocks_cap = cap / blk_rows;
+  a.blk_rows = blk_rows;
   a.num_experts = b_rows_total / b_rows_per_expert;
   a.group_max = sched_group_max(K, 1);
   watchdog_params(&a.limit_ns, &a.never_arrive);

@@ -62,7 +62,7 @@ static_assert(32 * (CTRL_REGS + 2 * EPI_REGS) <= 16384, "register-file partition
 constexpr int RING = 4;                       // tile-index slots
 // leader MMA issuer + peer producer + the promotion warps of both CTAs
 constexpr int RING_READERS = 2 + 2 * NUM_EPI_WARPS;
-constexpr int SCHED_BYTES = 16 + 4 * kSchedMaxRuns * 2 + 4 * kSchedMaxBlocks;
+constexpr int SCHED_BYTES = kSchedBytes + 4 * (kSchedMaxRuns + 1);   // + pairs per segment
 constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + 256 + SCHED_BYTES;
 static_assert(SMEM_BYTES <= 232448, "shared memory");
 
@@ -98,10 +98,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 2 * NPART + 1 + 2 * RING);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
   int* s_ring = reinterpret_cast<int*>(tmem_holder + 2);   // RING tile indices
-  int* s_nruns = reinterpret_cast<int*>(smem + STAGES * STAGE_BYTES + 256);
-  int* s_runs = s_nruns + 4;
-  int* s_pairs = s_runs + kSchedMaxRuns;       // prefix of pairs per run
-  int* s_ids = s_pairs + kSchedMaxRuns;
+  int* s_sched = reinterpret_cast<int*>(smem + STAGES * STAGE_BYTES + 256);
+  int* s_pairs = s_sched + kSchedBytes / 4;    // prefix of pairs per segment
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = cluster_ctarank();
@@ -151,35 +149,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   tc_fence_after();
   const uint32_t tmem_base = *tmem_holder;
 
-  const int nb_valid =
-      min(min(*args.num_post_padded / BM, args.m_blocks_cap), kSchedMaxBlocks);
-  const int nruns = sched_build(args.block_expert_ids, nb_valid, s_ids, s_runs, s_nruns);
-  if (threadIdx.x == 0) {
-    int acc = 0;
-    for (int r = 0; r < nruns; ++r) {
-      s_pairs[r] = acc;
-      acc += (s_runs[r + 1] - s_runs[r] + 1) >> 1;
-    }
-    s_pairs[nruns] = acc;
-  }
+  // 128-row blocks (the pair forms take no other block size)
+  const int nb_valid = min(*args.num_post_padded / BM, args.m_blocks_cap);
+  const TileSched sched =
+      sched_build(args.block_expert_ids, nb_valid, BM, args.num_experts, s_sched,
+                  reinterpret_cast<int*>(smem), args.n_tiles, 1 << 20);
+  sched_pairs_build(sched, s_pairs);
   __syncthreads();
-  const int total = s_pairs[nruns] * args.n_tiles;
-
-  // tile t -> (leader block m0, peer block m1, n-tile); m1 == m0 for a lone block
-  auto decode = [&](int t, int& m0, int& m1, bool& has1, int& n_tile) {
-    const int q = t / args.n_tiles;
-    int lo = 0, hi = nruns - 1;
-    while (lo < hi) {
-      const int mid = (lo + hi + 1) >> 1;
-      if (s_pairs[mid] <= q) lo = mid; else hi = mid - 1;
-    }
-    const int np = s_pairs[lo + 1] - s_pairs[lo];
-    const int local = t - s_pairs[lo] * args.n_tiles;
-    n_tile = local / np;
-    m0 = s_runs[lo] + 2 * (local - n_tile * np);
-    has1 = m0 + 1 < s_runs[lo + 1];
-    m1 = has1 ? m0 + 1 : m0;
-  };
+  const int total = s_pairs[sched.nruns] * args.n_tiles;
 
   // Tile ring: the leader's producer publishes tile j in slot j % RING (-1:
   // no tiles left); every reader takes the slots in the same order.
@@ -234,12 +211,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         t = ring_take(j);
         if (t < 0) break;
       }
-      int m0, m1, n_tile;
-      bool has1;
-      decode(t, m0, m1, has1, n_tile);
-      const int e = s_ids[m0];
-      if (e < 0 || e >= args.num_experts) continue;
-      const int my_m = leader ? m0 : m1;
+      const PairTile P = sched_pair_tile(sched, s_pairs, t);
+      const int e = P.e, n_tile = P.n_tile;
+      const int my_row = leader ? P.row0 : P.row1;
       // weight rows [brow, brow + 128): the leader's half, the peer's the next 128
       const int brow = e * args.b_rows_per_expert + n_tile * BN + (leader ? 0 : BN / 2);
       bool ok = true;
@@ -258,7 +232,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             issued_mask |= 1u << stage;
             issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
           }
-          tma_load_2d_pair(sa, &tmA, bar, kb * BK, my_m * BM, pol_a);
+          tma_load_2d_pair(sa, &tmA, bar, kb * BK, my_row, pol_a);
           tma_load_2d_pair(sa + A_BYTES, &tmB, bar, kb * BK, brow, pol_b);
         }
         if (++stage == STAGES) {
@@ -283,11 +257,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     for (int j = 0; ok; ++j) {
       const int t = ring_take(j);
       if (t < 0) break;
-      int m0, m1, n_tile;
-      bool has1;
-      decode(t, m0, m1, has1, n_tile);
-      const int e = s_ids[m0];
-      if (e < 0 || e >= args.num_experts) continue;
       for (int kb = 0; kb < args.num_kb; ++kb, ++pc) {
         const uint32_t buf = pc % NPART, pphase = (pc / NPART) & 1;
         if (!mbar_wait_bounded(pempty_bar(buf), pphase ^ 1, abort_flag, args.limit_ns,
@@ -328,15 +297,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       if (lane == 0) t = ring_take(j);
       t = __shfl_sync(0xffffffffu, t, 0);
       if (t < 0) break;
-      int m0, m1, n_tile;
-      bool has1;
-      decode(t, m0, m1, has1, n_tile);
-      const int e = s_ids[m0];
-      if (e < 0 || e >= args.num_experts) continue;
+      const PairTile P = sched_pair_tile(sched, s_pairs, t);
+      const int e = P.e, n_tile = P.n_tile;
+      const bool has1 = P.has1;
       const bool store = leader || has1;          // a lone block's peer half is a repeat
       const int nblk = 2 * n_tile + half;
       const bool active = nblk < args.n_blocks;   // false: past N on a ragged last tile
-      const size_t row = (size_t)(leader ? m0 : m1) * BM + row_in_tile;
+      const size_t row = (size_t)(leader ? P.row0 : P.row1) + row_in_tile;
       const float* sa_row = args.a_scale + row * args.num_kb;
       const float* sb_blk =
           args.b_scale + ((size_t)e * args.n_blocks + (active ? nblk : 0)) * (size_t)args.num_kb;

@@ -92,10 +92,6 @@ constexpr int BM = 128, BN = 256, BK = 128, STAGES = 4, SSLOTS = 4;
 // Staged weight scales (K % 512 == 0): 16 bytes = 4 K blocks of each of the
 // tile's 256 rows per TMA box, NSTG groups in flight.
 constexpr int NSTG = 2, STG_BYTES = 16 * BN;
-// Blocks the schedule can hold: M * topk + E * 127 rows at the boundary's limits.
-constexpr int kMaxBlocks = 3072;
-static_assert((MOE_MAX_TOKENS * MOE_MAX_TOPK + MOE_MAX_EXPERTS * 127) / 128 <= kMaxBlocks,
-              "schedule capacity");
 constexpr int A_BYTES = BM * BK;          // e4m3
 constexpr int B_BYTES = BN * BK;          // 4-bit values padded to one byte each in smem
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
@@ -107,9 +103,8 @@ constexpr int SF_SLOT = 16;               // stage s: A at SF_COL0 + 32 s, B at 
 constexpr int TMEM_COLS = 512;
 constexpr int NUM_EPI_WARPS = 4, EPI_WARP0 = 4;
 constexpr int NUM_THREADS = (EPI_WARP0 + NUM_EPI_WARPS) * 32;
-constexpr int SCHED_BYTES = 16 + 4 * kSchedMaxRuns + 4 * kMaxBlocks;
 constexpr int SMEM_BYTES =
-    STAGES * STAGE_BYTES + SSLOTS * SF_BYTES + NSTG * STG_BYTES + 1024 + 256 + SCHED_BYTES;
+    STAGES * STAGE_BYTES + SSLOTS * SF_BYTES + NSTG * STG_BYTES + 1024 + 256 + kSchedBytes;
 static_assert(SF_COL0 + SF_SLOT * (2 * STAGES - 1) + BN / 32 <= TMEM_COLS, "tensor memory");
 static_assert(SMEM_BYTES <= 232448, "shared memory");
 
@@ -123,7 +118,8 @@ struct Mx4Args {
   int num_kb;               // K / 128
   int n_tiles;              // ceil(N / 256)
   int b_rows_per_expert;    // N
-  int m_blocks_cap;
+  int blocks_cap;           // blocks of blk_rows rows the buffers hold
+  int blk_rows;             // rows per block of the padded layout
   int num_experts;
   int group_max;
   uint64_t limit_ns;
@@ -145,13 +141,17 @@ template <bool MX8>
 struct AGroup {
   float4 v[4][MX8 ? 4 : 1];
 };
-// Loads the scales of K blocks g .. g+3 (those past num_kb read as 2^0).
+// Loads the scales of K blocks g .. g+3 (those past num_kb read as 2^0) of
+// this lane's rows lane + 32 c of the m-tile starting at tile_row0; rows at
+// or past `rows` (past the expert's segment: their results are not stored)
+// read the tile's first row instead, inside the buffer.
 template <bool MX8>
-__device__ __forceinline__ void load_ascales(AGroup<MX8>& A, const float* a_scale, size_t row0,
-                                             int num_kb, int g) {
+__device__ __forceinline__ void load_ascales(AGroup<MX8>& A, const float* a_scale,
+                                             size_t tile_row0, int rows, int lane, int num_kb,
+                                             int g) {
 #pragma unroll
   for (int c = 0; c < 4; ++c) {
-    const size_t row = row0 + 32 * c;
+    const size_t row = tile_row0 + (lane + 32 * c < rows ? lane + 32 * c : 0);
     if constexpr (MX8) {
       const float* pa = a_scale + row * (size_t)(4 * num_kb);
 #pragma unroll
@@ -196,9 +196,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   // full[S], empty[S], sfull[SS], sempty[SS], tfull, tempty, drain, stg_full[NSTG]
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 2 * SSLOTS + 3 + NSTG);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
-  int* s_nruns = reinterpret_cast<int*>(stg_ring + NSTG * STG_BYTES + 256);
-  int* s_runs = s_nruns + 4;
-  int* s_ids = s_runs + kSchedMaxRuns;
+  int* s_sched = reinterpret_cast<int*>(stg_ring + NSTG * STG_BYTES + 256);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t smem_base = smem_u32(smem);
@@ -244,13 +242,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   tc_fence_after();
   const uint32_t tmem_base = *tmem_holder;
 
-  const int nb_valid = min(min(*args.num_post_padded / BM, args.m_blocks_cap), kMaxBlocks);
-  const int total = nb_valid * args.n_tiles;
-  TileSched sched;
-  sched.nruns = sched_build(args.block_expert_ids, nb_valid, s_ids, s_runs, s_nruns);
-  sched.runs = s_runs;
-  sched.n_tiles = args.n_tiles;
-  sched.group_max = args.group_max;
+  const int nb_valid = min(*args.num_post_padded / args.blk_rows, args.blocks_cap);
+  const TileSched sched =
+      sched_build(args.block_expert_ids, nb_valid, args.blk_rows, args.num_experts, s_sched,
+                  reinterpret_cast<int*>(smem), args.n_tiles, args.group_max);
+  const int total = sched_mtiles(sched) * args.n_tiles;
   const int N = args.b_rows_per_expert;
 
   if (warp == 0 && lane == 0) {
@@ -260,10 +256,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     uint32_t stage = 0, phase = 0, issued_mask = 0, issued_parity = 0;
     bool skip_first = args.never_arrive != 0;
     for (int t = blockIdx.x; t < total; t += gridDim.x) {
-      int m_blk, n_tile;
-      sched_tile(sched, t, m_blk, n_tile);
-      const int e = s_ids[m_blk];
-      if (e < 0 || e >= args.num_experts) continue;
+      const Tile T = sched_tile(sched, t);
+      const int e = T.e, n_tile = T.n_tile;
       // B tile: 256 consecutive weight rows, or (FUSE) gate rows
       // [128 j, 128 j + 128) and the matching up rows I + 128 j ...
       const int brow = FUSE ? e * N + n_tile * 128 : e * N + n_tile * BN;
@@ -279,7 +273,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         } else {
           const uint32_t sa = smem_base + stage * STAGE_BYTES;
           mbar_arrive_expect_tx(full_bar(stage), MX8 ? A_BYTES + B_BYTES : TX_BYTES);
-          tma_load_2d(sa, &tmA, full_bar(stage), kb * BK, m_blk * BM, pol_a);
+          tma_load_2d(sa, &tmA, full_bar(stage), kb * BK, T.row0, pol_a);
           tma_load_2d(sa + A_BYTES, &tmB, full_bar(stage), kb * BK, brow, pol_b);
           tma_load_2d(sa + A_BYTES + B_BYTES / 2, &tmB, full_bar(stage), kb * BK, brow2, pol_b);
           issued_mask |= 1u << stage;
@@ -339,13 +333,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const uint64_t pol_s = l2_policy(MOE_GEMM_L2_B);
       const uint32_t stg_base = smem_u32(stg_ring);
       struct Cursor {
-        int t, g, m_blk, n_tile, e;
+        int t, g, row0, rows, n_tile, e;
       };
-      auto seek = [&](Cursor& c) {             // first tile at or after c.t with a valid expert
+      auto seek = [&](Cursor& c) {             // the tile at c.t, if any
         for (; c.t < total; c.t += gridDim.x) {
-          sched_tile(sched, c.t, c.m_blk, c.n_tile);
-          c.e = s_ids[c.m_blk];
-          if (c.e >= 0 && c.e < args.num_experts) {
+          const Tile T = sched_tile(sched, c.t);
+          c.row0 = T.row0;
+          c.rows = T.rows;
+          c.n_tile = T.n_tile;
+          c.e = T.e;
+          {
             c.g = 0;
             return true;
           }
@@ -362,7 +359,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       bool ok = true;
       if (wa) {
         auto load_a = [&](const Cursor& c, AGroup<MX8>& A) {
-          load_ascales<MX8>(A, args.a_scale, (size_t)c.m_blk * BM + lane, args.num_kb, 4 * c.g);
+          load_ascales<MX8>(A, args.a_scale, (size_t)c.row0, c.rows, lane, args.num_kb, 4 * c.g);
         };
         Cursor anext = use;
         bool anext_ok = use_ok;
@@ -416,7 +413,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         Cursor anext = use;
         bool anext_ok = use_ok;
         auto load_a = [&](const Cursor& c, AGroup<MX8>& A) {
-          load_ascales<MX8>(A, args.a_scale, (size_t)c.m_blk * BM + lane, args.num_kb, 4 * c.g);
+          load_ascales<MX8>(A, args.a_scale, (size_t)c.row0, c.rows, lane, args.num_kb, 4 * c.g);
         };
         if constexpr (!MX8) {
           if (use_ok) {
@@ -489,15 +486,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const bool writes_b = !wa;
       bool ok = true;
       for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-        int m_blk, n_tile;
-        sched_tile(sched, t, m_blk, n_tile);
-        const int e = s_ids[m_blk];
-        if (e < 0 || e >= args.num_experts) continue;
-        const size_t arow = (size_t)m_blk * BM + lane;
+        const Tile T = sched_tile(sched, t);
+        const int e = T.e, n_tile = T.n_tile;
+        auto load_a = [&](AGroup<MX8>& A, int g) {
+          load_ascales<MX8>(A, args.a_scale, (size_t)T.row0, T.rows, lane, args.num_kb, g);
+        };
         AGroup<MX8> a_cur, a_nxt;
         if (writes_a) {
-          load_ascales<MX8>(a_cur, args.a_scale, arow, args.num_kb, 0);
-          if (args.num_kb > 4) load_ascales<MX8>(a_nxt, args.a_scale, arow, args.num_kb, 4);
+          load_a(a_cur, 0);
+          if (args.num_kb > 4) load_a(a_nxt, 4);
         }
         // group offsets (in 512-byte blocks) of the operand's two halves
         const int g0 = FUSE ? n_tile : 2 * n_tile;
@@ -550,8 +547,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           }
           if (writes_a) {
             a_cur = a_nxt;
-            if (kb0 + 8 < args.num_kb)
-              load_ascales<MX8>(a_nxt, args.a_scale, arow, args.num_kb, kb0 + 8);
+            if (kb0 + 8 < args.num_kb) load_a(a_nxt, kb0 + 8);
           }
         }
       }
@@ -560,22 +556,22 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const bool vec = (args.num_kb & 3) == 0;   // rows 16-byte aligned: vector loads
       bool ok = true;
       for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-        int m_blk, n_tile;
-        sched_tile(sched, t, m_blk, n_tile);
-        const int e = s_ids[m_blk];
-        if (e < 0 || e >= args.num_experts) continue;
+        const Tile T = sched_tile(sched, t);
+        const int e = T.e, n_tile = T.n_tile;
+        auto load_a = [&](AGroup<MX8>& A, int g) {
+          load_ascales<MX8>(A, args.a_scale, (size_t)T.row0, T.rows, lane, args.num_kb, g);
+        };
         // activation scales of 4 K blocks per load (W4A8, built by warp 3
         // with the weight operand: one group ahead; MXFP8, warp 2: its 4x
         // larger scales at the group's start)
         AGroup<MX8> a_cur, a_nxt;
         if constexpr (!MX8) {
-          load_ascales<MX8>(a_cur, args.a_scale, (size_t)m_blk * BM + lane, args.num_kb, 0);
-          if (args.num_kb > 4)
-            load_ascales<MX8>(a_nxt, args.a_scale, (size_t)m_blk * BM + lane, args.num_kb, 4);
+          load_a(a_cur, 0);
+          if (args.num_kb > 4) load_a(a_nxt, 4);
         }
         if (wa) {
           for (int kb0 = 0; kb0 < args.num_kb && ok; kb0 += 4) {
-            load_ascales<MX8>(a_cur, args.a_scale, (size_t)m_blk * BM + lane, args.num_kb, kb0);
+            load_a(a_cur, kb0);
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
               if (kb0 + j >= args.num_kb) break;
@@ -640,9 +636,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             if (kb0 + 8 < args.num_kb) load_b(kb0 + 8, b_nxt);
             if constexpr (!MX8) {
               a_cur = a_nxt;
-              if (kb0 + 8 < args.num_kb)
-                load_ascales<MX8>(a_nxt, args.a_scale, (size_t)m_blk * BM + lane, args.num_kb,
-                                  kb0 + 8);
+              if (kb0 + 8 < args.num_kb) load_a(a_nxt, kb0 + 8);
             }
           }
         }
@@ -654,10 +648,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     int local = 0;
     bool ok = true;
     for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-      int m_blk, n_tile;
-      sched_tile(sched, t, m_blk, n_tile);
-      const int e = s_ids[m_blk];
-      if (e < 0 || e >= args.num_experts) continue;
       if (!mbar_wait_bounded(tempty_bar, (local & 1) ^ 1, abort_flag, args.limit_ns, args.err))
         break;
       tc_fence_after();
@@ -706,17 +696,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const int row_in_tile = q * 32 + lane;
     int local = 0;
     for (int t = blockIdx.x; t < total; t += gridDim.x) {
-      int m_blk, n_tile;
-      sched_tile(sched, t, m_blk, n_tile);
-      const int e = s_ids[m_blk];
-      if (e < 0 || e >= args.num_experts) continue;
+      const Tile T = sched_tile(sched, t);
+      const int e = T.e, n_tile = T.n_tile;
       int ok = 0;
       if (lane == 0)
         ok = mbar_wait_bounded(tfull_bar, local & 1, abort_flag, args.limit_ns, args.err);
       ok = __shfl_sync(0xffffffffu, ok, 0);
       if (!ok) break;
       tc_fence_after();
-      const size_t row = (size_t)m_blk * BM + row_in_tile;
+      // rows past the expert's segment (a partial last m-tile) are not stored
+      const bool live = row_in_tile < T.rows;
+      const size_t row = (size_t)T.row0 + row_in_tile;
       if constexpr (FUSE) {
         // Gated activation + dynamic quantisation of z (as act_mul_quant
         // does from a stored H1): columns [0, 128) hold this row's gate sums
@@ -768,9 +758,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             }
             const float sc = act_scale(amax, args.ue8m0 != 0);
             const float rc = __frcp_rn(sc);
-            zdst[2 * c] = quant16(z, sc, rc);
-            zdst[2 * c + 1] = quant16(z + 16, sc, rc);
-            zs_row[c] = sc;
+            if (live) {
+              zdst[2 * c] = quant16(z, sc, rc);
+              zdst[2 * c + 1] = quant16(z + 16, sc, rc);
+              zs_row[c] = sc;
+            }
           }
         } else {
           float z[128];
@@ -792,18 +784,20 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           if (lane == 0) mbar_arrive(tempty_bar);
           const float sc = act_scale(amax, args.ue8m0 != 0);
           const float rc = __frcp_rn(sc);
+          if (live) {
 #pragma unroll
-          for (int v = 0; v < 8; ++v) zdst[v] = quant16(z + 16 * v, sc, rc);
-          zs_row[0] = sc;
+            for (int v = 0; v < 8; ++v) zdst[v] = quant16(z + 16 * v, sc, rc);
+            zs_row[0] = sc;
+          }
         }
       } else {
-      const float w = epi_row_weight(args.ep, row);
-      const bool bias = args.ep.bias != nullptr;
+      const float w = live ? epi_row_weight(args.ep, row) : 0.0f;
 #pragma unroll 1
       for (int half = 0; half < 2; ++half) {        // 128 columns at a time
         const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + half * 128;
         __nv_bfloat16* out_row = args.out + row * args.ldo + (size_t)n_tile * BN + half * 128;
-        const bool store = half * 128 < N - n_tile * BN;   // 256 columns, or 128 if ragged
+        // 256 columns, or 128 if ragged; live rows only
+        const bool store = live && half * 128 < N - n_tile * BN;
         uint32_t r[4][32];
 #pragma unroll
         for (int c = 0; c < 4; ++c) tmem_ld_32x32b_x32(taddr + c * 32, r[c]);
@@ -867,8 +861,9 @@ cudaError_t launch_ggemm_mxfp4(const void* A, const float* a_scale, int cap, int
                                int n_out, const int32_t* block_expert_ids,
                                const int32_t* num_post_padded, void* out, bool b_e4m3,
                                const Epilogue& ep, cudaStream_t stream, float* z_scale,
-                               bool fuse_act, bool ue8m0, bool scales_prepacked) {
+                               bool fuse_act, bool ue8m0, bool scales_prepacked, int blk_rows) {
   if (cap <= 0) return cudaSuccess;
+  if (blk_rows <= 0 || blk_rows > BM || cap % blk_rows != 0) return cudaErrorInvalidValue;
   // packed E2M1 tensor maps want 32-byte aligned bases, byte maps 16; bulk
   // copies of prepacked scales 16
   if ((reinterpret_cast<uintptr_t>(B) & (b_e4m3 ? 15u : 31u)) != 0 ||
@@ -901,7 +896,8 @@ cudaError_t launch_ggemm_mxfp4(const void* A, const float* a_scale, int cap, int
   a.zs = z_scale;
   a.ue8m0 = ue8m0 ? 1 : 0;
   a.b_rows_per_expert = b_rows_per_expert;
-  a.m_blocks_cap = cap / BM;
+  a.blocks_cap = cap / blk_rows;
+  a.blk_rows = blk_rows;
   a.num_experts = b_rows_total / b_rows_per_expert;
   a.group_max = sched_group_max(K, 1);
   watchdog_params(&a.limit_ns, &a.never_arrive);

@@ -103,6 +103,10 @@ cudaError_t launch_topk_router(const void* logits, bool bf16, int M, int E, int 
                                bool renorm, const int32_t* expert_map, float* w, int32_t* ids,
                                int32_t* tei, cudaStream_t stream);
 
+// The grouped GEMMs below walk each expert's segment of the padded layout in
+// 128-row m-tiles (tile_sched.cuh); blk_rows is the layout's block size (16,
+// 32, 64 or 128: the block ids' granularity).  The SM-pair forms take 128 only.
+//
 // bf16 grouped GEMM on tcgen05: out[row, n] = sum_k A[row, k] * B[e*b_rows + n, k].
 //   fuse_act: B tile = 128 gate rows + 128 up rows; writes SiLU(g)*u (bf16).
 //   part != nullptr (not with fuse_act): K is cut into `splits` slices (a
@@ -114,7 +118,7 @@ cudaError_t launch_ggemm_bf16(const void* A, int cap, int K, const void* B, int 
                               const int32_t* num_post_padded, void* out, bool fuse_act,
                               const Epilogue& ep, cudaStream_t stream, int splits = 1,
                               float* part = nullptr, const int32_t* part_ids = nullptr,
-                              int part_R = 0);
+                              int part_R = 0, int blk_rows = 128);
 
 // Weighted top-k reduce of split-K GEMM2 partials: y[t, :] = bf16( sum_i w[t,i] *
 // bf16( sum_s part[s, t*k + i, :] ) ), fp32, slots and slices in order; slots
@@ -148,7 +152,7 @@ cudaError_t launch_ggemm_fp8(const void* A, const float* a_scale, int cap, int K
                              int n_out, const int32_t* block_expert_ids,
                              const int32_t* num_post_padded, void* out, const Epilogue& ep,
                              cudaStream_t stream, float* z_scale = nullptr,
-                             bool fuse_act = false, bool ue8m0 = false);
+                             bool fuse_act = false, bool ue8m0 = false, int blk_rows = 128);
 
 // The same FP8 GEMM (no fused activation) issued on SM pairs (cta_group::2,
 // 256 x 256 tiles); n_out == b_rows_per_expert, a multiple of 128.  Tile
@@ -171,7 +175,8 @@ cudaError_t launch_ggemm_mxfp4(const void* A, const float* a_scale, int cap, int
                                const int32_t* num_post_padded, void* out, bool b_e4m3,
                                const Epilogue& ep, cudaStream_t stream,
                                float* z_scale = nullptr, bool fuse_act = false,
-                               bool ue8m0 = true, bool scales_prepacked = false);
+                               bool ue8m0 = true, bool scales_prepacked = false,
+                               int blk_rows = 128);
 
 // E8M0 weight scales [E, N, K/32] -> the operand layout the block-scaled MMA
 // copies into tensor memory: [E][K/128][N/128] blocks of 512 bytes, block

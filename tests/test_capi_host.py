@@ -85,14 +85,23 @@ def test_null_pointers_and_small_workspace_rejected():
     assert L.fused_experts(ctypes.byref(p.c()), *args, 1 << 40, None) == 1
 
 
-def test_gemm_block_size_must_equal_tile_height():
-    """A GEMM block taller than the padding granularity would read another
-    expert's id (page "Blackwell 上的 DeepGEMM FusedMoE（vLLM）", §2.6.3); the
-    GEMM entry points refuse block_size != 128 before launching."""
-    p = moe.Problem(M=16, H=256, I=128, E=8, topk=2, block_size=64)
+@pytest.mark.parametrize("bs", [0, 8, 48, 96, 256])
+def test_gemm_block_size_outside_the_validated_set_is_rejected(bs):
+    """block_size is one of 16, 32, 64, 128 (the GEMMs cut 128-row tiles
+    inside each expert's segment, so every one of them is served); anything
+    else is an invalid problem, refused before any launch."""
+    p = moe.Problem(M=16, H=256, I=128, E=8, topk=2, block_size=bs)
     L = moe.lib()
     d = ctypes.c_void_p(16)
-    assert L.grouped_gemm_w13(ctypes.byref(p.c()), d, None, d, None, d, d, d, None, 1, None) == 2
+    assert L.grouped_gemm_w13(ctypes.byref(p.c()), d, None, d, None, d, d, d, None, 1, None) == 1
+    assert moe.moe_m_sum_bound(p) == 0
+
+
+def test_batched_layout_takes_block_size_128_only():
+    """The batched layout's blocks are the 128-row tiles themselves."""
+    p = moe.Problem(M=16, H=256, I=128, E=8, topk=2, block_size=64)
+    assert moe.moe_m_sum_bound(p) > 0
+    assert moe.lib().moe_batched_workspace_bytes(ctypes.byref(p.c()), 128) == 0
 
 
 @pytest.mark.parametrize("M,E,k,scoring", [(-1, 8, 2, 0), (16385, 8, 2, 0), (4, 0, 1, 0),

@@ -86,12 +86,13 @@ CASES = [("bf16", "single"), ("bf16", "pairs"), ("fp8", "single"), ("fp8", "pair
 
 @pytest.mark.parametrize("quant,form", CASES)
 @pytest.mark.parametrize("fuse", [False, True])
-def test_no_stage_writes_outside_its_rows(quant, form, fuse):
+@pytest.mark.parametrize("bs", [128, 32])
+def test_no_stage_writes_outside_its_rows(quant, form, fuse, bs):
     # bf16 GEMM2 tiles are 256 columns wide (H % 256 == 0); the quantised
     # GEMMs take H = 640, a 128-wide last column tile
     counts, H, I = [0, 1, 127, 128, 129, 300, 0], (512 if quant == "bf16" else 640), 256
     cfg, d = _ragged(quant, counts, H, I, 31)
-    p = moe.Problem.from_config(cfg)
+    p = moe.Problem.from_config(cfg, block_size=bs)
     bufs = _buffers(p)
     b = {k: v[0] for k, v in bufs.items()}
     b["align_ws"] = torch.empty(max(moe.moe_align_workspace_bytes(p), 1), dtype=torch.uint8,
