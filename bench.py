@@ -233,16 +233,45 @@ def _traffic(cfg):
     return None
 
 
-def _gemm1_roofline(cfg, peaks, peak, ratio, flops, w13_bytes, ms):
+def gemm_bytes(cfg, S):
+    """Algorithmic DRAM bytes of one launch of each grouped GEMM, with S the
+    used rows of the padded layout: the weights and their scales read once,
+    the used activation rows (and their scales) read once, the output written
+    once -- GEMM1 writes z (the fused activation; bf16, or e4m3 codes + fp32
+    scales) except in the FP8-block mode, where it writes H1 (bf16); GEMM2
+    reads z and writes Y2 (bf16)."""
+    E, H, I, q = cfg.E, cfg.H, cfg.I, cfg.quant
+    wb = {"bf16": 2, "fp8": 1, "mxfp4": 0.5, "mxfp8": 1}[q]
+    ab = 2 if q == "bf16" else 1
+    g = 32 if q == "mxfp8" else 128
+
+    def wscales(N, K):
+        if q == "fp8":
+            return E * (N // 128) * (K // 128) * 4
+        return E * N * (K // 32) if q in ("mxfp4", "mxfp8") else 0
+
+    def act(rows, K):
+        return rows * K * ab + (rows * (K // g) * 4 if q != "bf16" else 0)
+
+    w13 = E * 2 * I * H * wb + wscales(2 * I, H)
+    w2 = E * H * I * wb + wscales(H, I)
+    out1 = S * 2 * I * 2 if q == "fp8" else act(S, I)
+    return {"gemm1": w13 + act(S, H) + out1, "gemm2": w2 + act(S, I) + S * H * 2,
+            "w13": w13, "w2": w2}
+
+
+def _gemm1_roofline(cfg, peaks, peak, ratio, flops, nbytes, w13_bytes, ms):
     """Roofline object of GEMM1: tensor-bound when its FLOPs take at least as
-    long at the tensor peak as its weights at the HBM peak, else HBM-bound
-    (decode and the one-block-per-expert MXFP4 workload stream weights)."""
+    long at the tensor peak as its algorithmic bytes at the HBM peak, else
+    HBM-bound (decode, and the E = 256 layers whose weights outweigh their
+    FLOPs)."""
     t_flop = flops / (peak * 1e12)
-    t_mem = w13_bytes / (peaks["hbm_gbs"] * 1e9)
+    t_mem = nbytes / (peaks["hbm_gbs"] * 1e9)
     tflops = flops / (ms * 1e-3) / 1e12
-    gbs = w13_bytes / (ms * 1e-3) / 1e9
+    gbs = nbytes / (ms * 1e-3) / 1e9
     common = {"kernel": gemm1_kernel(cfg)[1], "traffic": _traffic(cfg),
-              "tensor_frac": tflops / peak, "weight_hbm_frac": gbs / peaks["hbm_gbs"]}
+              "tensor_frac": tflops / peak, "hbm_frac": gbs / peaks["hbm_gbs"],
+              "weight_hbm_frac": w13_bytes / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"]}
     if t_flop >= t_mem:
         return {"bound": "tensor", "achieved": tflops, "peak": peak, "unit": "TFLOP/s",
                 "frac": tflops / peak,
@@ -250,7 +279,8 @@ def _gemm1_roofline(cfg, peaks, peak, ratio, flops, w13_bytes, ms):
                 "algorithmic_per_launch": f"2*R*H*2I = {flops:.4e} FLOP", **common}
     return {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
             "frac": gbs / peaks["hbm_gbs"], "peak_source": f"hbm_gbs ({peaks['source']})",
-            "algorithmic_per_launch": f"w13 bytes E*2I*H*b = {w13_bytes:.4e} B", **common}
+            "algorithmic_per_launch": f"weights + scales, used activation rows in, output out "
+                                      f"= {nbytes:.4e} B", **common}
 
 
 def _cores():
@@ -445,6 +475,7 @@ def _measure(moe, cfg, args, dev, world, rank, full, fp8_tflops=None):
         raise RuntimeError("device error in the timed region")
     stage_ms = {name: sum(e[i].elapsed_time(e[i + 1]) for e in evs) / args.steps
                 for i, (name, _) in enumerate(plan)}
+    S_used = int(b["num_post_padded"].item())     # after the timed region
 
     # the fused_experts call itself (same kernels, one entry point)
     f_steps = max(3, args.steps // 4)
@@ -523,11 +554,10 @@ def _measure(moe, cfg, args, dev, world, rank, full, fp8_tflops=None):
         g1 = [n for n, _ in plan if n.startswith("gemm1")][0]
         g2 = [n for n, _ in plan if n.startswith("gemm2")][0]
         peak, ratio, peak_src = _peak_for(peaks, q, elapsed_ms * 1e-3)
-        wbytes = {"bf16": 2.0, "fp8": 1.0, "mxfp4": 0.5, "mxfp8": 1.0}[cfg.quant]
-        w13_bytes = cfg.E * 2 * cfg.I * cfg.H * wbytes
-        w2_bytes = cfg.E * cfg.H * cfg.I * wbytes
+        gb = gemm_bytes(cfg, S_used)
         g2_tf = gemm2_flops / (stage_ms[g2] * 1e-3) / 1e12
-        roof = _gemm1_roofline(cfg, peaks, peak, ratio, gemm1_flops, w13_bytes, stage_ms[g1])
+        roof = _gemm1_roofline(cfg, peaks, peak, ratio, gemm1_flops, gb["gemm1"], gb["w13"],
+                               stage_ms[g1])
         roof["peak_source"] = peak_src if roof["bound"] == "tensor" else roof["peak_source"]
         sust = peaks["bf16_tflops_sustained"] * ratio
         roof["tensor_frac_vs_sustained"] = roof["tensor_frac"] * peak / sust
@@ -546,8 +576,11 @@ def _measure(moe, cfg, args, dev, world, rank, full, fp8_tflops=None):
             "fused_call_ms": fused_ms,
             "roofline": roof,
             "gemm2_roofline": {"kernel": g2, "achieved": g2_tf, "frac": g2_tf / peak,
-                               "weight_hbm_frac": w2_bytes / (stage_ms[g2] * 1e-3) / 1e9 /
+                               "hbm_frac": gb["gemm2"] / (stage_ms[g2] * 1e-3) / 1e9 /
+                               peaks["hbm_gbs"],
+                               "weight_hbm_frac": gb["w2"] / (stage_ms[g2] * 1e-3) / 1e9 /
                                peaks["hbm_gbs"]},
+            "used_rows": S_used,
             "e2e": {"value": world * R / e2e_s, "unit": UNIT, "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "ms_per_step": e2e_s * 1e3,
                     "path": "fused_experts_from_host on pinned host buffers: topk ids/weights "
@@ -606,8 +639,8 @@ def run_ours(args):
         for name in EXTRA_WORKLOADS:
             rec = _measure(moe, get_config(name), args, dev, world, rank, False, fp8_tf)
             keep = ("value", "unit", "ms_per_step", "dtype", "config", "tflops", "stages_ms",
-                    "fused_call_ms", "roofline", "gemm2_roofline", "e2e", "gpu_launches",
-                    "clocks")
+                    "fused_call_ms", "roofline", "gemm2_roofline", "used_rows", "e2e",
+                    "gpu_launches", "clocks")
             extra[name] = {k: rec[k] for k in keep}
     if rank == 0:
         if extra:

@@ -560,10 +560,10 @@ __device__ __forceinline__ void epi_glu_store32(const Epilogue& ep, int e, int g
   }
   st_row64(dst, w);
 }
-// Plain epilogue for 32 columns of one row: bf16((acc + bias) * w) at dst.
-__device__ __forceinline__ void epi_store32(const Epilogue& ep, int e, int col0, float w,
-                                            const uint32_t (&r)[32], __nv_bfloat16* dst) {
-  uint32_t pk[16];
+// Plain epilogue values of 32 columns of one row: bf16((acc + bias) * w),
+// packed two per word in memory order.
+__device__ __forceinline__ void epi_pack32(const Epilogue& ep, int e, int col0, float w,
+                                           const uint32_t (&r)[32], uint32_t (&pk)[16]) {
   const bool bias = ep.bias != nullptr;
 #pragma unroll
   for (int j = 0; j < 16; ++j) {
@@ -574,6 +574,12 @@ __device__ __forceinline__ void epi_store32(const Epilogue& ep, int e, int col0,
     }
     pk[j] = bf16x2_bits(__float2bfloat16_rn(v0 * w), __float2bfloat16_rn(v1 * w));
   }
+}
+// Plain epilogue for 32 columns of one row: bf16((acc + bias) * w) at dst.
+__device__ __forceinline__ void epi_store32(const Epilogue& ep, int e, int col0, float w,
+                                            const uint32_t (&r)[32], __nv_bfloat16* dst) {
+  uint32_t pk[16];
+  epi_pack32(ep, e, col0, w, r, pk);
   st_row64(dst, pk);
 }
 
