@@ -458,15 +458,17 @@ const char* moe_last_error_string(void);
  * (0, 0) to restore the defaults.  Not thread-safe; affects later launches. */
 void moe_debug_set_watchdog(int64_t limit_ns, int never_arrive);
 
-/* Test hook for the bf16 and FP8-block grouped GEMMs (stages 2 and 4), which
- * come in two forms with identical results up to fp32 summation order:
- * 128 x 256 tiles on one SM, and 256 x 256 tiles on SM pairs (cta_group::2).
- * By default bf16 uses the pair form when the experts average at least two
- * 128-row blocks (M * topk >= 256 * E) and FP8 always uses one SM (its pair
- * form measured no faster; the FP8 GEMM1 with the activation fused has the
- * single-SM form only).  mode 0 restores that choice, 1 forces the single-SM
- * form, 2 the pair form.  Not thread-safe; affects later launches.  No
- * counterpart on the pages: it only lets tests reach both forms at any size. */
+/* Test hook for the grouped GEMMs (stages 2 and 4), which come in two forms
+ * with identical results up to fp32 summation order: 128 x 256 tiles on one
+ * SM, and 256 x 256 tiles on SM pairs (cta_group::2).  By default bf16 uses
+ * the pair form when the experts average at least two 128-row blocks
+ * (M * topk >= 256 * E); FP8-block, MXFP4 and MXFP8 always use one SM (their
+ * pair forms measured no faster; the FP8 GEMM1 with the activation fused has
+ * the single-SM form only, the block-scaled pair form needs prepacked weight
+ * scales).  The pair forms take block size 128 only.  mode 0 restores the
+ * default, 1 forces the single-SM form, 2 the pair form where one exists.
+ * Not thread-safe; affects later launches.  No counterpart on the pages: it
+ * only lets tests reach both forms at any size. */
 void moe_debug_set_bf16_gemm_form(int mode);
 
 #ifdef __cplusplus

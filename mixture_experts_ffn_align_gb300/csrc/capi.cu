@@ -403,6 +403,14 @@ bool use_pairs(int64_t rows_per_expert, int block_size) {
 // measured 2.64 / 1.70 ms against 2.54 / 1.54 ms for the DeepSeek-class
 // GEMM1 / GEMM2).
 bool use_fp8_pairs(int block_size) { return block_size == 128 && g_bf16_form == 2; }
+// The block-scaled GEMMs run on one SM unless the debug hook forces the pair
+// form (prepacked weight scales and 128-row blocks only): on the DeepSeek-class
+// MXFP8 layer the pair form with no scale synchronisation at all (a timing
+// variant) was 2.20 against 2.35 ms for GEMM1, and delivering each K block's
+// scale operands to both CTAs costs more than that (3.64 ms).
+bool use_mx_pairs(const moe_problem* p) {
+  return p->weight_scales_prepacked && p->block_size == 128 && g_bf16_form == 2;
+}
 bool use_pairs_for(const moe_problem* p, int64_t rows_per_expert) {
   return use_pairs(rows_per_expert, p->block_size);
 }
@@ -448,6 +456,12 @@ moe_status gemm_w13(const moe_problem* p, const void* x_perm, const float* x_sca
   }
   if (!x_scale || !w13_scale) return MOE_ERR_INVALID_ARG;
   if (fuse_act && !out_scale) return MOE_ERR_INVALID_ARG;
+  if (block_scaled(p) && use_mx_pairs(p))
+    return cuda_status(launch_ggemm_mx_2sm(
+        x_perm, x_scale, cap, p->H, w13, static_cast<const uint8_t*>(w13_scale), p->E * 2 * p->I,
+        2 * p->I, 2 * p->I, block_expert_ids, num_post_padded, out,
+        p->quant == MOE_Q_MXFP8_1X32, ep, s, out_scale, fuse_act != 0,
+        p->act_scale_fmt == MOE_SCALE_UE8M0, tile_ctr));
   if (block_scaled(p))
     return cuda_status(launch_ggemm_mxfp4(
         x_perm, x_scale, cap, p->H, w13, static_cast<const uint8_t*>(w13_scale), p->E * 2 * p->I,
@@ -526,6 +540,12 @@ moe_status gemm_w2(const moe_problem* p, const void* z, const float* z_scale, co
                                         p->block_size));
   }
   if (!z_scale || !w2_scale) return MOE_ERR_INVALID_ARG;
+  if (block_scaled(p) && use_mx_pairs(p))
+    return cuda_status(launch_ggemm_mx_2sm(z, z_scale, cap, p->I, w2,
+                                           static_cast<const uint8_t*>(w2_scale), p->E * p->H,
+                                           p->H, p->H, block_expert_ids, num_post_padded, y2,
+                                           p->quant == MOE_Q_MXFP8_1X32, ep, s, nullptr, false,
+                                           true, tile_ctr));
   if (block_scaled(p))
     return cuda_status(launch_ggemm_mxfp4(z, z_scale, cap, p->I, w2,
                                           static_cast<const uint8_t*>(w2_scale), p->E * p->H,

@@ -69,6 +69,7 @@
 #include "e4m3_pack.cuh"
 #include "moe_common.cuh"
 #include "moe_internal.h"
+#include "mx_common.cuh"
 #include "tile_sched.cuh"
 
 namespace moe {
@@ -133,55 +134,6 @@ struct Mx4Args {
   int I;
   int ue8m0;
 };
-
-// Activation scales of 4 K blocks for this lane's rows (lane + 32 c):
-// W4A8: one fp32 per K block (a 1x128 group covers the 4 chunks of 32);
-// MXFP8: four fp32 per K block (one per 1x32 chunk).
-template <bool MX8>
-struct AGroup {
-  float4 v[4][MX8 ? 4 : 1];
-};
-// Loads the scales of K blocks g .. g+3 (those past num_kb read as 2^0) of
-// this lane's rows lane + 32 c of the m-tile starting at tile_row0; rows at
-// or past `rows` (past the expert's segment: their results are not stored)
-// read the tile's first row instead, inside the buffer.
-template <bool MX8>
-__device__ __forceinline__ void load_ascales(AGroup<MX8>& A, const float* a_scale,
-                                             size_t tile_row0, int rows, int lane, int num_kb,
-                                             int g) {
-#pragma unroll
-  for (int c = 0; c < 4; ++c) {
-    const size_t row = tile_row0 + (lane + 32 * c < rows ? lane + 32 * c : 0);
-    if constexpr (MX8) {
-      const float* pa = a_scale + row * (size_t)(4 * num_kb);
-#pragma unroll
-      for (int j = 0; j < 4; ++j)
-        A.v[c][j] = g + j < num_kb ? __ldg(reinterpret_cast<const float4*>(pa + 4 * (g + j)))
-                                   : make_float4(1.0f, 1.0f, 1.0f, 1.0f);
-    } else {
-      const float* pa = a_scale + row * (size_t)num_kb + g;
-      const int n = num_kb - g;
-      if ((num_kb & 3) == 0)
-        A.v[c][0] = __ldg(reinterpret_cast<const float4*>(pa));
-      else
-        A.v[c][0] = make_float4(__ldg(pa), n > 1 ? __ldg(pa + 1) : 1.0f,
-                                n > 2 ? __ldg(pa + 2) : 1.0f, n > 3 ? __ldg(pa + 3) : 1.0f);
-    }
-  }
-}
-// a power-of-two fp32 scale 2^(x-127) has biased exponent x = its E8M0 code
-__device__ __forceinline__ uint32_t e8m0_of(float s) { return (__float_as_uint(s) >> 23) & 0xFFu; }
-// The scale word of row c for K block j of the group: byte q for chunk q.
-template <bool MX8>
-__device__ __forceinline__ uint32_t a_word(const AGroup<MX8>& A, int c, int j) {
-  if constexpr (MX8) {
-    const float4 f = A.v[c][j];
-    return e8m0_of(f.x) | e8m0_of(f.y) << 8 | e8m0_of(f.z) << 16 | e8m0_of(f.w) << 24;
-  } else {
-    const float4 f = A.v[c][0];
-    return e8m0_of(j == 0 ? f.x : j == 1 ? f.y : j == 2 ? f.z : f.w) * 0x01010101u;
-  }
-}
 
 template <int SRC, bool MX8, bool FUSE>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
@@ -707,113 +659,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       // rows past the expert's segment (a partial last m-tile) are not stored
       const bool live = row_in_tile < T.rows;
       const size_t row = (size_t)T.row0 + row_in_tile;
-      if constexpr (FUSE) {
-        // Gated activation + dynamic quantisation of z (as act_mul_quant
-        // does from a stored H1): columns [0, 128) hold this row's gate sums
-        // of n-block n_tile, [128, 256) the matching up sums; each is rounded
-        // to bf16 as H1 would be, z = act(g, u) in fp32, then e4m3 codes with
-        // one scale per group of 32 (MXFP8) or 128 columns.
-        const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16);
-        const int gcol0 = n_tile * 128, ucol0 = args.I + n_tile * 128;
-        const bool bias = args.ep.bias != nullptr;
-        uint4* zdst = reinterpret_cast<uint4*>(args.zq + row * (size_t)args.I + (size_t)gcol0);
-        constexpr int ZG = MX8 ? 32 : 128;                  // quantisation group
-        float* zs_row = args.zs + row * (size_t)(args.I / ZG) + (size_t)n_tile * (128 / ZG);
-        auto zval = [&](uint32_t g, uint32_t u, int col) {
-          float gs = __uint_as_float(g), us = __uint_as_float(u);
-          if (bias) {
-            gs += epi_bias(args.ep, e, gcol0 + col);
-            us += epi_bias(args.ep, e, ucol0 + col);
-          }
-          return act_glu(args.ep, bf16_round(gs), bf16_round(us));
-        };
-        // 16 codes -> uint4; power-of-two scales: v * (1/s) is the exact quotient
-        const bool p2 = args.ue8m0 != 0;
-        auto quant16 = [&](const float* z, float sc, float rc) {
-          float qv[16];
-#pragma unroll
-          for (int b = 0; b < 16; ++b) qv[b] = p2 ? z[b] * rc : quot_rn(z[b], sc, rc);
-          return make_uint4(e4m3x4(qv[0], qv[1], qv[2], qv[3]), e4m3x4(qv[4], qv[5], qv[6], qv[7]),
-                            e4m3x4(qv[8], qv[9], qv[10], qv[11]),
-                            e4m3x4(qv[12], qv[13], qv[14], qv[15]));
-        };
-        if constexpr (MX8) {
-#pragma unroll 1
-          for (int c = 0; c < 4; ++c) {                    // one 1x32 group per chunk
-            uint32_t g[32], u[32];
-            tmem_ld_32x32b_x32(taddr + c * 32, g);
-            tmem_ld_32x32b_x32(taddr + 128 + c * 32, u);
-            tmem_ld_wait();
-            if (c == 3) {                                  // the accumulator is read
-              tc_fence_before();
-              __syncwarp();
-              if (lane == 0) mbar_arrive(tempty_bar);
-            }
-            float z[32];
-            float amax = 0.0f;
-#pragma unroll
-            for (int jj = 0; jj < 32; ++jj) {
-              z[jj] = zval(g[jj], u[jj], c * 32 + jj);
-              amax = fmaxf(amax, fabsf(z[jj]));
-            }
-            const float sc = act_scale(amax, args.ue8m0 != 0);
-            const float rc = __frcp_rn(sc);
-            if (live) {
-              zdst[2 * c] = quant16(z, sc, rc);
-              zdst[2 * c + 1] = quant16(z + 16, sc, rc);
-              zs_row[c] = sc;
-            }
-          }
-        } else {
-          float z[128];
-          float amax = 0.0f;
-#pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            uint32_t g[32], u[32];
-            tmem_ld_32x32b_x32(taddr + c * 32, g);
-            tmem_ld_32x32b_x32(taddr + 128 + c * 32, u);
-            tmem_ld_wait();
-#pragma unroll
-            for (int jj = 0; jj < 32; ++jj) {
-              z[c * 32 + jj] = zval(g[jj], u[jj], c * 32 + jj);
-              amax = fmaxf(amax, fabsf(z[c * 32 + jj]));
-            }
-          }
-          tc_fence_before();                               // the accumulator is read
-          __syncwarp();
-          if (lane == 0) mbar_arrive(tempty_bar);
-          const float sc = act_scale(amax, args.ue8m0 != 0);
-          const float rc = __frcp_rn(sc);
-          if (live) {
-#pragma unroll
-            for (int v = 0; v < 8; ++v) zdst[v] = quant16(z + 16 * v, sc, rc);
-            zs_row[0] = sc;
-          }
-        }
-      } else {
-      const float w = live ? epi_row_weight(args.ep, row) : 0.0f;
-#pragma unroll 1
-      for (int half = 0; half < 2; ++half) {        // 128 columns at a time
-        const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + half * 128;
-        __nv_bfloat16* out_row = args.out + row * args.ldo + (size_t)n_tile * BN + half * 128;
-        // 256 columns, or 128 if ragged; live rows only
-        const bool store = live && half * 128 < N - n_tile * BN;
-        uint32_t r[4][32];
-#pragma unroll
-        for (int c = 0; c < 4; ++c) tmem_ld_32x32b_x32(taddr + c * 32, r[c]);
-        tmem_ld_wait();
-        if (half == 1) {                            // the accumulator is read: hand it back
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(tempty_bar);
-        }
-        if (store) {
-          const int col0 = n_tile * BN + half * 128;
-#pragma unroll
-          for (int c = 0; c < 4; ++c) epi_store32(args.ep, e, col0 + 32 * c, w, r[c], out_row + 32 * c);
-        }
-      }
-      }
+      mx_row_epilogue<MX8, FUSE>(tmem_base + ((uint32_t)(q * 32) << 16), row, live, args.ep, e,
+                                 n_tile, args.I, args.ue8m0 != 0, args.zq, args.zs, args.out,
+                                 args.ldo, N, [&] {
+                                   tc_fence_before();   // the accumulator is read: hand it back
+                                   __syncwarp();
+                                   if (lane == 0) mbar_arrive(tempty_bar);
+                                 });
       ++local;
     }
   }

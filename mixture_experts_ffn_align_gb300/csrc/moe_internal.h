@@ -178,6 +178,18 @@ cudaError_t launch_ggemm_mxfp4(const void* A, const float* a_scale, int cap, int
                                bool ue8m0 = true, bool scales_prepacked = false,
                                int blk_rows = 128);
 
+// The block-scaled GEMM on SM pairs (cta_group::2, 256 x 256 tiles) for
+// prepacked weight scales (b_scale_packed, the layout below) and 128-row
+// blocks; otherwise as launch_ggemm_mxfp4.  Tile counter as for
+// launch_ggemm_bf16_2sm.
+cudaError_t launch_ggemm_mx_2sm(const void* A, const float* a_scale, int cap, int K, const void* B,
+                                const uint8_t* b_scale_packed, int b_rows_total,
+                                int b_rows_per_expert, int n_out,
+                                const int32_t* block_expert_ids, const int32_t* num_post_padded,
+                                void* out, bool b_e4m3, const Epilogue& ep, cudaStream_t stream,
+                                float* z_scale = nullptr, bool fuse_act = false,
+                                bool ue8m0 = true, int* tile_ctr = nullptr);
+
 // E8M0 weight scales [E, N, K/32] -> the operand layout the block-scaled MMA
 // copies into tensor memory: [E][K/128][N/128] blocks of 512 bytes, block
 // byte 16 l + 4 c + j = scale of row 32 c + l of the group, K chunk 4 kb + j.

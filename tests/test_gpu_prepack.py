@@ -15,7 +15,7 @@ import torch
 import mixture_experts_ffn_align_gb300 as moe
 from moe_synth import CONFIGS, MoEConfig, make_inputs
 
-from .gpu_util import np32
+from .gpu_util import bf16_gemm_form, np32
 
 pytestmark = pytest.mark.gpu
 
@@ -82,14 +82,20 @@ def _stages(p, d, w13s, w2s, fuse):
 @pytest.mark.parametrize("quant", ["mxfp4", "mxfp8"])
 @pytest.mark.parametrize("fuse", [False, True])
 @pytest.mark.parametrize("counts,H,I", [([0, 1, 127, 128, 129, 300], 640, 256),
-                                        ([7, 0, 260], 1024, 512)])
-def test_prepacked_stages_equal_unpacked(quant, fuse, counts, H, I):
+                                        ([7, 0, 260], 1024, 512),
+                                        ([256, 384, 5, 128], 1024, 256)])
+@pytest.mark.parametrize("form", ["auto", "pairs"])
+def test_prepacked_stages_equal_unpacked(quant, fuse, counts, H, I, form):
+    """Both forms of the block-scaled GEMM on prepacked scales (one SM, and SM
+    pairs: lone and paired blocks, a 128-wide last column tile) against the
+    single-SM GEMM on the scales as given, bit for bit."""
     cfg, d = _ragged(quant, counts, H, I, 17)
     p = moe.Problem.from_config(cfg)
     pp = moe.Problem.from_config(cfg, weight_scales_prepacked=True)
     a, b = _packed(p, d)
     ref = _stages(p, d, d["w13_scale"], d["w2_scale"], fuse)
-    got = _stages(pp, d, a, b, fuse)
+    with bf16_gemm_form(form):
+        got = _stages(pp, d, a, b, fuse)
     n = int(ref["num_post_padded"].item())
     keys = ("z", "z_scale", "y2") if fuse else ("h1", "z", "z_scale", "y2")
     for k in keys:

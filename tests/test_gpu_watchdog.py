@@ -25,10 +25,28 @@ CASES = {
                       seed=81),
     "fp8": MoEConfig("wd8", M=200, H=512, I=256, E=4, topk=2, quant="fp8", routing="softmax",
                      seed=82),
+    # prepacked weight scales: the block-scaled GEMM's pair form needs them
+    "mxfp8": MoEConfig("wdm8", M=200, H=512, I=256, E=4, topk=2, quant="mxfp8",
+                       routing="softmax", seed=83, act_scale_fmt="ue8m0"),
 }
 
 
 def _fused(cfg, d):
+    if cfg.quant == "mxfp8":
+        p = moe.Problem.from_config(cfg, weight_scales_prepacked=True)
+        if "w13_scale_packed" not in d:
+            q = moe.Problem.from_config(cfg)
+            d["w13_scale_packed"] = torch.empty(moe.moe_prepacked_scale_bytes(q, 0),
+                                                dtype=torch.uint8, device="cuda")
+            d["w2_scale_packed"] = torch.empty(moe.moe_prepacked_scale_bytes(q, 1),
+                                               dtype=torch.uint8, device="cuda")
+            moe.moe_prepack_weights(q, d["w13_scale"], d["w2_scale"], d["w13_scale_packed"],
+                                    d["w2_scale_packed"])
+        ws = torch.empty(moe.moe_workspace_bytes(p), dtype=torch.uint8, device="cuda")
+        y = torch.empty_like(d["x"])
+        moe.fused_experts(p, d["x"], d["w13"], d["w13_scale_packed"], d["w2"],
+                          d["w2_scale_packed"], d["topk_weights"], d["topk_ids"], y, ws)
+        return y
     p = moe.Problem.from_config(cfg)
     ws = torch.empty(moe.moe_workspace_bytes(p), dtype=torch.uint8, device="cuda")
     y = torch.empty_like(d["x"])
@@ -38,7 +56,7 @@ def _fused(cfg, d):
 
 
 @pytest.mark.parametrize("name,form", [("bf16", "single"), ("bf16", "pairs"), ("fp8", "auto"),
-                                       ("fp8", "pairs")])
+                                       ("fp8", "pairs"), ("mxfp8", "auto"), ("mxfp8", "pairs")])
 def test_wait_that_runs_out_reports_timeout_and_context_survives(name, form):
     with bf16_gemm_form(form):
         _timeout_then_recover(name)
@@ -60,5 +78,5 @@ def _timeout_then_recover(name):
     assert moe.moe_sync_status() == 0
     ref, items, w = experts.fused_experts_per_token(
         **oracle_inputs(d), quant=cfg.quant, act_scale_fmt=cfg.act_scale_fmt, return_items=True)
-    check_close(np32(y), ref, BF16_TOL if cfg.quant == "bf16" else QUANT_TOL, name,
+    check_close(np32(y), ref, BF16_TOL if cfg.quant == "bf16" else QUANT_TOL, f"{name} watchdog",
                 flip_allowance(ref, items, w))
