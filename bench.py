@@ -187,8 +187,10 @@ _KERNEL_SOURCES = {
     "bf16": ["gemm_bf16.cu", "moe_common.cuh", "tile_sched.cuh"],
     "bf16_2sm": ["gemm_bf16_2sm.cu", "moe_common.cuh", "tile_sched.cuh"],
     "fp8": ["gemm_fp8.cu", "moe_common.cuh", "tile_sched.cuh", "e4m3_pack.cuh"],
-    "mxfp4": ["gemm_mxfp4.cu", "moe_common.cuh", "tile_sched.cuh", "e4m3_pack.cuh"],
-    "mxfp8": ["gemm_mxfp4.cu", "moe_common.cuh", "tile_sched.cuh", "e4m3_pack.cuh"],
+    "mxfp4": ["gemm_mxfp4.cu", "mx_common.cuh", "moe_common.cuh", "tile_sched.cuh",
+              "e4m3_pack.cuh"],
+    "mxfp8": ["gemm_mxfp4.cu", "mx_common.cuh", "moe_common.cuh", "tile_sched.cuh",
+              "e4m3_pack.cuh"],
 }
 
 

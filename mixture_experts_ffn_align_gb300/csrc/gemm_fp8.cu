@@ -14,13 +14,16 @@
 //  * warp 0 lane 0: TMA producer, 4-stage ring of (A 128x128, B 256x128) e4m3
 //    tiles -- one stage is exactly one 128-wide K block;
 //  * warp 1 lane 0: four kind::f8f6f4 MMAs (M=128, N=256, K=32) per K block
-//    into one of two 256-column tensor-memory partials, alternating.  (128x128
-//    MMAs ran at about half the tensor rate on GB300; N=256 keeps the pipe fed.)
+//    into one of two 256-column tensor-memory partials, alternating, and one
+//    tcgen05.commit (partial full).  (128x128 MMAs ran at about half the
+//    tensor rate on GB300; N=256 keeps the pipe fed.)
 //  * warps 4-11 (warpgroups 1 and 2): warp w owns TMEM lane quadrant w%4 (32
 //    rows) and one 128-column half of the tile -- exactly one 128x128
 //    weight-scale block, so one scale product sa[row,kb]*sb[kb] per thread
 //    and K block; it reads the partial with tcgen05.ld (four 16-column loads
-//    per wait), releases it, and accumulates in fp32 registers; at the end of
+//    per wait), releases it, and accumulates in fp32 registers (the first of
+//    these warps also returns the K block's operand stage to the producer
+//    once the partial is complete); at the end of
 //    the tile the sum is rounded to bf16 and stored.  The 128 accumulators a
 //    thread holds need the register split below (setmaxnreg): warpgroup 0
 //    (producer, MMA issuer, two idle warps) gives registers up.
@@ -211,8 +214,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const uint32_t d_tmem = tmem_base + buf * BN;
 #pragma unroll
         for (int k = 0; k < BK / 32; ++k) umma_f8(d_tmem, adesc + 2 * k, bdesc + 2 * k, idesc, k);
-        tc_commit(empty_bar(stage));
-        tc_commit(pfull_bar(buf));
+        tc_commit(pfull_bar(buf));     // also frees the stage: see the epilogue
         if (++stage == STAGES) {
           stage = 0;
           phase ^= 1;
@@ -279,6 +281,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             ok = false;
             break;
           }
+          // The K block's MMAs have completed, so they are done reading its
+          // operand stage (one stage per K block, in the same order): hand
+          // it back to the producer from here rather than with a second
+          // tcgen05.commit per K block (that commit cost ~45 cycles of
+          // the tensor pipe's 512 a K block).
+          if (warp == EPI_WARP0 && lane == 0) mbar_arrive(empty_bar(pc % STAGES));
           tc_fence_after();
           // FUSE: columns [64 half, +64) of the gate half, then of the up half
           const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + buf * BN +
