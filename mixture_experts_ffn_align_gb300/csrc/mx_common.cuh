@@ -64,7 +64,8 @@ __device__ __forceinline__ uint32_t a_word(const AGroup<MX8>& A, int c, int j) {
 // the next tile may then overwrite it).
 //  FUSE (GEMM1 with the activation): columns [0, 128) hold the row's gate
 //    sums of n-block n_tile, [128, 256) the matching up sums; each is rounded
-//    to bf16 as a stored H1 would be, z = act(g, u) in fp32 (as act_mul_quant
+//    to bf16 as a stored H1 would be (all of them read before the
+//    accumulator is released), z = act(g, u) in fp32 (as act_mul_quant
 //    computes it), then e4m3 codes with one scale per group of 32 (MXFP8) or
 //    128 columns into zq [rows, I] / zs [rows, I / group].
 //  otherwise: bf16((sum + bias) * router weight) into out [rows, ldo], 256
@@ -83,67 +84,75 @@ __device__ __forceinline__ void mx_row_epilogue(uint32_t taddr, size_t row, bool
     uint4* zdst = reinterpret_cast<uint4*>(zq + row * (size_t)I + (size_t)gcol0);
     constexpr int ZG = MX8 ? 32 : 128;                  // quantisation group
     float* zs_row = zs + row * (size_t)(I / ZG) + (size_t)n_tile * (128 / ZG);
-    auto zval = [&](uint32_t g, uint32_t u, int col) {
-      float gs = __uint_as_float(g), us = __uint_as_float(u);
-      if (bias) {
-        gs += epi_bias(ep, e, gcol0 + col);
-        us += epi_bias(ep, e, ucol0 + col);
+    // First read the whole accumulator row, keeping each (gate, up) pair as
+    // the two bf16 roundings the activation takes (what a stored H1 would
+    // hold), and hand the accumulator back: the next tile's MMAs then wait
+    // only for these loads, not for the activation arithmetic.
+    uint32_t w[128];                                   // column c: g low, u high
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      uint32_t g[32], u[32];
+      tmem_ld_32x32b_x32(taddr + c * 32, g);
+      tmem_ld_32x32b_x32(taddr + 128 + c * 32, u);
+      tmem_ld_wait();
+#pragma unroll
+      for (int jj = 0; jj < 32; ++jj) {
+        float gs = __uint_as_float(g[jj]), us = __uint_as_float(u[jj]);
+        if (bias) {
+          gs += epi_bias(ep, e, gcol0 + c * 32 + jj);
+          us += epi_bias(ep, e, ucol0 + c * 32 + jj);
+        }
+        w[c * 32 + jj] = bf16x2_bits(__float2bfloat16_rn(gs), __float2bfloat16_rn(us));
       }
-      return act_glu(ep, bf16_round(gs), bf16_round(us));
+    }
+    release();                                         // the accumulator is read
+    // z = act(g, u) in fp32 (as act_mul_quant computes it), in place
+    auto zval = [&](uint32_t gu) {
+      return act_glu(ep, __uint_as_float(gu << 16), __uint_as_float(gu & 0xFFFF0000u));
     };
     // 16 codes -> uint4; power-of-two scales: v * (1/s) is the exact quotient
-    auto quant16 = [&](const float* z, float sc, float rc) {
+    auto quant16 = [&](const uint32_t* zb, float sc, float rc) {
       float qv[16];
 #pragma unroll
-      for (int b = 0; b < 16; ++b) qv[b] = ue8m0 ? z[b] * rc : quot_rn(z[b], sc, rc);
+      for (int b = 0; b < 16; ++b) {
+        const float z = __uint_as_float(zb[b]);
+        qv[b] = ue8m0 ? z * rc : quot_rn(z, sc, rc);
+      }
       return make_uint4(e4m3x4(qv[0], qv[1], qv[2], qv[3]), e4m3x4(qv[4], qv[5], qv[6], qv[7]),
                         e4m3x4(qv[8], qv[9], qv[10], qv[11]),
                         e4m3x4(qv[12], qv[13], qv[14], qv[15]));
     };
     if constexpr (MX8) {
-#pragma unroll 1
+#pragma unroll
       for (int c = 0; c < 4; ++c) {                    // one 1x32 group per chunk
-        uint32_t g[32], u[32];
-        tmem_ld_32x32b_x32(taddr + c * 32, g);
-        tmem_ld_32x32b_x32(taddr + 128 + c * 32, u);
-        tmem_ld_wait();
-        if (c == 3) release();                         // the accumulator is read
-        float z[32];
         float amax = 0.0f;
 #pragma unroll
         for (int jj = 0; jj < 32; ++jj) {
-          z[jj] = zval(g[jj], u[jj], c * 32 + jj);
-          amax = fmaxf(amax, fabsf(z[jj]));
+          const float z = zval(w[c * 32 + jj]);
+          w[c * 32 + jj] = __float_as_uint(z);
+          amax = fmaxf(amax, fabsf(z));
         }
         const float sc = act_scale(amax, ue8m0);
         const float rc = __frcp_rn(sc);
         if (live) {
-          zdst[2 * c] = quant16(z, sc, rc);
-          zdst[2 * c + 1] = quant16(z + 16, sc, rc);
+          zdst[2 * c] = quant16(w + c * 32, sc, rc);
+          zdst[2 * c + 1] = quant16(w + c * 32 + 16, sc, rc);
           zs_row[c] = sc;
         }
       }
     } else {
-      float z[128];
       float amax = 0.0f;
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint32_t g[32], u[32];
-        tmem_ld_32x32b_x32(taddr + c * 32, g);
-        tmem_ld_32x32b_x32(taddr + 128 + c * 32, u);
-        tmem_ld_wait();
-#pragma unroll
-        for (int jj = 0; jj < 32; ++jj) {
-          z[c * 32 + jj] = zval(g[jj], u[jj], c * 32 + jj);
-          amax = fmaxf(amax, fabsf(z[c * 32 + jj]));
-        }
+      for (int j = 0; j < 128; ++j) {
+        const float z = zval(w[j]);
+        w[j] = __float_as_uint(z);
+        amax = fmaxf(amax, fabsf(z));
       }
-      release();                                       // the accumulator is read
       const float sc = act_scale(amax, ue8m0);
       const float rc = __frcp_rn(sc);
       if (live) {
 #pragma unroll
-        for (int v = 0; v < 8; ++v) zdst[v] = quant16(z + 16 * v, sc, rc);
+        for (int v = 0; v < 8; ++v) zdst[v] = quant16(w + 16 * v, sc, rc);
         zs_row[0] = sc;
       }
     }
