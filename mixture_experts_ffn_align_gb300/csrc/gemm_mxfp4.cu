@@ -48,7 +48,12 @@
 //    issues four MMAs (M=128, N=256, K=32) into the 256-column accumulator
 //    (N=128 MMAs run at about half the tensor rate); copy and MMAs run in
 //    issue order in the tensor pipe, so no thread waits between them, and
-//    tcgen05.commit frees the stage and the scale slot.  (Writing the scales
+//    one tcgen05.commit frees the stage and its scale slot.  W4A8: lane 0 of
+//    warp 2 (no scale writing to do there) makes the copies and commits
+//    each slot's readiness, and the MMA issuer only waits for it: a thread's
+//    shared-memory waits stall behind its own copies still queued in the
+//    tensor pipe (~80 cycles a K block, measured), so they are better taken
+//    off the issuer.  (Writing the scales
 //    into tensor memory with tcgen05.st from four warps cost 0.34 of 1.13 ms
 //    on the DeepSeek-shaped GEMM1.)  Each smem stage has its own tensor-memory
 //    scale slot (16-column aligned: an odd-column scale address raised a
@@ -105,8 +110,8 @@ constexpr int TMEM_COLS = 512;
 constexpr int NUM_EPI_WARPS = 4, EPI_WARP0 = 4;
 constexpr int NUM_THREADS = (EPI_WARP0 + NUM_EPI_WARPS) * 32;
 constexpr int SMEM_BYTES =
-    STAGES * STAGE_BYTES + SSLOTS * SF_BYTES + NSTG * STG_BYTES + 1024 + 256 + kSchedBytes;
-static_assert(SF_COL0 + SF_SLOT * (2 * STAGES - 1) + BN / 32 <= TMEM_COLS, "tensor memory");
+    STAGES * STAGE_BYTES + SSLOTS * SF_BYTES + NSTG * STG_BYTES + 1024 + 512 + kSchedBytes;
+static_assert(SF_COL0 + SF_SLOT * (2 * SSLOTS - 1) + BN / 32 <= TMEM_COLS, "tensor memory");
 static_assert(SMEM_BYTES <= 232448, "shared memory");
 
 struct Mx4Args {
@@ -142,13 +147,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
+  constexpr bool COPIER = !MX8;   // warp 2 copies the scales into tensor memory (W4A8)
   uint8_t* sf_ring = smem + STAGES * STAGE_BYTES;    // SSLOTS x SF_BYTES, 16-byte aligned
   uint8_t* stg_ring = sf_ring + SSLOTS * SF_BYTES;     // NSTG x STG_BYTES (SRC_STAGED)
   uint64_t* bars = reinterpret_cast<uint64_t*>(stg_ring + NSTG * STG_BYTES);
-  // full[S], empty[S], sfull[SS], sempty[SS], tfull, tempty, drain, stg_full[NSTG]
-  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 2 * SSLOTS + 3 + NSTG);
+  // full[S], empty[S], sfull[SS], (SS unused), tfull, tempty, drain, stg_full[NSTG],
+  // sready[SS], cdrain
+  uint32_t* tmem_holder =
+      reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 3 * SSLOTS + 4 + NSTG);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
-  int* s_sched = reinterpret_cast<int*>(stg_ring + NSTG * STG_BYTES + 256);
+  int* s_sched = reinterpret_cast<int*>(stg_ring + NSTG * STG_BYTES + 512);
+  static_assert(8 * (2 * STAGES + 3 * SSLOTS + 4 + NSTG) + 8 <= 512, "barrier area");
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t smem_base = smem_u32(smem);
@@ -157,11 +166,19 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   auto full_bar = [&](int s) { return bar_base + 8u * s; };
   auto empty_bar = [&](int s) { return bar_base + 8u * (STAGES + s); };
   auto sfull_bar = [&](int s) { return bar_base + 8u * (2 * STAGES + s); };
-  auto sempty_bar = [&](int s) { return bar_base + 8u * (2 * STAGES + SSLOTS + s); };
+  // A scale slot is free once the MMAs of its K block have completed, which
+  // is when the operand stage of that K block is (one slot per stage): the
+  // stage's barrier serves both, one tcgen05.commit per K block.
+  static_assert(SSLOTS == STAGES, "one scale slot per operand stage");
+  auto sempty_bar = [&](int s) { return empty_bar(s); };
   const uint32_t tfull_bar = bar_base + 8u * (2 * STAGES + 2 * SSLOTS);
   const uint32_t tempty_bar = bar_base + 8u * (2 * STAGES + 2 * SSLOTS + 1);
   const uint32_t drain_bar = bar_base + 8u * (2 * STAGES + 2 * SSLOTS + 2);
   auto stg_full = [&](int s) { return bar_base + 8u * (2 * STAGES + 2 * SSLOTS + 3 + s); };
+  auto sready_bar = [&](int s) {
+    return bar_base + 8u * (2 * STAGES + 2 * SSLOTS + 3 + NSTG + s);
+  };
+  const uint32_t cdrain_bar = bar_base + 8u * (2 * STAGES + 3 * SSLOTS + 3 + NSTG);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -170,8 +187,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
     for (int s = 0; s < SSLOTS; ++s) {
       mbar_init(sfull_bar(s), MX8 ? 2 : 1);   // one arrival per scale writer
-      mbar_init(sempty_bar(s), 1);
+      mbar_init(sready_bar(s), 1);
     }
+    mbar_init(cdrain_bar, 1);
     mbar_init(tfull_bar, 1);
     mbar_init(tempty_bar, NUM_EPI_WARPS);
     for (int s = 0; s < NSTG; ++s) mbar_init(stg_full(s), 1);
@@ -241,6 +259,41 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     for (int s = 0; s < STAGES; ++s)
       if (issued_mask & (1u << s))
         mbar_wait_bounded(full_bar(s), (issued_parity >> s) & 1, nullptr, args.limit_ns, args.err);
+  } else if (COPIER && warp == 2) {
+    // ------------------------------------------------------------ scale copier
+    // W4A8 (one scale writer, warp 3): lane 0 of warp 2 copies each complete
+    // slot into its tensor-memory scale slot (tcgen05.cp) and commits
+    // sready, so the MMA issuer only waits for ready scales.  When the
+    // issuer made the copies, each of its later shared-memory waits stalled
+    // behind its own copies still queued in the tensor pipe (~80 cycles of a
+    // 512-cycle K block); a thread with no other work can take that stall.
+    // The tensor memory of slot s is free: the slot was rewritten only after
+    // its MMAs of SSLOTS K blocks earlier completed (sempty).
+    if (lane == 0) {
+      uint32_t cslot = 0, cphase = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+        for (int kb = 0; kb < args.num_kb; ++kb) {
+          if (!mbar_wait_bounded(sfull_bar(cslot), cphase, abort_flag, args.limit_ns, args.err)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sfa = tmem_base + SF_COL0 + SF_SLOT * 2 * cslot;
+          const uint32_t src = sf_base + cslot * SF_BYTES;
+          tmem_cp_32x128b_x4(sfa, sdesc_rows16(src));
+          tmem_cp_32x128b_x4(sfa + SF_SLOT, sdesc_rows16(src + SF_A_BYTES));
+          tmem_cp_32x128b_x4(sfa + SF_SLOT + 4, sdesc_rows16(src + SF_A_BYTES + 512));
+          tc_commit(sready_bar(cslot));
+          if (++cslot == SSLOTS) {
+            cslot = 0;
+            cphase ^= 1;
+          }
+        }
+      }
+      tc_commit(cdrain_bar);   // this thread's copies complete before the CTA tears down
+      mbar_wait_bounded(cdrain_bar, 0, nullptr, args.limit_ns, args.err);
+    }
   } else if ((MX8 && warp == 2) || warp == 3) {
     // ------------------------------------------------------------ scale writers
     // Warp 3 builds the weight-scale operand of each K block (the E8M0 bytes
@@ -605,7 +658,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       tc_fence_after();
       for (int kb = 0; kb < args.num_kb; ++kb) {
         if (!mbar_wait_bounded(full_bar(stage), phase, abort_flag, args.limit_ns, args.err) ||
-            !mbar_wait_bounded(sfull_bar(sslot), sphase, abort_flag, args.limit_ns, args.err)) {
+            !mbar_wait_bounded(COPIER ? sready_bar(sslot) : sfull_bar(sslot), sphase, abort_flag,
+                               args.limit_ns, args.err)) {
           ok = false;
           break;
         }
@@ -613,11 +667,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const uint32_t sa = smem_base + stage * STAGE_BYTES;
         const uint64_t adesc = sdesc_k_sw128(sa);
         const uint64_t bdesc = sdesc_k_sw128(sa + A_BYTES);
-        const uint32_t sfa = tmem_base + SF_COL0 + SF_SLOT * 2 * stage;
-        const uint32_t sf_src = sf_base + sslot * SF_BYTES;
-        tmem_cp_32x128b_x4(sfa, sdesc_rows16(sf_src));
-        tmem_cp_32x128b_x4(sfa + SF_SLOT, sdesc_rows16(sf_src + SF_A_BYTES));
-        tmem_cp_32x128b_x4(sfa + SF_SLOT + 4, sdesc_rows16(sf_src + SF_A_BYTES + 512));
+        const uint32_t sfa = tmem_base + SF_COL0 + SF_SLOT * 2 * sslot;
+        if constexpr (!COPIER) {
+          const uint32_t sf_src = sf_base + sslot * SF_BYTES;
+          tmem_cp_32x128b_x4(sfa, sdesc_rows16(sf_src));
+          tmem_cp_32x128b_x4(sfa + SF_SLOT, sdesc_rows16(sf_src + SF_A_BYTES));
+          tmem_cp_32x128b_x4(sfa + SF_SLOT + 4, sdesc_rows16(sf_src + SF_A_BYTES + 512));
+        }
 #pragma unroll
         for (int j = 0; j < BK / 32; ++j) {
           umma_mxf8f6f4(tmem_base, adesc + 2 * j, bdesc + 2 * j,
@@ -625,8 +681,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         sfa,
                         sfa + SF_SLOT, (kb | j) != 0);
         }
-        tc_commit(empty_bar(stage));
-        tc_commit(sempty_bar(sslot));
+        tc_commit(empty_bar(stage));   // frees the stage and its scale slot
         if (++stage == STAGES) {
           stage = 0;
           phase ^= 1;
