@@ -28,11 +28,14 @@ CASES = {
     # prepacked weight scales: the block-scaled GEMM's pair form needs them
     "mxfp8": MoEConfig("wdm8", M=200, H=512, I=256, E=4, topk=2, quant="mxfp8",
                        routing="softmax", seed=83, act_scale_fmt="ue8m0"),
+    # W4A8: a warp of its own copies the scale operands into tensor memory
+    "mxfp4": MoEConfig("wdm4", M=200, H=512, I=256, E=4, topk=2, quant="mxfp4",
+                       routing="softmax", seed=84, act_scale_fmt="ue8m0"),
 }
 
 
 def _fused(cfg, d):
-    if cfg.quant == "mxfp8":
+    if cfg.quant in ("mxfp4", "mxfp8"):
         p = moe.Problem.from_config(cfg, weight_scales_prepacked=True)
         if "w13_scale_packed" not in d:
             q = moe.Problem.from_config(cfg)
@@ -56,7 +59,8 @@ def _fused(cfg, d):
 
 
 @pytest.mark.parametrize("name,form", [("bf16", "single"), ("bf16", "pairs"), ("fp8", "auto"),
-                                       ("fp8", "pairs"), ("mxfp8", "auto"), ("mxfp8", "pairs")])
+                                       ("fp8", "pairs"), ("mxfp8", "auto"), ("mxfp8", "pairs"),
+                                       ("mxfp4", "auto"), ("mxfp4", "pairs")])
 def test_wait_that_runs_out_reports_timeout_and_context_survives(name, form):
     with bf16_gemm_form(form):
         _timeout_then_recover(name)
