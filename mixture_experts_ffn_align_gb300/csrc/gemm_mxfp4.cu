@@ -487,6 +487,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       // words are built as in the other forms (warp 2 for MXFP8, warp 3 for
       // W4A8), one group of 4 K blocks ahead.
       const int G = N / 128;                     // 128-row scale groups per expert
+      constexpr int SCALE_PF = 8;                // K blocks ahead for the L2 prefetch
       const bool writes_a = wa || !MX8;
       const bool writes_b = !wa;
       bool ok = true;
@@ -522,6 +523,20 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             uint8_t* slot = sf_ring + sslot * SF_BYTES;
             if (writes_b && lane == 0) {
               const uint8_t* src = args.b_scale + ((size_t)e * args.num_kb + kb) * G * 512;
+              // The slot's copy waits for these bytes a few K blocks from now,
+              // and they are read once from HBM (at W4A8 rates that latency
+              // showed through the slot ring): ask for those of K block
+              // kb + SCALE_PF in L2 already.  (Running on into the CTA's next
+              // tile measured slower on GEMM1.)
+              if (kb + SCALE_PF < args.num_kb) {
+                const uint8_t* pf = src + (size_t)SCALE_PF * G * 512;
+                if (FUSE || !two) {
+                  bulk_prefetch_l2(pf + (size_t)g0 * 512, 512);
+                  if (two) bulk_prefetch_l2(pf + (size_t)g1 * 512, 512);
+                } else {
+                  bulk_prefetch_l2(pf + (size_t)g0 * 512, 1024);
+                }
+              }
               const uint32_t dst = smem_u32(slot + SF_A_BYTES);
               const uint32_t bytes = two ? 1024u : 512u;
               // MXFP8: this arrival is warp 3's; W4A8: warp 3 arrives below

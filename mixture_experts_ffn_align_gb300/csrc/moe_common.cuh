@@ -145,6 +145,12 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
       : "memory");
 }
 
+// Asks for `bytes` (a multiple of 16, 16-byte aligned) of global memory to be
+// brought into L2; no completion to wait for.
+__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
 // Asks for a 2-D box of a tensor to be brought into L2 (no shared memory,
 // no completion to wait for); used ahead of the loads of a streamed operand.
 __device__ __forceinline__ void tma_prefetch_l2_2d(const CUtensorMap* map, int32_t c0,
