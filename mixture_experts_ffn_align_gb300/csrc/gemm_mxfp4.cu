@@ -23,9 +23,10 @@
 //    padded 4-bit TMA type (each 16 values -> 8 bytes + 8-byte gap, so a row
 //    of 128 values fills one 128-byte swizzled smem row; the copy counts the
 //    packed bytes toward the barrier), 128-byte swizzle;
-//  * warps 2 and 3: scale writers (warp 2 the A operand, warp 3 the B
-//    operand; one warp doing both measured busy ~90 % of the kernel and
-//    stalled the MMA issuer ~27 % of the DeepSeek-shaped MXFP8 GEMM1).  Per
+//  * scale writers: MXFP8, warps 2 and 3 (warp 2 the A operand, warp 3 the
+//    B operand; one warp doing both measured busy ~90 % of the kernel and
+//    stalled the MMA issuer ~27 % of the DeepSeek-shaped MXFP8 GEMM1); W4A8,
+//    warp 3 alone (warp 2 copies the slots into tensor memory, below).  Per
 //    K block they build the two scale operands in
 //    a shared-memory ring of SSLOTS slots: the A operand (each row's UE8M0
 //    exponent in all 4 bytes: one scale covers 128 = 4 x 32) and the B
